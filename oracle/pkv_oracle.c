@@ -1,0 +1,381 @@
+/*
+ * pkv_oracle.c -- reference oracle for the batched paged-KV decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline leg load this file's library. The CUDA library
+ * never links it, calls it or includes anything from it, and this file includes
+ * nothing from the CUDA library.
+ *
+ * Plain, slow, single-threaded C in fp64 (build with -ffp-contract=off so that
+ * every product and sum is rounded exactly as written). Each function cites the
+ * passage it follows:
+ *
+ *  [P2] "手写LLM推理引擎：Tokenizer、Transformer与Detokenizer三段式实现",
+ *       section 3.2 (the two RoPE equations and the cos/sin precompute routine,
+ *       whose inverse frequency is base^(-2j/dim)).
+ *  [P3] "Hours of YouTube and 85 handtyped pages of notes on LLM Inference –
+ *       Start here" (the samir-vllm README), feature list: the shared BF16 KV
+ *       page pool item (16 tokens of K and V per physical page, block table
+ *       per sequence and layer, decode appends the new token at its absolute
+ *       RoPE position) and the direct paged decode attention item (each query
+ *       head streams its sequence's cached pages, FP32 online softmax).
+ *  [P4] "llmc — 从零写一个大模型推理引擎（配套代码）", file table (an explicit
+ *       softmax operator) and the introduction (negative return = error).
+ *
+ * Readings taken where the pages are silent or at odds (all listed in the
+ * design notes):
+ *  - RoPE pairs dimension j with j + D/2 ("rotate-half"), not (2j, 2j+1) as
+ *    [P2]'s equations print them; the workload statement fixes rotate-half.
+ *    No frequency scaling: inv_freq_j = theta^(-2j/D) exactly as [P2].
+ *  - The rotated key is computed in fp64 (two rounded products, one rounded
+ *    sum) and rounded once, to nearest-even, from double to bf16. V is copied.
+ *  - The rotated query is kept in fp64 (the GPU keeps fp32); it is not
+ *    rounded to bf16.
+ *  - Query head i reads KV head i / (Hq/Hkv) (consecutive groups).
+ *  - The attention is the plain definition: gather, scores, explicit
+ *    two-pass softmax, weighted sum of V. The online form of [P3] computes the
+ *    same value up to rounding order.
+ *
+ * Pool layout (the library's documented contract; the oracle indexes it with
+ * its own function): element (page, kv head h, kind K=0/V=1, slot s, dim d)
+ * lives at bf16 offset ((((page*Hkv + h)*2 + kind)*P + s)*D + d).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_MAX_DIM 256
+
+/* bf16 bits -> double. A bf16 value is the top half of a binary32 value, and
+ * every binary32 value is exact in double. */
+double oracle_bf16_to_double(uint16_t bits)
+{
+	uint32_t u = (uint32_t)bits << 16;
+	float f;
+	memcpy(&f, &u, sizeof f);
+	return (double)f;
+}
+
+/* double -> bf16, round to nearest, ties to even, from the format's
+ * definition: sign, 8 exponent bits (bias 127), 7 fraction bits; below 2^-126
+ * the grid is the subnormal grid of spacing 2^-133. The value is scaled so that
+ * one unit in the last place is 1, rounded to an integer (ties to even), and
+ * scaled back; the result has at most 8 significant bits and is therefore
+ * exact in binary32, whose upper half is the bf16 encoding. NaN maps to the
+ * canonical quiet NaN 0x7FC0. */
+uint16_t oracle_bf16_from_double(double x)
+{
+	if (isnan(x))
+		return 0x7FC0;
+	uint16_t sign = signbit(x) ? 0x8000 : 0;
+	double a = fabs(x);
+	if (isinf(a))
+		return sign | 0x7F80;
+	if (a == 0.0)
+		return sign;
+	int e;
+	frexp(a, &e);              /* a = f * 2^e, f in [0.5, 1): floor(log2 a) = e - 1 */
+	int binade = e - 1;
+	if (binade < -126)
+		binade = -126;         /* subnormals share the spacing of the lowest binade */
+	int ulp_exp = binade - 7;  /* 7 fraction bits */
+	double n = nearbyint(ldexp(a, -ulp_exp)); /* exact scaling; default mode: ties to even */
+	double r = ldexp(n, ulp_exp);
+	if (r >= 0x1p128)
+		return sign | 0x7F80;  /* rounds past the largest finite bf16 */
+	float f = (float)r;        /* exact */
+	uint32_t u;
+	memcpy(&u, &f, sizeof u);
+	return sign | (uint16_t)((u >> 16) & 0x7FFF);
+}
+
+void oracle_bf16_from_double_array(const double *x, uint16_t *out, long n)
+{
+	for (long i = 0; i < n; i++)
+		out[i] = oracle_bf16_from_double(x[i]);
+}
+
+/* [P2] section 3.2, cos/sin precompute: inverse frequency base^(-2j/dim). */
+double oracle_rope_inv_freq(double theta, int j, int head_dim)
+{
+	return pow(theta, -(2.0 * (double)j) / (double)head_dim);
+}
+
+/* [P2] section 3.2, the two RoPE equations, read with rotate-half pairing:
+ * for j < D/2, with angle = pos * inv_freq_j,
+ *   y_j       = x_j * cos - x_{j+D/2} * sin
+ *   y_{j+D/2} = x_{j+D/2} * cos + x_j * sin
+ * Each product and each sum is one fp64 rounding (no fused multiply-add). */
+void oracle_rope_rotate(const double *x, double *y, int head_dim, long pos, double theta)
+{
+	int half = head_dim / 2;
+	for (int j = 0; j < half; j++) {
+		double angle = (double)pos * oracle_rope_inv_freq(theta, j, head_dim);
+		double c = cos(angle);
+		double s = sin(angle);
+		double a = x[j];
+		double b = x[j + half];
+		double ac = a * c;
+		double bs = b * s;
+		double bc = b * c;
+		double as = a * s;
+		y[j] = ac - bs;
+		y[j + half] = bc + as;
+	}
+}
+
+/* Rotate n vectors of length head_dim, vector i at position pos[i]. */
+void oracle_rope_rotate_many(const double *x, double *y, long n, int head_dim,
+			     const int32_t *pos, double theta)
+{
+	for (long i = 0; i < n; i++)
+		oracle_rope_rotate(x + i * head_dim, y + i * head_dim, head_dim, pos[i], theta);
+}
+
+static size_t pool_offset(long page, int h, int kind, int slot, int d,
+			  int num_kv_heads, int head_dim, int page_size)
+{
+	return ((((size_t)page * num_kv_heads + h) * 2 + kind) * page_size + slot) * head_dim + d;
+}
+
+/*
+ * [P3] shared page pool item: decode appends the new token at its absolute
+ * RoPE position. For sequence b the new token is cache index t = seq_lens[b]-1
+ * (seq_lens counts the token), stored in slot t % P of page
+ * block_tables[b][t / P]; it is rotated at positions[b].
+ *
+ * q, k, v are bf16 bits, [B][Hq][D], [B][Hkv][D], [B][Hkv][D]. The rotated
+ * query goes to q_rot (fp64, [B][Hq][D]). Returns 0, or -1 for a bad length,
+ * -2 for a bad page id, -3 for a bad shape (nothing after the failing sequence
+ * is written).
+ */
+int oracle_append_rope(uint16_t *pool, long num_pages, int num_kv_heads, int head_dim,
+		       int page_size, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+		       double *q_rot, const int32_t *block_tables, int max_blocks,
+		       const int32_t *seq_lens, const int32_t *positions, int batch,
+		       int num_q_heads, double theta)
+{
+	double in[ORACLE_MAX_DIM], out[ORACLE_MAX_DIM];
+	if (head_dim <= 0 || head_dim > ORACLE_MAX_DIM || head_dim % 2 || page_size <= 0)
+		return -3;
+	for (int b = 0; b < batch; b++) {
+		int n = seq_lens[b];
+		if (n < 1 || n > max_blocks * page_size)
+			return -1;
+		int t = n - 1;
+		long page = block_tables[(size_t)b * max_blocks + t / page_size];
+		if (page < 0 || page >= num_pages)
+			return -2;
+		int slot = t % page_size;
+		long pos = positions[b];
+		for (int h = 0; h < num_kv_heads; h++) {
+			const uint16_t *kh = k + ((size_t)b * num_kv_heads + h) * head_dim;
+			const uint16_t *vh = v + ((size_t)b * num_kv_heads + h) * head_dim;
+			for (int d = 0; d < head_dim; d++)
+				in[d] = oracle_bf16_to_double(kh[d]);
+			oracle_rope_rotate(in, out, head_dim, pos, theta);
+			for (int d = 0; d < head_dim; d++) {
+				pool[pool_offset(page, h, 0, slot, d, num_kv_heads, head_dim, page_size)] =
+					oracle_bf16_from_double(out[d]);
+				pool[pool_offset(page, h, 1, slot, d, num_kv_heads, head_dim, page_size)] = vh[d];
+			}
+		}
+		for (int i = 0; i < num_q_heads; i++) {
+			const uint16_t *qh = q + ((size_t)b * num_q_heads + i) * head_dim;
+			for (int d = 0; d < head_dim; d++)
+				in[d] = oracle_bf16_to_double(qh[d]);
+			oracle_rope_rotate(in, q_rot + ((size_t)b * num_q_heads + i) * head_dim,
+					   head_dim, pos, theta);
+		}
+	}
+	return 0;
+}
+
+/* Copy tokens [t0, t1) of (sequence b, kv head h) out of the pool, in logical
+ * order, as doubles: K into kd, V into vd ([t1-t0][D] each). */
+static int gather(const uint16_t *pool, long num_pages, int num_kv_heads, int head_dim,
+		  int page_size, const int32_t *bt_row, int h, int t0, int t1,
+		  double *kd, double *vd)
+{
+	for (int t = t0; t < t1; t++) {
+		long page = bt_row[t / page_size];
+		if (page < 0 || page >= num_pages)
+			return -2;
+		int slot = t % page_size;
+		for (int d = 0; d < head_dim; d++) {
+			kd[(size_t)(t - t0) * head_dim + d] = oracle_bf16_to_double(
+				pool[pool_offset(page, h, 0, slot, d, num_kv_heads, head_dim, page_size)]);
+			vd[(size_t)(t - t0) * head_dim + d] = oracle_bf16_to_double(
+				pool[pool_offset(page, h, 1, slot, d, num_kv_heads, head_dim, page_size)]);
+		}
+	}
+	return 0;
+}
+
+/* Attention of one query vector over n gathered tokens with an explicit
+ * two-pass softmax ([P4] softmax operator): scores, max, exponentials, sum,
+ * weighted sum of V. Also returns the log-sum-exp of the scores. */
+static double attend(const double *qv, const double *kd, const double *vd, int n,
+		     int head_dim, double scale, double *s, double *o)
+{
+	double m = -INFINITY;
+	for (int t = 0; t < n; t++) {
+		double acc = 0.0;
+		for (int d = 0; d < head_dim; d++)
+			acc += qv[d] * kd[(size_t)t * head_dim + d];
+		s[t] = scale * acc;
+		if (s[t] > m)
+			m = s[t];
+	}
+	double z = 0.0;
+	for (int t = 0; t < n; t++) {
+		s[t] = exp(s[t] - m);
+		z += s[t];
+	}
+	for (int d = 0; d < head_dim; d++)
+		o[d] = 0.0;
+	for (int t = 0; t < n; t++) {
+		double p = s[t] / z;
+		for (int d = 0; d < head_dim; d++)
+			o[d] += p * vd[(size_t)t * head_dim + d];
+	}
+	return m + log(z);
+}
+
+/*
+ * [P3] direct paged decode attention item, written as its definition: for
+ * every sequence b, every query head i (KV head i / g), attend over the
+ * seq_lens[b] tokens the block table maps. q_rot fp64 [B][Hq][D] -> out fp64
+ * [B][Hq][D]. Returns 0, -1 bad length, -2 bad page id, -3 bad shape, -4 no
+ * memory.
+ */
+int oracle_gqa_decode(const uint16_t *pool, long num_pages, int num_kv_heads, int head_dim,
+		      int page_size, const double *q_rot, const int32_t *block_tables,
+		      int max_blocks, const int32_t *seq_lens, int batch, int num_q_heads,
+		      double scale, double *out)
+{
+	if (num_kv_heads <= 0 || num_q_heads % num_kv_heads || head_dim <= 0)
+		return -3;
+	int g = num_q_heads / num_kv_heads;
+	int nmax = max_blocks * page_size;
+	double *kd = malloc(sizeof(double) * (size_t)nmax * head_dim);
+	double *vd = malloc(sizeof(double) * (size_t)nmax * head_dim);
+	double *s = malloc(sizeof(double) * (size_t)nmax);
+	int rc = 0;
+	if (!kd || !vd || !s) {
+		rc = -4;
+		goto done;
+	}
+	for (int b = 0; b < batch && !rc; b++) {
+		int n = seq_lens[b];
+		if (n < 1 || n > nmax) {
+			rc = -1;
+			break;
+		}
+		const int32_t *bt_row = block_tables + (size_t)b * max_blocks;
+		for (int h = 0; h < num_kv_heads && !rc; h++) {
+			rc = gather(pool, num_pages, num_kv_heads, head_dim, page_size, bt_row, h, 0, n,
+				    kd, vd);
+			for (int i = h * g; i < (h + 1) * g && !rc; i++) {
+				size_t row = (size_t)b * num_q_heads + i;
+				attend(q_rot + row * head_dim, kd, vd, n, head_dim, scale, s,
+				       out + row * head_dim);
+			}
+		}
+	}
+done:
+	free(kd);
+	free(vd);
+	free(s);
+	return rc;
+}
+
+/*
+ * Split-KV form (flash-decoding; not on the pages, defined by its closed
+ * form): the tokens of each (b, i) row are cut into consecutive splits of
+ * tokens_per_split; split j yields its own softmax-normalised output o_j and
+ * the log-sum-exp of its scores lse_j. Row r = b*Hq + i has num_splits[r]
+ * splits stored at o_part[(r*max_splits + j)*D], lse_part[r*max_splits + j].
+ */
+int oracle_gqa_decode_split(const uint16_t *pool, long num_pages, int num_kv_heads,
+			    int head_dim, int page_size, const double *q_rot,
+			    const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
+			    int batch, int num_q_heads, double scale, int tokens_per_split,
+			    int max_splits, double *o_part, double *lse_part, int32_t *num_splits)
+{
+	if (num_kv_heads <= 0 || num_q_heads % num_kv_heads || tokens_per_split <= 0)
+		return -3;
+	int g = num_q_heads / num_kv_heads;
+	int nmax = max_blocks * page_size;
+	double *kd = malloc(sizeof(double) * (size_t)nmax * head_dim);
+	double *vd = malloc(sizeof(double) * (size_t)nmax * head_dim);
+	double *s = malloc(sizeof(double) * (size_t)nmax);
+	int rc = 0;
+	if (!kd || !vd || !s) {
+		rc = -4;
+		goto done;
+	}
+	for (int b = 0; b < batch && !rc; b++) {
+		int n = seq_lens[b];
+		if (n < 1 || n > nmax) {
+			rc = -1;
+			break;
+		}
+		int nsplit = (n + tokens_per_split - 1) / tokens_per_split;
+		if (nsplit > max_splits) {
+			rc = -3;
+			break;
+		}
+		const int32_t *bt_row = block_tables + (size_t)b * max_blocks;
+		for (int h = 0; h < num_kv_heads && !rc; h++) {
+			rc = gather(pool, num_pages, num_kv_heads, head_dim, page_size, bt_row, h, 0, n,
+				    kd, vd);
+			for (int i = h * g; i < (h + 1) * g && !rc; i++) {
+				size_t row = (size_t)b * num_q_heads + i;
+				num_splits[row] = nsplit;
+				for (int j = 0; j < nsplit; j++) {
+					int t0 = j * tokens_per_split;
+					int t1 = t0 + tokens_per_split < n ? t0 + tokens_per_split : n;
+					size_t slot = row * max_splits + j;
+					lse_part[slot] = attend(q_rot + row * head_dim,
+								kd + (size_t)t0 * head_dim,
+								vd + (size_t)t0 * head_dim, t1 - t0,
+								head_dim, scale, s,
+								o_part + slot * head_dim);
+				}
+			}
+		}
+	}
+done:
+	free(kd);
+	free(vd);
+	free(s);
+	return rc;
+}
+
+/* Log-sum-exp merge of split results (closed form): with M = max_j lse_j and
+ * w_j = exp(lse_j - M), out = sum_j w_j o_j / sum_j w_j. */
+void oracle_lse_combine(const double *o_part, const double *lse_part, const int32_t *num_splits,
+			int rows, int max_splits, int head_dim, double *out)
+{
+	for (int r = 0; r < rows; r++) {
+		int ns = num_splits[r];
+		double m = -INFINITY;
+		for (int j = 0; j < ns; j++)
+			if (lse_part[(size_t)r * max_splits + j] > m)
+				m = lse_part[(size_t)r * max_splits + j];
+		double wsum = 0.0;
+		for (int d = 0; d < head_dim; d++)
+			out[(size_t)r * head_dim + d] = 0.0;
+		for (int j = 0; j < ns; j++) {
+			size_t slot = (size_t)r * max_splits + j;
+			double w = exp(lse_part[slot] - m);
+			wsum += w;
+			for (int d = 0; d < head_dim; d++)
+				out[(size_t)r * head_dim + d] += w * o_part[slot * head_dim + d];
+		}
+		for (int d = 0; d < head_dim; d++)
+			out[(size_t)r * head_dim + d] /= wsum;
+	}
+}
