@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched paged-KV decode step on GB300.
+
+A step is one pass of the whole hot path over one batch: for every layer,
+RoPE + append of the new token (paged_kv_append_rope) and paged GQA decode
+with split-KV and its fused log-sum-exp merge (paged_gqa_decode).
+
+Prints ONE JSON line (rank 0). The metric is decode-attention KV read GB/s
+(algorithmic bytes: K and V of every valid token, per layer, per step) over the
+device-timed step; the line also carries us per step, the decode kernel's
+roofline, an end-to-end figure with host buffers, the fp64 oracle's CPU
+baseline, and the SM clocks seen during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+With N > 1 (torchrun) every rank runs an independent replica of the workload
+(different seed) on its own GPU: the path has no exchange step, so there is no
+data-path collective; the barrier and the max over ranks use torch.distributed.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = "llama1b_b64_l16_u2048"
+METRIC = "decode-attention KV read GB/s (% of GB300 HBM peak); us per batched decode step"
+L2_BYTES = 129 * 10**6
+
+# DRAM traffic (read + write bytes) per decode launch from one ncu capture, with
+# the hash of the decode source it was taken on; reported only while the source
+# is unchanged.
+TRAFFIC = {
+    # workload -> (sha256 of gqa_decode.cu prefix, bytes per launch)
+}
+
+
+def _decode_source_hash() -> str:
+    p = os.path.join(ROOT, "paged_kv_decode_rope_gb300", "csrc", "gqa_decode.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _peaks() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            ident = str(device)
+        self.ident = ident
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except Exception:
+            return None
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier_max(value: float, ws: int) -> float:
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier_sum(value: float, ws: int) -> float:
+    if ws == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def _barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _config(wl: workloads.Workload) -> dict:
+    step_bytes = wl.kv_bytes_per_step()
+    return {"workload": wl.name, "batch": wl.batch, "layers": wl.num_layers, "q_heads": wl.num_q_heads,
+            "kv_heads": wl.num_kv_heads, "head_dim": 64, "page_size": 16,
+            "seq_len_min": int(wl.seq_lens.min()), "seq_len_max": int(wl.seq_lens.max()),
+            "seq_len_mean": round(float(wl.seq_lens.mean()), 1), "pool_pages": wl.num_pages,
+            "kv_bytes_per_step": step_bytes,
+            "l2": ("inputs larger than L2: %.2f GB of KV per step vs 129 MB L2, every layer reads distinct pages"
+                   % (step_bytes / 1e9)) if step_bytes > 4 * L2_BYTES else
+                  "L2 flushed before every timed step (write of 2x L2)",
+            "description": wl.description}
+
+
+def oracle_sample_step(wl: workloads.Workload, pool_src: torch.Tensor, layer: int, seqs: np.ndarray):
+    """One sampled step of the fp64 oracle: append + decode of `seqs` in `layer`.
+
+    Returns (KV bytes read, seconds). Only the pages these sequences use are
+    copied to the host (outside the timed part)."""
+    import oracle
+    bt = wl.block_tables[layer][seqs]
+    used = np.unique(bt[bt >= 0])
+    remap = np.full(wl.num_pages, -1, dtype=np.int64)
+    remap[used] = np.arange(len(used))
+    pages = pool_src.view(wl.num_pages, -1)[torch.from_numpy(used).to(pool_src.device)]
+    mini = pages.contiguous().view(torch.int16).cpu().numpy().view(np.uint16).reshape(-1).copy()
+    bt2 = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    u = lambda t: t[layer][torch.from_numpy(seqs).to(t.device)].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+    q, k, v = u(wl.q), u(wl.k), u(wl.v)
+    sl, pos = wl.seq_lens[seqs], wl.positions[seqs]
+    t0 = time.perf_counter()
+    q_rot = oracle.append_rope(mini, num_kv_heads=wl.num_kv_heads, q=q, k=k, v=v, block_tables=bt2,
+                               max_blocks=wl.max_blocks, seq_lens=sl, positions=pos, batch=len(seqs),
+                               num_q_heads=wl.num_q_heads, theta=wl.rope_theta)
+    oracle.gqa_decode(mini, num_kv_heads=wl.num_kv_heads, q_rot=q_rot, block_tables=bt2,
+                      max_blocks=wl.max_blocks, seq_lens=sl, batch=len(seqs),
+                      num_q_heads=wl.num_q_heads, scale=wl.scale)
+    dt = time.perf_counter() - t0
+    nbytes = int(sl.astype(np.int64).sum()) * wl.num_kv_heads * 64 * 2 * 2
+    return nbytes, dt
+
+
+def cpu_baseline(wl, pool_src, budget_s: float = 12.0) -> dict:
+    """The oracle as it stands, single-threaded, on a bounded sample of the workload."""
+    rng = np.random.default_rng(123)
+    nseq = max(1, min(wl.batch, 16))
+    total_b, total_t, layers = 0, 0.0, 0
+    for layer in range(wl.num_layers):
+        seqs = np.sort(rng.choice(wl.batch, size=nseq, replace=False))
+        b, t = oracle_sample_step(wl, pool_src, layer, seqs)
+        total_b += b
+        total_t += t
+        layers += 1
+        if total_t >= budget_s:
+            break
+    return {"value": round(total_b / total_t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"fp64 C oracle, 1 thread: append+decode of {nseq} of {wl.batch} sequences in each of "
+                      f"{layers} of {wl.num_layers} layers ({total_b / 1e6:.1f} MB of KV, {total_t:.1f} s)"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wl = workloads.make(args.workload, seed=args.seed, device=dev)
+    rng = np.random.default_rng(7)
+    nseq = max(1, min(wl.batch, 4))
+    samples = [(i % wl.num_layers, np.sort(rng.choice(wl.batch, size=nseq, replace=False)))
+               for i in range(args.warmup + args.steps)]
+    for layer, seqs in samples[:args.warmup]:
+        oracle_sample_step(wl, wl.pool, layer, seqs)
+    tb, tt = 0, 0.0
+    for layer, seqs in samples[args.warmup:]:
+        b, t = oracle_sample_step(wl, wl.pool, layer, seqs)
+        tb += b
+        tt += t
+    value = tb / tt / 1e9
+    step_ms = tt / args.steps * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)", "config": _config(wl),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step: fp64 C oracle append+decode of {nseq} of {wl.batch} "
+                                       f"sequences of one layer (layers in turn)"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, ws, rank, local):
+    import paged_kv_decode_rope_gb300 as pkv
+    from paged_kv_decode_rope_gb300.build import build
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device")
+    build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workloads.make(args.workload, seed=args.seed + 1000 * rank, device=dev)
+    pool = wl.pool  # appended into in place; the append is idempotent across steps
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    sl = torch.from_numpy(wl.seq_lens).to(dev)
+    pos = torch.from_numpy(wl.positions).to(dev)
+    step = pkv.DecodeStep(pool, num_kv_heads=wl.num_kv_heads, num_q_heads=wl.num_q_heads,
+                          num_layers=wl.num_layers, block_tables=bt, seq_lens=sl, positions=pos,
+                          rope_theta=wl.rope_theta, scale=wl.scale, pages_per_split=args.pages_per_split)
+    stream = torch.cuda.current_stream()
+    step_bytes = wl.kv_bytes_per_step()
+    layer_bytes = wl.kv_bytes_per_layer()
+    flush = None
+    if step_bytes <= 4 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    # Eager warm-up (first calls cache kernel attributes), then capture one step
+    # (all layers: append + decode) and the decode launches alone as CUDA graphs.
+    for _ in range(3):
+        step.run(wl.q, wl.k, wl.v)
+    torch.cuda.synchronize()
+    assert step.error_bits() == 0, "device error flags set during warm-up"
+    nl = wl.num_layers
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step.run(wl.q, wl.k, wl.v)
+    g_dec = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_dec):
+        for layer in range(nl):
+            step.decode(layer)
+    for _ in range(args.warmup):
+        g_step.replay()
+    torch.cuda.synchronize()
+
+    def timed(graph, steps):
+        """Device ms per replay; with a flush buffer, L2 is flushed before each replay."""
+        if flush is None:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / steps
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for s in range(steps):
+            flush.fill_(float(s))
+            evs[s][0].record(stream)
+            graph.replay()
+            evs[s][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / steps
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    ms_per_step = timed(g_step, args.steps)
+    wall = time.perf_counter() - t_wall
+    dec_graph_ms = timed(g_dec, args.steps)
+    clk = clocks.stop()
+    _barrier(ws)
+    ms_step_max = _barrier_max(ms_per_step, ws)
+    total_bytes = _barrier_sum(float(step_bytes), ws)
+    value = total_bytes / (ms_step_max / 1e3) / 1e9
+    assert step.error_bits() == 0, "device error flags set during the timed steps"
+
+    # end to end: host buffers in pinned memory; per step copy q/k/v, tables,
+    # lengths and positions in, run the step through the C ABI, copy outputs out.
+    hq = wl.q.cpu().pin_memory()
+    hk = wl.k.cpu().pin_memory()
+    hv = wl.v.cpu().pin_memory()
+    hbt = torch.from_numpy(wl.block_tables).pin_memory()
+    hsl = torch.from_numpy(wl.seq_lens).pin_memory()
+    hpos = torch.from_numpy(wl.positions).pin_memory()
+    hout = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(wl.q), torch.empty_like(wl.k), torch.empty_like(wl.v)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hbt, hsl, hpos))
+    d2h = hout.numel() * 4
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        bt.copy_(hbt, non_blocking=True)
+        sl.copy_(hsl, non_blocking=True)
+        pos.copy_(hpos, non_blocking=True)
+        out = step.run(dq, dk, dv)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        if flush is not None:
+            flush.fill_(1.0)
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _barrier_max(e0.elapsed_time(e1) / e2e_steps, ws)
+    e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
+
+    peak, peak_kind = _peaks()
+    dec_avg_s = dec_graph_ms / nl / 1e3
+    achieved = layer_bytes / dec_avg_s / 1e9
+    h = _decode_source_hash()
+    traffic = None
+    if wl.name in TRAFFIC and TRAFFIC[wl.name][0] == h:
+        traffic = TRAFFIC[wl.name][1]
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4), "us_per_step": round(ms_step_max * 1e3, 2),
+        "pct_of_hbm_peak": round(100 * value / ws / peak, 2), "pct_of_8tbs": round(100 * value / ws / 8000, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "storage": "bf16 KV pages; fp64 key rotation; fp32 softmax and accumulation",
+        "data": "synthetic (seeded; bf16 N(0,1) q/k/v and cache)", "config": _config(wl),
+        "roofline": {"bound": "hbm", "kernel": "gqa_decode_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+                     "bytes_per_launch": layer_bytes, "launch_us_mean": round(dec_avg_s * 1e6, 2),
+                     "timing": f"CUDA events around {args.steps} replays of a graph of the {nl} decode "
+                               "launches of one step (inter-kernel gaps included)",
+                     "decode_source": h},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": step.launches_per_step * args.steps,
+        "timing": "CUDA events around K replays of a CUDA graph of one whole step",
+        "clocks": clk, "wall_s_timed": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, pool)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    step.close()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--pages-per-split", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            return run_reference(args, ws, rank)
+        return run_ours(args, ws, rank, local)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,201 @@
+/*
+ * pkv.h -- paged KV-cache decode step with RoPE for one GPU (sm_103a), C ABI.
+ *
+ * The operation, in the words of the source pages (restated):
+ *   For every sequence in a decode batch, rotate the new token's query and key
+ *   with RoPE at the token's absolute position, store its key and value in a
+ *   shared pool of BF16 pages (16 tokens per page, one block table per
+ *   sequence and layer), then let every query head attend over its own
+ *   sequence's cached pages with a softmax accumulated online in FP32, never
+ *   gathering a contiguous prefix and never storing the scores.
+ *   ("Hours of YouTube and 85 handtyped pages of notes on LLM Inference –
+ *   Start here": the shared BF16 KV page pool item, the batched decode item
+ *   and the direct paged decode attention item. The RoPE equations are those
+ *   of "手写LLM推理引擎：Tokenizer、Transformer与Detokenizer三段式实现"
+ *   section 3.2, read with rotate-half pairing.)
+ *
+ * Conventions shared by every entry point:
+ *  - The return value is 0 on success or a negative errno value, as in the C
+ *    engine of "llmc — 从零写一个大模型推理引擎（配套代码）" (introduction):
+ *      -EINVAL  bad argument (null pointer, bad shape, misaligned storage,
+ *               workspace too small, ...); nothing is launched.
+ *      -ENOSPC  the storage given to kv_pool_create holds no page.
+ *      -EIO     a CUDA runtime call failed; pkv_last_cuda_error() returns the
+ *               cudaError_t value of the calling thread's last failure.
+ *  - Tensor arguments are device pointers that the caller owns and keeps
+ *    alive until the work queued on `stream` has finished. The library frees
+ *    none of them and allocates no device memory except the pool's 4-byte
+ *    error word (kv_pool_create).
+ *  - `stream` is a cudaStream_t passed as void* (NULL: the legacy default
+ *    stream). Every call only enqueues work on it; nothing synchronises except
+ *    pkv_get_error.
+ *  - Checks that need device data (lengths, page ids) are made by the
+ *    kernels. A failed check skips the affected sequence or page and sets a
+ *    bit (PKV_ERR_*) in the pool's error word; no kernel traps.
+ *  - Fixed geometry: head_dim 64, page_size 16 tokens, bf16 cache.
+ *
+ * Pool layout (the contract between the append and the decode, and what the
+ * test oracle indexes independently): physical page p is a contiguous block of
+ * num_kv_heads * 2 * 16 * 64 bf16 values; the element for (page p, kv head h,
+ * kind K=0 / V=1, slot s, dim d) is at bf16 offset
+ *     (((p * num_kv_heads + h) * 2 + kind) * 16 + s) * 64 + d.
+ * One kv head's keys and values for one page are one contiguous 4 KiB block.
+ *
+ * Sequence conventions: seq_lens[b] is the attention length AFTER the append
+ * (cached tokens + the new one); the new token goes to cache index
+ * seq_lens[b] - 1, i.e. slot (seq_lens[b]-1) % 16 of page
+ * block_tables[b * max_blocks + (seq_lens[b]-1) / 16]; positions[b] is the
+ * RoPE position it is rotated at. block_tables is the table of ONE layer,
+ * row-major [batch][max_blocks]; entries past ceil(seq_lens[b]/16) are never
+ * read. Query head i reads kv head i / (num_q_heads / num_kv_heads).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_HEAD_DIM 64
+#define PKV_PAGE_SIZE 16
+/* Largest query-head group (num_q_heads / num_kv_heads) the decode serves. */
+#define PKV_MAX_GROUP 8
+
+/* Bits of the pool's device error word. */
+#define PKV_ERR_SEQ_LEN 0x1  /* seq_lens[b] < 1 or > max_blocks*16: sequence skipped, its output rows zeroed */
+#define PKV_ERR_PAGE_ID 0x2  /* block-table entry outside [0, num_pages): that page skipped */
+#define PKV_ERR_TIMEOUT 0x4  /* a bounded wait for a shared-memory copy gave up; results incomplete */
+#define PKV_ERR_SPLITS  0x8  /* a row needed more than max_splits partial results: row skipped */
+
+typedef struct pkv_pool pkv_pool_t;
+
+/*
+ * Wrap caller-owned device storage as a page pool. ("Hours of YouTube …",
+ * shared BF16 KV page pool item: one pool of physical pages, shared by all
+ * sequences and layers, each page 16 tokens of K and V.)
+ *   storage        device pointer, 16-byte aligned (-EINVAL otherwise)
+ *   storage_bytes  size of storage; num_pages = storage_bytes / page bytes
+ *                  (-ENOSPC if that is 0)
+ *   num_kv_heads   1 .. 256
+ *   head_dim       must be 64;  page_size  must be 16
+ * On success *pool receives a handle; the storage is neither cleared nor
+ * owned. Allocates the 4-byte device error word (zeroed) on the current
+ * device, which must stay current for every call that uses the pool.
+ */
+int kv_pool_create(pkv_pool_t **pool, void *storage, size_t storage_bytes, int num_kv_heads,
+                   int head_dim, int page_size);
+
+/* Free the handle and its error word (not the storage). NULL is accepted. */
+int kv_pool_destroy(pkv_pool_t *pool);
+
+/* Number of physical pages, or -EINVAL for a NULL pool. */
+int kv_pool_num_pages(const pkv_pool_t *pool);
+
+/* Bytes of one physical page (0 for an unsupported geometry). Host only. */
+size_t kv_pool_page_bytes(int num_kv_heads, int head_dim, int page_size);
+
+/*
+ * RoPE + append for one layer. ("Hours of YouTube …", shared BF16 KV page pool
+ * item: decode appends the new token at its absolute RoPE position;
+ * "手写LLM推理引擎…" section 3.2: the rotation, inverse frequency
+ * rope_theta^(-2j/64), pairs (j, j+32).)
+ *   q             bf16 [batch][num_q_heads][64]
+ *   k, v          bf16 [batch][num_kv_heads][64]
+ *   q_rot         fp32 [batch][num_q_heads][64] out: the rotated query
+ *   block_tables  int32 [batch][max_blocks], this layer
+ *   seq_lens      int32 [batch], length after the append (>= 1)
+ *   positions     int32 [batch], RoPE position of the new token
+ *   rope_theta    RoPE base (> 0, finite)
+ * The rotated key is computed in fp64 and rounded once to bf16 (nearest,
+ * ties to even); v is copied bit for bit. q_rot is fp32, not rounded to bf16.
+ * A sequence with a bad length or page id gets its q_rot written but nothing
+ * stored in the pool (error bit set). batch == 0 is a no-op.
+ * num_q_heads must be a multiple of the pool's num_kv_heads.
+ */
+int paged_kv_append_rope(pkv_pool_t *pool, const void *q, const void *k, const void *v,
+                         float *q_rot, const int32_t *block_tables, int max_blocks,
+                         const int32_t *seq_lens, const int32_t *positions, int batch,
+                         int num_q_heads, double rope_theta, void *stream);
+
+/*
+ * Device bytes of workspace paged_gqa_decode needs for these sizes on the
+ * current device (0 for invalid sizes). pages_per_split: as for
+ * paged_gqa_decode (0 = automatic).
+ */
+size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                        int max_blocks, int pages_per_split);
+
+/*
+ * Paged GQA decode attention for one layer, split-KV with a fused
+ * log-sum-exp merge. ("Hours of YouTube …", direct paged decode attention
+ * item: each query head streams its sequence's cached pages and accumulates
+ * softmax-weighted values online in FP32, with no gathered prefix and no
+ * stored scores. The split-KV form and its merge are flash-decoding, not on
+ * the pages.)
+ *   q_rot        fp32 [batch][num_q_heads][64], as written by paged_kv_append_rope
+ *   out          fp32 [batch][num_q_heads][64]
+ *   block_tables int32 [batch][max_blocks];  seq_lens int32 [batch] (>= 1)
+ *   scale        softmax scale applied to q.k (typically 1/8)
+ *   pages_per_split  0: balance all (sequence, kv head, page) work items
+ *                evenly over the persistent grid; > 0: cut the work into
+ *                ranges of this many pages (used to force splits in tests).
+ *   workspace    device memory of at least paged_gqa_decode_workspace_bytes(),
+ *                256-byte aligned. Its first batch*num_kv_heads int32 are
+ *                arrival counters that MUST be zero before the first call
+ *                (e.g. allocate it zeroed); every call leaves them zero again,
+ *                unless a PKV_ERR_TIMEOUT occurred, after which the caller
+ *                must zero it again. Calls that share a workspace must not
+ *                overlap on the GPU.
+ * Constraints: num_q_heads = g * num_kv_heads with 1 <= g <= PKV_MAX_GROUP.
+ * Rows of a sequence with a bad length are written as zeros.
+ */
+int paged_gqa_decode(const pkv_pool_t *pool, const float *q_rot, float *out,
+                     const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
+                     int batch, int num_q_heads, float scale, int pages_per_split,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The same decode, but every (sequence, query head) row leaves its split
+ * results for paged_kv_split_combine instead of merging them:
+ *   o_part     fp32 [batch*num_q_heads][max_splits][64]: split j's normalised output
+ *   lse_part   fp32 [batch*num_q_heads][max_splits]: split j's log-sum-exp of the
+ *              scaled scores (natural log)
+ *   num_splits int32 [batch*num_q_heads]: number of splits of the row
+ * pages_per_split must be > 0; max_splits must be at least
+ * max_blocks / pages_per_split + 2 (integer division), else -EINVAL.
+ */
+int paged_gqa_decode_partials(const pkv_pool_t *pool, const float *q_rot,
+                              const int32_t *block_tables, int max_blocks,
+                              const int32_t *seq_lens, int batch, int num_q_heads, float scale,
+                              int pages_per_split, float *o_part, float *lse_part,
+                              int32_t *num_splits, int max_splits, void *stream);
+
+/*
+ * Log-sum-exp merge of split results (flash-decoding; not on the pages):
+ * for each row r, with M = max_j lse[r][j] over j < num_splits[r] and
+ * w_j = exp(lse[r][j] - M): out[r] = sum_j w_j o[r][j] / sum_j w_j.
+ *   o_part [rows][max_splits][head_dim], lse_part [rows][max_splits],
+ *   num_splits [rows] (rows with a count outside [1, max_splits], or whose
+ *   every lse is -inf, are written as zeros), out [rows][head_dim] fp32.
+ *   head_dim 1 .. 1024.
+ */
+int paged_kv_split_combine(const float *o_part, const float *lse_part, const int32_t *num_splits,
+                           float *out, int rows, int max_splits, int head_dim, void *stream);
+
+/*
+ * Read the pool's device error word (PKV_ERR_* bits) into *bits; with reset
+ * != 0 also clear it. Synchronises the device.
+ */
+int pkv_get_error(pkv_pool_t *pool, int *bits, int reset);
+
+/* cudaError_t value of the calling thread's last CUDA failure (0 if none). */
+int pkv_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

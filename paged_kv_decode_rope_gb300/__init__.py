@@ -1,0 +1,36 @@
+"""Paged KV-cache decode step with RoPE for GB300 (sm_103a).
+
+The CUDA library behind include/pkv.h does the work: RoPE of the new token and
+its append into a shared BF16 page pool (``paged_kv_append_rope``), paged
+grouped-query decode attention with split-KV and a log-sum-exp merge
+(``paged_gqa_decode``), and the standalone merge
+(``paged_kv_split_combine``). This package is the thin Python binding with the
+same names; it only marshals torch tensors into pointers.
+"""
+from ._binding import (  # noqa: F401
+    ERR_PAGE_ID,
+    ERR_SEQ_LEN,
+    ERR_SPLITS,
+    ERR_TIMEOUT,
+    HEAD_DIM,
+    LIBRARY,
+    MAX_GROUP,
+    PAGE_SIZE,
+    KVPool,
+    PkvError,
+    alloc_decode_workspace,
+    decode_max_splits,
+    kv_pool_create,
+    kv_pool_destroy,
+    kv_pool_num_pages,
+    kv_pool_page_bytes,
+    lib,
+    paged_gqa_decode,
+    paged_gqa_decode_partials,
+    paged_gqa_decode_workspace_bytes,
+    paged_kv_append_rope,
+    paged_kv_split_combine,
+    pkv_get_error,
+    pkv_last_cuda_error,
+)
+from .step import DecodeStep  # noqa: F401

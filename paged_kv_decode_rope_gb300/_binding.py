@@ -1,0 +1,227 @@
+"""ctypes binding of the pkv C ABI (include/pkv.h).
+
+Argument marshalling only: shapes and pointers are read off torch tensors and
+passed to the CUDA library, which does all of the work on the device. There is
+no fallback: if libpkv.so is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libpkv.so")
+
+HEAD_DIM = 64
+PAGE_SIZE = 16
+MAX_GROUP = 8
+ERR_SEQ_LEN, ERR_PAGE_ID, ERR_TIMEOUT, ERR_SPLITS = 0x1, 0x2, 0x4, 0x8
+
+_lib = None
+_lock = threading.Lock()
+
+_vp, _i, _sz, _f, _d = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float, ctypes.c_double
+
+_SIGNATURES = {
+    "kv_pool_create": (_i, [ctypes.POINTER(_vp), _vp, _sz, _i, _i, _i]),
+    "kv_pool_destroy": (_i, [_vp]),
+    "kv_pool_num_pages": (_i, [_vp]),
+    "kv_pool_page_bytes": (_sz, [_i, _i, _i]),
+    "paged_kv_append_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _d, _vp]),
+    "paged_gqa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "paged_gqa_decode": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp, _sz, _vp]),
+    "paged_gqa_decode_partials": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp, _vp, _vp, _i, _vp]),
+    "paged_kv_split_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
+    "pkv_get_error": (_i, [_vp, ctypes.POINTER(_i), _i]),
+    "pkv_last_cuda_error": (_i, []),
+}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn: str, rc: int):
+        names = {-22: "EINVAL", -28: "ENOSPC", -5: "EIO", -12: "ENOMEM"}
+        extra = ""
+        if rc == -5 and _lib is not None:
+            extra = f" (cudaError {_lib.pkv_last_cuda_error()})"
+        super().__init__(f"{fn} failed: {names.get(rc, rc)}{extra}")
+        self.rc = rc
+
+
+def lib():
+    """Load libpkv.so once. Raises if it is not built: there is no other path."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIBRARY):
+                raise RuntimeError(f"{LIBRARY} is not built; run paged_kv_decode_rope_gb300.build.build()")
+            L = ctypes.CDLL(LIBRARY)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(fn: str, rc: int) -> None:
+    if rc != 0:
+        raise PkvError(fn, rc)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, dtype: torch.dtype, name: str, ndim: int | None = None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    return t.data_ptr()
+
+
+class KVPool:
+    """A page pool over caller storage (the handle of kv_pool_create)."""
+
+    def __init__(self, handle: int, storage: torch.Tensor, num_kv_heads: int):
+        self._handle = handle
+        self.storage = storage  # keeps the storage alive as long as the pool
+        self.num_kv_heads = num_kv_heads
+
+    @property
+    def handle(self) -> int:
+        if not self._handle:
+            raise ValueError("pool destroyed")
+        return self._handle
+
+    @property
+    def num_pages(self) -> int:
+        return lib().kv_pool_num_pages(self.handle)
+
+    def close(self) -> None:
+        if self._handle:
+            h, self._handle = self._handle, None
+            _check("kv_pool_destroy", lib().kv_pool_destroy(h))
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def kv_pool_page_bytes(num_kv_heads: int, head_dim: int = HEAD_DIM, page_size: int = PAGE_SIZE) -> int:
+    return lib().kv_pool_page_bytes(num_kv_heads, head_dim, page_size)
+
+
+def kv_pool_create(storage: torch.Tensor, num_kv_heads: int, head_dim: int = HEAD_DIM,
+                   page_size: int = PAGE_SIZE) -> KVPool:
+    if storage.device.type != "cuda" or not storage.is_contiguous():
+        raise ValueError("storage must be a contiguous CUDA tensor")
+    h = _vp()
+    nbytes = storage.numel() * storage.element_size()
+    _check("kv_pool_create", lib().kv_pool_create(ctypes.byref(h), storage.data_ptr(), nbytes,
+                                                  num_kv_heads, head_dim, page_size))
+    return KVPool(h.value, storage, num_kv_heads)
+
+
+def kv_pool_destroy(pool: KVPool) -> None:
+    pool.close()
+
+
+def kv_pool_num_pages(pool: KVPool) -> int:
+    return pool.num_pages
+
+
+def paged_kv_append_rope(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                         q_rot: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                         positions: torch.Tensor, rope_theta: float, stream=None) -> None:
+    """q [B,Hq,64] bf16, k/v [B,Hkv,64] bf16, q_rot [B,Hq,64] fp32 out,
+    block_tables [B,max_blocks] int32, seq_lens/positions [B] int32."""
+    batch, hq = q.shape[0], q.shape[1]
+    rc = lib().paged_kv_append_rope(
+        pool.handle, _dev(q, torch.bfloat16, "q", 3), _dev(k, torch.bfloat16, "k", 3),
+        _dev(v, torch.bfloat16, "v", 3), _dev(q_rot, torch.float32, "q_rot", 3),
+        _dev(block_tables, torch.int32, "block_tables", 2), block_tables.shape[1],
+        _dev(seq_lens, torch.int32, "seq_lens", 1), _dev(positions, torch.int32, "positions", 1),
+        batch, hq, float(rope_theta), _stream(stream))
+    _check("paged_kv_append_rope", rc)
+
+
+def paged_gqa_decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int,
+                                     max_blocks: int, pages_per_split: int = 0) -> int:
+    return lib().paged_gqa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, max_blocks,
+                                                  pages_per_split)
+
+
+def alloc_decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, max_blocks: int,
+                           pages_per_split: int = 0, device=None) -> torch.Tensor:
+    """A zeroed workspace buffer of the required size (the counters must start at zero)."""
+    n = paged_gqa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, max_blocks, pages_per_split)
+    if n == 0:
+        raise ValueError("invalid decode sizes")
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def paged_gqa_decode(pool: KVPool, q_rot: torch.Tensor, out: torch.Tensor,
+                     block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                     workspace: torch.Tensor, pages_per_split: int = 0, stream=None) -> None:
+    """q_rot/out [B,Hq,64] fp32; workspace from alloc_decode_workspace()."""
+    batch, hq = q_rot.shape[0], q_rot.shape[1]
+    rc = lib().paged_gqa_decode(
+        pool.handle, _dev(q_rot, torch.float32, "q_rot", 3), _dev(out, torch.float32, "out", 3),
+        _dev(block_tables, torch.int32, "block_tables", 2), block_tables.shape[1],
+        _dev(seq_lens, torch.int32, "seq_lens", 1), batch, hq, float(scale), pages_per_split,
+        _dev(workspace, torch.uint8, "workspace", 1), workspace.numel(), _stream(stream))
+    _check("paged_gqa_decode", rc)
+
+
+def decode_max_splits(max_blocks: int, pages_per_split: int) -> int:
+    return max_blocks // pages_per_split + 2
+
+
+def paged_gqa_decode_partials(pool: KVPool, q_rot: torch.Tensor, block_tables: torch.Tensor,
+                              seq_lens: torch.Tensor, scale: float, pages_per_split: int,
+                              o_part: torch.Tensor, lse_part: torch.Tensor,
+                              num_splits: torch.Tensor, stream=None) -> None:
+    """o_part [B*Hq, S, 64] fp32, lse_part [B*Hq, S] fp32, num_splits [B*Hq] int32 (outputs)."""
+    batch, hq = q_rot.shape[0], q_rot.shape[1]
+    rc = lib().paged_gqa_decode_partials(
+        pool.handle, _dev(q_rot, torch.float32, "q_rot", 3),
+        _dev(block_tables, torch.int32, "block_tables", 2), block_tables.shape[1],
+        _dev(seq_lens, torch.int32, "seq_lens", 1), batch, hq, float(scale), pages_per_split,
+        _dev(o_part, torch.float32, "o_part", 3), _dev(lse_part, torch.float32, "lse_part", 2),
+        _dev(num_splits, torch.int32, "num_splits", 1), o_part.shape[1], _stream(stream))
+    _check("paged_gqa_decode_partials", rc)
+
+
+def paged_kv_split_combine(o_part: torch.Tensor, lse_part: torch.Tensor, num_splits: torch.Tensor,
+                           out: torch.Tensor, stream=None) -> None:
+    """o_part [rows, S, D], lse_part [rows, S], num_splits [rows] -> out [rows, D]."""
+    rows, max_splits, head_dim = o_part.shape
+    rc = lib().paged_kv_split_combine(
+        _dev(o_part, torch.float32, "o_part", 3), _dev(lse_part, torch.float32, "lse_part", 2),
+        _dev(num_splits, torch.int32, "num_splits", 1), _dev(out, torch.float32, "out"),
+        rows, max_splits, head_dim, _stream(stream))
+    _check("paged_kv_split_combine", rc)
+
+
+def pkv_get_error(pool: KVPool, reset: bool = False) -> int:
+    bits = _i(0)
+    _check("pkv_get_error", lib().pkv_get_error(pool.handle, ctypes.byref(bits), int(reset)))
+    return bits.value
+
+
+def pkv_last_cuda_error() -> int:
+    return lib().pkv_last_cuda_error()

@@ -1,0 +1,246 @@
+// pkv_abi.cu -- the C ABI declared in include/pkv.h: argument checks, the pool
+// handle, and the launches. Returns 0 or a negative errno, the convention of
+// "llmc — 从零写一个大模型推理引擎（配套代码）" (introduction).
+#include <cerrno>
+#include <cmath>
+#include <cstdlib>
+#include <new>
+
+#include "../../include/pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return -EIO;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool geometry_ok(int num_kv_heads, int head_dim, int page_size) {
+  return num_kv_heads >= 1 && num_kv_heads <= pkv::kMaxKvHeads && head_dim == PKV_HEAD_DIM &&
+         page_size == PKV_PAGE_SIZE;
+}
+
+// Shapes shared by the decode entry points.
+bool decode_shape_ok(const pkv_pool_t* pool, int batch, int num_q_heads, int max_blocks) {
+  if (!pool || batch < 0 || max_blocks < 1 || num_q_heads < 1) return false;
+  if (num_q_heads % pool->num_kv_heads) return false;
+  const int group = num_q_heads / pool->num_kv_heads;
+  if (group > PKV_MAX_GROUP) return false;
+  // work items (sequence, kv head, page) of one launch are counted in int32
+  const long long chunk = batch < pkv::kDecodeBatchChunk ? batch : pkv::kDecodeBatchChunk;
+  if (chunk * pool->num_kv_heads * max_blocks >= (1ll << 31)) return false;
+  if (static_cast<long long>(max_blocks) * PKV_PAGE_SIZE >= (1ll << 31)) return false;
+  return true;
+}
+
+}  // namespace
+
+namespace pkv {
+int device_sm_count(int device) {
+  static int cache[64] = {0};
+  const int d = device & 63;
+  if (cache[d] > 0) return cache[d];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return -1;
+  cache[d] = n;
+  return n;
+}
+}  // namespace pkv
+
+extern "C" {
+
+size_t kv_pool_page_bytes(int num_kv_heads, int head_dim, int page_size) {
+  if (!geometry_ok(num_kv_heads, head_dim, page_size)) return 0;
+  return static_cast<size_t>(num_kv_heads) * 2 * page_size * head_dim * 2;
+}
+
+int kv_pool_create(pkv_pool_t** pool, void* storage, size_t storage_bytes, int num_kv_heads,
+                   int head_dim, int page_size) {
+  if (!pool) return -EINVAL;
+  *pool = nullptr;
+  if (!storage || !aligned16(storage) || !geometry_ok(num_kv_heads, head_dim, page_size))
+    return -EINVAL;
+  const size_t page_bytes = kv_pool_page_bytes(num_kv_heads, head_dim, page_size);
+  const size_t pages = storage_bytes / page_bytes;
+  if (pages == 0) return -ENOSPC;
+  if (pages > 0x7fffffffull) return -EINVAL;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e);
+  int* d_err = nullptr;
+  e = cudaMalloc(&d_err, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e);
+  e = cudaMemset(d_err, 0, sizeof(int));
+  if (e != cudaSuccess) {
+    cudaFree(d_err);
+    return cuda_fail(e);
+  }
+  pkv_pool_t* h = new (std::nothrow) pkv_pool_t;
+  if (!h) {
+    cudaFree(d_err);
+    return -ENOMEM;
+  }
+  h->storage = storage;
+  h->storage_bytes = storage_bytes;
+  h->num_pages = static_cast<long long>(pages);
+  h->num_kv_heads = num_kv_heads;
+  h->d_err = d_err;
+  h->device = device;
+  *pool = h;
+  return 0;
+}
+
+int kv_pool_destroy(pkv_pool_t* pool) {
+  if (!pool) return 0;
+  cudaError_t e = cudaFree(pool->d_err);
+  delete pool;
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
+int kv_pool_num_pages(const pkv_pool_t* pool) {
+  if (!pool) return -EINVAL;
+  return static_cast<int>(pool->num_pages);
+}
+
+int paged_kv_append_rope(pkv_pool_t* pool, const void* q, const void* k, const void* v,
+                         float* q_rot, const int32_t* block_tables, int max_blocks,
+                         const int32_t* seq_lens, const int32_t* positions, int batch,
+                         int num_q_heads, double rope_theta, void* stream) {
+  if (!pool || batch < 0 || max_blocks < 1 || num_q_heads < 1 ||
+      num_q_heads % pool->num_kv_heads || !(rope_theta > 0.0) || !std::isfinite(rope_theta))
+    return -EINVAL;
+  if (static_cast<long long>(max_blocks) * PKV_PAGE_SIZE >= (1ll << 31)) return -EINVAL;
+  if (batch == 0) return 0;
+  if (!q || !k || !v || !q_rot || !block_tables || !seq_lens || !positions) return -EINVAL;
+  if (!aligned16(v)) return -EINVAL;
+  pkv::AppendLaunch a;
+  a.pool = static_cast<uint16_t*>(pool->storage);
+  a.num_pages = pool->num_pages;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.q_rot = q_rot;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.positions = positions;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.rope_theta = rope_theta;
+  a.err = pool->d_err;
+  cudaError_t e = pkv::launch_append_rope(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
+size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads,
+                                        int max_blocks, int pages_per_split) {
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return 0;
+  const int sms = pkv::device_sm_count(device);
+  if (sms < 1) return 0;
+  return pkv::decode_workspace_bytes(batch, num_q_heads, num_kv_heads, max_blocks, pages_per_split,
+                                     sms);
+}
+
+int paged_gqa_decode(const pkv_pool_t* pool, const float* q_rot, float* out,
+                     const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                     int batch, int num_q_heads, float scale, int pages_per_split,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (!decode_shape_ok(pool, batch, num_q_heads, max_blocks) || pages_per_split < 0 ||
+      !std::isfinite(scale))
+    return -EINVAL;
+  if (batch == 0) return 0;
+  if (!q_rot || !out || !block_tables || !seq_lens || !workspace) return -EINVAL;
+  if (!aligned16(q_rot) || !aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return -EINVAL;
+  const size_t need = paged_gqa_decode_workspace_bytes(batch, num_q_heads, pool->num_kv_heads,
+                                                       max_blocks, pages_per_split);
+  if (need == 0 || workspace_bytes < need) return -EINVAL;
+  pkv::DecodeLaunch a = {};
+  a.pool = static_cast<const uint8_t*>(pool->storage);
+  a.num_pages = pool->num_pages;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.q_rot = q_rot;
+  a.out = out;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.scale = scale;
+  a.pages_per_split = pages_per_split;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err = pool->d_err;
+  cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
+int paged_gqa_decode_partials(const pkv_pool_t* pool, const float* q_rot,
+                              const int32_t* block_tables, int max_blocks,
+                              const int32_t* seq_lens, int batch, int num_q_heads, float scale,
+                              int pages_per_split, float* o_part, float* lse_part,
+                              int32_t* num_splits, int max_splits, void* stream) {
+  if (!decode_shape_ok(pool, batch, num_q_heads, max_blocks) || pages_per_split < 1 ||
+      !std::isfinite(scale))
+    return -EINVAL;
+  if (max_splits < max_blocks / pages_per_split + 2) return -EINVAL;
+  if (batch == 0) return 0;
+  if (!q_rot || !block_tables || !seq_lens || !o_part || !lse_part || !num_splits)
+    return -EINVAL;
+  if (!aligned16(q_rot) || !aligned16(o_part)) return -EINVAL;
+  pkv::DecodeLaunch a = {};
+  a.pool = static_cast<const uint8_t*>(pool->storage);
+  a.num_pages = pool->num_pages;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.q_rot = q_rot;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.scale = scale;
+  a.pages_per_split = pages_per_split;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.num_splits = num_splits;
+  a.max_splits = max_splits;
+  a.err = pool->d_err;
+  cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
+int paged_kv_split_combine(const float* o_part, const float* lse_part, const int32_t* num_splits,
+                           float* out, int rows, int max_splits, int head_dim, void* stream) {
+  if (rows < 0 || max_splits < 1 || head_dim < 1 || head_dim > 1024) return -EINVAL;
+  if (rows == 0) return 0;
+  if (!o_part || !lse_part || !num_splits || !out) return -EINVAL;
+  cudaError_t e = pkv::launch_split_combine(o_part, lse_part, num_splits, out, rows, max_splits,
+                                            head_dim, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
+int pkv_get_error(pkv_pool_t* pool, int* bits, int reset) {
+  if (!pool || !bits) return -EINVAL;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  int v = 0;
+  e = cudaMemcpy(&v, pool->d_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *bits = v;
+  if (reset) {
+    e = cudaMemset(pool->d_err, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return 0;
+}
+
+int pkv_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

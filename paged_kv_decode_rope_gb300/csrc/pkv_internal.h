@@ -1,0 +1,80 @@
+// pkv_internal.h -- host-side interfaces between the C ABI and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+struct pkv_pool {
+  void* storage;
+  size_t storage_bytes;
+  long long num_pages;
+  int num_kv_heads;
+  int* d_err;  // device error word (PKV_ERR_* bits)
+  int device;
+};
+
+namespace pkv {
+
+constexpr int kMaxKvHeads = 256;
+
+struct AppendLaunch {
+  uint16_t* pool;
+  long long num_pages;
+  int num_kv_heads;
+  const uint16_t* q;
+  const uint16_t* k;
+  const uint16_t* v;
+  float* q_rot;
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* seq_lens;
+  const int32_t* positions;
+  int batch;
+  int num_q_heads;
+  double rope_theta;
+  int* err;
+};
+
+cudaError_t launch_append_rope(const AppendLaunch& a, cudaStream_t stream);
+
+struct DecodeLaunch {
+  const uint8_t* pool;
+  long long num_pages;
+  int num_kv_heads;
+  const float* q_rot;
+  float* out;  // fused mode
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* seq_lens;
+  int batch;
+  int num_q_heads;
+  float scale;
+  int pages_per_split;  // 0 = balance over the persistent grid
+  // fused merge: workspace (counters first, then partial slots)
+  void* workspace;
+  size_t workspace_bytes;
+  // partials mode (o_part != nullptr)
+  float* o_part;
+  float* lse_part;
+  int32_t* num_splits;
+  int max_splits;
+  int* err;
+};
+
+// Largest batch one decode launch serves (sequence lengths and page prefix sums
+// are staged in shared memory); larger batches are cut into several launches.
+constexpr int kDecodeBatchChunk = 2048;
+
+size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int max_blocks,
+                              int pages_per_split, int sm_count);
+cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream);
+
+cudaError_t launch_split_combine(const float* o_part, const float* lse_part,
+                                 const int32_t* num_splits, float* out, int rows, int max_splits,
+                                 int head_dim, cudaStream_t stream);
+
+int device_sm_count(int device);
+
+}  // namespace pkv

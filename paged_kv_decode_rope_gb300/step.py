@@ -1,0 +1,67 @@
+"""One batched decode step over all layers, through the C ABI.
+
+Per layer l, on one stream: ``paged_kv_append_rope`` (RoPE of the new token's
+q and k at its position, K/V appended into the layer's pages), then
+``paged_gqa_decode`` (every query head over its sequence's pages). This is
+the decode half of the per-layer loop the "Hours of YouTube and 85 handtyped
+pages of notes on LLM Inference – Start here" engine runs for each packed
+decode batch (its batched decode item); the projections around it are not
+part of this library.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as B
+
+
+class DecodeStep:
+    def __init__(self, pool_storage: torch.Tensor, *, num_kv_heads: int, num_q_heads: int,
+                 num_layers: int, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                 positions: torch.Tensor, rope_theta: float, scale: float,
+                 pages_per_split: int = 0):
+        dev = pool_storage.device
+        self.num_layers = num_layers
+        self.batch = int(seq_lens.shape[0])
+        self.num_q_heads = num_q_heads
+        self.num_kv_heads = num_kv_heads
+        self.rope_theta = float(rope_theta)
+        self.scale = float(scale)
+        self.pages_per_split = pages_per_split
+        self.pool = B.kv_pool_create(pool_storage, num_kv_heads)
+        self.block_tables = block_tables
+        self.seq_lens = seq_lens
+        self.positions = positions
+        self.max_blocks = int(block_tables.shape[-1])
+        self.q_rot = torch.empty(num_layers, self.batch, num_q_heads, B.HEAD_DIM,
+                                 dtype=torch.float32, device=dev)
+        self.out = torch.empty_like(self.q_rot)
+        self.workspace = B.alloc_decode_workspace(self.batch, num_q_heads, num_kv_heads,
+                                                  self.max_blocks, pages_per_split, device=dev)
+
+    @property
+    def launches_per_step(self) -> int:
+        chunks = -(-self.batch // 2048) if self.batch else 0
+        return self.num_layers * (1 + chunks) if self.batch else 0
+
+    def append(self, layer: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+        B.paged_kv_append_rope(self.pool, q[layer], k[layer], v[layer], self.q_rot[layer],
+                               self.block_tables[layer], self.seq_lens, self.positions,
+                               self.rope_theta, stream)
+
+    def decode(self, layer: int, stream=None) -> None:
+        B.paged_gqa_decode(self.pool, self.q_rot[layer], self.out[layer], self.block_tables[layer],
+                           self.seq_lens, self.scale, self.workspace, self.pages_per_split, stream)
+
+    def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None) -> torch.Tensor:
+        """q [NL,B,Hq,64], k/v [NL,B,Hkv,64] bf16 on the device -> out [NL,B,Hq,64] fp32."""
+        for layer in range(self.num_layers):
+            self.append(layer, q, k, v, stream)
+            self.decode(layer, stream)
+        return self.out
+
+    def error_bits(self, reset: bool = False) -> int:
+        return B.pkv_get_error(self.pool, reset)
+
+    def close(self) -> None:
+        self.pool.close()

@@ -1,0 +1,103 @@
+"""The C-ABI library loads and exports every symbol include/pkv.h declares.
+
+No compute call runs here (no GPU needed): only host-side entry points and the
+argument checks that reject a call before any CUDA work.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.golden.figures import page_figures
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+EINVAL, ENOSPC = -22, -28
+
+
+def _declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_decode_rope_gb300 import build
+    build.build()
+    return ctypes.CDLL(build.LIBRARY)
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("kv_pool_create", "paged_kv_append_rope", "paged_gqa_decode",
+                     "paged_kv_split_combine"):
+        assert required in names
+    assert len(names) >= 10
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"libpkv.so does not export {name}"
+
+
+def test_binding_has_every_declared_name():
+    import paged_kv_decode_rope_gb300 as pkv
+    for name in _declared_functions():
+        assert hasattr(pkv, name), f"binding lacks {name}"
+
+
+def test_page_bytes_and_page_figures(lib):
+    lib.kv_pool_page_bytes.restype = ctypes.c_size_t
+    figs = page_figures()
+    page = lib.kv_pool_page_bytes(8, 64, figs["tokens_per_page"])
+    assert page == 8 * 2 * 16 * 64 * 2 == 32768
+    # The default 128 MiB pool holds 4096 Llama-3.2-1B pages = 65536 token slots,
+    # i.e. 4096 tokens of context in each of the 16 layers.
+    pages = figs["default_pool_mib"] * 2**20 // page
+    assert pages == 4096
+    assert pages * figs["tokens_per_page"] // figs["llama_layers"] == 4096
+    # 32 query heads of dim 64 make the 2048-wide hidden state.
+    assert 32 * 64 == figs["llama_hidden"]
+    assert lib.kv_pool_page_bytes(2, 64, 16) == 8192
+    assert lib.kv_pool_page_bytes(8, 128, 16) == 0
+    assert lib.kv_pool_page_bytes(8, 64, 32) == 0
+    assert lib.kv_pool_page_bytes(0, 64, 16) == 0
+
+
+def test_argument_checks_before_any_cuda_call(lib):
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.kv_pool_create.argtypes = [ctypes.POINTER(vp), vp, sz, i, i, i]
+    h = vp()
+    assert lib.kv_pool_create(None, 256, 1 << 20, 8, 64, 16) == EINVAL
+    assert lib.kv_pool_create(ctypes.byref(h), None, 1 << 20, 8, 64, 16) == EINVAL
+    assert lib.kv_pool_create(ctypes.byref(h), 0x1008, 1 << 20, 8, 64, 16) == EINVAL  # misaligned
+    assert lib.kv_pool_create(ctypes.byref(h), 0x1000, 1 << 20, 8, 128, 16) == EINVAL
+    assert lib.kv_pool_create(ctypes.byref(h), 0x1000, 1 << 20, 8, 64, 8) == EINVAL
+    assert lib.kv_pool_create(ctypes.byref(h), 0x1000, 100, 8, 64, 16) == ENOSPC
+    lib.paged_kv_append_rope.argtypes = [vp] * 6 + [i, vp, vp, i, i, ctypes.c_double, vp]
+    assert lib.paged_kv_append_rope(None, 1, 1, 1, 1, 1, 4, 1, 1, 2, 32, 1e4, None) == EINVAL
+    lib.paged_gqa_decode.argtypes = [vp, vp, vp, vp, i, vp, i, i, ctypes.c_float, i, vp, sz, vp]
+    assert lib.paged_gqa_decode(None, 1, 1, 1, 4, 1, 2, 32, 0.125, 0, 1, 1 << 20, None) == EINVAL
+    lib.paged_gqa_decode_partials.argtypes = [vp, vp, vp, i, vp, i, i, ctypes.c_float, i, vp, vp,
+                                              vp, i, vp]
+    assert lib.paged_gqa_decode_partials(None, 1, 1, 4, 1, 2, 32, 0.125, 1, 1, 1, 1, 8, None) == EINVAL
+    lib.paged_kv_split_combine.argtypes = [vp, vp, vp, vp, i, i, i, vp]
+    assert lib.paged_kv_split_combine(1, 1, 1, 1, -1, 4, 64, None) == EINVAL
+    assert lib.paged_kv_split_combine(1, 1, 1, 1, 4, 0, 64, None) == EINVAL
+    assert lib.paged_kv_split_combine(None, 1, 1, 1, 4, 2, 64, None) == EINVAL
+    assert lib.paged_kv_split_combine(1, 1, 1, 1, 0, 2, 64, None) == 0  # nothing to do
+    lib.pkv_get_error.argtypes = [vp, ctypes.POINTER(i), i]
+    assert lib.pkv_get_error(None, None, 0) == EINVAL
+    assert lib.kv_pool_destroy(None) == 0
+    assert lib.kv_pool_num_pages(None) == EINVAL
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import paged_kv_decode_rope_gb300._binding as B
+    monkeypatch.setattr(B, "_lib", None)
+    monkeypatch.setattr(B, "LIBRARY", str(tmp_path / "libpkv.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        B.lib()
