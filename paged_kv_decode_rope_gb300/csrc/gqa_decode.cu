@@ -11,25 +11,30 @@
 // and the splits merged by their log-sum-exp (flash-decoding; not on the
 // pages).
 //
-// Design (GB300-first, HBM bound: per token and kv head it reads 256 B and
-// does 256*G flops, G = 4 or 7 on the two model shapes):
+// Design (GB300-first, HBM bound: per token and kv head it reads 256 B; the
+// G query heads of a group make the work a tiny dense contraction):
 //  * Work items are (sequence, kv head, page) triples, enumerated sequence-
-//    major. A persistent grid of one CTA per SM (8 warps) cuts the item list
-//    into equal contiguous ranges, one range per warp, so long and short
-//    sequences balance at page granularity with no host-side planning.
-//  * Each warp streams its range through its own 4-stage shared-memory ring:
-//    lane 0 issues 1-D bulk asynchronous copies (cp.async.bulk, completion
-//    counted in bytes on an mbarrier) of the head's 2 KiB K block and 2 KiB V
-//    block of each page, only the valid rows of a partial last page, plus the
-//    G query rows whenever a new (sequence, head) piece starts. No thread
-//    spends registers or issue slots on global loads.
-//  * In a warp, lane (t, c) = (lane>>3, lane&7) holds dims [8c, 8c+8) of token
-//    row t of a 4-row step; q for those dims and all G heads stays in
-//    registers. Partial dot products are reduced over the 8 lanes of a row
-//    with an exchanging butterfly that leaves each lane one head's score, so
-//    each score is exponentiated once. Softmax state is per page: one max
-//    per head over the page's 16 tokens, one rescale of the accumulators when
-//    the max grows. Products use the packed fp32x2 FMA of sm_100+.
+//    major. A persistent grid of one CTA per SM cuts the item list into equal
+//    contiguous ranges, one range per warp, so long and short sequences
+//    balance at page granularity with no host-side planning.
+//  * Each warp streams its range through its own 3-stage shared-memory ring:
+//    lane 0 issues TMA tensor loads (cp.async.bulk.tensor, 128-byte swizzle,
+//    completion counted in bytes on an mbarrier) of the head's K and V rows of
+//    each page in 8-row boxes (a partial last page loads only the boxes that
+//    hold valid rows), plus a 1-D bulk copy of the G query rows whenever a
+//    new (sequence, head) piece starts. No thread spends registers or issue
+//    slots on global loads.
+//  * Per page the warp runs two m16n8k16 bf16 tensor-core products with fp32
+//    accumulation. Scores S[16 x 16 tokens] = Q K^T take Q as A with rows
+//    0-7 = the G heads' q (pre-scaled by scale*log2 e) rounded to bf16 and rows
+//    8-15 = the rounding remainders, so row h + row h+8 is q.k to ~2^-16
+//    relative. The softmax is online per page: one max per head over its 16
+//    tokens (two shuffles), exp2, one rescale of the accumulator when the max
+//    grows. The score accumulator's register layout is exactly the A operand
+//    of O += P V, so P goes straight from registers into the second product,
+//    again as bf16 hi rows 0-7 and remainder rows 8-15. K fragments come from
+//    ldmatrix, V fragments from ldmatrix.trans, conflict-free thanks to the
+//    swizzle.
 //  * A (sequence, head) piece that spans several warp ranges writes its
 //    unnormalised accumulator, max and sum to a workspace slot; the last warp
 //    to arrive (an atomic counter per (sequence, head)) merges the pieces and
@@ -43,26 +48,24 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
-constexpr int kStages = 4;
-constexpr int kHdrBytes = 512;  // mbarriers (kWarps*kStages*8 = 256 B) + scan scratch
-constexpr int kScanScratch = 256;
-constexpr int kStepBytes = 4 * kRowBytes;  // 4 token rows per warp step = 512 B
+constexpr int kStages = 3;                 // ring depth per warp
+constexpr int kScanOffset = 512;           // scan scratch (16 ints) after the mbarriers
+constexpr int kHdrBytes = 1024;            // mbarriers (<= 16 warps * 3 * 8 B) + scan scratch
+constexpr int kBoxRows = 8;                // rows per TMA box (1 KiB, one 128-byte swizzle atom)
+constexpr int kBoxBytes = kBoxRows * kRowBytes;
+constexpr int kMinRangePages = 4;          // smallest automatic range (fewer, cheaper merges)
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int G>
-struct Geo {
-  static constexpr int GP = G <= 1 ? 1 : G <= 2 ? 2 : G <= 4 ? 4 : 8;  // padded to a power of 2
-  static constexpr int kLogGP = GP == 1 ? 0 : GP == 2 ? 1 : GP == 4 ? 2 : 3;
-  static constexpr int kShift = 3 - kLogGP;  // head of lane = (lane & 7) >> kShift
-  static constexpr int kQBytes = G * kHeadDim * 4;
-  static constexpr int kStageBytes = kHeadPageBytes + ((kQBytes + 127) / 128) * 128;
+struct Cfg {
+  static constexpr int kWarps = G <= 4 ? 12 : 10;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kQBytes = G * kHeadDim * 4;  // the group's fp32 query rows
+  static constexpr int kStageBytes = kHeadPageBytes + ((kQBytes + 1023) / 1024) * 1024;
   static constexpr int kSlotFloats = ((G * kHeadDim + 2 * G) + 3) / 4 * 4;
 };
 
 struct DecodeParams {
-  const uint8_t* pool;
   long long num_pages;
   int hkv;
   const float* q_rot;  // [batch][hq][64] (already offset to this launch's first sequence)
@@ -81,41 +84,19 @@ struct DecodeParams {
   int32_t* num_splits;
   int max_splits;
   int* err;
-  int ring_offset;  // byte offset of the copy rings in dynamic shared memory
+  int ring_offset;  // byte offset of the copy rings in dynamic shared memory (rounded up to 1 KiB)
 };
 
 size_t ring_offset_bytes() {
   return static_cast<size_t>(kHdrBytes) +
-         ((sizeof(int) * (2 * kDecodeBatchChunk + 1) + 127) / 128) * 128;
+         ((sizeof(int) * (2 * kDecodeBatchChunk + 1) + 1023) / 1024) * 1024;
 }
 
 template <int G>
 size_t smem_bytes() {
-  return ring_offset_bytes() + static_cast<size_t>(kWarps) * kStages * Geo<G>::kStageBytes;
-}
-
-// Butterfly over the 8 lanes of a token row that halves the number of values
-// each lane carries at every level it can: on return v[0] is, for head
-// (lane & 7) >> (3 - log2 GP), the sum of the 8 lanes' partial dot products.
-template <int GP>
-__device__ __forceinline__ float exchange_reduce(float (&v)[GP], int lane) {
-#pragma unroll
-  for (int level = 0; level < 3; ++level) {
-    const int mask = 4 >> level;
-    const int n = GP >> level;
-    if (n >= 2) {
-      const bool upper = (lane & mask) != 0;
-#pragma unroll
-      for (int j = 0; j < n / 2; ++j) {
-        const float send = upper ? v[j] : v[j + n / 2];
-        const float keep = upper ? v[j + n / 2] : v[j];
-        v[j] = keep + __shfl_xor_sync(kFull, send, mask);
-      }
-    } else {
-      v[0] += __shfl_xor_sync(kFull, v[0], mask);
-    }
-  }
-  return v[0];
+  // +1 KiB so the rings can start on a 1 KiB boundary (128-byte swizzle atoms)
+  return ring_offset_bytes() + 1024 +
+         static_cast<size_t>(Cfg<G>::kWarps) * kStages * Cfg<G>::kStageBytes;
 }
 
 struct Cursor {
@@ -140,26 +121,11 @@ __device__ __forceinline__ Cursor locate(int item, const int* s_pre, const int* 
   return c;
 }
 
-__device__ __forceinline__ void advance(Cursor& c, const int* s_pre, const int* s_len, int batch,
-                                        int hkv) {
-  ++c.item;
-  if (++c.pg < c.np) return;
-  c.pg = 0;
-  if (++c.h < hkv) return;
-  c.h = 0;
-  do {
-    ++c.b;
-  } while (c.b < batch && s_len[c.b] == 0);
-  if (c.b < batch) {
-    c.np = s_pre[c.b + 1] - s_pre[c.b];
-    c.len = s_len[c.b];
-  }
-}
-
 // Exclusive prefix sum of pages per sequence into s_pre[0..batch], total last.
+template <int kT>
 __device__ void scan_pages(const int* s_len, int* s_pre, int batch, int* s_warp) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (batch + kThreads - 1) / kThreads;
+  const int per = (batch + kT - 1) / kT;
   const int beg = min(tid * per, batch), end = min(beg + per, batch);
   int local = 0;
   for (int b = beg; b < end; ++b) local += (s_len[b] + kPage - 1) / kPage;
@@ -178,25 +144,119 @@ __device__ void scan_pages(const int* s_len, int* s_pre, int batch, int* s_warp)
     s_pre[b] = run;
     run += (s_len[b] + kPage - 1) / kPage;
   }
-  if (tid == kThreads - 1) s_pre[batch] = wofs + incl;
+  if (tid == kT - 1) s_pre[batch] = wofs + incl;
   __syncthreads();
 }
 
+// The warp's lanes have written a piece to the workspace; count its arrival
+// at the (sequence, head)'s counter and return the count before it. __syncwarp
+// orders every lane's stores before lane 0's release; the acquire half orders
+// the merge's loads (after the broadcast) after the other pieces' stores.
+__device__ __forceinline__ int arrive_counter(int* counter, int lane) {
+  __syncwarp();
+  int old = 0;
+  if (lane == 0)
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+  old = __shfl_sync(kFull, old, 0);
+  __syncwarp();
+  return old;
+}
+
+// Log-sum-exp merge of the `pieces` partial results of one (sequence, kv
+// head), read from the workspace slots the pieces' warps published (L2 loads:
+// they were written by other SMs during this launch). Piece jp came from
+// range r0 + jp; piece 0 sits in slot 2 r0 + 1 when it was that range's last
+// segment rather than its first. Lanes first cover pieces (max and weights of
+// each head), then dims (the weighted sum); all loads of a pass are
+// independent, so they overlap.
+template <int G>
+__device__ __noinline__ void merge_pieces(const float* slots, float* out, int r0, bool r0_mid,
+                                          int pieces, size_t row0, int lane) {
+  constexpr int kSF = Cfg<G>::kSlotFloats;
+  auto slot_of = [&](int jp) -> const float* {
+    const int slot = 2 * (r0 + jp) + ((jp == 0 && r0_mid) ? 1 : 0);
+    return slots + static_cast<size_t>(slot) * kSF;
+  };
+  float mx[G], lsum[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    mx[g] = -INFINITY;
+    lsum[g] = 0.f;
+  }
+  // pass 1: per-head max over pieces
+  for (int j0 = 0; j0 < pieces; j0 += 32) {
+    const int jp = j0 + lane;
+    if (jp < pieces) {
+      const float* q = slot_of(jp);
+#pragma unroll
+      for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], ld_cg(q + G * kHeadDim + g));
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(kFull, mx[g], o));
+  // pass 2: per piece weights; per head weighted sums of the l's and the accumulators
+  float2 acc[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
+  for (int j0 = 0; j0 < pieces; j0 += 32) {
+    const int jp = j0 + lane;
+    float w[G];
+    if (jp < pieces) {
+      const float* q = slot_of(jp);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float mj = ld_cg(q + G * kHeadDim + g);
+        w[g] = (mj == -INFINITY) ? 0.f : fast_exp2(mj - mx[g]);
+        lsum[g] += w[g] * ld_cg(q + G * kHeadDim + G + g);
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < G; ++g) w[g] = 0.f;
+    }
+    const int n = min(32, pieces - j0);
+#pragma unroll 4
+    for (int t = 0; t < n; ++t) {
+      const float2* q = reinterpret_cast<const float2*>(slot_of(j0 + t));
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float wt = __shfl_sync(kFull, w[g], t);
+        const float2 a = ld_cg2(q + g * (kHeadDim / 2) + lane);
+        acc[g].x += wt * a.x;
+        acc[g].y += wt * a.y;
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) lsum[g] += __shfl_xor_sync(kFull, lsum[g], o);
+    const float inv = lsum[g] > 0.f ? 1.f / lsum[g] : 0.f;
+    reinterpret_cast<float2*>(out + (row0 + g) * kHeadDim)[lane] =
+        make_float2(acc[g].x * inv, acc[g].y * inv);
+  }
+}
+
 template <int G, bool kPartials>
-__global__ void __launch_bounds__(kThreads, 1) gqa_decode_kernel(const DecodeParams p) {
-  using Ge = Geo<G>;
-  constexpr int GP = Ge::GP;
-  constexpr int kShift = Ge::kShift;
+__global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
+  using C = Cfg<G>;
+  constexpr int kW = C::kWarps;
+  constexpr int kT = C::kThreads;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tg = lane >> 3;         // token row within a 4-row step
-  const int c8 = (lane & 7) * 8;    // first of this lane's 8 dims
-  int* s_warp = reinterpret_cast<int*>(smem + kHdrBytes - kScanScratch);
+  const int g8 = lane >> 2;                 // mma row group: head g8 (rows g8 and g8+8)
+  const int tig = lane & 3;                 // thread in group
+  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: which matrix / which row this lane addresses
+  int* s_warp = reinterpret_cast<int*>(smem + kScanOffset);
   int* s_len = reinterpret_cast<int*>(smem + kHdrBytes);
   int* s_pre = s_len + p.batch;
   __shared__ int s_bad_len;
   const uint32_t bar0 = smem_addr(smem) + warp * kStages * 8;
-  const uint32_t ring0 = smem_addr(smem + p.ring_offset) + warp * kStages * Ge::kStageBytes;
+  const uint32_t ring_base = (smem_addr(smem) + p.ring_offset + 1023u) & ~1023u;
+  const uint32_t ring0 = ring_base + warp * kStages * C::kStageBytes;
+  const void* map = &kv_map;
 
   // Sequence lengths (invalid ones become empty) and the page prefix sums.
   if (tid == 0) s_bad_len = 0;
@@ -205,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_decode_kernel(const DecodePar
   fence_mbar_init();
   __syncthreads();
   const int cap = p.max_blocks * kPage;
-  for (int b = tid; b < p.batch; b += kThreads) {
+  for (int b = tid; b < p.batch; b += kT) {
     int n = p.seq_lens[b];
     if (n < 1 || n > cap) {
       n = 0;
@@ -214,12 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_decode_kernel(const DecodePar
     s_len[b] = n;
   }
   __syncthreads();
-  scan_pages(s_len, s_pre, p.batch, s_warp);
+  scan_pages<kT>(s_len, s_pre, p.batch, s_warp);
 
   if (s_bad_len) {  // rows of invalid sequences: zero output (or zero split count)
     if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, PKV_ERR_SEQ_LEN);
     const int rows = p.batch * p.hq;
-    for (int idx = blockIdx.x * kThreads + tid; idx < rows; idx += gridDim.x * kThreads) {
+    for (int idx = blockIdx.x * kT + tid; idx < rows; idx += gridDim.x * kT) {
       if (s_len[idx / p.hq] != 0) continue;
       if (kPartials) {
         p.num_splits[idx] = 0;
@@ -233,66 +293,93 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_decode_kernel(const DecodePar
 
   const int n_items = s_pre[p.batch] * p.hkv;
   if (n_items == 0) return;
-  const int nwarps = gridDim.x * kWarps;
-  const int c = p.pages_per_split > 0 ? p.pages_per_split : (n_items + nwarps - 1) / nwarps;
+  const int nwarps = gridDim.x * kW;
+  const int c = p.pages_per_split > 0 ? p.pages_per_split
+                                      : max(kMinRangePages, (n_items + nwarps - 1) / nwarps);
   const int n_ranges = (n_items + c - 1) / c;
   const float qs = p.qscale;
 
   uint32_t phase_bits = 0;  // bit s: parity of the next completion of stage s
   int stage = 0;            // next stage to consume
-  uint32_t bad_bits = 0;    // bit s: stage s carries no K/V (bad page id)
   bool failed = false;
-  int win_b = -1, win_base = 0, win_val = -1;  // lane-parallel window of one block-table row
 
-  auto issue = [&](const Cursor& pc, bool first, int st) {
-    if (pc.b != win_b || pc.pg < win_base || pc.pg >= win_base + 32) {
-      win_b = pc.b;
-      win_base = pc.pg & ~31;
-      const int idx = win_base + lane;
-      win_val = idx < p.max_blocks
-                    ? __ldg(p.block_tables + static_cast<size_t>(pc.b) * p.max_blocks + idx)
-                    : -1;
+  // Work-item descriptors, 32 items per batch, lane t describing item base + t:
+  //   y    TMA row of the page's first K row of its kv head (-1: bad page id)
+  //   meta valid rows (bits 0-4) | first item of a piece (5) | last (6) |
+  //        bad page (7) | page index within the sequence (8+)
+  //   bh   sequence * hkv + kv head
+  // The producer (copy issue) runs at most kStages items ahead of the consumer,
+  // hence at most one batch ahead; the consumer keeps its own copy.
+  int pd_base = 0, pd_y = -1, pd_meta = 0, pd_bh = 0;
+  int cd_base = 0, cd_meta = 0, cd_bh = 0;
+
+  auto describe = [&](int base, int i0, int i1) {
+    pd_base = base;
+    const int item = base + lane;
+    pd_y = -1;
+    pd_meta = 0;
+    pd_bh = 0;
+    bool bad = false;
+    if (item < i1) {
+      const Cursor ci = locate(item, s_pre, s_len, p.batch, p.hkv);
+      const int page = __ldg(p.block_tables + static_cast<size_t>(ci.b) * p.max_blocks + ci.pg);
+      const int nv = min(kPage, ci.len - ci.pg * kPage);
+      const int first = (item == i0 || ci.pg == 0) ? 1 : 0;
+      const int last = (item == i1 - 1 || ci.pg == ci.np - 1) ? 1 : 0;
+      bad = page < 0 || static_cast<long long>(page) >= p.num_pages;
+      pd_meta = nv | (first << 5) | (last << 6) | ((bad ? 1 : 0) << 7) | (ci.pg << 8);
+      pd_bh = ci.b * p.hkv + ci.h;
+      pd_y = bad ? -1 : (page * p.hkv + ci.h) * (2 * kPage);
     }
-    const int page = __shfl_sync(kFull, win_val, pc.pg - win_base);
-    const bool bad = page < 0 || static_cast<long long>(page) >= p.num_pages;
-    const int nv = min(kPage, pc.len - pc.pg * kPage);
-    bad_bits = bad ? (bad_bits | (1u << st)) : (bad_bits & ~(1u << st));
+    if (__any_sync(kFull, bad) && lane == 0) atomicOr(p.err, PKV_ERR_PAGE_ID);
+  };
+
+  auto issue = [&](int item, int st, int i0, int i1) {
+    if (item >= pd_base + 32) describe(pd_base + 32, i0, i1);
+    const int t = item - pd_base;
+    const int y = __shfl_sync(kFull, pd_y, t);
+    const int meta = __shfl_sync(kFull, pd_meta, t);
+    const int bh = __shfl_sync(kFull, pd_bh, t);
     if (lane == 0) {
+      const int nv = meta & 31;
+      const bool first = (meta >> 5) & 1;
+      const int nb = (nv + kBoxRows - 1) / kBoxRows;  // boxes holding valid rows
       const uint32_t bar = bar0 + 8 * st;
-      const uint32_t dst = ring0 + st * Ge::kStageBytes;
-      const uint32_t bytes = (bad ? 0u : 2u * nv * kRowBytes) + (first ? Ge::kQBytes : 0u);
-      if (bad) atomicOr(p.err, PKV_ERR_PAGE_ID);
+      const uint32_t dst = ring0 + st * C::kStageBytes;
+      const uint32_t bytes = (y < 0 ? 0u : 2u * nb * kBoxBytes) + (first ? C::kQBytes : 0u);
       if (bytes == 0) {
         mbar_arrive(bar);
       } else {
         mbar_arrive_expect_tx(bar, bytes);
-        if (!bad) {
-          const uint8_t* src =
-              p.pool + (static_cast<size_t>(page) * p.hkv + pc.h) * kHeadPageBytes;
-          bulk_g2s(dst, src, nv * kRowBytes, bar);
-          bulk_g2s(dst + kHalfBytes, src + kHalfBytes, nv * kRowBytes, bar);
+        if (y >= 0) {
+          tma_load_2d(dst, map, 0, y, bar);
+          tma_load_2d(dst + kHalfBytes, map, 0, y + kPage, bar);
+          if (nb == 2) {
+            tma_load_2d(dst + kBoxBytes, map, 0, y + kBoxRows, bar);
+            tma_load_2d(dst + kHalfBytes + kBoxBytes, map, 0, y + kPage + kBoxRows, bar);
+          }
         }
-        if (first)
-          bulk_g2s(dst + kHeadPageBytes,
-                   p.q_rot + (static_cast<size_t>(pc.b) * p.hq + pc.h * G) * kHeadDim,
-                   Ge::kQBytes, bar);
+        if (first)  // rows b*hq + h*G .. +G-1 of q_rot start at bh * G * 64
+          bulk_g2s(dst + kHeadPageBytes, p.q_rot + static_cast<size_t>(bh) * G * kHeadDim,
+                   C::kQBytes, bar);
       }
     }
   };
 
-  float2 q2[G][4];
-  float2 acc[G][4];
-  float m_own = -INFINITY, l_own = 0.f;
+  uint32_t aq[4][4];  // Q as the A operand, one k-step (16 dims) each: bf16 rows g8, remainders g8+8
+  float o[8][4];      // O accumulator, dims 8d..8d+7: rows g8 (from P) and g8+8 (from P's remainder)
+  float m_run = -INFINITY, l_run = 0.f;
 
-  for (int r = blockIdx.x * kWarps + warp; r < n_ranges && !failed; r += nwarps) {
+  for (int r = blockIdx.x * kW + warp; r < n_ranges && !failed; r += nwarps) {
     const int i0 = r * c, i1 = min(i0 + c, n_items);
-    Cursor cur = locate(i0, s_pre, s_len, p.batch, p.hkv);
-    Cursor pc = cur;
+    describe(i0, i0, i1);
+    cd_base = pd_base;
+    cd_meta = pd_meta;
+    cd_bh = pd_bh;
     {
       int st = stage;
       for (int k = 0; k < kStages && i0 + k < i1; ++k) {
-        issue(pc, pc.item == i0 || pc.pg == 0, st);
-        advance(pc, s_pre, s_len, p.batch, p.hkv);
+        issue(i0 + k, st, i0, i1);
         st = (st + 1 == kStages) ? 0 : st + 1;
       }
     }
@@ -305,216 +392,184 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_decode_kernel(const DecodePar
         break;
       }
       phase_bits ^= 1u << st;
-      const uint32_t sbase = ring0 + st * Ge::kStageBytes;
-      const bool first = (i == i0) || cur.pg == 0;
-      const bool last = (i == i1 - 1) || cur.pg == cur.np - 1;
-      if (first) {
-        start_pg = cur.pg;
-        first_in_range = (i == i0);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 a = lds128f(sbase + kHeadPageBytes + (g * kHeadDim + c8) * 4);
-          const float4 e = lds128f(sbase + kHeadPageBytes + (g * kHeadDim + c8 + 4) * 4);
-          q2[g][0] = make_float2(a.x * qs, a.y * qs);
-          q2[g][1] = make_float2(a.z * qs, a.w * qs);
-          q2[g][2] = make_float2(e.x * qs, e.y * qs);
-          q2[g][3] = make_float2(e.z * qs, e.w * qs);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) acc[g][j] = make_float2(0.f, 0.f);
-        }
-        m_own = -INFINITY;
-        l_own = 0.f;
+      if (i >= cd_base + 32) {  // the producer has already described this batch
+        cd_base = pd_base;
+        cd_meta = pd_meta;
+        cd_bh = pd_bh;
       }
-      if (!((bad_bits >> st) & 1u)) {
-        const int nv = min(kPage, cur.len - cur.pg * kPage);
-        // Scores of the page's 16 tokens: this lane ends with token 4r+tg, head (lane&7)>>kShift.
-        float s[4];
+      const int t = i - cd_base;
+      const int meta = __shfl_sync(kFull, cd_meta, t);
+      const int nv = meta & 31;
+      const bool first = (meta >> 5) & 1;
+      const bool last = (meta >> 6) & 1;
+      const bool bad = (meta >> 7) & 1;
+      const uint32_t sK = ring0 + st * C::kStageBytes;
+      const uint32_t sV = sK + kHalfBytes;
+      if (first) {
+        start_pg = meta >> 8;
+        first_in_range = (i == i0);
+        const uint32_t sQ = sK + kHeadPageBytes;
 #pragma unroll
-        for (int rs = 0; rs < 4; ++rs) {
-          const uint4 kw = lds128(sbase + rs * kStepBytes + lane * 16);
-          const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
-          const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
-          float part[GP];
-#pragma unroll
-          for (int g = 0; g < GP; ++g) {
-            if (g < G) {
-              float2 t = __fmul2_rn(q2[g][0], k0);
-              t = __ffma2_rn(q2[g][1], k1, t);
-              t = __ffma2_rn(q2[g][2], k2, t);
-              t = __ffma2_rn(q2[g][3], k3, t);
-              part[g] = t.x + t.y;
-            } else {
-              part[g] = 0.f;
-            }
+        for (int s = 0; s < 4; ++s) {
+          if (g8 < G) {
+            float2 x0 = lds64f(sQ + (g8 * kHeadDim + 16 * s + 2 * tig) * 4);
+            float2 x1 = lds64f(sQ + (g8 * kHeadDim + 16 * s + 8 + 2 * tig) * 4);
+            x0.x *= qs; x0.y *= qs; x1.x *= qs; x1.y *= qs;
+            const uint32_t h0 = pack_bf16x2(x0.x, x0.y), h1 = pack_bf16x2(x1.x, x1.y);
+            const float2 r0 = bf16x2_to_float2(h0), r1 = bf16x2_to_float2(h1);
+            aq[s][0] = h0;
+            aq[s][1] = pack_bf16x2(x0.x - r0.x, x0.y - r0.y);
+            aq[s][2] = h1;
+            aq[s][3] = pack_bf16x2(x1.x - r1.x, x1.y - r1.y);
+          } else {
+            aq[s][0] = aq[s][1] = aq[s][2] = aq[s][3] = 0u;
           }
-          s[rs] = exchange_reduce<GP>(part, lane);
         }
-        if (nv < kPage) {
 #pragma unroll
-          for (int rs = 0; rs < 4; ++rs)
-            if (rs * 4 + tg >= nv) s[rs] = -INFINITY;
+        for (int d = 0; d < 8; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+        m_run = -INFINITY;
+        l_run = 0.f;
+      }
+      if (!bad) {
+        // S = Q K^T for this page's 16 tokens (n-tiles j: tokens 8j..8j+7).
+        uint32_t kb[2][4][2];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int j = q >> 1, s0 = 2 * (q & 1);
+          const int row = 8 * j + ri, chunk = 4 * (q & 1) + mi;
+          ldsm_x4(sK + row * kRowBytes + ((chunk ^ ri) << 4), kb[j][s0][0], kb[j][s0][1],
+                  kb[j][s0 + 1][0], kb[j][s0 + 1][1]);
         }
-        float pm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-        pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 8));
-        pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 16));
-        const float m_new = fmaxf(m_own, pm);
-        const bool grew = m_new > m_own;
-        const float alpha = grew ? fast_exp2(m_own - m_new) : 1.f;
+        float sc[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+          for (int s = 0; s < 4; ++s) mma_bf16_16816(sc[j], aq[s], kb[j][s][0], kb[j][s][1]);
+        }
+        // head g8, tokens 2tig, 2tig+1, 8+2tig, 9+2tig
+        float sv[4] = {sc[0][0] + sc[0][2], sc[0][1] + sc[0][3], sc[1][0] + sc[1][2],
+                       sc[1][1] + sc[1][3]};
+        if (nv < kPage) {
+          const int t0 = 2 * tig;
+          if (t0 >= nv) sv[0] = -INFINITY;
+          if (t0 + 1 >= nv) sv[1] = -INFINITY;
+          if (t0 + 8 >= nv) sv[2] = -INFINITY;
+          if (t0 + 9 >= nv) sv[3] = -INFINITY;
+        }
+        float pm = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+        pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 1));
+        pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 2));
+        const float m_new = fmaxf(m_run, pm);
+        const bool grew = m_new > m_run;
+        const float alpha = grew ? fast_exp2(m_run - m_new) : 1.f;
         float pr[4];
 #pragma unroll
-        for (int rs = 0; rs < 4; ++rs) pr[rs] = fast_exp2(s[rs] - m_new);
-        l_own = l_own * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-        m_own = m_new;
+        for (int k = 0; k < 4; ++k) pr[k] = fast_exp2(sv[k] - m_new);
+        l_run = l_run * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+        m_run = m_new;
         if (__any_sync(kFull, grew)) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float a = __shfl_sync(kFull, alpha, (lane & ~7) | (g << kShift));
-            const float2 a2 = make_float2(a, a);
+          for (int d = 0; d < 8; ++d) {
+            o[d][0] *= alpha; o[d][1] *= alpha; o[d][2] *= alpha; o[d][3] *= alpha;
+          }
+        }
+        // P as the A operand: rows g8 = bf16(p), rows g8+8 = remainder.
+        uint32_t ap[4];
+        {
+          const uint32_t h01 = pack_bf16x2(pr[0], pr[1]), h23 = pack_bf16x2(pr[2], pr[3]);
+          const float2 f01 = bf16x2_to_float2(h01), f23 = bf16x2_to_float2(h23);
+          ap[0] = h01;
+          ap[1] = pack_bf16x2(pr[0] - f01.x, pr[1] - f01.y);
+          ap[2] = h23;
+          ap[3] = pack_bf16x2(pr[2] - f23.x, pr[3] - f23.y);
+        }
+        // O += P V (n-tiles d: dims 8d..8d+7), V fragments transposed by ldmatrix.
+        uint32_t vb[8][2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[g][j] = __fmul2_rn(acc[g][j], a2);
+        for (int q = 0; q < 4; ++q) {
+          const int chunk = 2 * q + (mi >> 1), row = 8 * (mi & 1) + ri;
+          ldsm_x4_trans(sV + row * kRowBytes + ((chunk ^ ri) << 4), vb[2 * q][0], vb[2 * q][1],
+                        vb[2 * q + 1][0], vb[2 * q + 1][1]);
+        }
+        if (nv < kPage) {  // rows past the valid tokens hold stale shared memory
+          const int t0 = 2 * tig;
+          const uint32_t m0 = (t0 < nv ? 0x0000ffffu : 0u) | (t0 + 1 < nv ? 0xffff0000u : 0u);
+          const uint32_t m1 = (t0 + 8 < nv ? 0x0000ffffu : 0u) | (t0 + 9 < nv ? 0xffff0000u : 0u);
+#pragma unroll
+          for (int d = 0; d < 8; ++d) {
+            vb[d][0] &= m0;
+            vb[d][1] &= m1;
           }
         }
 #pragma unroll
-        for (int rs = 0; rs < 4; ++rs) {
-          const uint4 vw = lds128(sbase + kHalfBytes + rs * kStepBytes + lane * 16);
-          float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
-          float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
-          if (nv < kPage && rs * 4 + tg >= nv) {  // stale shared memory past the valid rows
-            v0 = v1 = v2 = v3 = make_float2(0.f, 0.f);
-          }
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float pg = __shfl_sync(kFull, pr[rs], (lane & ~7) | (g << kShift));
-            const float2 p2 = make_float2(pg, pg);
-            acc[g][0] = __ffma2_rn(p2, v0, acc[g][0]);
-            acc[g][1] = __ffma2_rn(p2, v1, acc[g][1]);
-            acc[g][2] = __ffma2_rn(p2, v2, acc[g][2]);
-            acc[g][3] = __ffma2_rn(p2, v3, acc[g][3]);
-          }
-        }
+        for (int d = 0; d < 8; ++d) mma_bf16_16816(o[d], ap, vb[d][0], vb[d][1]);
       }
 
       if (last) {
-        // Sum the four token rows' accumulators and sums; fetch each head's max and sum.
+        // Head g8's unnormalised output at dims 8d+2tig, +1; its max and sum.
+        float2 of[8];
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            acc[g][j].x += __shfl_xor_sync(kFull, acc[g][j].x, 8);
-            acc[g][j].y += __shfl_xor_sync(kFull, acc[g][j].y, 8);
-            acc[g][j].x += __shfl_xor_sync(kFull, acc[g][j].x, 16);
-            acc[g][j].y += __shfl_xor_sync(kFull, acc[g][j].y, 16);
-          }
-        l_own += __shfl_xor_sync(kFull, l_own, 8);
-        l_own += __shfl_xor_sync(kFull, l_own, 16);
-        float mh[G], lh[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          mh[g] = __shfl_sync(kFull, m_own, g << kShift);
-          lh[g] = __shfl_sync(kFull, l_own, g << kShift);
-        }
-        const int seg_start = p.hkv * s_pre[cur.b] + cur.h * cur.np;
-        const int pieces = (seg_start + cur.np - 1) / c - seg_start / c + 1;
-        const size_t row0 = static_cast<size_t>(cur.b) * p.hq + cur.h * G;
-        const bool complete = (start_pg == 0) && (cur.pg == cur.np - 1);
+        for (int d = 0; d < 8; ++d) of[d] = make_float2(o[d][0] + o[d][2], o[d][1] + o[d][3]);
+        float lsum = l_run + __shfl_xor_sync(kFull, l_run, 1);
+        lsum += __shfl_xor_sync(kFull, lsum, 2);
+        const float mh = m_run;
+        const bool live = g8 < G;
+        const int bh = __shfl_sync(kFull, cd_bh, t);
+        const int b = bh / p.hkv, h = bh - b * p.hkv;
+        const int np = s_pre[b + 1] - s_pre[b];
+        const int seg_start = p.hkv * s_pre[b] + h * np;
+        const int pieces = (seg_start + np - 1) / c - seg_start / c + 1;
+        const size_t row0 = static_cast<size_t>(bh) * G;  // = b*hq + h*G
+        const bool complete = (start_pg == 0) && ((meta >> 8) == np - 1);
         if (kPartials) {
           const int j = r - seg_start / c;
           if (pieces > p.max_splits) {
             if (lane == 0) atomicOr(p.err, PKV_ERR_SPLITS);
-          } else {
+          } else if (live) {
+            const size_t row = row0 + g8;
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            float2* dst = reinterpret_cast<float2*>(p.o_part + (row * p.max_splits + j) * kHeadDim);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const size_t row = row0 + g;
-              if ((g & 3) == tg) {
-                const float inv = lh[g] > 0.f ? 1.f / lh[g] : 0.f;
-                float4* o = reinterpret_cast<float4*>(
-                    p.o_part + (row * p.max_splits + j) * kHeadDim + c8);
-                o[0] = make_float4(acc[g][0].x * inv, acc[g][0].y * inv, acc[g][1].x * inv,
-                                   acc[g][1].y * inv);
-                o[1] = make_float4(acc[g][2].x * inv, acc[g][2].y * inv, acc[g][3].x * inv,
-                                   acc[g][3].y * inv);
-              }
-              if (lane == g) {
-                p.lse_part[row * p.max_splits + j] =
-                    lh[g] > 0.f ? (mh[g] + __log2f(lh[g])) * kLn2 : -INFINITY;
-                p.num_splits[row] = pieces;
-              }
+            for (int d = 0; d < 8; ++d) dst[4 * d + tig] = make_float2(of[d].x * inv, of[d].y * inv);
+            if (tig == 0) {
+              p.lse_part[row * p.max_splits + j] = lsum > 0.f ? (mh + __log2f(lsum)) * kLn2 : -INFINITY;
+              p.num_splits[row] = pieces;
             }
           }
         } else if (complete) {
+          if (live) {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            float2* dst = reinterpret_cast<float2*>(p.out + (row0 + g8) * kHeadDim);
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            if ((g & 3) == tg) {
-              const float inv = lh[g] > 0.f ? 1.f / lh[g] : 0.f;
-              float4* o = reinterpret_cast<float4*>(p.out + (row0 + g) * kHeadDim + c8);
-              o[0] = make_float4(acc[g][0].x * inv, acc[g][0].y * inv, acc[g][1].x * inv,
-                                 acc[g][1].y * inv);
-              o[1] = make_float4(acc[g][2].x * inv, acc[g][2].y * inv, acc[g][3].x * inv,
-                                 acc[g][3].y * inv);
-            }
+            for (int d = 0; d < 8; ++d) dst[4 * d + tig] = make_float2(of[d].x * inv, of[d].y * inv);
           }
         } else {
-          // A piece of a split (sequence, head): publish it, and merge if last.
-          float* sp = p.slots + static_cast<size_t>(2 * r + (first_in_range ? 0 : 1)) *
-                                    Ge::kSlotFloats;
+          // A piece of a split (sequence, head): publish it; the last of the
+          // pieces to arrive merges them.
+          float* sp = p.slots + static_cast<size_t>(2 * r + (first_in_range ? 0 : 1)) * C::kSlotFloats;
+          if (live) {
+            float2* acc = reinterpret_cast<float2*>(sp + g8 * kHeadDim);
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            if ((g & 3) == tg) {
-              float4* o = reinterpret_cast<float4*>(sp + g * kHeadDim + c8);
-              o[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
-              o[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
-            }
-            if (lane == g) {
-              sp[G * kHeadDim + g] = mh[g];
-              sp[G * kHeadDim + G + g] = lh[g];
+            for (int d = 0; d < 8; ++d) acc[4 * d + tig] = of[d];
+            if (tig == 0) {
+              sp[G * kHeadDim + g8] = mh;
+              sp[G * kHeadDim + G + g8] = lsum;
             }
           }
-          __threadfence();
-          __syncwarp();
-          int old = 0;
-          int* counter = p.counters + cur.b * p.hkv + cur.h;
-          if (lane == 0) old = atomicAdd(counter, 1);
-          old = __shfl_sync(kFull, old, 0);
+          int* counter = p.counters + bh;
+          const int old = arrive_counter(counter, lane);
           if (old == pieces - 1) {
-            __threadfence();
-            const int r0 = seg_start / c;
-            const bool r0_mid = (seg_start != r0 * c);  // piece 0 is range r0's last segment
-#pragma unroll 1
-            for (int g = 0; g < G; ++g) {
-              float mx = -INFINITY;
-              for (int jp = 0; jp < pieces; ++jp) {
-                const int slot = 2 * (r0 + jp) + ((jp == 0 && r0_mid) ? 1 : 0);
-                mx = fmaxf(mx, ld_cg(p.slots + static_cast<size_t>(slot) * Ge::kSlotFloats +
-                                     G * kHeadDim + g));
-              }
-              float lsum = 0.f;
-              float2 o = make_float2(0.f, 0.f);
-              for (int jp = 0; jp < pieces; ++jp) {
-                const int slot = 2 * (r0 + jp) + ((jp == 0 && r0_mid) ? 1 : 0);
-                const float* q = p.slots + static_cast<size_t>(slot) * Ge::kSlotFloats;
-                const float mj = ld_cg(q + G * kHeadDim + g);
-                const float w = (mj == -INFINITY) ? 0.f : fast_exp2(mj - mx);
-                lsum += w * ld_cg(q + G * kHeadDim + G + g);
-                const float2 a = ld_cg2(reinterpret_cast<const float2*>(q + g * kHeadDim) + lane);
-                o.x += w * a.x;
-                o.y += w * a.y;
-              }
-              const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-              reinterpret_cast<float2*>(p.out + (row0 + g) * kHeadDim)[lane] =
-                  make_float2(o.x * inv, o.y * inv);
-            }
+            merge_pieces<G>(p.slots, p.out, seg_start / c, seg_start % c != 0, pieces, row0, lane);
             if (lane == 0) *counter = 0;
           }
         }
       }
 
-      fence_proxy_async_smem();
+      // Every lane has consumed this stage (its ldmatrix results fed the mma
+      // above) before lane 0 reissues it, so no proxy fence is needed.
       __syncwarp();
-      if (i + kStages < i1) {
-        issue(pc, pc.pg == 0, st);
-        advance(pc, s_pre, s_len, p.batch, p.hkv);
-      }
-      advance(cur, s_pre, s_len, p.batch, p.hkv);
+      if (i + kStages < i1) issue(i + kStages, st, i0, i1);
       stage = (stage + 1 == kStages) ? 0 : stage + 1;
     }
   }
@@ -531,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) gqa_decode_kernel(const DecodePar
 }
 
 template <int G>
-struct Occupancy {
+struct Launcher {
   static int blocks_per_sm(int device, bool partials) {
     static std::atomic<int> cache[2][64];
     const int d = device & 63;
@@ -546,42 +601,52 @@ struct Occupancy {
                              static_cast<int>(smem)) != cudaSuccess)
       return -1;
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, partials ? fn_p : fn_f, kThreads, smem) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, partials ? fn_p : fn_f, Cfg<G>::kThreads,
+                                                      smem) != cudaSuccess)
       return -1;
     v = nb < 1 ? 1 : nb;
     cache[partials][d].store(v, std::memory_order_relaxed);
     return v;
   }
+
+  static cudaError_t launch(const CUtensorMap& map, const DecodeParams& p, int grid,
+                            cudaStream_t stream, bool partials) {
+    const size_t smem = smem_bytes<G>();
+    if (partials)
+      gqa_decode_kernel<G, true><<<grid, Cfg<G>::kThreads, smem, stream>>>(map, p);
+    else
+      gqa_decode_kernel<G, false><<<grid, Cfg<G>::kThreads, smem, stream>>>(map, p);
+    return cudaGetLastError();
+  }
 };
 
-int blocks_per_sm_for(int group, int device, bool partials) {
-  switch (group) {
-    case 1: return Occupancy<1>::blocks_per_sm(device, partials);
-    case 2: return Occupancy<2>::blocks_per_sm(device, partials);
-    case 3: return Occupancy<3>::blocks_per_sm(device, partials);
-    case 4: return Occupancy<4>::blocks_per_sm(device, partials);
-    case 5: return Occupancy<5>::blocks_per_sm(device, partials);
-    case 6: return Occupancy<6>::blocks_per_sm(device, partials);
-    case 7: return Occupancy<7>::blocks_per_sm(device, partials);
-    case 8: return Occupancy<8>::blocks_per_sm(device, partials);
-    default: return -1;
+#define PKV_FOR_GROUP(group, CALL)       \
+  switch (group) {                       \
+    case 1: return Launcher<1>::CALL;    \
+    case 2: return Launcher<2>::CALL;    \
+    case 3: return Launcher<3>::CALL;    \
+    case 4: return Launcher<4>::CALL;    \
+    case 5: return Launcher<5>::CALL;    \
+    case 6: return Launcher<6>::CALL;    \
+    case 7: return Launcher<7>::CALL;    \
+    case 8: return Launcher<8>::CALL;    \
+    default: break;                      \
   }
+
+int blocks_per_sm_for(int group, int device, bool partials) {
+  PKV_FOR_GROUP(group, blocks_per_sm(device, partials));
+  return -1;
 }
 
-int slot_floats_for(int group) {
-  return ((group * kHeadDim + 2 * group) + 3) / 4 * 4;
+cudaError_t launch_group(int group, const CUtensorMap& map, const DecodeParams& p, int grid,
+                         cudaStream_t stream, bool partials) {
+  PKV_FOR_GROUP(group, launch(map, p, grid, stream, partials));
+  return cudaErrorInvalidValue;
 }
 
-template <int G>
-cudaError_t launch_g(const DecodeParams& p, int grid, cudaStream_t stream, bool partials) {
-  const size_t smem = smem_bytes<G>();
-  if (partials)
-    gqa_decode_kernel<G, true><<<grid, kThreads, smem, stream>>>(p);
-  else
-    gqa_decode_kernel<G, false><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
-}
+int warps_per_cta(int group) { return group <= 4 ? Cfg<4>::kWarps : Cfg<8>::kWarps; }
+
+int slot_floats_for(int group) { return ((group * kHeadDim + 2 * group) + 3) / 4 * 4; }
 
 }  // namespace
 
@@ -596,7 +661,7 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int 
   if (cudaGetDevice(&device) != cudaSuccess) return 0;
   const int bps = blocks_per_sm_for(group, device, false);
   if (bps < 1) return 0;
-  const long long warps = static_cast<long long>(sm_count) * bps * kWarps;
+  const long long warps = static_cast<long long>(sm_count) * bps * warps_per_cta(group);
   long long ranges = warps;
   if (pages_per_split > 0) {
     const long long chunk = batch < kDecodeBatchChunk ? batch : kDecodeBatchChunk;
@@ -627,7 +692,6 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
   for (int b0 = 0; b0 < a.batch; b0 += kDecodeBatchChunk) {
     const int nb = a.batch - b0 < kDecodeBatchChunk ? a.batch - b0 : kDecodeBatchChunk;
     DecodeParams p;
-    p.pool = a.pool;
     p.num_pages = a.num_pages;
     p.hkv = a.num_kv_heads;
     p.q_rot = a.q_rot + static_cast<size_t>(b0) * a.num_q_heads * kHeadDim;
@@ -650,17 +714,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
     p.max_splits = a.max_splits;
     p.err = a.err;
     p.ring_offset = static_cast<int>(ring_offset_bytes());
-    switch (group) {
-      case 1: e = launch_g<1>(p, grid, stream, partials); break;
-      case 2: e = launch_g<2>(p, grid, stream, partials); break;
-      case 3: e = launch_g<3>(p, grid, stream, partials); break;
-      case 4: e = launch_g<4>(p, grid, stream, partials); break;
-      case 5: e = launch_g<5>(p, grid, stream, partials); break;
-      case 6: e = launch_g<6>(p, grid, stream, partials); break;
-      case 7: e = launch_g<7>(p, grid, stream, partials); break;
-      case 8: e = launch_g<8>(p, grid, stream, partials); break;
-      default: e = cudaErrorInvalidValue;
-    }
+    e = launch_group(group, *a.kv_map, p, grid, stream, partials);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -6,6 +6,8 @@
 #include <cstdlib>
 #include <new>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/pkv.h"
 #include "pkv_internal.h"
 
@@ -41,6 +43,31 @@ bool decode_shape_ok(const pkv_pool_t* pool, int batch, int num_q_heads, int max
 }  // namespace
 
 namespace pkv {
+
+cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, int num_kv_heads) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    const cudaError_t e =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  // rows of 64 bf16 (128 B): one token's K or V of one kv head, row index
+  // ((page * num_kv_heads + h) * 2 + kind) * 16 + slot
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(PKV_HEAD_DIM),
+                              static_cast<cuuint64_t>(num_pages) * num_kv_heads * 2 * PKV_PAGE_SIZE};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(PKV_HEAD_DIM) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(PKV_HEAD_DIM), 8};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, storage, dims, strides, box, elem,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 int device_sm_count(int device) {
   static int cache[64] = {0};
   const int d = device & 63;
@@ -68,22 +95,28 @@ int kv_pool_create(pkv_pool_t** pool, void* storage, size_t storage_bytes, int n
   const size_t page_bytes = kv_pool_page_bytes(num_kv_heads, head_dim, page_size);
   const size_t pages = storage_bytes / page_bytes;
   if (pages == 0) return -ENOSPC;
-  if (pages > 0x7fffffffull) return -EINVAL;
+  // token rows (page, head, K/V, slot) are addressed with 32-bit coordinates
+  if (pages * static_cast<size_t>(num_kv_heads) * 2 * page_size >= (1ull << 31)) return -EINVAL;
+  pkv_pool_t* h = new (std::nothrow) pkv_pool_t;
+  if (!h) return -ENOMEM;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess) return cuda_fail(e);
+  if (e == cudaSuccess) e = pkv::encode_kv_map(&h->kv_map, storage, static_cast<long long>(pages), num_kv_heads);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e);
+  }
   int* d_err = nullptr;
   e = cudaMalloc(&d_err, sizeof(int));
-  if (e != cudaSuccess) return cuda_fail(e);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_fail(e);
+  }
   e = cudaMemset(d_err, 0, sizeof(int));
   if (e != cudaSuccess) {
     cudaFree(d_err);
+    delete h;
     return cuda_fail(e);
-  }
-  pkv_pool_t* h = new (std::nothrow) pkv_pool_t;
-  if (!h) {
-    cudaFree(d_err);
-    return -ENOMEM;
   }
   h->storage = storage;
   h->storage_bytes = storage_bytes;
@@ -163,6 +196,7 @@ int paged_gqa_decode(const pkv_pool_t* pool, const float* q_rot, float* out,
                                                        max_blocks, pages_per_split);
   if (need == 0 || workspace_bytes < need) return -EINVAL;
   pkv::DecodeLaunch a = {};
+  a.kv_map = &pool->kv_map;
   a.pool = static_cast<const uint8_t*>(pool->storage);
   a.num_pages = pool->num_pages;
   a.num_kv_heads = pool->num_kv_heads;
@@ -196,6 +230,7 @@ int paged_gqa_decode_partials(const pkv_pool_t* pool, const float* q_rot,
     return -EINVAL;
   if (!aligned16(q_rot) || !aligned16(o_part)) return -EINVAL;
   pkv::DecodeLaunch a = {};
+  a.kv_map = &pool->kv_map;
   a.pool = static_cast<const uint8_t*>(pool->storage);
   a.num_pages = pool->num_pages;
   a.num_kv_heads = pool->num_kv_heads;

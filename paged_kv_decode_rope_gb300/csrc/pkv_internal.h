@@ -4,9 +4,14 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 struct pkv_pool {
+  // TMA descriptor of the pool seen as a 2-D bf16 tensor of 128-byte rows
+  // (one token's K or V of one kv head): [num_pages*num_kv_heads*2*16][64],
+  // 8-row boxes, 128-byte swizzle.
+  CUtensorMap kv_map;  // 64-byte aligned by its type
   void* storage;
   size_t storage_bytes;
   long long num_pages;
@@ -40,6 +45,7 @@ struct AppendLaunch {
 cudaError_t launch_append_rope(const AppendLaunch& a, cudaStream_t stream);
 
 struct DecodeLaunch {
+  const CUtensorMap* kv_map;
   const uint8_t* pool;
   long long num_pages;
   int num_kv_heads;
@@ -76,5 +82,8 @@ cudaError_t launch_split_combine(const float* o_part, const float* lse_part,
                                  int head_dim, cudaStream_t stream);
 
 int device_sm_count(int device);
+
+// Encode the pool's TMA descriptor (see pkv_pool::kv_map).
+cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, int num_kv_heads);
 
 }  // namespace pkv

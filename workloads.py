@@ -202,8 +202,21 @@ WORKLOADS = (
 
 
 def make(name: str, seed: int = 0, device="cpu", sentinel: bool = False,
-         materialize: bool = True) -> Workload:
-    """Build one of the named workloads with the given seed."""
+         materialize: bool = True, layers: int | None = None) -> Workload:
+    """Build one of the named workloads with the given seed.
+
+    ``layers`` keeps the workload's shapes and lengths but uses that many
+    layers and a pool just large enough for them (1.1x): a smaller case of the
+    same kernel launches, for profiling.
+    """
+    if layers is not None:
+        full = make(name, seed=seed, materialize=False)
+        return build(f"{name}_first{layers}l", batch=full.batch, num_layers=layers,
+                     num_q_heads=full.num_q_heads, num_kv_heads=full.num_kv_heads,
+                     cached_lens=full.cached_lens, rope_theta=full.rope_theta, pool_slack=1.1,
+                     max_blocks=full.max_blocks, seed=seed, device=device, sentinel=sentinel,
+                     materialize=materialize, big_key_frac=0.1 if "u2048" in name and "b64" in name else 0.0,
+                     description=full.description + f"; first {layers} layers, pool fitted")
     rng = np.random.default_rng([seed, 0x5EED])
     common = dict(seed=seed, device=device, sentinel=sentinel, materialize=materialize)
     if name == "llama1b_b1_l1_len37":
