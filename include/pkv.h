@@ -157,6 +157,36 @@ int paged_gqa_decode(const pkv_pool_t *pool, const float *q_rot, float *out,
                      int batch, int num_q_heads, float scale, int pages_per_split,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* Bytes of the fixed device array paged_gqa_decode_no_alloc uses as workspace. */
+#define PKV_NO_ALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * paged_gqa_decode for callers that cannot allocate device memory. The source
+ * pages have no counterpart: this entry point exists because some callers may
+ * not call cudaMalloc -- code running under a host framework whose memory
+ * manager owns all device memory (a direct cudaMalloc there would synchronise
+ * the device and escape the manager's accounting), or a plugin that a runtime
+ * only hands its input and output buffers. It takes no workspace: the decode's
+ * scratch lives in a fixed array of PKV_NO_ALLOC_SCRATCH_BYTES inside this
+ * library, which every GPU that loads the library holds until the process
+ * exits. It calls no allocation routine.
+ *   Arguments, layouts and results are those of paged_gqa_decode.
+ *   Returns -E2BIG when these sizes need more scratch than the array holds
+ *   (paged_gqa_decode_workspace_bytes() > PKV_NO_ALLOC_SCRATCH_BYTES; with
+ *   pages_per_split = 0 this covers group sizes up to 8 and batches of a few
+ *   thousand sequences on a 152-SM GPU).
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   Every call clears the array's arrival counters on `stream` before the
+ *   decode, so an earlier call's leftovers never matter. All calls share the
+ *   one array: calls that overlap on the GPU (other streams, other threads)
+ *   race and give wrong results; order them on one stream.
+ */
+int paged_gqa_decode_no_alloc(const pkv_pool_t *pool, const float *q_rot, float *out,
+                              const int32_t *block_tables, int max_blocks,
+                              const int32_t *seq_lens, int batch, int num_q_heads, float scale,
+                              int pages_per_split, void *stream);
+
 /*
  * The same decode, but every (sequence, query head) row leaves its split
  * results for paged_kv_split_combine instead of merging them:

@@ -26,6 +26,7 @@ from ._binding import (  # noqa: F401
     kv_pool_page_bytes,
     lib,
     paged_gqa_decode,
+    paged_gqa_decode_no_alloc,
     paged_gqa_decode_partials,
     paged_gqa_decode_workspace_bytes,
     paged_kv_append_rope,

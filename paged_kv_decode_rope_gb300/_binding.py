@@ -34,6 +34,7 @@ _SIGNATURES = {
     "paged_gqa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "paged_gqa_decode": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp, _sz, _vp]),
     "paged_gqa_decode_partials": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp, _vp, _vp, _i, _vp]),
+    "paged_gqa_decode_no_alloc": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp]),
     "paged_kv_split_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "pkv_get_error": (_i, [_vp, ctypes.POINTER(_i), _i]),
     "pkv_last_cuda_error": (_i, []),
@@ -42,7 +43,7 @@ _SIGNATURES = {
 
 class PkvError(RuntimeError):
     def __init__(self, fn: str, rc: int):
-        names = {-22: "EINVAL", -28: "ENOSPC", -5: "EIO", -12: "ENOMEM"}
+        names = {-22: "EINVAL", -28: "ENOSPC", -5: "EIO", -12: "ENOMEM", -7: "E2BIG"}
         extra = ""
         if rc == -5 and _lib is not None:
             extra = f" (cudaError {_lib.pkv_last_cuda_error()})"
@@ -185,6 +186,21 @@ def paged_gqa_decode(pool: KVPool, q_rot: torch.Tensor, out: torch.Tensor,
         _dev(seq_lens, torch.int32, "seq_lens", 1), batch, hq, float(scale), pages_per_split,
         _dev(workspace, torch.uint8, "workspace", 1), workspace.numel(), _stream(stream))
     _check("paged_gqa_decode", rc)
+
+
+def paged_gqa_decode_no_alloc(pool: KVPool, q_rot: torch.Tensor, out: torch.Tensor,
+                              block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                              pages_per_split: int = 0, stream=None) -> None:
+    """paged_gqa_decode without a workspace: for callers that cannot allocate
+    device memory, the library's fixed scratch array serves instead. Calls
+    that overlap on the GPU share that array and race."""
+    batch, hq = q_rot.shape[0], q_rot.shape[1]
+    rc = lib().paged_gqa_decode_no_alloc(
+        pool.handle, _dev(q_rot, torch.float32, "q_rot", 3), _dev(out, torch.float32, "out", 3),
+        _dev(block_tables, torch.int32, "block_tables", 2), block_tables.shape[1],
+        _dev(seq_lens, torch.int32, "seq_lens", 1), batch, hq, float(scale), pages_per_split,
+        _stream(stream))
+    _check("paged_gqa_decode_no_alloc", rc)
 
 
 def decode_max_splits(max_blocks: int, pages_per_split: int) -> int:

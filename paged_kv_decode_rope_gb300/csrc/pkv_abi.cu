@@ -68,6 +68,8 @@ cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, 
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+void record_cuda_error(cudaError_t e) { g_last_cuda_error = static_cast<int>(e); }
+
 int device_sm_count(int device) {
   static int cache[64] = {0};
   const int d = device & 63;

@@ -83,6 +83,9 @@ cudaError_t launch_split_combine(const float* o_part, const float* lse_part,
 
 int device_sm_count(int device);
 
+// Remember a CUDA failure for pkv_last_cuda_error() (calling thread).
+void record_cuda_error(cudaError_t e);
+
 // Encode the pool's TMA descriptor (see pkv_pool::kv_map).
 cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, int num_kv_heads);
 
