@@ -129,8 +129,9 @@ size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_h
                                         int max_blocks, int pages_per_split);
 
 /*
- * Paged GQA decode attention for one layer, split-KV with a fused
- * log-sum-exp merge. ("Hours of YouTube …", direct paged decode attention
+ * Paged GQA decode attention for one layer, split-KV with a log-sum-exp
+ * merge (two kernel launches on `stream`: the decode, then the merge of the
+ * segments it split). ("Hours of YouTube …", direct paged decode attention
  * item: each query head streams its sequence's cached pages and accumulates
  * softmax-weighted values online in FP32, with no gathered prefix and no
  * stored scores. The split-KV form and its merge are flash-decoding, not on
@@ -143,12 +144,9 @@ size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_h
  *                evenly over the persistent grid; > 0: cut the work into
  *                ranges of this many pages (used to force splits in tests).
  *   workspace    device memory of at least paged_gqa_decode_workspace_bytes(),
- *                256-byte aligned. Its first batch*num_kv_heads int32 are
- *                arrival counters that MUST be zero before the first call
- *                (e.g. allocate it zeroed); every call leaves them zero again,
- *                unless a PKV_ERR_TIMEOUT occurred, after which the caller
- *                must zero it again. Calls that share a workspace must not
- *                overlap on the GPU.
+ *                256-byte aligned, contents irrelevant (every call writes each
+ *                part it reads). Calls that share a workspace must not overlap
+ *                on the GPU.
  * Constraints: num_q_heads = g * num_kv_heads with 1 <= g <= PKV_MAX_GROUP.
  * Rows of a sequence with a bad length are written as zeros.
  */
@@ -156,6 +154,44 @@ int paged_gqa_decode(const pkv_pool_t *pool, const float *q_rot, float *out,
                      const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
                      int batch, int num_q_heads, float scale, int pages_per_split,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * RoPE angles of a decode step: cos_sin[b][j] = {cos, sin} of
+ * positions[b] * rope_theta^(-2j/64), j < 32, in fp64 (the product rounded
+ * once, then the CUDA math library's fp64 sincos). ("手写LLM推理引擎…"
+ * section 3.2 precomputes such a cos/sin table once instead of per use.)
+ * The positions are the same in every layer, so one table serves all the
+ * layers of a step.
+ *   positions  int32 [batch];  cos_sin  fp64 [batch][32][2] out (16-byte aligned)
+ */
+int paged_rope_cos_sin(const int32_t *positions, int batch, double rope_theta, double *cos_sin,
+                       void *stream);
+
+/*
+ * The whole decode step of one layer in one call: paged_kv_append_rope
+ * followed by paged_gqa_decode, fused. ("Hours of YouTube …", batched decode
+ * item: per layer, the new token of every sequence is rotated and appended,
+ * then attention reads the sequence's pages; "手写LLM推理引擎…" section 4.2
+ * proposes folding RoPE into the attention kernel to save launches.) The
+ * decode warp that owns a sequence's last page rotates and stores the new
+ * key and value (the same bytes paged_kv_append_rope stores, from the same
+ * fp64 cos/sin), and each warp rotates the query rows it uses; the split
+ * pieces are then merged by a second kernel.
+ *   q            bf16 [batch][num_q_heads][64];  k, v bf16 [batch][num_kv_heads][64]
+ *   cos_sin      fp64 [batch][32][2] from paged_rope_cos_sin for this step's positions
+ *   q_rot        fp32 [batch][num_q_heads][64] out, or NULL: the rotated query
+ *                (rows of sequences with a bad length are zeroed)
+ *   out          fp32 [batch][num_q_heads][64]
+ *   other arguments as for paged_gqa_decode; the workspace is sized by
+ *   paged_gqa_decode_workspace_bytes().
+ * A sequence whose new-token page id is bad gets no append and no attention
+ * over that page (error bit set).
+ */
+int paged_decode_step(pkv_pool_t *pool, const void *q, const void *k, const void *v,
+                      const double *cos_sin, float *q_rot, float *out,
+                      const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
+                      int batch, int num_q_heads, float scale, int pages_per_split,
+                      void *workspace, size_t workspace_bytes, void *stream);
 
 /* Bytes of the fixed device array paged_gqa_decode_no_alloc uses as workspace. */
 #define PKV_NO_ALLOC_SCRATCH_BYTES (8u << 20)
@@ -177,10 +213,10 @@ int paged_gqa_decode(const pkv_pool_t *pool, const float *q_rot, float *out,
  *   thousand sequences on a 152-SM GPU).
  *   The first call on each device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
- *   Every call clears the array's arrival counters on `stream` before the
- *   decode, so an earlier call's leftovers never matter. All calls share the
- *   one array: calls that overlap on the GPU (other streams, other threads)
- *   race and give wrong results; order them on one stream.
+ *   The array keeps the previous call's contents; nothing in it has to start
+ *   at zero, because every call writes each part of it that it reads. All
+ *   calls share the one array: calls that overlap on the GPU (other streams,
+ *   other threads) race and give wrong results; order them on one stream.
  */
 int paged_gqa_decode_no_alloc(const pkv_pool_t *pool, const float *q_rot, float *out,
                               const int32_t *block_tables, int max_blocks,

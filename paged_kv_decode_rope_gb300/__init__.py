@@ -3,8 +3,8 @@
 The CUDA library behind include/pkv.h does the work: RoPE of the new token and
 its append into a shared BF16 page pool (``paged_kv_append_rope``), paged
 grouped-query decode attention with split-KV and a log-sum-exp merge
-(``paged_gqa_decode``), and the standalone merge
-(``paged_kv_split_combine``). This package is the thin Python binding with the
+(``paged_gqa_decode``), both fused into one step (``paged_decode_step``), and
+the standalone merge (``paged_kv_split_combine``). This package is the thin Python binding with the
 same names; it only marshals torch tensors into pointers.
 """
 from ._binding import (  # noqa: F401
@@ -25,12 +25,14 @@ from ._binding import (  # noqa: F401
     kv_pool_num_pages,
     kv_pool_page_bytes,
     lib,
+    paged_decode_step,
     paged_gqa_decode,
     paged_gqa_decode_no_alloc,
     paged_gqa_decode_partials,
     paged_gqa_decode_workspace_bytes,
     paged_kv_append_rope,
     paged_kv_split_combine,
+    paged_rope_cos_sin,
     pkv_get_error,
     pkv_last_cuda_error,
 )

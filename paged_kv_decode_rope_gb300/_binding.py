@@ -35,6 +35,9 @@ _SIGNATURES = {
     "paged_gqa_decode": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp, _sz, _vp]),
     "paged_gqa_decode_partials": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp, _vp, _vp, _i, _vp]),
     "paged_gqa_decode_no_alloc": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp]),
+    "paged_rope_cos_sin": (_i, [_vp, _i, _d, _vp, _vp]),
+    "paged_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp,
+                               _sz, _vp]),
     "paged_kv_split_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "pkv_get_error": (_i, [_vp, ctypes.POINTER(_i), _i]),
     "pkv_last_cuda_error": (_i, []),
@@ -168,11 +171,11 @@ def paged_gqa_decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads:
 
 def alloc_decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, max_blocks: int,
                            pages_per_split: int = 0, device=None) -> torch.Tensor:
-    """A zeroed workspace buffer of the required size (the counters must start at zero)."""
+    """A workspace buffer of the required size (its contents need no initialisation)."""
     n = paged_gqa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, max_blocks, pages_per_split)
     if n == 0:
         raise ValueError("invalid decode sizes")
-    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
 
 
 def paged_gqa_decode(pool: KVPool, q_rot: torch.Tensor, out: torch.Tensor,
@@ -201,6 +204,35 @@ def paged_gqa_decode_no_alloc(pool: KVPool, q_rot: torch.Tensor, out: torch.Tens
         _dev(seq_lens, torch.int32, "seq_lens", 1), batch, hq, float(scale), pages_per_split,
         _stream(stream))
     _check("paged_gqa_decode_no_alloc", rc)
+
+
+def paged_rope_cos_sin(positions: torch.Tensor, rope_theta: float, cos_sin: torch.Tensor,
+                       stream=None) -> None:
+    """positions [B] int32 -> cos_sin [B,32,2] fp64 (cos, sin of each RoPE angle)."""
+    rc = lib().paged_rope_cos_sin(_dev(positions, torch.int32, "positions", 1), positions.shape[0],
+                                  float(rope_theta), _dev(cos_sin, torch.float64, "cos_sin", 3),
+                                  _stream(stream))
+    _check("paged_rope_cos_sin", rc)
+
+
+def paged_decode_step(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                      cos_sin: torch.Tensor, out: torch.Tensor, block_tables: torch.Tensor,
+                      seq_lens: torch.Tensor, scale: float, workspace: torch.Tensor,
+                      q_rot: torch.Tensor | None = None, pages_per_split: int = 0,
+                      stream=None) -> None:
+    """One layer's whole step (RoPE + append + decode) in one call.
+    q [B,Hq,64], k/v [B,Hkv,64] bf16; cos_sin [B,32,2] fp64 from paged_rope_cos_sin;
+    out [B,Hq,64] fp32; q_rot optional fp32 out."""
+    batch, hq = q.shape[0], q.shape[1]
+    rc = lib().paged_decode_step(
+        pool.handle, _dev(q, torch.bfloat16, "q", 3), _dev(k, torch.bfloat16, "k", 3),
+        _dev(v, torch.bfloat16, "v", 3), _dev(cos_sin, torch.float64, "cos_sin", 3),
+        None if q_rot is None else _dev(q_rot, torch.float32, "q_rot", 3),
+        _dev(out, torch.float32, "out", 3), _dev(block_tables, torch.int32, "block_tables", 2),
+        block_tables.shape[1], _dev(seq_lens, torch.int32, "seq_lens", 1), batch, hq,
+        float(scale), pages_per_split, _dev(workspace, torch.uint8, "workspace", 1),
+        workspace.numel(), _stream(stream))
+    _check("paged_decode_step", rc)
 
 
 def decode_max_splits(max_blocks: int, pages_per_split: int) -> int:

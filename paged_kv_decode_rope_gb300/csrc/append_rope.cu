@@ -26,6 +26,10 @@ namespace {
 constexpr int kAppendThreads = 256;
 constexpr int kHalf = kHeadDim / 2;
 
+struct InvFreq {
+  double v[kHalf];  // theta^(-2j/64), evaluated on the host with the C library's pow
+};
+
 struct AppendParams {
   uint16_t* pool;
   long long num_pages;
@@ -42,40 +46,6 @@ struct AppendParams {
   int* err;
   double inv_freq[kHalf];
 };
-
-__device__ __forceinline__ double bf16_bits_to_double(uint16_t b) {
-  return static_cast<double>(__uint_as_float(static_cast<uint32_t>(b) << 16));
-}
-
-// Round a double to the nearest bf16, ties to even, by integer manipulation
-// of its IEEE-754 encoding. NaN becomes the quiet NaN 0x7FC0.
-__device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
-  const unsigned long long u = static_cast<unsigned long long>(__double_as_longlong(x));
-  const uint16_t sign = static_cast<uint16_t>((u >> 48) & 0x8000u);
-  const int biased = static_cast<int>((u >> 52) & 0x7ff);
-  const unsigned long long frac = u & ((1ull << 52) - 1);
-  if (biased == 0x7ff) return frac ? 0x7FC0 : static_cast<uint16_t>(sign | 0x7F80);
-  if (biased == 0) return sign;  // |x| < 2^-1022 rounds to zero in bf16
-  int e = biased - 1023;
-  const unsigned long long sig = frac | (1ull << 52);  // 53-bit significand
-  // bits to drop: to 8 significant bits for a normal bf16, more below 2^-126
-  const int shift = (e >= -126) ? 45 : 45 + (-126 - e);
-  if (shift >= 64) return sign;
-  unsigned long long kept = sig >> shift;
-  const unsigned long long rem = sig & ((1ull << shift) - 1);
-  const unsigned long long half = 1ull << (shift - 1);
-  if (rem > half || (rem == half && (kept & 1))) ++kept;
-  if (e >= -126) {
-    if (kept == (1ull << 8)) {  // carried into the next binade
-      kept >>= 1;
-      ++e;
-    }
-    if (e > 127) return static_cast<uint16_t>(sign | 0x7F80);
-    return static_cast<uint16_t>(sign | ((e + 127) << 7) | (kept & 0x7f));
-  }
-  // subnormal bf16 (kept <= 128; 128 is the smallest normal, encoded the same way)
-  return static_cast<uint16_t>(sign | kept);
-}
 
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const AppendParams p) {
   __shared__ double cos_d[kHalf], sin_d[kHalf];
@@ -125,14 +95,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   const uint16_t* kb = p.k + static_cast<size_t>(b) * p.hkv * kHeadDim;
   for (int idx = tid; idx < p.hkv * kHalf; idx += kAppendThreads) {
     const int h = idx / kHalf, j = idx % kHalf;
-    const double x0 = bf16_bits_to_double(kb[h * kHeadDim + j]);
-    const double x1 = bf16_bits_to_double(kb[h * kHeadDim + j + kHalf]);
-    const double c = cos_d[j], s = sin_d[j];
-    const double y0 = __dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s));
-    const double y1 = __dadd_rn(__dmul_rn(x1, c), __dmul_rn(x0, s));
+    uint16_t y0, y1;
+    rotate_key_pair(kb[h * kHeadDim + j], kb[h * kHeadDim + j + kHalf], cos_d[j], sin_d[j], y0, y1);
     uint16_t* krow = page_base + (h * 2 + 0) * (kHalfBytes / 2) + slot * kHeadDim;
-    krow[j] = double_to_bf16_rne(y0);
-    krow[j + kHalf] = double_to_bf16_rne(y1);
+    krow[j] = y0;
+    krow[j + kHalf] = y1;
   }
   // Value: 16-byte copies.
   const uint4* vb = reinterpret_cast<const uint4*>(p.v + static_cast<size_t>(b) * p.hkv * kHeadDim);
@@ -143,7 +110,32 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   }
 }
 
+// One thread per (sequence, frequency): cos and sin of pos * inv_freq_j in
+// fp64, the same values the append kernel forms for its rotation.
+__global__ void rope_cos_sin_kernel(const int32_t* __restrict__ positions, int batch,
+                                    const InvFreq inv, double2* __restrict__ cos_sin) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= batch * kHalf) return;
+  const int b = idx / kHalf, j = idx % kHalf;
+  const double angle = __dmul_rn(static_cast<double>(positions[b]), inv.v[j]);
+  double s, c;
+  sincos(angle, &s, &c);
+  cos_sin[idx] = make_double2(c, s);
+}
+
 }  // namespace
+
+cudaError_t launch_rope_cos_sin(const int32_t* positions, int batch, double rope_theta,
+                                double* cos_sin, cudaStream_t stream) {
+  if (batch == 0) return cudaSuccess;
+  InvFreq inv;
+  for (int j = 0; j < kHalf; ++j)
+    inv.v[j] = std::pow(rope_theta, -(2.0 * j) / static_cast<double>(kHeadDim));
+  const int n = batch * kHalf;
+  rope_cos_sin_kernel<<<(n + 255) / 256, 256, 0, stream>>>(positions, batch, inv,
+                                                            reinterpret_cast<double2*>(cos_sin));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_append_rope(const AppendLaunch& a, cudaStream_t stream) {
   if (a.batch == 0) return cudaSuccess;

@@ -58,11 +58,9 @@ extern "C" int paged_gqa_decode_no_alloc(const pkv_pool_t* pool, const float* q_
   cudaError_t e = cudaGetDevice(&device);
   void* scratch = nullptr;
   if (e == cudaSuccess) e = scratch_address(device, &scratch);
-  // The array keeps the previous call's contents: the arrival counters at its
-  // start must be zero when the decode starts, so clear them on every call.
-  const size_t counters = static_cast<size_t>(batch) * pool->num_kv_heads * sizeof(int);
-  if (e == cudaSuccess)
-    e = cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream));
+  // The array keeps the previous call's contents. Nothing in it has to start
+  // at zero: the decode writes every segment record and split piece that the
+  // merge then reads.
   if (e != cudaSuccess) {
     pkv::record_cuda_error(e);
     return -EIO;

@@ -35,10 +35,12 @@
 //    again as bf16 hi rows 0-7 and remainder rows 8-15. K fragments come from
 //    ldmatrix, V fragments from ldmatrix.trans, conflict-free thanks to the
 //    swizzle.
-//  * A (sequence, head) piece that spans several warp ranges writes its
-//    unnormalised accumulator, max and sum to a workspace slot; the last warp
-//    to arrive (an atomic counter per (sequence, head)) merges the pieces and
-//    resets the counter. Nothing ever waits on another warp.
+//  * A (sequence, head) segment that lies inside one warp range is finished
+//    by that warp. A segment cut by range boundaries leaves one piece per
+//    range (unnormalised accumulator, max and sum) in a workspace slot, and a
+//    second small kernel merges the pieces by their log-sum-exp, one warp per
+//    segment. Publishing a piece is a handful of plain stores: no atomics, no
+//    fences, and nothing ever waits on another warp.
 #include <atomic>
 #include <cmath>
 
@@ -48,20 +50,40 @@
 namespace pkv {
 namespace {
 
-constexpr int kStages = 3;                 // ring depth per warp
 constexpr int kScanOffset = 512;           // scan scratch (16 ints) after the mbarriers
-constexpr int kHdrBytes = 1024;            // mbarriers (<= 16 warps * 3 * 8 B) + scan scratch
+constexpr int kHdrBytes = 1024;            // mbarriers (<= 32 warp-stages * 8 B) + scan scratch
 constexpr int kBoxRows = 8;                // rows per TMA box (1 KiB, one 128-byte swizzle atom)
 constexpr int kBoxBytes = kBoxRows * kRowBytes;
 constexpr int kMinRangePages = 4;          // smallest automatic range (fewer, cheaper merges)
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kHalfDim = kHeadDim / 2;
 
+// Kernel modes: decode with split pieces merged by the merge kernel; decode
+// leaving every piece for paged_kv_split_combine; and the whole step (RoPE of
+// the new token's q and k, its append into the pool, then the decode).
+constexpr int kModeDecode = 0;
+constexpr int kModePartials = 1;
+constexpr int kModeStep = 2;
+
+
+// Each warp owns a ring of Cfg::kStages stages. A stage is a 1 KiB-aligned 4 KiB
+// K/V block (8-row TMA boxes, 128-byte swizzle) plus a side buffer for the
+// small rows a page may bring along: the group's fp32 q_rot rows (decode
+// mode) or, in step mode, the sequence's cos/sin row (32 x fp64 pairs), the
+// group's raw bf16 q rows and the new token's raw k and v rows.
+constexpr int kTrigBytes = kHalfDim * 16;  // cos/sin of the 32 frequencies, fp64 pairs
+
+// Warps per CTA and ring depth: small groups (little compute per page) hide
+// latency with more warps and double buffering; groups of 5-8 heads need the
+// registers of fewer warps and keep three stages in flight.
 template <int G>
 struct Cfg {
-  static constexpr int kWarps = G <= 4 ? 12 : 10;
+  static constexpr int kWarps = G <= 4 ? 16 : 10;
+  static constexpr int kStages = G <= 4 ? 2 : 3;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kQBytes = G * kHeadDim * 4;  // the group's fp32 query rows
-  static constexpr int kStageBytes = kHeadPageBytes + ((kQBytes + 1023) / 1024) * 1024;
+  static constexpr int kStepSideBytes = kTrigBytes + G * kRowBytes + 2 * kRowBytes;
+  static constexpr int kSideBytes = kQBytes > kStepSideBytes ? kQBytes : kStepSideBytes;
   static constexpr int kSlotFloats = ((G * kHeadDim + 2 * G) + 3) / 4 * 4;
 };
 
@@ -77,7 +99,7 @@ struct DecodeParams {
   int hq;
   float qscale;  // scale * log2(e): scores live in the base-2 domain
   int pages_per_split;
-  int* counters;  // [batch][hkv]
+  int2* seg_info;  // [batch][hkv]: split segments' (2*first range + mid flag, piece count)
   float* slots;
   float* o_part;
   float* lse_part;
@@ -85,18 +107,27 @@ struct DecodeParams {
   int max_splits;
   int* err;
   int ring_offset;  // byte offset of the copy rings in dynamic shared memory (rounded up to 1 KiB)
+  // step mode
+  const uint16_t* q_raw;    // bf16 [batch][hq][64]
+  const uint16_t* k_new;    // bf16 [batch][hkv][64]
+  const uint16_t* v_new;    // bf16 [batch][hkv][64]
+  const double* cos_sin;    // fp64 [batch][32][2]: cos, sin of each sequence's 32 angles
+  float* q_rot_out;         // fp32 [batch][hq][64] or null
+  uint8_t* pool_w;          // the pool's bytes, for the new token's rows
 };
 
 size_t ring_offset_bytes() {
+  // sequence lengths and page prefix sums
   return static_cast<size_t>(kHdrBytes) +
          ((sizeof(int) * (2 * kDecodeBatchChunk + 1) + 1023) / 1024) * 1024;
 }
 
 template <int G>
 size_t smem_bytes() {
-  // +1 KiB so the rings can start on a 1 KiB boundary (128-byte swizzle atoms)
+  // +1 KiB so the K/V rings can start on a 1 KiB boundary (128-byte swizzle
+  // atoms); the side rings follow them.
   return ring_offset_bytes() + 1024 +
-         static_cast<size_t>(Cfg<G>::kWarps) * kStages * Cfg<G>::kStageBytes;
+         static_cast<size_t>(Cfg<G>::kWarps) * Cfg<G>::kStages * (kHeadPageBytes + Cfg<G>::kSideBytes);
 }
 
 struct Cursor {
@@ -148,100 +179,150 @@ __device__ void scan_pages(const int* s_len, int* s_pre, int batch, int* s_warp)
   __syncthreads();
 }
 
-// The warp's lanes have written a piece to the workspace; count its arrival
-// at the (sequence, head)'s counter and return the count before it. __syncwarp
-// orders every lane's stores before lane 0's release; the acquire half orders
-// the merge's loads (after the broadcast) after the other pieces' stores.
-__device__ __forceinline__ int arrive_counter(int* counter, int lane) {
-  __syncwarp();
-  int old = 0;
-  if (lane == 0)
-    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
-  old = __shfl_sync(kFull, old, 0);
-  __syncwarp();
-  return old;
-}
-
-// Log-sum-exp merge of the `pieces` partial results of one (sequence, kv
-// head), read from the workspace slots the pieces' warps published (L2 loads:
-// they were written by other SMs during this launch). Piece jp came from
-// range r0 + jp; piece 0 sits in slot 2 r0 + 1 when it was that range's last
-// segment rather than its first. Lanes first cover pieces (max and weights of
-// each head), then dims (the weighted sum); all loads of a pass are
-// independent, so they overlap.
+// Log-sum-exp merge of head g of one split (sequence, kv head) segment, from
+// the workspace slots the decode's warps wrote. Piece jp came from range
+// r0 + jp; piece 0 sits in slot 2 r0 + 1 when it was that range's last
+// segment rather than its first. Lanes first take one piece each (max,
+// weight, weighted sum), then two dims each for the weighted sum of the
+// accumulators; loads of different pieces are independent, so they overlap.
 template <int G>
-__device__ __noinline__ void merge_pieces(const float* slots, float* out, int r0, bool r0_mid,
-                                          int pieces, size_t row0, int lane) {
+__device__ __forceinline__ void merge_head(const float* slots, float* out_row, int r0, bool r0_mid,
+                                           int pieces, int g, int lane) {
   constexpr int kSF = Cfg<G>::kSlotFloats;
   auto slot_of = [&](int jp) -> const float* {
     const int slot = 2 * (r0 + jp) + ((jp == 0 && r0_mid) ? 1 : 0);
     return slots + static_cast<size_t>(slot) * kSF;
   };
-  float mx[G], lsum[G];
+  float mx = -INFINITY;
+  for (int jp = lane; jp < pieces; jp += 32) mx = fmaxf(mx, slot_of(jp)[G * kHeadDim + g]);
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    mx[g] = -INFINITY;
-    lsum[g] = 0.f;
-  }
-  // pass 1: per-head max over pieces
+  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  float lsum = 0.f;
+  float2 acc = make_float2(0.f, 0.f);
   for (int j0 = 0; j0 < pieces; j0 += 32) {
     const int jp = j0 + lane;
+    float w = 0.f;
     if (jp < pieces) {
       const float* q = slot_of(jp);
-#pragma unroll
-      for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], ld_cg(q + G * kHeadDim + g));
-    }
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(kFull, mx[g], o));
-  // pass 2: per piece weights; per head weighted sums of the l's and the accumulators
-  float2 acc[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
-  for (int j0 = 0; j0 < pieces; j0 += 32) {
-    const int jp = j0 + lane;
-    float w[G];
-    if (jp < pieces) {
-      const float* q = slot_of(jp);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float mj = ld_cg(q + G * kHeadDim + g);
-        w[g] = (mj == -INFINITY) ? 0.f : fast_exp2(mj - mx[g]);
-        lsum[g] += w[g] * ld_cg(q + G * kHeadDim + G + g);
-      }
-    } else {
-#pragma unroll
-      for (int g = 0; g < G; ++g) w[g] = 0.f;
+      const float mj = q[G * kHeadDim + g];
+      w = (mj == -INFINITY) ? 0.f : fast_exp2(mj - mx);
+      lsum += w * q[G * kHeadDim + G + g];
     }
     const int n = min(32, pieces - j0);
-#pragma unroll 4
+#pragma unroll 8
     for (int t = 0; t < n; ++t) {
-      const float2* q = reinterpret_cast<const float2*>(slot_of(j0 + t));
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float wt = __shfl_sync(kFull, w[g], t);
-        const float2 a = ld_cg2(q + g * (kHeadDim / 2) + lane);
-        acc[g].x += wt * a.x;
-        acc[g].y += wt * a.y;
-      }
+      const float wt = __shfl_sync(kFull, w, t);
+      const float2 a = reinterpret_cast<const float2*>(slot_of(j0 + t) + g * kHeadDim)[lane];
+      acc.x += wt * a.x;
+      acc.y += wt * a.y;
     }
   }
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
+  for (int o = 16; o >= 1; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  reinterpret_cast<float2*>(out_row)[lane] = make_float2(acc.x * inv, acc.y * inv);
+}
+
+// Step mode, first page of a piece: rotate the group's raw q rows at the
+// sequence's position and build the mma A operand. The side buffer sS holds
+// the sequence's cos/sin row (fp64 pairs) and then the raw q rows.
+// Thread (g8, tig) owns dims 16s + {2tig, 2tig+1, 8+2tig, 9+2tig} of head g8,
+// s = 0..3, so each rotate-half pair (d, d+32) is in one thread and it needs
+// cos/sin of the 8 frequencies j in {2tig, 2tig+1, 8+2tig, 9+2tig} + {0, 16}
+// (lane j rounds pair j to fp32; shuffles hand them out). The rotation is
+// fp32. The piece that holds page 0 also writes the rotated q (before
+// scaling) to q_rot_out.
+template <int G>
+__device__ __forceinline__ void rope_query(const DecodeParams& p, uint32_t sS, int bh,
+                                           bool write_qrot, int g8, int tig, int lane, float qs,
+                                           uint32_t (&aq)[4][4]) {
+  const float cs = static_cast<float>(lds64d(sS + 16 * lane));
+  const float sn = static_cast<float>(lds64d(sS + 16 * lane + 8));
+  float cj[8], sj[8];  // j = (q & 1) + 2 tig + 8 (q >> 1), q = 0..7
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) lsum[g] += __shfl_xor_sync(kFull, lsum[g], o);
-    const float inv = lsum[g] > 0.f ? 1.f / lsum[g] : 0.f;
-    reinterpret_cast<float2*>(out + (row0 + g) * kHeadDim)[lane] =
-        make_float2(acc[g].x * inv, acc[g].y * inv);
+  for (int q = 0; q < 8; ++q) {
+    const int j = (q & 1) + 2 * tig + 8 * (q >> 1);
+    cj[q] = __shfl_sync(kFull, cs, j);
+    sj[q] = __shfl_sync(kFull, sn, j);
+  }
+  if (g8 >= G) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) aq[s][0] = aq[s][1] = aq[s][2] = aq[s][3] = 0u;
+    return;
+  }
+  const uint32_t sQ = sS + kTrigBytes;
+  // x[s][u]: dims 16s + 2tig + {0, 1} (u = 0, 1) and 16s + 8 + 2tig + {0, 1} (u = 2, 3)
+  float x[4][4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const float2 a = bf16x2_to_float2(lds32(sQ + (g8 * kHeadDim + 16 * s + 2 * tig) * 2));
+    const float2 b = bf16x2_to_float2(lds32(sQ + (g8 * kHeadDim + 16 * s + 8 + 2 * tig) * 2));
+    x[s][0] = a.x; x[s][1] = a.y; x[s][2] = b.x; x[s][3] = b.y;
+  }
+  float y[4][4];
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = (u & 1) + 2 * ((u >> 1) + 2 * s);  // frequency index of dim 16s + ...
+      const float c = cj[q], sv = sj[q];
+      y[s][u] = x[s][u] * c - x[s + 2][u] * sv;
+      y[s + 2][u] = x[s + 2][u] * c + x[s][u] * sv;
+    }
+  if (write_qrot && p.q_rot_out) {
+    float* qo = p.q_rot_out + (static_cast<size_t>(bh) * G + g8) * kHeadDim;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      *reinterpret_cast<float2*>(qo + 16 * s + 2 * tig) = make_float2(y[s][0], y[s][1]);
+      *reinterpret_cast<float2*>(qo + 16 * s + 8 + 2 * tig) = make_float2(y[s][2], y[s][3]);
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const float a0 = y[s][0] * qs, a1 = y[s][1] * qs, b0 = y[s][2] * qs, b1 = y[s][3] * qs;
+    const uint32_t h0 = pack_bf16x2(a0, a1), h1 = pack_bf16x2(b0, b1);
+    const float2 r0 = bf16x2_to_float2(h0), r1 = bf16x2_to_float2(h1);
+    aq[s][0] = h0;
+    aq[s][1] = pack_bf16x2(a0 - r0.x, a1 - r0.y);
+    aq[s][2] = h1;
+    aq[s][3] = pack_bf16x2(b0 - r1.x, b1 - r1.y);
   }
 }
 
-template <int G, bool kPartials>
+// Step mode, the sequence's last page: lane j rotates the pair (j, j+32) of
+// the new key in fp64 with the sequence's fp64 cos/sin of frequency j (the
+// arithmetic of the append kernel, so the stored bytes are identical) and
+// copies v dims 2j, 2j+1. Both rows go into the stage (128-byte swizzled, row
+// `row`) and into the pool (K rows start at TMA row y, V rows at y + 16).
+// sS is the side buffer: cos/sin row, then G raw q rows, then raw k and v.
+template <int G>
+__device__ __forceinline__ void append_new_token(const DecodeParams& p, uint32_t sK, uint32_t sV,
+                                                 uint32_t sS, int y, int row, int lane) {
+  const int j = lane;
+  const double cs = lds64d(sS + 16 * j), sn = lds64d(sS + 16 * j + 8);
+  const uint32_t sKV = sS + kTrigBytes + G * kRowBytes;
+  uint16_t y0, y1;
+  rotate_key_pair(lds16(sKV + 2 * j), lds16(sKV + 2 * (j + kHalfDim)), cs, sn, y0, y1);
+  const uint32_t v01 = lds32(sKV + kRowBytes + 4 * j);
+  auto swz = [&](int d) {
+    return static_cast<uint32_t>(row * kRowBytes + (((d >> 3) ^ (row & 7)) << 4) + (d & 7) * 2);
+  };
+  sts16(sK + swz(j), y0);
+  sts16(sK + swz(j + kHalfDim), y1);
+  sts32(sV + swz(2 * j), v01);
+  uint8_t* krow = p.pool_w + (static_cast<size_t>(y) + row) * kRowBytes;
+  uint8_t* vrow = p.pool_w + (static_cast<size_t>(y) + kPage + row) * kRowBytes;
+  reinterpret_cast<uint16_t*>(krow)[j] = y0;
+  reinterpret_cast<uint16_t*>(krow)[j + kHalfDim] = y1;
+  reinterpret_cast<uint32_t*>(vrow)[j] = v01;
+}
+
+template <int G, int kMode>
 __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeParams p) {
   using C = Cfg<G>;
+  constexpr bool kPartials = kMode == kModePartials;
+  constexpr bool kStep = kMode == kModeStep;
   constexpr int kW = C::kWarps;
   constexpr int kT = C::kThreads;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -253,15 +334,16 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   int* s_len = reinterpret_cast<int*>(smem + kHdrBytes);
   int* s_pre = s_len + p.batch;
   __shared__ int s_bad_len;
-  const uint32_t bar0 = smem_addr(smem) + warp * kStages * 8;
+  const uint32_t bar0 = smem_addr(smem) + warp * C::kStages * 8;
   const uint32_t ring_base = (smem_addr(smem) + p.ring_offset + 1023u) & ~1023u;
-  const uint32_t ring0 = ring_base + warp * kStages * C::kStageBytes;
+  const uint32_t ring0 = ring_base + warp * C::kStages * kHeadPageBytes;
+  const uint32_t side0 = ring_base + kW * C::kStages * kHeadPageBytes + warp * C::kStages * C::kSideBytes;
   const void* map = &kv_map;
 
   // Sequence lengths (invalid ones become empty) and the page prefix sums.
   if (tid == 0) s_bad_len = 0;
   if (lane == 0)
-    for (int s = 0; s < kStages; ++s) mbar_init(bar0 + 8 * s, 1);
+    for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
   fence_mbar_init();
   __syncthreads();
   const int cap = p.max_blocks * kPage;
@@ -284,6 +366,12 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
       if (kPartials) {
         p.num_splits[idx] = 0;
       } else {
+        if (idx % G == 0) p.seg_info[idx / G] = make_int2(0, 0);  // nothing to merge
+        if (kStep && p.q_rot_out) {
+          float4* qo = reinterpret_cast<float4*>(p.q_rot_out + static_cast<size_t>(idx) * kHeadDim);
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 4; ++k) qo[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         float4* o = reinterpret_cast<float4*>(p.out + static_cast<size_t>(idx) * kHeadDim);
 #pragma unroll
         for (int k = 0; k < kHeadDim / 4; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -305,13 +393,14 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
 
   // Work-item descriptors, 32 items per batch, lane t describing item base + t:
   //   y    TMA row of the page's first K row of its kv head (-1: bad page id)
-  //   meta valid rows (bits 0-4) | first item of a piece (5) | last (6) |
-  //        bad page (7) | page index within the sequence (8+)
+  //   meta valid rows (bits 0-4) | first item of a piece (5) | last item of
+  //        a piece (6) | bad page (7) | last page of the sequence (8) |
+  //        page index within the sequence (9+)
   //   bh   sequence * hkv + kv head
   // The producer (copy issue) runs at most kStages items ahead of the consumer,
   // hence at most one batch ahead; the consumer keeps its own copy.
   int pd_base = 0, pd_y = -1, pd_meta = 0, pd_bh = 0;
-  int cd_base = 0, cd_meta = 0, cd_bh = 0;
+  int cd_base = 0, cd_y = -1, cd_meta = 0, cd_bh = 0;
 
   auto describe = [&](int base, int i0, int i1) {
     pd_base = base;
@@ -327,7 +416,9 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
       const int first = (item == i0 || ci.pg == 0) ? 1 : 0;
       const int last = (item == i1 - 1 || ci.pg == ci.np - 1) ? 1 : 0;
       bad = page < 0 || static_cast<long long>(page) >= p.num_pages;
-      pd_meta = nv | (first << 5) | (last << 6) | ((bad ? 1 : 0) << 7) | (ci.pg << 8);
+      const int seg_last = (ci.pg == ci.np - 1) ? 1 : 0;
+      pd_meta = nv | (first << 5) | (last << 6) | ((bad ? 1 : 0) << 7) | (seg_last << 8) |
+                (ci.pg << 9);
       pd_bh = ci.b * p.hkv + ci.h;
       pd_y = bad ? -1 : (page * p.hkv + ci.h) * (2 * kPage);
     }
@@ -345,8 +436,14 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
       const bool first = (meta >> 5) & 1;
       const int nb = (nv + kBoxRows - 1) / kBoxRows;  // boxes holding valid rows
       const uint32_t bar = bar0 + 8 * st;
-      const uint32_t dst = ring0 + st * C::kStageBytes;
-      const uint32_t bytes = (y < 0 ? 0u : 2u * nb * kBoxBytes) + (first ? C::kQBytes : 0u);
+      const uint32_t dst = ring0 + st * kHeadPageBytes;
+      const uint32_t side = side0 + st * C::kSideBytes;
+      const bool seg_last = (meta >> 8) & 1;
+      const uint32_t side_bytes =
+          kStep ? ((first || seg_last) ? kTrigBytes : 0u) + (first ? G * kRowBytes : 0u) +
+                      (seg_last ? 2u * kRowBytes : 0u)
+                : (first ? C::kQBytes : 0u);
+      const uint32_t bytes = (y < 0 ? 0u : 2u * nb * kBoxBytes) + side_bytes;
       if (bytes == 0) {
         mbar_arrive(bar);
       } else {
@@ -359,9 +456,24 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
             tma_load_2d(dst + kHalfBytes + kBoxBytes, map, 0, y + kPage + kBoxRows, bar);
           }
         }
-        if (first)  // rows b*hq + h*G .. +G-1 of q_rot start at bh * G * 64
-          bulk_g2s(dst + kHeadPageBytes, p.q_rot + static_cast<size_t>(bh) * G * kHeadDim,
-                   C::kQBytes, bar);
+        if (kStep) {
+          // the sequence's cos/sin row; the group's raw q rows on a piece's
+          // first page; the new token's raw k and v rows on the sequence's last
+          if (first || seg_last)
+            bulk_g2s(side, p.cos_sin + static_cast<size_t>(bh / p.hkv) * (2 * kHalfDim),
+                     kTrigBytes, bar);
+          if (first)
+            bulk_g2s(side + kTrigBytes, p.q_raw + static_cast<size_t>(bh) * G * kHeadDim,
+                     G * kRowBytes, bar);
+          if (seg_last) {
+            bulk_g2s(side + kTrigBytes + G * kRowBytes, p.k_new + static_cast<size_t>(bh) * kHeadDim,
+                     kRowBytes, bar);
+            bulk_g2s(side + kTrigBytes + (G + 1) * kRowBytes,
+                     p.v_new + static_cast<size_t>(bh) * kHeadDim, kRowBytes, bar);
+          }
+        } else if (first) {  // rows b*hq + h*G .. +G-1 of q_rot start at bh * G * 64
+          bulk_g2s(side, p.q_rot + static_cast<size_t>(bh) * G * kHeadDim, C::kQBytes, bar);
+        }
       }
     }
   };
@@ -374,13 +486,14 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     const int i0 = r * c, i1 = min(i0 + c, n_items);
     describe(i0, i0, i1);
     cd_base = pd_base;
+    cd_y = pd_y;
     cd_meta = pd_meta;
     cd_bh = pd_bh;
     {
       int st = stage;
-      for (int k = 0; k < kStages && i0 + k < i1; ++k) {
+      for (int k = 0; k < C::kStages && i0 + k < i1; ++k) {
         issue(i0 + k, st, i0, i1);
-        st = (st + 1 == kStages) ? 0 : st + 1;
+        st = (st + 1 == C::kStages) ? 0 : st + 1;
       }
     }
     int start_pg = 0;
@@ -394,6 +507,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
       phase_bits ^= 1u << st;
       if (i >= cd_base + 32) {  // the producer has already described this batch
         cd_base = pd_base;
+        cd_y = pd_y;
         cd_meta = pd_meta;
         cd_bh = pd_bh;
       }
@@ -403,17 +517,21 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
       const bool first = (meta >> 5) & 1;
       const bool last = (meta >> 6) & 1;
       const bool bad = (meta >> 7) & 1;
-      const uint32_t sK = ring0 + st * C::kStageBytes;
+      const uint32_t sK = ring0 + st * kHeadPageBytes;
+      const uint32_t sS = side0 + st * C::kSideBytes;
       const uint32_t sV = sK + kHalfBytes;
+      const bool seg_last = (meta >> 8) & 1;
       if (first) {
-        start_pg = meta >> 8;
+        start_pg = meta >> 9;
         first_in_range = (i == i0);
-        const uint32_t sQ = sK + kHeadPageBytes;
+        if (kStep) {
+          rope_query<G>(p, sS, __shfl_sync(kFull, cd_bh, t), start_pg == 0, g8, tig, lane, qs, aq);
+        } else {
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           if (g8 < G) {
-            float2 x0 = lds64f(sQ + (g8 * kHeadDim + 16 * s + 2 * tig) * 4);
-            float2 x1 = lds64f(sQ + (g8 * kHeadDim + 16 * s + 8 + 2 * tig) * 4);
+            float2 x0 = lds64f(sS + (g8 * kHeadDim + 16 * s + 2 * tig) * 4);
+            float2 x1 = lds64f(sS + (g8 * kHeadDim + 16 * s + 8 + 2 * tig) * 4);
             x0.x *= qs; x0.y *= qs; x1.x *= qs; x1.y *= qs;
             const uint32_t h0 = pack_bf16x2(x0.x, x0.y), h1 = pack_bf16x2(x1.x, x1.y);
             const float2 r0 = bf16x2_to_float2(h0), r1 = bf16x2_to_float2(h1);
@@ -425,10 +543,19 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
             aq[s][0] = aq[s][1] = aq[s][2] = aq[s][3] = 0u;
           }
         }
+        }
 #pragma unroll
         for (int d = 0; d < 8; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
         m_run = -INFINITY;
         l_run = 0.f;
+      }
+      if (kStep && seg_last && !bad) {
+        // The sequence's new token is this page's last valid row: rotate its
+        // key, put K and V into the stage (the copy brought the stale slot)
+        // and into the pool.
+        const int y = __shfl_sync(kFull, cd_y, t);
+        append_new_token<G>(p, sK, sV, sS, y, nv - 1, lane);
+        __syncwarp();
       }
       if (!bad) {
         // S = Q K^T for this page's 16 tokens (n-tiles j: tokens 8j..8j+7).
@@ -506,6 +633,13 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
         for (int d = 0; d < 8; ++d) mma_bf16_16816(o[d], ap, vb[d][0], vb[d][1]);
       }
 
+      // Every lane has consumed this stage (its ldmatrix results fed the mma
+      // above) before lane 0 reissues it, so no proxy fence is needed. The
+      // copy goes out before any piece bookkeeping, so the ring keeps streaming.
+      __syncwarp();
+      if (i + C::kStages < i1) issue(i + C::kStages, st, i0, i1);
+      stage = (stage + 1 == C::kStages) ? 0 : stage + 1;
+
       if (last) {
         // Head g8's unnormalised output at dims 8d+2tig, +1; its max and sum.
         float2 of[8];
@@ -521,7 +655,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
         const int seg_start = p.hkv * s_pre[b] + h * np;
         const int pieces = (seg_start + np - 1) / c - seg_start / c + 1;
         const size_t row0 = static_cast<size_t>(bh) * G;  // = b*hq + h*G
-        const bool complete = (start_pg == 0) && ((meta >> 8) == np - 1);
+        const bool complete = (start_pg == 0) && ((meta >> 9) == np - 1);
         if (kPartials) {
           const int j = r - seg_start / c;
           if (pieces > p.max_splits) {
@@ -538,6 +672,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
             }
           }
         } else if (complete) {
+          if (lane == 0) p.seg_info[bh] = make_int2(0, 1);  // final output written here
           if (live) {
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             float2* dst = reinterpret_cast<float2*>(p.out + (row0 + g8) * kHeadDim);
@@ -545,8 +680,9 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
             for (int d = 0; d < 8; ++d) dst[4 * d + tig] = make_float2(of[d].x * inv, of[d].y * inv);
           }
         } else {
-          // A piece of a split (sequence, head): publish it; the last of the
-          // pieces to arrive merges them.
+          // A piece of a split (sequence, head): leave its unnormalised
+          // accumulator, max and sum in the range's slot for the merge kernel;
+          // the piece holding page 0 records where the pieces are.
           float* sp = p.slots + static_cast<size_t>(2 * r + (first_in_range ? 0 : 1)) * C::kSlotFloats;
           if (live) {
             float2* acc = reinterpret_cast<float2*>(sp + g8 * kHeadDim);
@@ -557,20 +693,10 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
               sp[G * kHeadDim + G + g8] = lsum;
             }
           }
-          int* counter = p.counters + bh;
-          const int old = arrive_counter(counter, lane);
-          if (old == pieces - 1) {
-            merge_pieces<G>(p.slots, p.out, seg_start / c, seg_start % c != 0, pieces, row0, lane);
-            if (lane == 0) *counter = 0;
-          }
+          if (start_pg == 0 && lane == 0)
+            p.seg_info[bh] = make_int2(2 * r + (first_in_range ? 0 : 1), pieces);
         }
       }
-
-      // Every lane has consumed this stage (its ldmatrix results fed the mma
-      // above) before lane 0 reissues it, so no proxy fence is needed.
-      __syncwarp();
-      if (i + kStages < i1) issue(i + kStages, st, i0, i1);
-      stage = (stage + 1 == kStages) ? 0 : stage + 1;
     }
   }
 
@@ -578,44 +704,70 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     // Report, then let every copy this warp may still have in flight land
     // before the CTA's shared memory is released.
     if (lane == 0) atomicOr(p.err, PKV_ERR_TIMEOUT);
-    for (int s = 0; s < kStages; ++s) {
-      const int st = (stage + s) % kStages;
+    for (int s = 0; s < C::kStages; ++s) {
+      const int st = (stage + s) % C::kStages;
       mbar_wait_bounded(bar0 + 8 * st, (phase_bits >> st) & 1u);
     }
   }
 }
 
+
+// Merge of the split (sequence, kv head) segments the decode left in the
+// workspace: one warp per (segment, query head of its group); segments the
+// decode finished itself are skipped.
+constexpr int kMergeWarps = 8;
+
+template <int G>
+__global__ void __launch_bounds__(kMergeWarps * 32)
+    merge_kernel(const int2* __restrict__ seg_info, const float* __restrict__ slots,
+                 float* __restrict__ out, int segments) {
+  const int lane = threadIdx.x & 31;
+  const int unit = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  const int seg = unit / G, g = unit - seg * G;
+  if (seg >= segments) return;
+  const int2 info = seg_info[seg];
+  if (info.y < 2) return;
+  merge_head<G>(slots, out + (static_cast<size_t>(seg) * G + g) * kHeadDim, info.x >> 1,
+                info.x & 1, info.y, g, lane);
+}
+
 template <int G>
 struct Launcher {
-  static int blocks_per_sm(int device, bool partials) {
-    static std::atomic<int> cache[2][64];
+  using Fn = void (*)(CUtensorMap, DecodeParams);
+  static Fn kernel(int mode) {
+    return mode == kModePartials ? gqa_decode_kernel<G, kModePartials>
+           : mode == kModeStep   ? gqa_decode_kernel<G, kModeStep>
+                                 : gqa_decode_kernel<G, kModeDecode>;
+  }
+
+  static int blocks_per_sm(int device, int mode) {
+    static std::atomic<int> cache[3][64];
     const int d = device & 63;
-    int v = cache[partials][d].load(std::memory_order_relaxed);
+    int v = cache[mode][d].load(std::memory_order_relaxed);
     if (v > 0) return v;
     const size_t smem = smem_bytes<G>();
-    auto fn_f = gqa_decode_kernel<G, false>;
-    auto fn_p = gqa_decode_kernel<G, true>;
-    if (cudaFuncSetAttribute(fn_f, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess ||
-        cudaFuncSetAttribute(fn_p, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(kernel(mode), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return -1;
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, partials ? fn_p : fn_f, Cfg<G>::kThreads,
-                                                      smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kernel(mode), Cfg<G>::kThreads, smem) !=
+        cudaSuccess)
       return -1;
     v = nb < 1 ? 1 : nb;
-    cache[partials][d].store(v, std::memory_order_relaxed);
+    cache[mode][d].store(v, std::memory_order_relaxed);
     return v;
   }
 
   static cudaError_t launch(const CUtensorMap& map, const DecodeParams& p, int grid,
-                            cudaStream_t stream, bool partials) {
+                            cudaStream_t stream, int mode) {
     const size_t smem = smem_bytes<G>();
-    if (partials)
-      gqa_decode_kernel<G, true><<<grid, Cfg<G>::kThreads, smem, stream>>>(map, p);
-    else
-      gqa_decode_kernel<G, false><<<grid, Cfg<G>::kThreads, smem, stream>>>(map, p);
+    kernel(mode)<<<grid, Cfg<G>::kThreads, smem, stream>>>(map, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || mode == kModePartials) return e;
+    const int segments = p.batch * p.hkv;
+    const int units = segments * G;
+    merge_kernel<G><<<(units + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32, 0, stream>>>(
+        p.seg_info, p.slots, p.out, segments);
     return cudaGetLastError();
   }
 };
@@ -633,14 +785,14 @@ struct Launcher {
     default: break;                      \
   }
 
-int blocks_per_sm_for(int group, int device, bool partials) {
-  PKV_FOR_GROUP(group, blocks_per_sm(device, partials));
+int blocks_per_sm_for(int group, int device, int mode) {
+  PKV_FOR_GROUP(group, blocks_per_sm(device, mode));
   return -1;
 }
 
 cudaError_t launch_group(int group, const CUtensorMap& map, const DecodeParams& p, int grid,
-                         cudaStream_t stream, bool partials) {
-  PKV_FOR_GROUP(group, launch(map, p, grid, stream, partials));
+                         cudaStream_t stream, int mode) {
+  PKV_FOR_GROUP(group, launch(map, p, grid, stream, mode));
   return cudaErrorInvalidValue;
 }
 
@@ -659,7 +811,7 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int 
   if (group < 1 || group > PKV_MAX_GROUP) return 0;
   int device = 0;
   if (cudaGetDevice(&device) != cudaSuccess) return 0;
-  const int bps = blocks_per_sm_for(group, device, false);
+  const int bps = blocks_per_sm_for(group, device, kModeDecode);
   if (bps < 1) return 0;
   const long long warps = static_cast<long long>(sm_count) * bps * warps_per_cta(group);
   long long ranges = warps;
@@ -669,9 +821,9 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int 
     const long long need = (items + pages_per_split - 1) / pages_per_split;
     if (need > ranges) ranges = need;
   }
-  const size_t counters = ((static_cast<size_t>(batch) * num_kv_heads * sizeof(int) + 255) / 256) * 256;
+  const size_t info = ((static_cast<size_t>(batch) * num_kv_heads * sizeof(int2) + 255) / 256) * 256;
   const size_t slots = static_cast<size_t>(2 * ranges) * slot_floats_for(group) * sizeof(float);
-  return counters + slots;
+  return info + slots;
 }
 
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
@@ -681,20 +833,22 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int group = a.num_q_heads / a.num_kv_heads;
   const bool partials = a.o_part != nullptr;
-  const int bps = blocks_per_sm_for(group, device, partials);
+  const bool step = a.q_raw != nullptr;
+  const int mode = partials ? kModePartials : step ? kModeStep : kModeDecode;
+  const int bps = blocks_per_sm_for(group, device, mode);
   if (bps < 1) return cudaErrorInvalidConfiguration;
   const int sms = device_sm_count(device);
   if (sms < 1) return cudaErrorInvalidDevice;
   const int grid = sms * bps;
-  const size_t counters_bytes =
-      ((static_cast<size_t>(a.batch) * a.num_kv_heads * sizeof(int) + 255) / 256) * 256;
+  const size_t info_bytes =
+      ((static_cast<size_t>(a.batch) * a.num_kv_heads * sizeof(int2) + 255) / 256) * 256;
   const double log2e = 1.4426950408889634;
   for (int b0 = 0; b0 < a.batch; b0 += kDecodeBatchChunk) {
     const int nb = a.batch - b0 < kDecodeBatchChunk ? a.batch - b0 : kDecodeBatchChunk;
     DecodeParams p;
     p.num_pages = a.num_pages;
     p.hkv = a.num_kv_heads;
-    p.q_rot = a.q_rot + static_cast<size_t>(b0) * a.num_q_heads * kHeadDim;
+    p.q_rot = a.q_rot ? a.q_rot + static_cast<size_t>(b0) * a.num_q_heads * kHeadDim : nullptr;
     p.out = partials ? nullptr : a.out + static_cast<size_t>(b0) * a.num_q_heads * kHeadDim;
     p.block_tables = a.block_tables + static_cast<size_t>(b0) * a.max_blocks;
     p.max_blocks = a.max_blocks;
@@ -703,10 +857,10 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
     p.hq = a.num_q_heads;
     p.qscale = static_cast<float>(static_cast<double>(a.scale) * log2e);
     p.pages_per_split = a.pages_per_split;
-    p.counters = partials ? nullptr
-                          : static_cast<int*>(a.workspace) + static_cast<size_t>(b0) * a.num_kv_heads;
+    p.seg_info = partials ? nullptr
+                          : static_cast<int2*>(a.workspace) + static_cast<size_t>(b0) * a.num_kv_heads;
     p.slots = partials ? nullptr
-                       : reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + counters_bytes);
+                       : reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + info_bytes);
     const size_t row0 = static_cast<size_t>(b0) * a.num_q_heads;
     p.o_part = partials ? a.o_part + row0 * a.max_splits * kHeadDim : nullptr;
     p.lse_part = partials ? a.lse_part + row0 * a.max_splits : nullptr;
@@ -714,7 +868,15 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
     p.max_splits = a.max_splits;
     p.err = a.err;
     p.ring_offset = static_cast<int>(ring_offset_bytes());
-    e = launch_group(group, *a.kv_map, p, grid, stream, partials);
+    const size_t qrow0 = static_cast<size_t>(b0) * a.num_q_heads * kHeadDim;
+    const size_t krow0 = static_cast<size_t>(b0) * a.num_kv_heads * kHeadDim;
+    p.q_raw = step ? a.q_raw + qrow0 : nullptr;
+    p.k_new = step ? a.k_new + krow0 : nullptr;
+    p.v_new = step ? a.v_new + krow0 : nullptr;
+    p.cos_sin = step ? a.cos_sin + static_cast<size_t>(b0) * 2 * kHalfDim : nullptr;
+    p.q_rot_out = (step && a.q_rot_out) ? a.q_rot_out + qrow0 : nullptr;
+    p.pool_w = const_cast<uint8_t*>(a.pool);
+    e = launch_group(group, *a.kv_map, p, grid, stream, mode);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

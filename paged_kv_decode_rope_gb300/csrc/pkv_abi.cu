@@ -218,6 +218,58 @@ int paged_gqa_decode(const pkv_pool_t* pool, const float* q_rot, float* out,
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
 
+int paged_rope_cos_sin(const int32_t* positions, int batch, double rope_theta, double* cos_sin,
+                       void* stream) {
+  if (batch < 0 || !(rope_theta > 0.0) || !std::isfinite(rope_theta)) return -EINVAL;
+  if (batch == 0) return 0;
+  if (!positions || !cos_sin || !aligned16(cos_sin)) return -EINVAL;
+  cudaError_t e = pkv::launch_rope_cos_sin(positions, batch, rope_theta, cos_sin,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
+int paged_decode_step(pkv_pool_t* pool, const void* q, const void* k, const void* v,
+                      const double* cos_sin, float* q_rot, float* out, const int32_t* block_tables,
+                      int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads,
+                      float scale, int pages_per_split, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (!decode_shape_ok(pool, batch, num_q_heads, max_blocks) || pages_per_split < 0 ||
+      !std::isfinite(scale))
+    return -EINVAL;
+  if (batch == 0) return 0;
+  if (!q || !k || !v || !cos_sin || !out || !block_tables || !seq_lens || !workspace)
+    return -EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(cos_sin) || !aligned16(out) ||
+      (q_rot && !aligned16(q_rot)) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return -EINVAL;
+  const size_t need = paged_gqa_decode_workspace_bytes(batch, num_q_heads, pool->num_kv_heads,
+                                                       max_blocks, pages_per_split);
+  if (need == 0 || workspace_bytes < need) return -EINVAL;
+  pkv::DecodeLaunch a = {};
+  a.kv_map = &pool->kv_map;
+  a.pool = static_cast<const uint8_t*>(pool->storage);
+  a.num_pages = pool->num_pages;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.out = out;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks;
+  a.seq_lens = seq_lens;
+  a.batch = batch;
+  a.num_q_heads = num_q_heads;
+  a.scale = scale;
+  a.pages_per_split = pages_per_split;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err = pool->d_err;
+  a.q_raw = static_cast<const uint16_t*>(q);
+  a.k_new = static_cast<const uint16_t*>(k);
+  a.v_new = static_cast<const uint16_t*>(v);
+  a.cos_sin = cos_sin;
+  a.q_rot_out = q_rot;
+  cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
 int paged_gqa_decode_partials(const pkv_pool_t* pool, const float* q_rot,
                               const int32_t* block_tables, int max_blocks,
                               const int32_t* seq_lens, int batch, int num_q_heads, float scale,

@@ -130,6 +130,32 @@ __device__ __forceinline__ float2 lds64f(uint32_t addr) {
   return v;
 }
 
+__device__ __forceinline__ double lds64d(uint32_t addr) {
+  double v;
+  asm volatile("ld.shared.f64 %0, [%1];" : "=d"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t lds16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -157,6 +183,50 @@ __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ double bf16_bits_to_double(uint16_t b) {
+  return static_cast<double>(__uint_as_float(static_cast<uint32_t>(b) << 16));
+}
+
+// Round a double to the nearest bf16, ties to even, by integer manipulation
+// of its IEEE-754 encoding. NaN becomes the quiet NaN 0x7FC0.
+__device__ __forceinline__ uint16_t double_to_bf16_rne(double x) {
+  const unsigned long long u = static_cast<unsigned long long>(__double_as_longlong(x));
+  const uint16_t sign = static_cast<uint16_t>((u >> 48) & 0x8000u);
+  const int biased = static_cast<int>((u >> 52) & 0x7ff);
+  const unsigned long long frac = u & ((1ull << 52) - 1);
+  if (biased == 0x7ff) return frac ? 0x7FC0 : static_cast<uint16_t>(sign | 0x7F80);
+  if (biased == 0) return sign;  // |x| < 2^-1022 rounds to zero in bf16
+  int e = biased - 1023;
+  const unsigned long long sig = frac | (1ull << 52);  // 53-bit significand
+  // bits to drop: to 8 significant bits for a normal bf16, more below 2^-126
+  const int shift = (e >= -126) ? 45 : 45 + (-126 - e);
+  if (shift >= 64) return sign;
+  unsigned long long kept = sig >> shift;
+  const unsigned long long rem = sig & ((1ull << shift) - 1);
+  const unsigned long long half = 1ull << (shift - 1);
+  if (rem > half || (rem == half && (kept & 1))) ++kept;
+  if (e >= -126) {
+    if (kept == (1ull << 8)) {  // carried into the next binade
+      kept >>= 1;
+      ++e;
+    }
+    if (e > 127) return static_cast<uint16_t>(sign | 0x7F80);
+    return static_cast<uint16_t>(sign | ((e + 127) << 7) | (kept & 0x7f));
+  }
+  // subnormal bf16 (kept <= 128; 128 is the smallest normal, encoded the same way)
+  return static_cast<uint16_t>(sign | kept);
+}
+
+// The new key's rotation, shared by the append kernel and the fused decode:
+// y0 = x0*c - x1*s, y1 = x1*c + x0*s in fp64, every product and sum rounded
+// once (no fused multiply-add), then each rounded once to bf16.
+__device__ __forceinline__ void rotate_key_pair(uint16_t k0, uint16_t k1, double c, double s,
+                                                uint16_t& y0, uint16_t& y1) {
+  const double x0 = bf16_bits_to_double(k0), x1 = bf16_bits_to_double(k1);
+  y0 = double_to_bf16_rne(__dsub_rn(__dmul_rn(x0, c), __dmul_rn(x1, s)));
+  y1 = double_to_bf16_rne(__dadd_rn(__dmul_rn(x1, c), __dmul_rn(x0, s)));
 }
 
 // L2-coherent loads for data another CTA wrote during this launch.

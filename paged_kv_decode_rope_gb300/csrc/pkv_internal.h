@@ -67,6 +67,12 @@ struct DecodeLaunch {
   int32_t* num_splits;
   int max_splits;
   int* err;
+  // the fused step (q_raw != nullptr): RoPE + append of the new token, then the decode
+  const uint16_t* q_raw;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const double* cos_sin;  // fp64 [batch][32][2] from launch_rope_cos_sin
+  float* q_rot_out;
 };
 
 // Largest batch one decode launch serves (sequence lengths and page prefix sums
@@ -76,6 +82,11 @@ constexpr int kDecodeBatchChunk = 2048;
 size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int max_blocks,
                               int pages_per_split, int sm_count);
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream);
+
+// fp64 cos and sin of pos * theta^(-2j/64), j < 32, for every sequence:
+// cos_sin[b][j] = {cos, sin}.
+cudaError_t launch_rope_cos_sin(const int32_t* positions, int batch, double rope_theta,
+                                double* cos_sin, cudaStream_t stream);
 
 cudaError_t launch_split_combine(const float* o_part, const float* lse_part,
                                  const int32_t* num_splits, float* out, int rows, int max_splits,

@@ -1,8 +1,10 @@
 """One batched decode step over all layers, through the C ABI.
 
-Per layer l, on one stream: ``paged_kv_append_rope`` (RoPE of the new token's
-q and k at its position, K/V appended into the layer's pages), then
-``paged_gqa_decode`` (every query head over its sequence's pages). This is
+Per layer l, on one stream: RoPE of the new token's q and k at its position
+and the append of its K/V into the layer's pages, then every query head's
+attention over its sequence's pages. By default one ``paged_decode_step``
+call does both; with ``fused=False`` the two separate entry points
+``paged_kv_append_rope`` and ``paged_gqa_decode`` run instead. This is
 the decode half of the per-layer loop the "Hours of YouTube and 85 handtyped
 pages of notes on LLM Inference – Start here" engine runs for each packed
 decode batch (its batched decode item); the projections around it are not
@@ -38,11 +40,16 @@ class DecodeStep:
         self.out = torch.empty_like(self.q_rot)
         self.workspace = B.alloc_decode_workspace(self.batch, num_q_heads, num_kv_heads,
                                                   self.max_blocks, pages_per_split, device=dev)
+        self.cos_sin = torch.empty(self.batch, 32, 2, dtype=torch.float64, device=dev)
 
-    @property
-    def launches_per_step(self) -> int:
-        chunks = -(-self.batch // 2048) if self.batch else 0
-        return self.num_layers * (1 + chunks) if self.batch else 0
+    def launches_per_step(self, fused: bool = True) -> int:
+        """Kernels one step launches: per layer and batch chunk of 2048 a decode
+        and a merge, plus per layer the append kernel when not fused, or once
+        per step the cos/sin table when fused."""
+        if not self.batch:
+            return 0
+        chunks = -(-self.batch // 2048)
+        return self.num_layers * (2 * chunks + (0 if fused else 1)) + (1 if fused else 0)
 
     def append(self, layer: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
         B.paged_kv_append_rope(self.pool, q[layer], k[layer], v[layer], self.q_rot[layer],
@@ -53,11 +60,28 @@ class DecodeStep:
         B.paged_gqa_decode(self.pool, self.q_rot[layer], self.out[layer], self.block_tables[layer],
                            self.seq_lens, self.scale, self.workspace, self.pages_per_split, stream)
 
-    def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None) -> torch.Tensor:
+    def rope_table(self, stream=None) -> None:
+        """The step's cos/sin table (same positions in every layer)."""
+        B.paged_rope_cos_sin(self.positions, self.rope_theta, self.cos_sin, stream)
+
+    def fused_layer(self, layer: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                    stream=None) -> None:
+        B.paged_decode_step(self.pool, q[layer], k[layer], v[layer], self.cos_sin, self.out[layer],
+                            self.block_tables[layer], self.seq_lens, self.scale, self.workspace,
+                            q_rot=self.q_rot[layer], pages_per_split=self.pages_per_split,
+                            stream=stream)
+
+    def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None,
+            fused: bool = True) -> torch.Tensor:
         """q [NL,B,Hq,64], k/v [NL,B,Hkv,64] bf16 on the device -> out [NL,B,Hq,64] fp32."""
+        if fused:
+            self.rope_table(stream)
         for layer in range(self.num_layers):
-            self.append(layer, q, k, v, stream)
-            self.decode(layer, stream)
+            if fused:
+                self.fused_layer(layer, q, k, v, stream)
+            else:
+                self.append(layer, q, k, v, stream)
+                self.decode(layer, stream)
         return self.out
 
     def error_bits(self, reset: bool = False) -> int:

@@ -26,8 +26,7 @@ class DeviceWorkload:
     def __init__(self, wl: workloads.Workload, pages_per_split: int = 0, device="cuda"):
         from paged_kv_decode_rope_gb300 import DecodeStep
         self.wl = wl
-        self.pool = wl.pool.to(device).contiguous()
-        self.pool_before = self.pool.clone() if wl.pool.numel() * 2 <= (1 << 30) else None
+        self.pool = wl.pool.to(device, copy=True).contiguous()  # wl.pool stays the "before" state
         self.q, self.k, self.v = (t.to(device).contiguous() for t in (wl.q, wl.k, wl.v))
         self.block_tables = torch.from_numpy(wl.block_tables).to(device)
         self.seq_lens = torch.from_numpy(wl.seq_lens).to(device)
@@ -38,8 +37,8 @@ class DeviceWorkload:
                                rope_theta=wl.rope_theta, scale=wl.scale,
                                pages_per_split=pages_per_split)
 
-    def run(self):
-        out = self.step.run(self.q, self.k, self.v)
+    def run(self, fused: bool = True):
+        out = self.step.run(self.q, self.k, self.v, fused=fused)
         torch.cuda.synchronize()
         return out
 
