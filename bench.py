@@ -45,7 +45,9 @@ L2_BYTES = 129 * 10**6
 # the hash of the decode source it was taken on; reported only while the source
 # is unchanged.
 TRAFFIC = {
-    # workload -> (sha256 of gqa_decode.cu prefix, bytes per launch)
+    # workload -> (sha256 of gqa_decode.cu prefix, bytes per layer call: step kernel + merge kernel)
+    # profiles/gqa_decode_step_llama1b_b64_l16_u2048.md: 157.740 + 3.960 MB (step), 3.173 MB (merge)
+    "llama1b_b64_l16_u2048": ("04797bc8f8511cbc", 164873472),
 }
 
 
