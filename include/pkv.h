@@ -155,16 +155,24 @@ int paged_gqa_decode(const pkv_pool_t *pool, const float *q_rot, float *out,
                      int batch, int num_q_heads, float scale, int pages_per_split,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* Bytes of the RoPE table of a step with `batch` sequences. */
+#define PKV_ROPE_TABLE_BYTES(batch) ((size_t)(batch) * 1024u)
+
 /*
- * RoPE angles of a decode step: cos_sin[b][j] = {cos, sin} of
- * positions[b] * rope_theta^(-2j/64), j < 32, in fp64 (the product rounded
- * once, then the CUDA math library's fp64 sincos). ("手写LLM推理引擎…"
+ * RoPE angles of a decode step: for each sequence b and frequency j < 32,
+ * cos and sin of positions[b] * rope_theta^(-2j/64) in fp64 (the product
+ * rounded once, then the CUDA math library's fp64 sincos). ("手写LLM推理引擎…"
  * section 3.2 precomputes such a cos/sin table once instead of per use.)
  * The positions are the same in every layer, so one table serves all the
- * layers of a step.
- *   positions  int32 [batch];  cos_sin  fp64 [batch][32][2] out (16-byte aligned)
+ * layers of a step. Layout of the PKV_ROPE_TABLE_BYTES(batch) bytes:
+ *   float[batch][32][4]  {cos_hi, cos_lo, sin_hi, sin_lo}: cos_hi = cos
+ *                        rounded to fp32, cos_lo = (cos - cos_hi) rounded to
+ *                        fp32 (so cos_hi + cos_lo is within 2^-48 |cos|), the
+ *                        same for sin; then
+ *   double[batch][32][2] {cos, sin}.
+ *   positions  int32 [batch];  table  out, 16-byte aligned
  */
-int paged_rope_cos_sin(const int32_t *positions, int batch, double rope_theta, double *cos_sin,
+int paged_rope_cos_sin(const int32_t *positions, int batch, double rope_theta, void *table,
                        void *stream);
 
 /*
@@ -174,11 +182,11 @@ int paged_rope_cos_sin(const int32_t *positions, int batch, double rope_theta, d
  * then attention reads the sequence's pages; "手写LLM推理引擎…" section 4.2
  * proposes folding RoPE into the attention kernel to save launches.) The
  * decode warp that owns a sequence's last page rotates and stores the new
- * key and value (the same bytes paged_kv_append_rope stores, from the same
- * fp64 cos/sin), and each warp rotates the query rows it uses; the split
- * pieces are then merged by a second kernel.
+ * key and value (the same bytes paged_kv_append_rope stores: the rotation is
+ * rounded to bf16 exactly as fp64 arithmetic on the same fp64 cos/sin rounds
+ * it), and each warp rotates the query rows it uses (in fp32).
  *   q            bf16 [batch][num_q_heads][64];  k, v bf16 [batch][num_kv_heads][64]
- *   cos_sin      fp64 [batch][32][2] from paged_rope_cos_sin for this step's positions
+ *   rope_table   from paged_rope_cos_sin for this step's positions (same batch)
  *   q_rot        fp32 [batch][num_q_heads][64] out, or NULL: the rotated query
  *                (rows of sequences with a bad length are zeroed)
  *   out          fp32 [batch][num_q_heads][64]
@@ -188,7 +196,7 @@ int paged_rope_cos_sin(const int32_t *positions, int batch, double rope_theta, d
  * over that page (error bit set).
  */
 int paged_decode_step(pkv_pool_t *pool, const void *q, const void *k, const void *v,
-                      const double *cos_sin, float *q_rot, float *out,
+                      const void *rope_table, float *q_rot, float *out,
                       const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
                       int batch, int num_q_heads, float scale, int pages_per_split,
                       void *workspace, size_t workspace_bytes, void *stream);

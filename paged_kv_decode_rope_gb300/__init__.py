@@ -19,6 +19,7 @@ from ._binding import (  # noqa: F401
     KVPool,
     PkvError,
     alloc_decode_workspace,
+    alloc_rope_table,
     decode_max_splits,
     kv_pool_create,
     kv_pool_destroy,

@@ -18,6 +18,7 @@ LIBRARY = os.path.join(_HERE, "libpkv.so")
 HEAD_DIM = 64
 PAGE_SIZE = 16
 MAX_GROUP = 8
+ROPE_TABLE_BYTES_PER_SEQ = 1024  # PKV_ROPE_TABLE_BYTES(1)
 ERR_SEQ_LEN, ERR_PAGE_ID, ERR_TIMEOUT, ERR_SPLITS = 0x1, 0x2, 0x4, 0x8
 
 _lib = None
@@ -206,27 +207,40 @@ def paged_gqa_decode_no_alloc(pool: KVPool, q_rot: torch.Tensor, out: torch.Tens
     _check("paged_gqa_decode_no_alloc", rc)
 
 
-def paged_rope_cos_sin(positions: torch.Tensor, rope_theta: float, cos_sin: torch.Tensor,
+def alloc_rope_table(batch: int, device=None) -> torch.Tensor:
+    """A buffer for paged_rope_cos_sin's table of ``batch`` sequences."""
+    return torch.empty(batch * ROPE_TABLE_BYTES_PER_SEQ, dtype=torch.uint8,
+                       device=device or torch.device("cuda"))
+
+
+def paged_rope_cos_sin(positions: torch.Tensor, rope_theta: float, table: torch.Tensor,
                        stream=None) -> None:
-    """positions [B] int32 -> cos_sin [B,32,2] fp64 (cos, sin of each RoPE angle)."""
-    rc = lib().paged_rope_cos_sin(_dev(positions, torch.int32, "positions", 1), positions.shape[0],
-                                  float(rope_theta), _dev(cos_sin, torch.float64, "cos_sin", 3),
+    """positions [B] int32 -> the step's RoPE table (uint8 [B*1024], from
+    alloc_rope_table): float32 [B,32,4] {cos_hi, cos_lo, sin_hi, sin_lo}, then
+    float64 [B,32,2] {cos, sin}."""
+    batch = positions.shape[0]
+    if table.numel() < batch * ROPE_TABLE_BYTES_PER_SEQ:
+        raise ValueError("rope table too small")
+    rc = lib().paged_rope_cos_sin(_dev(positions, torch.int32, "positions", 1), batch,
+                                  float(rope_theta), _dev(table, torch.uint8, "table", 1),
                                   _stream(stream))
     _check("paged_rope_cos_sin", rc)
 
 
 def paged_decode_step(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
-                      cos_sin: torch.Tensor, out: torch.Tensor, block_tables: torch.Tensor,
+                      rope_table: torch.Tensor, out: torch.Tensor, block_tables: torch.Tensor,
                       seq_lens: torch.Tensor, scale: float, workspace: torch.Tensor,
                       q_rot: torch.Tensor | None = None, pages_per_split: int = 0,
                       stream=None) -> None:
     """One layer's whole step (RoPE + append + decode) in one call.
-    q [B,Hq,64], k/v [B,Hkv,64] bf16; cos_sin [B,32,2] fp64 from paged_rope_cos_sin;
-    out [B,Hq,64] fp32; q_rot optional fp32 out."""
+    q [B,Hq,64], k/v [B,Hkv,64] bf16; rope_table from paged_rope_cos_sin for
+    these B sequences; out [B,Hq,64] fp32; q_rot optional fp32 out."""
     batch, hq = q.shape[0], q.shape[1]
+    if rope_table.numel() < batch * ROPE_TABLE_BYTES_PER_SEQ:
+        raise ValueError("rope table too small")
     rc = lib().paged_decode_step(
         pool.handle, _dev(q, torch.bfloat16, "q", 3), _dev(k, torch.bfloat16, "k", 3),
-        _dev(v, torch.bfloat16, "v", 3), _dev(cos_sin, torch.float64, "cos_sin", 3),
+        _dev(v, torch.bfloat16, "v", 3), _dev(rope_table, torch.uint8, "rope_table", 1),
         None if q_rot is None else _dev(q_rot, torch.float32, "q_rot", 3),
         _dev(out, torch.float32, "out", 3), _dev(block_tables, torch.int32, "block_tables", 2),
         block_tables.shape[1], _dev(seq_lens, torch.int32, "seq_lens", 1), batch, hq,

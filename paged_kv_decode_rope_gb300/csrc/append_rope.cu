@@ -111,29 +111,37 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
 }
 
 // One thread per (sequence, frequency): cos and sin of pos * inv_freq_j in
-// fp64, the same values the append kernel forms for its rotation.
+// fp64 (the values the append kernel forms for its rotation), stored twice:
+// as fp32 pairs {hi, lo} (hi = the fp64 value rounded to fp32, lo = the
+// remainder rounded to fp32, so hi + lo is within 2^-48 of it) for the fused
+// step's fp32 paths, and in fp64 for its rare fp64 fallback.
 __global__ void rope_cos_sin_kernel(const int32_t* __restrict__ positions, int batch,
-                                    const InvFreq inv, double2* __restrict__ cos_sin) {
+                                    const InvFreq inv, float4* __restrict__ pairs,
+                                    double2* __restrict__ full) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= batch * kHalf) return;
   const int b = idx / kHalf, j = idx % kHalf;
   const double angle = __dmul_rn(static_cast<double>(positions[b]), inv.v[j]);
   double s, c;
   sincos(angle, &s, &c);
-  cos_sin[idx] = make_double2(c, s);
+  const float ch = __double2float_rn(c), sh = __double2float_rn(s);
+  pairs[idx] = make_float4(ch, __double2float_rn(__dsub_rn(c, static_cast<double>(ch))), sh,
+                           __double2float_rn(__dsub_rn(s, static_cast<double>(sh))));
+  full[idx] = make_double2(c, s);
 }
 
 }  // namespace
 
 cudaError_t launch_rope_cos_sin(const int32_t* positions, int batch, double rope_theta,
-                                double* cos_sin, cudaStream_t stream) {
+                                void* table, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
   InvFreq inv;
   for (int j = 0; j < kHalf; ++j)
     inv.v[j] = std::pow(rope_theta, -(2.0 * j) / static_cast<double>(kHeadDim));
   const int n = batch * kHalf;
-  rope_cos_sin_kernel<<<(n + 255) / 256, 256, 0, stream>>>(positions, batch, inv,
-                                                            reinterpret_cast<double2*>(cos_sin));
+  float4* pairs = static_cast<float4*>(table);
+  double2* full = reinterpret_cast<double2*>(pairs + n);
+  rope_cos_sin_kernel<<<(n + 255) / 256, 256, 0, stream>>>(positions, batch, inv, pairs, full);
   return cudaGetLastError();
 }
 

@@ -69,9 +69,10 @@ constexpr int kModeStep = 2;
 // Each warp owns a ring of Cfg::kStages stages. A stage is a 1 KiB-aligned 4 KiB
 // K/V block (8-row TMA boxes, 128-byte swizzle) plus a side buffer for the
 // small rows a page may bring along: the group's fp32 q_rot rows (decode
-// mode) or, in step mode, the sequence's cos/sin row (32 x fp64 pairs), the
-// group's raw bf16 q rows and the new token's raw k and v rows.
-constexpr int kTrigBytes = kHalfDim * 16;  // cos/sin of the 32 frequencies, fp64 pairs
+// mode) or, in step mode, the sequence's cos/sin row (32 frequencies, each
+// {cos_hi, cos_lo, sin_hi, sin_lo} in fp32), the group's raw bf16 q rows and
+// the new token's raw k and v rows.
+constexpr int kTrigBytes = kHalfDim * 16;  // one sequence's row of the fp32 pair table
 
 // Warps per CTA and ring depth: small groups (little compute per page) hide
 // latency with more warps and double buffering; groups of 5-8 heads need the
@@ -111,7 +112,8 @@ struct DecodeParams {
   const uint16_t* q_raw;    // bf16 [batch][hq][64]
   const uint16_t* k_new;    // bf16 [batch][hkv][64]
   const uint16_t* v_new;    // bf16 [batch][hkv][64]
-  const double* cos_sin;    // fp64 [batch][32][2]: cos, sin of each sequence's 32 angles
+  const float4* rope_ff;    // [batch][32] {cos_hi, cos_lo, sin_hi, sin_lo} (fp32 pairs)
+  const double2* rope_dd;   // [batch][32] {cos, sin} in fp64
   float* q_rot_out;         // fp32 [batch][hq][64] or null
   uint8_t* pool_w;          // the pool's bytes, for the new token's rows
 };
@@ -225,19 +227,19 @@ __device__ __forceinline__ void merge_head(const float* slots, float* out_row, i
 
 // Step mode, first page of a piece: rotate the group's raw q rows at the
 // sequence's position and build the mma A operand. The side buffer sS holds
-// the sequence's cos/sin row (fp64 pairs) and then the raw q rows.
+// the sequence's cos/sin row (fp32 pairs) and then the raw q rows.
 // Thread (g8, tig) owns dims 16s + {2tig, 2tig+1, 8+2tig, 9+2tig} of head g8,
 // s = 0..3, so each rotate-half pair (d, d+32) is in one thread and it needs
 // cos/sin of the 8 frequencies j in {2tig, 2tig+1, 8+2tig, 9+2tig} + {0, 16}
-// (lane j rounds pair j to fp32; shuffles hand them out). The rotation is
-// fp32. The piece that holds page 0 also writes the rotated q (before
+// (lane j reads cos_hi, sin_hi of frequency j, the fp32 roundings of the
+// fp64 values; shuffles hand them out). The rotation is fp32. The piece that holds page 0 also writes the rotated q (before
 // scaling) to q_rot_out.
 template <int G>
 __device__ __forceinline__ void rope_query(const DecodeParams& p, uint32_t sS, int bh,
                                            bool write_qrot, int g8, int tig, int lane, float qs,
                                            uint32_t (&aq)[4][4]) {
-  const float cs = static_cast<float>(lds64d(sS + 16 * lane));
-  const float sn = static_cast<float>(lds64d(sS + 16 * lane + 8));
+  const float cs = __uint_as_float(lds32(sS + 16 * lane));
+  const float sn = __uint_as_float(lds32(sS + 16 * lane + 8));
   float cj[8], sj[8];  // j = (q & 1) + 2 tig + 8 (q >> 1), q = 0..7
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -290,19 +292,30 @@ __device__ __forceinline__ void rope_query(const DecodeParams& p, uint32_t sS, i
 }
 
 // Step mode, the sequence's last page: lane j rotates the pair (j, j+32) of
-// the new key in fp64 with the sequence's fp64 cos/sin of frequency j (the
-// arithmetic of the append kernel, so the stored bytes are identical) and
-// copies v dims 2j, 2j+1. Both rows go into the stage (128-byte swizzled, row
-// `row`) and into the pool (K rows start at TMA row y, V rows at y + 16).
-// sS is the side buffer: cos/sin row, then G raw q rows, then raw k and v.
+// the new key and copies v dims 2j, 2j+1. The rotated pair is rounded to
+// bf16 exactly as fp64 arithmetic on the sequence's fp64 cos/sin rounds it
+// (the bytes the append kernel stores): rotated_bf16_fast certifies the
+// rounding from the fp32 pair table in the side buffer, and a lane it cannot
+// certify reads the fp64 cos/sin of its frequency and rotates in fp64. Both
+// rows go into the stage (128-byte swizzled, row `row`) and into the pool
+// (K rows start at TMA row y, V rows at y + 16). sS is the side buffer:
+// cos/sin row, then G raw q rows, then raw k and v.
 template <int G>
 __device__ __forceinline__ void append_new_token(const DecodeParams& p, uint32_t sK, uint32_t sV,
-                                                 uint32_t sS, int y, int row, int lane) {
+                                                 uint32_t sS, int b, int y, int row, int lane) {
   const int j = lane;
-  const double cs = lds64d(sS + 16 * j), sn = lds64d(sS + 16 * j + 8);
+  const float4 cs = lds128f(sS + 16 * j);  // cos_hi, cos_lo, sin_hi, sin_lo
   const uint32_t sKV = sS + kTrigBytes + G * kRowBytes;
+  const uint16_t k0 = lds16(sKV + 2 * j), k1 = lds16(sKV + 2 * (j + kHalfDim));
+  const float x0 = __uint_as_float(static_cast<uint32_t>(k0) << 16);
+  const float x1 = __uint_as_float(static_cast<uint32_t>(k1) << 16);
   uint16_t y0, y1;
-  rotate_key_pair(lds16(sKV + 2 * j), lds16(sKV + 2 * (j + kHalfDim)), cs, sn, y0, y1);
+  const bool fast = rotated_bf16_fast(x0, x1, cs.x, cs.y, cs.z, cs.w, y0) &&
+                    rotated_bf16_fast(x1, -x0, cs.x, cs.y, cs.z, cs.w, y1);
+  if (!fast) {
+    const double2 cd = p.rope_dd[static_cast<size_t>(b) * kHalfDim + j];
+    rotate_key_pair(k0, k1, cd.x, cd.y, y0, y1);
+  }
   const uint32_t v01 = lds32(sKV + kRowBytes + 4 * j);
   auto swz = [&](int d) {
     return static_cast<uint32_t>(row * kRowBytes + (((d >> 3) ^ (row & 7)) << 4) + (d & 7) * 2);
@@ -460,8 +473,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
           // the sequence's cos/sin row; the group's raw q rows on a piece's
           // first page; the new token's raw k and v rows on the sequence's last
           if (first || seg_last)
-            bulk_g2s(side, p.cos_sin + static_cast<size_t>(bh / p.hkv) * (2 * kHalfDim),
-                     kTrigBytes, bar);
+            bulk_g2s(side, p.rope_ff + static_cast<size_t>(bh / p.hkv) * kHalfDim, kTrigBytes, bar);
           if (first)
             bulk_g2s(side + kTrigBytes, p.q_raw + static_cast<size_t>(bh) * G * kHeadDim,
                      G * kRowBytes, bar);
@@ -554,7 +566,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
         // key, put K and V into the stage (the copy brought the stale slot)
         // and into the pool.
         const int y = __shfl_sync(kFull, cd_y, t);
-        append_new_token<G>(p, sK, sV, sS, y, nv - 1, lane);
+        append_new_token<G>(p, sK, sV, sS, __shfl_sync(kFull, cd_bh, t) / p.hkv, y, nv - 1, lane);
         __syncwarp();
       }
       if (!bad) {
@@ -873,7 +885,13 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
     p.q_raw = step ? a.q_raw + qrow0 : nullptr;
     p.k_new = step ? a.k_new + krow0 : nullptr;
     p.v_new = step ? a.v_new + krow0 : nullptr;
-    p.cos_sin = step ? a.cos_sin + static_cast<size_t>(b0) * 2 * kHalfDim : nullptr;
+    // the fp32 pair table, then the fp64 table (see launch_rope_cos_sin)
+    p.rope_ff = step ? static_cast<const float4*>(a.rope_table) + static_cast<size_t>(b0) * kHalfDim
+                     : nullptr;
+    p.rope_dd = step ? reinterpret_cast<const double2*>(static_cast<const float4*>(a.rope_table) +
+                                                        static_cast<size_t>(a.batch) * kHalfDim) +
+                           static_cast<size_t>(b0) * kHalfDim
+                     : nullptr;
     p.q_rot_out = (step && a.q_rot_out) ? a.q_rot_out + qrow0 : nullptr;
     p.pool_w = const_cast<uint8_t*>(a.pool);
     e = launch_group(group, *a.kv_map, p, grid, stream, mode);

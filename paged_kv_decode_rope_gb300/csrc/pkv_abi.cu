@@ -218,18 +218,18 @@ int paged_gqa_decode(const pkv_pool_t* pool, const float* q_rot, float* out,
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
 
-int paged_rope_cos_sin(const int32_t* positions, int batch, double rope_theta, double* cos_sin,
+int paged_rope_cos_sin(const int32_t* positions, int batch, double rope_theta, void* table,
                        void* stream) {
   if (batch < 0 || !(rope_theta > 0.0) || !std::isfinite(rope_theta)) return -EINVAL;
   if (batch == 0) return 0;
-  if (!positions || !cos_sin || !aligned16(cos_sin)) return -EINVAL;
-  cudaError_t e = pkv::launch_rope_cos_sin(positions, batch, rope_theta, cos_sin,
+  if (!positions || !table || !aligned16(table)) return -EINVAL;
+  cudaError_t e = pkv::launch_rope_cos_sin(positions, batch, rope_theta, table,
                                            static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
 
 int paged_decode_step(pkv_pool_t* pool, const void* q, const void* k, const void* v,
-                      const double* cos_sin, float* q_rot, float* out, const int32_t* block_tables,
+                      const void* rope_table, float* q_rot, float* out, const int32_t* block_tables,
                       int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads,
                       float scale, int pages_per_split, void* workspace, size_t workspace_bytes,
                       void* stream) {
@@ -237,9 +237,9 @@ int paged_decode_step(pkv_pool_t* pool, const void* q, const void* k, const void
       !std::isfinite(scale))
     return -EINVAL;
   if (batch == 0) return 0;
-  if (!q || !k || !v || !cos_sin || !out || !block_tables || !seq_lens || !workspace)
+  if (!q || !k || !v || !rope_table || !out || !block_tables || !seq_lens || !workspace)
     return -EINVAL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(cos_sin) || !aligned16(out) ||
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rope_table) || !aligned16(out) ||
       (q_rot && !aligned16(q_rot)) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return -EINVAL;
   const size_t need = paged_gqa_decode_workspace_bytes(batch, num_q_heads, pool->num_kv_heads,
@@ -264,7 +264,7 @@ int paged_decode_step(pkv_pool_t* pool, const void* q, const void* k, const void
   a.q_raw = static_cast<const uint16_t*>(q);
   a.k_new = static_cast<const uint16_t*>(k);
   a.v_new = static_cast<const uint16_t*>(v);
-  a.cos_sin = cos_sin;
+  a.rope_table = rope_table;
   a.q_rot_out = q_rot;
   cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? 0 : cuda_fail(e);

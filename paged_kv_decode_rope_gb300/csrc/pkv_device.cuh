@@ -229,6 +229,60 @@ __device__ __forceinline__ void rotate_key_pair(uint16_t k0, uint16_t k1, double
   y1 = double_to_bf16_rne(__dadd_rn(__dmul_rn(x1, c), __dmul_rn(x0, s)));
 }
 
+// Key rotation without fp64 arithmetic, rounded exactly as fp64 would round it.
+//
+// The stored key element is bf16(fl64(fl64(a c) - fl64(b s))): two fp64
+// products, their fp64 difference, then round-to-nearest-even to bf16 (the
+// arithmetic the oracle and the fp64 append use; y0 takes a = x0, b = x1,
+// y1 takes a = x1, b = -x0). fp64 throughput on this part is tiny, so the
+// fast path evaluates the same difference in fp32 double-word arithmetic:
+// c ~ ch + cl and s ~ sh + sl with |c - ch - cl| <= 2^-48 |c|; a ch = pa + ea
+// exactly by an FMA (Dekker's two-product), a cl is one rounded product, and
+// Knuth's two-sum keeps the cancellation of pa - pb exact. The result is the
+// unevaluated sum f + res, within 2^-42 M of the fp64 difference, where
+// M = max(|pa|, |pb|) (error terms: 2^-48 from the split of c, 2^-47 from
+// a cl, 2^-46 from each low-order sum, 2^-44 from the last one; the fp64
+// difference itself is within 3 2^-53 M of the exact one).
+//
+// bf16 rounding boundaries are the midpoints between neighbouring bf16
+// values. With upper = the top 16 bits of f's magnitude and lower = its
+// bottom 16, the nearest boundary is at magnitude (upper << 16) | 0x8000
+// (the one below is at least 2^-10 |f| away). When f + res is farther than
+// tol = 2^-36 M from it (64x the error bound), f + res, the fp64 difference
+// and the exact value all round to the same bf16, which is upper, plus one
+// when lower > 0x8000. Otherwise (a near-tie, a zero or subnormal result,
+// heavy cancellation, huge or non-finite inputs) the function returns false
+// and the caller takes the fp64 route.
+__device__ __forceinline__ bool rotated_bf16_fast(float a, float b, float ch, float cl, float sh,
+                                                  float sl, uint16_t& y) {
+  const float pa = __fmul_rn(a, ch), ea = __fmaf_rn(a, ch, -pa);
+  const float pb = __fmul_rn(b, sh), eb = __fmaf_rn(b, sh, -pb);
+  const float ta = __fmul_rn(a, cl), tb = __fmul_rn(b, sl);
+  // two-sum: s + t = pa - pb exactly
+  const float s = __fsub_rn(pa, pb);
+  const float sb = __fsub_rn(s, pa);
+  const float sa = __fsub_rn(s, sb);
+  const float t = __fadd_rn(__fsub_rn(pa, sa), __fsub_rn(-pb, sb));
+  const float lo = __fadd_rn(t, __fsub_rn(__fadd_rn(ea, ta), __fadd_rn(eb, tb)));
+  // two-sum: f + res = s + lo exactly
+  const float f = __fadd_rn(s, lo);
+  const float fb = __fsub_rn(f, s);
+  const float fa = __fsub_rn(f, fb);
+  const float res = __fadd_rn(__fsub_rn(s, fa), __fsub_rn(lo, fb));
+  const float m = fmaxf(fabsf(pa), fabsf(pb));
+  const float af = fabsf(f);
+  const float tol = __fmul_rn(m, 0x1p-36f);
+  // (comparisons with NaN are false, so non-finite values fail here too)
+  if (!(m <= 0x1p120f) || !(af >= 0x1p-100f) || !(__fmul_rn(af, 0x1p-12f) > tol)) return false;
+  const uint32_t u = __float_as_uint(f);
+  const uint32_t mag = u & 0x7fffffffu;
+  const uint32_t upper = mag >> 16, lower = mag & 0xffffu;
+  const float mid = __uint_as_float((upper << 16) | 0x8000u);  // same binade as af: exact difference
+  if (!(__fsub_rn(fabsf(__fsub_rn(mid, af)), fabsf(res)) > tol)) return false;
+  y = static_cast<uint16_t>(((u >> 16) & 0x8000u) | (upper + (lower > 0x8000u ? 1u : 0u)));
+  return true;
+}
+
 // L2-coherent loads for data another CTA wrote during this launch.
 __device__ __forceinline__ float ld_cg(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ float2 ld_cg2(const float2* p) { return __ldcg(p); }

@@ -71,7 +71,7 @@ struct DecodeLaunch {
   const uint16_t* q_raw;
   const uint16_t* k_new;
   const uint16_t* v_new;
-  const double* cos_sin;  // fp64 [batch][32][2] from launch_rope_cos_sin
+  const void* rope_table;  // from launch_rope_cos_sin for this batch
   float* q_rot_out;
 };
 
@@ -83,10 +83,11 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int 
                               int pages_per_split, int sm_count);
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream);
 
-// fp64 cos and sin of pos * theta^(-2j/64), j < 32, for every sequence:
-// cos_sin[b][j] = {cos, sin}.
+// cos and sin of pos * theta^(-2j/64), j < 32, for every sequence, in fp64,
+// and split into fp32 pairs: table = float4 [batch][32] {cos_hi, cos_lo,
+// sin_hi, sin_lo}, then double2 [batch][32] {cos, sin} (PKV_ROPE_TABLE_BYTES).
 cudaError_t launch_rope_cos_sin(const int32_t* positions, int batch, double rope_theta,
-                                double* cos_sin, cudaStream_t stream);
+                                void* table, cudaStream_t stream);
 
 cudaError_t launch_split_combine(const float* o_part, const float* lse_part,
                                  const int32_t* num_splits, float* out, int rows, int max_splits,

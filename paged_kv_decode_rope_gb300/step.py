@@ -40,7 +40,7 @@ class DecodeStep:
         self.out = torch.empty_like(self.q_rot)
         self.workspace = B.alloc_decode_workspace(self.batch, num_q_heads, num_kv_heads,
                                                   self.max_blocks, pages_per_split, device=dev)
-        self.cos_sin = torch.empty(self.batch, 32, 2, dtype=torch.float64, device=dev)
+        self.rope_cos_sin = B.alloc_rope_table(self.batch, device=dev)
 
     def launches_per_step(self, fused: bool = True) -> int:
         """Kernels one step launches: per layer and batch chunk of 2048 a decode
@@ -62,11 +62,11 @@ class DecodeStep:
 
     def rope_table(self, stream=None) -> None:
         """The step's cos/sin table (same positions in every layer)."""
-        B.paged_rope_cos_sin(self.positions, self.rope_theta, self.cos_sin, stream)
+        B.paged_rope_cos_sin(self.positions, self.rope_theta, self.rope_cos_sin, stream)
 
     def fused_layer(self, layer: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                     stream=None) -> None:
-        B.paged_decode_step(self.pool, q[layer], k[layer], v[layer], self.cos_sin, self.out[layer],
+        B.paged_decode_step(self.pool, q[layer], k[layer], v[layer], self.rope_cos_sin, self.out[layer],
                             self.block_tables[layer], self.seq_lens, self.scale, self.workspace,
                             q_rot=self.q_rot[layer], pages_per_split=self.pages_per_split,
                             stream=stream)
