@@ -55,6 +55,12 @@ constexpr int kHdrBytes = 1024;            // mbarriers (<= 32 warp-stages * 8 B
 constexpr int kBoxRows = 8;                // rows per TMA box (1 KiB, one 128-byte swizzle atom)
 constexpr int kBoxBytes = kBoxRows * kRowBytes;
 constexpr int kMinRangePages = 4;          // smallest automatic range (fewer, cheaper merges)
+// Automatic partition weights: a page costs kPageUnits, and each (sequence,
+// kv head) segment adds kSegUnits for the fixed work of its pieces (query
+// rows, the new token, the result stores), about 3/4 of a page. Without it a
+// range of many short segments takes visibly longer than the others.
+constexpr int kPageUnits = 4;
+constexpr int kSegUnits = 3;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kHalfDim = kHeadDim / 2;
 
@@ -184,45 +190,48 @@ __device__ void scan_pages(const int* s_len, int* s_pre, int batch, int* s_warp)
 // Log-sum-exp merge of head g of one split (sequence, kv head) segment, from
 // the workspace slots the decode's warps wrote. Piece jp came from range
 // r0 + jp; piece 0 sits in slot 2 r0 + 1 when it was that range's last
-// segment rather than its first. Lanes first take one piece each (max,
-// weight, weighted sum), then two dims each for the weighted sum of the
-// accumulators; loads of different pieces are independent, so they overlap.
+// segment rather than its first. Lane l owns dims 2l, 2l+1 and folds the
+// pieces into a running (max, sum, accumulator), eight pieces at a time whose
+// loads (max, sum and the lane's two accumulator values) are all in flight
+// together: one dependent round trip for up to eight pieces.
 template <int G>
 __device__ __forceinline__ void merge_head(const float* slots, float* out_row, int r0, bool r0_mid,
                                            int pieces, int g, int lane) {
   constexpr int kSF = Cfg<G>::kSlotFloats;
-  auto slot_of = [&](int jp) -> const float* {
-    const int slot = 2 * (r0 + jp) + ((jp == 0 && r0_mid) ? 1 : 0);
-    return slots + static_cast<size_t>(slot) * kSF;
-  };
-  float mx = -INFINITY;
-  for (int jp = lane; jp < pieces; jp += 32) mx = fmaxf(mx, slot_of(jp)[G * kHeadDim + g]);
+  constexpr int kB = 8;
+  float mrun = -INFINITY, lrun = 0.f;
+  float2 arun = make_float2(0.f, 0.f);
+  for (int j0 = 0; j0 < pieces; j0 += kB) {
+    float mj[kB], lj[kB];
+    float2 aj[kB];
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
-  float lsum = 0.f;
-  float2 acc = make_float2(0.f, 0.f);
-  for (int j0 = 0; j0 < pieces; j0 += 32) {
-    const int jp = j0 + lane;
-    float w = 0.f;
-    if (jp < pieces) {
-      const float* q = slot_of(jp);
-      const float mj = q[G * kHeadDim + g];
-      w = (mj == -INFINITY) ? 0.f : fast_exp2(mj - mx);
-      lsum += w * q[G * kHeadDim + G + g];
+    for (int u = 0; u < kB; ++u) {
+      const int jp = j0 + u;
+      if (jp < pieces) {
+        const int slot = 2 * (r0 + jp) + ((jp == 0 && r0_mid) ? 1 : 0);
+        const float* sp = slots + static_cast<size_t>(slot) * kSF;
+        mj[u] = sp[G * kHeadDim + g];
+        lj[u] = sp[G * kHeadDim + G + g];
+        aj[u] = reinterpret_cast<const float2*>(sp + g * kHeadDim)[lane];
+      } else {
+        mj[u] = -INFINITY;
+        lj[u] = 0.f;
+        aj[u] = make_float2(0.f, 0.f);
+      }
     }
-    const int n = min(32, pieces - j0);
-#pragma unroll 8
-    for (int t = 0; t < n; ++t) {
-      const float wt = __shfl_sync(kFull, w, t);
-      const float2 a = reinterpret_cast<const float2*>(slot_of(j0 + t) + g * kHeadDim)[lane];
-      acc.x += wt * a.x;
-      acc.y += wt * a.y;
+#pragma unroll
+    for (int u = 0; u < kB; ++u) {
+      const float mn = fmaxf(mrun, mj[u]);
+      if (mn == -INFINITY) continue;  // no token seen yet on either side
+      const float wa = fast_exp2(mrun - mn), wb = fast_exp2(mj[u] - mn);
+      lrun = lrun * wa + lj[u] * wb;
+      arun.x = arun.x * wa + aj[u].x * wb;
+      arun.y = arun.y * wa + aj[u].y * wb;
+      mrun = mn;
     }
   }
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) lsum += __shfl_xor_sync(kFull, lsum, o);
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  reinterpret_cast<float2*>(out_row)[lane] = make_float2(acc.x * inv, acc.y * inv);
+  const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
+  reinterpret_cast<float2*>(out_row)[lane] = make_float2(arun.x * inv, arun.y * inv);
 }
 
 // Step mode, first page of a piece: rotate the group's raw q rows at the
@@ -354,11 +363,15 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   const void* map = &kv_map;
 
   // Sequence lengths (invalid ones become empty) and the page prefix sums.
+  // Everything before grid_dependency_wait() touches only shared memory, so
+  // it overlaps the end of the previous kernel in the stream.
   if (tid == 0) s_bad_len = 0;
   if (lane == 0)
     for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
   fence_mbar_init();
   __syncthreads();
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int cap = p.max_blocks * kPage;
   for (int b = tid; b < p.batch; b += kT) {
     int n = p.seq_lens[b];
@@ -395,9 +408,42 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   const int n_items = s_pre[p.batch] * p.hkv;
   if (n_items == 0) return;
   const int nwarps = gridDim.x * kW;
-  const int c = p.pages_per_split > 0 ? p.pages_per_split
-                                      : max(kMinRangePages, (n_items + nwarps - 1) / nwarps);
-  const int n_ranges = (n_items + c - 1) / c;
+  // Ranges: work units are laid out segment by segment (segment s = sequence
+  // * hkv + kv head, its pages items P_s .. P_s + np - 1): su units of fixed
+  // cost, then pu units per page, so page item i of segment s starts at unit
+  // pu * i + su * (s + 1). Range r covers units [r cw, (r + 1) cw) and owns
+  // the pages that start there. pages_per_split > 0 gives plain ranges of
+  // that many pages (pu = 1, su = 0), as does a work list too long for 32-bit
+  // unit arithmetic.
+  const int n_seg = p.batch * p.hkv;
+  const bool weighted = p.pages_per_split == 0 && n_items < (1 << 28);
+  const int pu = weighted ? kPageUnits : 1;
+  const int su = weighted ? kSegUnits : 0;
+  const int total_units = pu * n_items + su * n_seg;
+  const int cw = p.pages_per_split > 0
+                     ? p.pages_per_split
+                     : max(pu * kMinRangePages, (total_units + nwarps - 1) / nwarps);
+  const int n_ranges = (total_units + cw - 1) / cw;
+  // First page item starting at or after unit u (n_items if none). Sequence b
+  // starts at unit hkv (pu s_pre[b] + su b) and each of its segments spans
+  // pu np + su units: find b by bisection, then the segment and page directly.
+  auto item_at = [&](int u) -> int {
+    if (u >= total_units) return n_items;
+    int lo = 0, hi = p.batch - 1;  // largest b whose first unit is <= u
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.hkv * (pu * s_pre[mid] + su * mid) <= u) lo = mid; else hi = mid - 1;
+    }
+    const int np = s_pre[lo + 1] - s_pre[lo];
+    const int off = u - p.hkv * (pu * s_pre[lo] + su * lo);
+    const int seg_units = pu * np + su;
+    const int h = off / seg_units;
+    const int within = off - h * seg_units;
+    const int pg = within <= su ? 0 : (within - su + pu - 1) / pu;
+    return p.hkv * s_pre[lo] + h * np + pg;  // pg == np: the next segment's first page
+  };
+  // Range of the unit at which segment sg's page item i starts.
+  auto range_of = [&](int i, int sg) { return (pu * i + su * (sg + 1)) / cw; };
   const float qs = p.qscale;
 
   uint32_t phase_bits = 0;  // bit s: parity of the next completion of stage s
@@ -495,7 +541,10 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   float m_run = -INFINITY, l_run = 0.f;
 
   for (int r = blockIdx.x * kW + warp; r < n_ranges && !failed; r += nwarps) {
-    const int i0 = r * c, i1 = min(i0 + c, n_items);
+    // lane 0 finds where range r starts, lane 1 where it ends
+    const int i_lane = item_at((r + (lane & 1)) * cw);
+    const int i0 = __shfl_sync(kFull, i_lane, 0), i1 = __shfl_sync(kFull, i_lane, 1);
+    if (i0 >= i1) continue;
     describe(i0, i0, i1);
     cd_base = pd_base;
     cd_y = pd_y;
@@ -665,11 +714,12 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
         const int b = bh / p.hkv, h = bh - b * p.hkv;
         const int np = s_pre[b + 1] - s_pre[b];
         const int seg_start = p.hkv * s_pre[b] + h * np;
-        const int pieces = (seg_start + np - 1) / c - seg_start / c + 1;
+        const int r_first = range_of(seg_start, bh);
+        const int pieces = range_of(seg_start + np - 1, bh) - r_first + 1;
         const size_t row0 = static_cast<size_t>(bh) * G;  // = b*hq + h*G
         const bool complete = (start_pg == 0) && ((meta >> 9) == np - 1);
         if (kPartials) {
-          const int j = r - seg_start / c;
+          const int j = r - r_first;
           if (pieces > p.max_splits) {
             if (lane == 0) atomicOr(p.err, PKV_ERR_SPLITS);
           } else if (live) {
@@ -736,6 +786,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32)
   const int lane = threadIdx.x & 31;
   const int unit = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int seg = unit / G, g = unit - seg * G;
+  grid_dependency_wait();  // the decode's stores
+  grid_launch_dependents();
   if (seg >= segments) return;
   const int2 info = seg_info[seg];
   if (info.y < 2) return;
@@ -770,17 +822,30 @@ struct Launcher {
     return v;
   }
 
+  // Both kernels are launched with programmatic stream serialization: each
+  // may start (shared-memory set-up only) while its predecessor finishes, and
+  // waits for it before touching global memory.
   static cudaError_t launch(const CUtensorMap& map, const DecodeParams& p, int grid,
                             cudaStream_t stream, int mode) {
-    const size_t smem = smem_bytes<G>();
-    kernel(mode)<<<grid, Cfg<G>::kThreads, smem, stream>>>(map, p);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(Cfg<G>::kThreads);
+    cfg.dynamicSmemBytes = smem_bytes<G>();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel(mode), map, p);
     if (e != cudaSuccess || mode == kModePartials) return e;
     const int segments = p.batch * p.hkv;
     const int units = segments * G;
-    merge_kernel<G><<<(units + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32, 0, stream>>>(
-        p.seg_info, p.slots, p.out, segments);
-    return cudaGetLastError();
+    cfg.gridDim = dim3((units + kMergeWarps - 1) / kMergeWarps);
+    cfg.blockDim = dim3(kMergeWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, merge_kernel<G>, static_cast<const int2*>(p.seg_info),
+                              static_cast<const float*>(p.slots), p.out, segments);
   }
 };
 

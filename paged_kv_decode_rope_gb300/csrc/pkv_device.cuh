@@ -283,6 +283,19 @@ __device__ __forceinline__ bool rotated_bf16_fast(float a, float b, float ch, fl
   return true;
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream is still
+// running; grid_dependency_wait() blocks until that kernel has completed and
+// its memory operations are visible (a no-op without such a predecessor), so
+// every read of data an earlier kernel may write comes after it.
+// grid_launch_dependents() lets the next kernel in the stream start early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // L2-coherent loads for data another CTA wrote during this launch.
 __device__ __forceinline__ float ld_cg(const float* p) { return __ldcg(p); }
 __device__ __forceinline__ float2 ld_cg2(const float2* p) { return __ldcg(p); }
