@@ -17,13 +17,13 @@
 //    major. A persistent grid of one CTA per SM cuts the item list into equal
 //    contiguous ranges, one range per warp, so long and short sequences
 //    balance at page granularity with no host-side planning.
-//  * Each warp streams its range through its own 3-stage shared-memory ring:
-//    lane 0 issues TMA tensor loads (cp.async.bulk.tensor, 128-byte swizzle,
-//    completion counted in bytes on an mbarrier) of the head's K and V rows of
-//    each page in 8-row boxes (a partial last page loads only the boxes that
-//    hold valid rows), plus a 1-D bulk copy of the G query rows whenever a
-//    new (sequence, head) piece starts. No thread spends registers or issue
-//    slots on global loads.
+//  * Each warp streams its range through its own shared-memory ring of 2-3
+//    stages: lane 0 issues one TMA tensor load per page (cp.async.bulk.tensor,
+//    a 32-row box holding the head's 16 K rows then its 16 V rows, 128-byte
+//    swizzle, completion counted in bytes on an mbarrier, L2 evict-first
+//    since each page is read once), plus 1-D bulk copies of the G query rows
+//    whenever a new (sequence, head) piece starts. No thread spends registers
+//    or issue slots on global loads.
 //  * Per page the warp runs two m16n8k16 bf16 tensor-core products with fp32
 //    accumulation. Scores S[16 x 16 tokens] = Q K^T take Q as A with rows
 //    0-7 = the G heads' q (pre-scaled by scale*log2 e) rounded to bf16 and rows
@@ -52,8 +52,6 @@ namespace {
 
 constexpr int kScanOffset = 512;           // scan scratch (16 ints) after the mbarriers
 constexpr int kHdrBytes = 1024;            // mbarriers (<= 32 warp-stages * 8 B) + scan scratch
-constexpr int kBoxRows = 8;                // rows per TMA box (1 KiB, one 128-byte swizzle atom)
-constexpr int kBoxBytes = kBoxRows * kRowBytes;
 constexpr int kMinRangePages = 4;          // smallest automatic range (fewer, cheaper merges)
 // Automatic partition weights: a page costs kPageUnits, and each (sequence,
 // kv head) segment adds kSegUnits for the fixed work of its pieces (query
@@ -73,7 +71,7 @@ constexpr int kModeStep = 2;
 
 
 // Each warp owns a ring of Cfg::kStages stages. A stage is a 1 KiB-aligned 4 KiB
-// K/V block (8-row TMA boxes, 128-byte swizzle) plus a side buffer for the
+// K/V block (one 32-row TMA box, 128-byte swizzle) plus a side buffer for the
 // small rows a page may bring along: the group's fp32 q_rot rows (decode
 // mode) or, in step mode, the sequence's cos/sin row (32 frequencies, each
 // {cos_hi, cos_lo, sin_hi, sin_lo} in fp32), the group's raw bf16 q rows and
@@ -176,8 +174,10 @@ __device__ void scan_pages(const int* s_len, int* s_pre, int batch, int* s_warp)
   }
   if (lane == 31) s_warp[warp] = incl;
   __syncthreads();
-  int wofs = 0;
-  for (int w = 0; w < warp; ++w) wofs += s_warp[w];
+  // this warp's offset: the warp totals before it, summed across lanes
+  int wofs = lane < warp ? s_warp[lane] : 0;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) wofs += __shfl_xor_sync(kFull, wofs, o);
   int run = wofs + incl - local;
   for (int b = beg; b < end; ++b) {
     s_pre[b] = run;
@@ -491,9 +491,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     const int meta = __shfl_sync(kFull, pd_meta, t);
     const int bh = __shfl_sync(kFull, pd_bh, t);
     if (lane == 0) {
-      const int nv = meta & 31;
       const bool first = (meta >> 5) & 1;
-      const int nb = (nv + kBoxRows - 1) / kBoxRows;  // boxes holding valid rows
       const uint32_t bar = bar0 + 8 * st;
       const uint32_t dst = ring0 + st * kHeadPageBytes;
       const uint32_t side = side0 + st * C::kSideBytes;
@@ -502,19 +500,13 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
           kStep ? ((first || seg_last) ? kTrigBytes : 0u) + (first ? G * kRowBytes : 0u) +
                       (seg_last ? 2u * kRowBytes : 0u)
                 : (first ? C::kQBytes : 0u);
-      const uint32_t bytes = (y < 0 ? 0u : 2u * nb * kBoxBytes) + side_bytes;
+      const uint32_t bytes = (y < 0 ? 0u : static_cast<uint32_t>(kHeadPageBytes)) + side_bytes;
       if (bytes == 0) {
         mbar_arrive(bar);
       } else {
         mbar_arrive_expect_tx(bar, bytes);
-        if (y >= 0) {
-          tma_load_2d(dst, map, 0, y, bar);
-          tma_load_2d(dst + kHalfBytes, map, 0, y + kPage, bar);
-          if (nb == 2) {
-            tma_load_2d(dst + kBoxBytes, map, 0, y + kBoxRows, bar);
-            tma_load_2d(dst + kHalfBytes + kBoxBytes, map, 0, y + kPage + kBoxRows, bar);
-          }
-        }
+        if (y >= 0)  // the page's 16 K rows, then its 16 V rows
+          tma_load_2d_hint(dst, map, 0, y, bar, l2_policy_evict_first());
         if (kStep) {
           // the sequence's cos/sin row; the group's raw q rows on a piece's
           // first page; the new token's raw k and v rows on the sequence's last

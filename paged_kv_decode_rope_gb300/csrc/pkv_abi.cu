@@ -60,7 +60,8 @@ cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, 
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(PKV_HEAD_DIM),
                               static_cast<cuuint64_t>(num_pages) * num_kv_heads * 2 * PKV_PAGE_SIZE};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(PKV_HEAD_DIM) * 2};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(PKV_HEAD_DIM), 8};
+  // one box = 32 rows = one kv head's K and V rows of one page (4 KiB)
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(PKV_HEAD_DIM), 2 * PKV_PAGE_SIZE};
   const cuuint32_t elem[2] = {1, 1};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, storage, dims, strides, box, elem,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

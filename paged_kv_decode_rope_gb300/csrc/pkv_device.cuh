@@ -92,6 +92,24 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x
       : "memory");
 }
 
+// The same load with an L2 cache policy (from l2_policy_evict_first): the
+// pages stream through once per launch, so they should leave L2 before the
+// small data around them (split pieces, tables, query rows) does.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* map, int x, int y,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  return policy;
+}
+
 // Four 8x8 b16 matrices from shared memory; lanes 8m..8m+7 give matrix m's row addresses.
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {

@@ -10,7 +10,7 @@
 struct pkv_pool {
   // TMA descriptor of the pool seen as a 2-D bf16 tensor of 128-byte rows
   // (one token's K or V of one kv head): [num_pages*num_kv_heads*2*16][64],
-  // 8-row boxes, 128-byte swizzle.
+  // 32-row boxes (a kv head's K and V rows of one page), 128-byte swizzle.
   CUtensorMap kv_map;  // 64-byte aligned by its type
   void* storage;
   size_t storage_bytes;
