@@ -46,8 +46,8 @@ L2_BYTES = 129 * 10**6
 # is unchanged.
 TRAFFIC = {
     # workload -> (sha256 of gqa_decode.cu prefix, bytes per layer call: step kernel + merge kernel)
-    # profiles/gqa_decode_step_llama1b_b64_l16_u2048.md: 157.740 + 3.960 MB (step), 3.173 MB (merge)
-    "llama1b_b64_l16_u2048": ("04797bc8f8511cbc", 164873472),
+    # profiles/gqa_decode_step_llama1b_b64_l16_u2048.md: 158.085 + 3.327 MB (step), 3.216 MB (merge)
+    "llama1b_b64_l16_u2048": ("9c7bb20b5805ae9f", 164628736),
 }
 
 
@@ -369,7 +369,7 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4), "us_per_step": round(ms_step_max * 1e3, 2),
         "pct_of_hbm_peak": round(100 * value / ws / peak, 2), "pct_of_8tbs": round(100 * value / ws / 8000, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "storage": "bf16 KV pages; fp64 key rotation; fp32 softmax and accumulation",
+        "storage": "bf16 KV pages; new key rounded as fp64 rotation would round it; fp32 softmax and accumulation",
         "data": "synthetic (seeded; bf16 N(0,1) q/k/v and cache)", "config": _config(wl),
         "roofline": {"bound": "hbm",
                      "kernel": "paged_decode_step call per layer: gqa_decode_kernel (step mode) + merge_kernel",
