@@ -194,6 +194,14 @@ int paged_rope_cos_sin(const int32_t *positions, int batch, double rope_theta, v
  *   paged_gqa_decode_workspace_bytes().
  * A sequence whose new-token page id is bad gets no append and no attention
  * over that page (error bit set).
+ * Launch order: the kernels are launched with programmatic dependent launch.
+ * This call reads seq_lens, block_tables and the pool's existing pages before
+ * it waits for the kernel that precedes it in `stream`. That kernel must
+ * therefore not write them if it lets its dependents start early
+ * (griddepcontrol.launch_dependents / cudaTriggerProgrammaticLaunchCompletion).
+ * A kernel that does not trigger early, a memcpy, or this library's own
+ * kernels (which never write another layer's pages) are fine. q, k, v, the
+ * RoPE table and all outputs are accessed only after that wait.
  */
 int paged_decode_step(pkv_pool_t *pool, const void *q, const void *k, const void *v,
                       const void *rope_table, float *q_rot, float *out,

@@ -69,6 +69,11 @@ constexpr int kModeDecode = 0;
 constexpr int kModePartials = 1;
 constexpr int kModeStep = 2;
 
+// How much of a stage's copies one issue() call starts (see the kernel).
+constexpr int kIssueAll = 0;
+constexpr int kIssuePage = 1;
+constexpr int kIssueSide = 2;
+
 
 // Each warp owns a ring of Cfg::kStages stages. A stage is a 1 KiB-aligned 4 KiB
 // K/V block (one 32-row TMA box, 128-byte swizzle) plus a side buffer for the
@@ -363,15 +368,19 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   const void* map = &kv_map;
 
   // Sequence lengths (invalid ones become empty) and the page prefix sums.
-  // Everything before grid_dependency_wait() touches only shared memory, so
-  // it overlaps the end of the previous kernel in the stream.
+  // Everything before grid_dependency_wait() overlaps the end of the previous
+  // kernel in the stream. In decode and partials mode that is shared-memory
+  // set-up only. In step mode it also covers the sequence lengths, the block
+  // tables and the first pages of each warp's range, which the previous
+  // kernel must not write (see paged_decode_step); the step's query and new
+  // token rows and all of its stores come after the wait.
   if (tid == 0) s_bad_len = 0;
   if (lane == 0)
     for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
   fence_mbar_init();
   __syncthreads();
-  grid_dependency_wait();
   grid_launch_dependents();
+  if (!kStep) grid_dependency_wait();
   const int cap = p.max_blocks * kPage;
   for (int b = tid; b < p.batch; b += kT) {
     int n = p.seq_lens[b];
@@ -384,29 +393,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   __syncthreads();
   scan_pages<kT>(s_len, s_pre, p.batch, s_warp);
 
-  if (s_bad_len) {  // rows of invalid sequences: zero output (or zero split count)
-    if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, PKV_ERR_SEQ_LEN);
-    const int rows = p.batch * p.hq;
-    for (int idx = blockIdx.x * kT + tid; idx < rows; idx += gridDim.x * kT) {
-      if (s_len[idx / p.hq] != 0) continue;
-      if (kPartials) {
-        p.num_splits[idx] = 0;
-      } else {
-        if (idx % G == 0) p.seg_info[idx / G] = make_int2(0, 0);  // nothing to merge
-        if (kStep && p.q_rot_out) {
-          float4* qo = reinterpret_cast<float4*>(p.q_rot_out + static_cast<size_t>(idx) * kHeadDim);
-#pragma unroll
-          for (int k = 0; k < kHeadDim / 4; ++k) qo[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float4* o = reinterpret_cast<float4*>(p.out + static_cast<size_t>(idx) * kHeadDim);
-#pragma unroll
-        for (int k = 0; k < kHeadDim / 4; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-  }
-
   const int n_items = s_pre[p.batch] * p.hkv;
-  if (n_items == 0) return;
   const int nwarps = gridDim.x * kW;
   // Ranges: work units are laid out segment by segment (segment s = sequence
   // * hkv + kv head, its pages items P_s .. P_s + np - 1): su units of fixed
@@ -484,7 +471,10 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     if (__any_sync(kFull, bad) && lane == 0) atomicOr(p.err, PKV_ERR_PAGE_ID);
   };
 
-  auto issue = [&](int item, int st, int i0, int i1) {
+  // part: kIssueAll, or for the first stages of step mode kIssuePage before
+  // the dependency wait (page bytes expected, no arrival) and kIssueSide after
+  // it (the side rows and the stage's arrival).
+  auto issue = [&](int item, int st, int i0, int i1, int part = kIssueAll) {
     if (item >= pd_base + 32) describe(pd_base + 32, i0, i1);
     const int t = item - pd_base;
     const int y = __shfl_sync(kFull, pd_y, t);
@@ -500,12 +490,20 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
           kStep ? ((first || seg_last) ? kTrigBytes : 0u) + (first ? G * kRowBytes : 0u) +
                       (seg_last ? 2u * kRowBytes : 0u)
                 : (first ? C::kQBytes : 0u);
-      const uint32_t bytes = (y < 0 ? 0u : static_cast<uint32_t>(kHeadPageBytes)) + side_bytes;
+      const uint32_t page_bytes = y < 0 ? 0u : static_cast<uint32_t>(kHeadPageBytes);
+      if (part == kIssuePage) {
+        if (y >= 0) {
+          mbar_expect_tx(bar, page_bytes);
+          tma_load_2d_hint(dst, map, 0, y, bar, l2_policy_evict_first());
+        }
+        return;
+      }
+      const uint32_t bytes = (part == kIssueSide ? 0u : page_bytes) + side_bytes;
       if (bytes == 0) {
         mbar_arrive(bar);
       } else {
         mbar_arrive_expect_tx(bar, bytes);
-        if (y >= 0)  // the page's 16 K rows, then its 16 V rows
+        if (y >= 0 && part == kIssueAll)  // the page's 16 K rows, then its 16 V rows
           tma_load_2d_hint(dst, map, 0, y, bar, l2_policy_evict_first());
         if (kStep) {
           // the sequence's cos/sin row; the group's raw q rows on a piece's
@@ -532,12 +530,53 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   float o[8][4];      // O accumulator, dims 8d..8d+7: rows g8 (from P) and g8+8 (from P's remainder)
   float m_run = -INFINITY, l_run = 0.f;
 
-  for (int r = blockIdx.x * kW + warp; r < n_ranges && !failed; r += nwarps) {
-    // lane 0 finds where range r starts, lane 1 where it ends
+  // lane 0 finds where range r starts, lane 1 where it ends
+  auto range_bounds = [&](int r, int& i0, int& i1) {
     const int i_lane = item_at((r + (lane & 1)) * cw);
-    const int i0 = __shfl_sync(kFull, i_lane, 0), i1 = __shfl_sync(kFull, i_lane, 1);
+    i0 = __shfl_sync(kFull, i_lane, 0);
+    i1 = __shfl_sync(kFull, i_lane, 1);
+  };
+  bool pre_issued = false;  // step mode: the first range's first pages are on their way
+  if (kStep) {
+    const int r = blockIdx.x * kW + warp;
+    int i0 = 0, i1 = 0;
+    if (r < n_ranges) range_bounds(r, i0, i1);
+    if (i0 < i1) {
+      describe(i0, i0, i1);
+      for (int k = 0; k < C::kStages && i0 + k < i1; ++k) issue(i0 + k, k, i0, i1, kIssuePage);
+      pre_issued = true;
+    }
+    grid_dependency_wait();
+  }
+
+  if (s_bad_len) {  // rows of invalid sequences: zero output (or zero split count)
+    if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, PKV_ERR_SEQ_LEN);
+    const int rows = p.batch * p.hq;
+    for (int idx = blockIdx.x * kT + tid; idx < rows; idx += gridDim.x * kT) {
+      if (s_len[idx / p.hq] != 0) continue;
+      if (kPartials) {
+        p.num_splits[idx] = 0;
+      } else {
+        if (idx % G == 0) p.seg_info[idx / G] = make_int2(0, 0);  // nothing to merge
+        if (kStep && p.q_rot_out) {
+          float4* qo = reinterpret_cast<float4*>(p.q_rot_out + static_cast<size_t>(idx) * kHeadDim);
+#pragma unroll
+          for (int k = 0; k < kHeadDim / 4; ++k) qo[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float4* o = reinterpret_cast<float4*>(p.out + static_cast<size_t>(idx) * kHeadDim);
+#pragma unroll
+        for (int k = 0; k < kHeadDim / 4; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  }
+
+  if (n_items == 0) return;
+
+  for (int r = blockIdx.x * kW + warp; r < n_ranges && !failed; r += nwarps) {
+    int i0, i1;
+    range_bounds(r, i0, i1);
     if (i0 >= i1) continue;
-    describe(i0, i0, i1);
+    if (!pre_issued) describe(i0, i0, i1);
     cd_base = pd_base;
     cd_y = pd_y;
     cd_meta = pd_meta;
@@ -545,10 +584,11 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     {
       int st = stage;
       for (int k = 0; k < C::kStages && i0 + k < i1; ++k) {
-        issue(i0 + k, st, i0, i1);
+        issue(i0 + k, st, i0, i1, pre_issued ? kIssueSide : kIssueAll);
         st = (st + 1 == C::kStages) ? 0 : st + 1;
       }
     }
+    pre_issued = false;
     int start_pg = 0;
     bool first_in_range = true;
     for (int i = i0; i < i1; ++i) {
