@@ -84,6 +84,55 @@ class DecodeStep:
                 self.decode(layer, stream)
         return self.out
 
+    def run_from_host(self, host_in: dict, dev_in: dict, host_out: torch.Tensor,
+                      copy_streams=None) -> None:
+        """One step with its inputs in pinned host memory, layer-pipelined.
+
+        host_in / dev_in map "q", "k", "v" ([NL,...] bf16), "block_tables",
+        "seq_lens" and "positions" to pinned host tensors and their device
+        copies (dev_in's tables, lengths and positions must be the tensors
+        this step was built with). The step (fused path) runs on the current
+        stream. copy_streams[0] copies the per-step tables and layer 0's
+        q/k/v, then the first half of the remaining layers' q/k/v, then the
+        rest; the step waits for each group just before the first layer that
+        needs it (three waits, so the chain of decode launches keeps its
+        programmatic overlap elsewhere). copy_streams[1] copies each layer's
+        output back to host_out as soon as that layer is done. The current
+        stream finally waits for both copy streams.
+        """
+        cur = torch.cuda.current_stream()
+        cs_in, cs_out = copy_streams or (torch.cuda.Stream(), torch.cuda.Stream())
+        nl = self.num_layers
+        cs_in.wait_stream(cur)
+        cs_out.wait_stream(cur)
+        half = 1 + (nl - 1 + 1) // 2
+        groups = [g for g in ((0, 1), (1, min(half, nl)), (min(half, nl), nl)) if g[0] < g[1]]
+        ready = []
+        with torch.cuda.stream(cs_in):
+            for key in ("block_tables", "seq_lens", "positions"):
+                dev_in[key].copy_(host_in[key], non_blocking=True)
+            for lo, hi in groups:
+                for key in ("q", "k", "v"):
+                    dev_in[key][lo:hi].copy_(host_in[key][lo:hi], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cs_in)
+                ready.append((lo, ev))
+        ev_done = [torch.cuda.Event() for _ in range(nl)]
+        for layer in range(nl):
+            for lo, ev in ready:
+                if lo == layer:
+                    cur.wait_event(ev)
+            if layer == 0:
+                self.rope_table()
+            self.fused_layer(layer, dev_in["q"], dev_in["k"], dev_in["v"])
+            ev_done[layer].record(cur)
+        with torch.cuda.stream(cs_out):
+            for layer in range(nl):
+                cs_out.wait_event(ev_done[layer])
+                host_out[layer].copy_(self.out[layer], non_blocking=True)
+        cur.wait_stream(cs_out)
+        cur.wait_stream(cs_in)
+
     def error_bits(self, reset: bool = False) -> int:
         return B.pkv_get_error(self.pool, reset)
 
