@@ -104,3 +104,13 @@ def test_many_tiny_sequences_repeat_deterministic():
     b = dw.run().clone()
     assert torch.equal(a, b)
     dw.step.close()
+
+
+def test_contiguous_page_placement():
+    # every (layer, sequence) on consecutive pages: the contiguous-cache baseline's layout
+    cached = [0, 15, 16, 100, 700, 1500]
+    wl = workloads.build("contig", batch=len(cached), num_layers=3, num_q_heads=32, num_kv_heads=8,
+                         cached_lens=cached, rope_theta=500000.0, seed=21, sentinel=True,
+                         contiguous=True)
+    assert (wl.block_tables[0, 4, 1:44] - wl.block_tables[0, 4, :43] == 1).all()
+    full_check(wl)

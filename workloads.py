@@ -100,13 +100,17 @@ def _bf16_normal(gen: torch.Generator, shape, device) -> torch.Tensor:
 
 
 def _assign_pages(rng: np.random.Generator, seq_lens: np.ndarray, num_layers: int,
-                  num_pages: int, max_blocks: int) -> np.ndarray:
-    """Hand out physical pages from a shuffled free list, layer by layer."""
+                  num_pages: int, max_blocks: int, contiguous: bool = False) -> np.ndarray:
+    """Hand out physical pages from a shuffled free list, layer by layer.
+
+    With ``contiguous`` the free list is in order, so every (layer, sequence)
+    gets consecutive pages: a contiguous cache per sequence and layer, the
+    baseline against which paging's scattered placement is measured."""
     npages = (seq_lens.astype(np.int64) + PAGE_SIZE - 1) // PAGE_SIZE
     need = int(npages.sum()) * num_layers
     if need > num_pages:
         raise ValueError(f"pool of {num_pages} pages cannot hold {need} pages")
-    free = rng.permutation(num_pages).astype(np.int32)
+    free = (np.arange(num_pages) if contiguous else rng.permutation(num_pages)).astype(np.int32)
     bt = np.full((num_layers, len(seq_lens), max_blocks), -1, dtype=np.int32)
     cur = 0
     for layer in range(num_layers):
@@ -139,7 +143,7 @@ def build(name: str, *, batch: int, num_layers: int, num_q_heads: int, num_kv_he
           pool_slack: float = 1.1, seed: int = 0, device="cpu", sentinel: bool = False,
           big_key_frac: float = 0.0, max_blocks: int | None = None,
           block_tables: np.ndarray | None = None, description: str = "",
-          materialize: bool = True) -> Workload:
+          materialize: bool = True, contiguous: bool = False) -> Workload:
     """Assemble a workload from explicit cached lengths (host arrays).
 
     With ``materialize=False`` only the host-side structure (lengths, page
@@ -154,7 +158,7 @@ def build(name: str, *, batch: int, num_layers: int, num_q_heads: int, num_kv_he
     if num_pages is None:
         num_pages = max(1, int(math.ceil(need * pool_slack)))
     if block_tables is None:
-        block_tables = _assign_pages(rng, seq_lens, num_layers, num_pages, max_blocks)
+        block_tables = _assign_pages(rng, seq_lens, num_layers, num_pages, max_blocks, contiguous)
     pool = q = k = v = None
     if not materialize:
         return Workload(
@@ -191,13 +195,14 @@ def build(name: str, *, batch: int, num_layers: int, num_q_heads: int, num_kv_he
 LLAMA = dict(num_q_heads=32, num_kv_heads=8, rope_theta=500000.0)
 QWEN = dict(num_q_heads=14, num_kv_heads=2, rope_theta=1e6)
 
-#: The five named workloads. Keys say what each one is.
+#: The named workloads. Keys say what each one is.
 WORKLOADS = (
     "llama1b_b1_l1_len37",
     "llama1b_b8_l16_u512",
     "llama1b_b64_l16_u2048",
     "qwen05b_b32_l24_u1024_4096",
     "llama1b_b256_l16_skew",
+    "llama1b_b64_l16_u2048_contig",
 )
 
 
@@ -231,6 +236,15 @@ def make(name: str, seed: int = 0, device="cpu", sentinel: bool = False,
         return build(name, batch=8, num_layers=16, cached_lens=cached, num_pages=4096,
                      max_blocks=33,
                      description="Llama-3.2-1B shape, batch 8, 16 layers, L~U[1,512], 128 MiB pool", **common, **LLAMA)
+    if name == "llama1b_b64_l16_u2048_contig":
+        # The batch-64 workload (same lengths, same data draw) with every
+        # (layer, sequence) on consecutive pages: the contiguous-cache baseline.
+        cached = rng.integers(1, 2048, size=64, endpoint=True)
+        return build(name, batch=64, num_layers=16, cached_lens=cached, num_pages=81920,
+                     max_blocks=129, big_key_frac=0.1, contiguous=True,
+                     description="batch-64 workload with each (layer, sequence) on consecutive pages "
+                                 "(contiguous-cache baseline)",
+                     **common, **LLAMA)
     if name == "llama1b_b64_l16_u2048":
         cached = rng.integers(1, 2048, size=64, endpoint=True)
         # 2.5 GiB pool = 81920 pages of 32 KiB; 10% of key rows scaled by 8.
