@@ -4,8 +4,9 @@ The CUDA library behind include/pkv.h does the work: RoPE of the new token and
 its append into a shared BF16 page pool (``paged_kv_append_rope``), paged
 grouped-query decode attention with split-KV and a log-sum-exp merge
 (``paged_gqa_decode``), both fused into one step (``paged_decode_step``), and
-the standalone merge (``paged_kv_split_combine``). This package is the thin Python binding with the
-same names; it only marshals torch tensors into pointers.
+the standalone merge (``paged_kv_split_combine``), and the host page allocator
+with page-budget admission (``pkv_sched_*``, include/pkv_sched.h). This package
+is the thin Python binding with the same names; it only marshals arguments.
 """
 from ._binding import (  # noqa: F401
     ERR_PAGE_ID,
@@ -36,5 +37,18 @@ from ._binding import (  # noqa: F401
     paged_rope_cos_sin,
     pkv_get_error,
     pkv_last_cuda_error,
+)
+from .sched import (  # noqa: F401
+    PageScheduler,
+    pkv_sched_admit,
+    pkv_sched_block_row,
+    pkv_sched_budget,
+    pkv_sched_create,
+    pkv_sched_destroy,
+    pkv_sched_finish,
+    pkv_sched_grow,
+    pkv_sched_note_batch,
+    pkv_sched_stats,
+    pkv_sched_submit,
 )
 from .step import DecodeStep  # noqa: F401

@@ -42,6 +42,17 @@ _SIGNATURES = {
     "paged_kv_split_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "pkv_get_error": (_i, [_vp, ctypes.POINTER(_i), _i]),
     "pkv_last_cuda_error": (_i, []),
+    # include/pkv_sched.h (host only)
+    "pkv_sched_create": (_i, [ctypes.POINTER(_vp), _i, _i, _i, _i, ctypes.c_uint64]),
+    "pkv_sched_destroy": (_i, [_vp]),
+    "pkv_sched_submit": (_i, [_vp, _i, _i, ctypes.POINTER(_i)]),
+    "pkv_sched_budget": (_i, [_vp, _i, _i]),
+    "pkv_sched_admit": (_i, [_vp, _vp, _i]),
+    "pkv_sched_grow": (_i, [_vp, _i, _i]),
+    "pkv_sched_block_row": (_i, [_vp, _i, _i, _vp, _i]),
+    "pkv_sched_finish": (_i, [_vp, _i]),
+    "pkv_sched_note_batch": (_i, [_vp, _i]),
+    "pkv_sched_stats": (_i, [_vp, _vp]),
 }
 
 

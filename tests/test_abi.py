@@ -1,4 +1,4 @@
-"""The C-ABI library loads and exports every symbol include/pkv.h declares.
+"""The C-ABI library loads and exports every symbol include/*.h declares.
 
 No compute call runs here (no GPU needed): only host-side entry points and the
 argument checks that reject a call before any CUDA work.
@@ -12,12 +12,12 @@ import pytest
 from tests.golden.figures import page_figures
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pkv.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("pkv.h", "pkv_sched.h")]
 EINVAL, ENOSPC = -22, -28
 
 
 def _declared_functions():
-    text = open(HEADER, encoding="utf-8").read()
+    text = "\n".join(open(h, encoding="utf-8").read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*([a-z_0-9]+)\s*\(", text, flags=re.M)
     return sorted(set(names))
@@ -35,7 +35,8 @@ def test_header_declares_the_boundary():
     for required in ("kv_pool_create", "paged_kv_append_rope", "paged_gqa_decode",
                      "paged_kv_split_combine"):
         assert required in names
-    assert len(names) >= 10
+    assert "pkv_sched_admit" in names and "pkv_sched_grow" in names
+    assert len(names) >= 20
 
 
 def test_library_exports_every_declared_symbol(lib):
