@@ -267,3 +267,53 @@ def make(name: str, seed: int = 0, device="cpu", sentinel: bool = False,
                      description="Llama-3.2-1B shape, batch 256, 16 layers, 230 x U[16,256] + 26 x U[1024,2048]",
                      **common, **LLAMA)
     raise KeyError(name)
+
+
+# ---------------------------------------------------------------------------
+# Multi-step decode traces (continuous batching over the page pool)
+
+
+@dataclasses.dataclass
+class TraceRequest:
+    """One request of a synthetic trace: prompt_len cached tokens after its
+    (stand-in) prefill, at most max_new generated tokens, and the number it
+    actually generates before stopping (<= max_new; early stop when smaller)."""
+    prompt_len: int
+    max_new: int
+    stop_after: int
+
+
+def trace_requests(n: int, seed: int, prompt_range=(1, 512), new_range=(1, 256),
+                   early_stop_frac: float = 0.3) -> list[TraceRequest]:
+    """n seeded requests: prompts and output budgets uniform in the ranges; a
+    fraction stops early at a uniform point of its budget."""
+    rng = np.random.default_rng([seed, 0x7ACE])
+    out = []
+    for _ in range(n):
+        p = int(rng.integers(prompt_range[0], prompt_range[1], endpoint=True))
+        m = int(rng.integers(new_range[0], new_range[1], endpoint=True))
+        stop = int(rng.integers(1, m, endpoint=True)) if rng.random() < early_stop_frac else m
+        out.append(TraceRequest(p, m, stop))
+    return out
+
+
+def trace_prompt_kv(seed: int, request: int, num_layers: int, num_kv_heads: int,
+                    prompt_len: int) -> torch.Tensor:
+    """The K/V a request's prefill leaves in its prompt slots: bf16 N(0,1)
+    [num_layers][num_kv_heads][2 (K, V)][prompt_len][64], on the CPU."""
+    gen = torch.Generator()
+    gen.manual_seed(hash((seed, request, 0x9E)) & 0x7FFFFFFF)
+    return _bf16_normal(gen, (num_layers, num_kv_heads, 2, prompt_len, HEAD_DIM), "cpu")
+
+
+def trace_step_qkv(seed: int, request: int, step: int, num_layers: int, num_q_heads: int,
+                   num_kv_heads: int):
+    """The new token's q, k, v of one request at one of its decode steps:
+    bf16 N(0,1) [num_layers][H][64] each, on the CPU; independent of which
+    other requests share the batch."""
+    gen = torch.Generator()
+    gen.manual_seed(hash((seed, request, step, 0x51)) & 0x7FFFFFFF)
+    q = _bf16_normal(gen, (num_layers, num_q_heads, HEAD_DIM), "cpu")
+    k = _bf16_normal(gen, (num_layers, num_kv_heads, HEAD_DIM), "cpu")
+    v = _bf16_normal(gen, (num_layers, num_kv_heads, HEAD_DIM), "cpu")
+    return q, k, v
