@@ -52,6 +52,10 @@ def lib():
             L.oracle_gqa_decode_split.restype = _c_int
             L.oracle_lse_combine.argtypes = [_f64p, _f64p, _i32p, _c_int, _c_int, _c_int, _f64p]
             L.oracle_lse_combine.restype = None
+            L.oracle_prefill.argtypes = [_u16p, _c_long, _c_int, _c_int, _c_int, _u16p, _u16p, _u16p,
+                                         _i32p, _c_int, _i32p, _i32p, _c_int, _c_int, _c_double,
+                                         _c_double, _f64p, _f64p]
+            L.oracle_prefill.restype = _c_int
             _lib = L
     return _lib
 
@@ -130,6 +134,29 @@ def gqa_decode(pool_u16: np.ndarray, *, num_kv_heads: int, q_rot, block_tables, 
     _check(rc, "gqa_decode")
     return out
 
+
+
+def prefill(pool_u16: np.ndarray, *, num_kv_heads: int, q, k, v, block_tables, max_blocks: int,
+            cu_tokens, start_pos, num_q_heads: int, theta: float, scale: float,
+            head_dim: int = 64, page_size: int = 16):
+    """Chunked causal prefill (appends into ``pool_u16`` in place). q [T,Hq,D],
+    k/v [T,Hkv,D] bf16 bits; cu_tokens [B+1], start_pos [B]. Returns
+    (q_rot [T,Hq,D], out [T,Hq,D]) in fp64."""
+    assert pool_u16.dtype == np.uint16 and pool_u16.flags.c_contiguous
+    page_elems = 2 * num_kv_heads * page_size * head_dim
+    num_pages = pool_u16.size // page_elems
+    cu = _i32(cu_tokens)
+    total = int(cu[-1])
+    batch = len(cu) - 1
+    q_rot = np.zeros((total, num_q_heads, head_dim), dtype=np.float64)
+    out = np.zeros((total, num_q_heads, head_dim), dtype=np.float64)
+    rc = lib().oracle_prefill(pool_u16.reshape(-1), num_pages, num_kv_heads, head_dim, page_size,
+                              _u16(q).reshape(-1), _u16(k).reshape(-1), _u16(v).reshape(-1),
+                              _i32(block_tables).reshape(-1), max_blocks, cu, _i32(start_pos),
+                              batch, num_q_heads, float(theta), float(scale), q_rot.reshape(-1),
+                              out.reshape(-1))
+    _check(rc, "prefill")
+    return q_rot, out
 
 def gqa_decode_split(pool_u16: np.ndarray, *, num_kv_heads: int, q_rot, block_tables,
                      max_blocks: int, seq_lens, batch: int, num_q_heads: int, scale: float,

@@ -291,6 +291,48 @@ done:
 	return rc;
 }
 
+/* [P3] feature list: "prefill fills prompt pages" and the dense causal
+ * prefill item; RoPE per [P2]. Chunked prefill of `batch` sequences: sequence
+ * b holds start_pos[b] cached tokens and brings the chunk of tokens
+ * cu_tokens[b] .. cu_tokens[b+1]-1 (rows of q, k, v, q_rot and out), at
+ * positions start_pos[b], start_pos[b]+1, ... Every chunk token is rotated
+ * and appended exactly as oracle_append_rope appends one decode token; then
+ * the queries of chunk token t attend causally, over the first
+ * start_pos[b] + t + 1 tokens of the sequence (the cached ones, the chunk's
+ * earlier tokens and itself), exactly as oracle_gqa_decode attends for one
+ * sequence of that length. */
+int oracle_prefill(uint16_t *pool, long num_pages, int num_kv_heads, int head_dim,
+		   int page_size, const uint16_t *q, const uint16_t *k, const uint16_t *v,
+		   const int32_t *block_tables, int max_blocks, const int32_t *cu_tokens,
+		   const int32_t *start_pos, int batch, int num_q_heads, double theta,
+		   double scale, double *q_rot, double *out)
+{
+	int rc = 0;
+	for (int pass = 0; pass < 2 && !rc; pass++) {
+		for (int b = 0; b < batch && !rc; b++) {
+			const int32_t *row = block_tables + (size_t)b * max_blocks;
+			if (cu_tokens[b + 1] < cu_tokens[b] || start_pos[b] < 0)
+				return -1;
+			for (int idx = cu_tokens[b]; idx < cu_tokens[b + 1] && !rc; idx++) {
+				int32_t pos = start_pos[b] + (idx - cu_tokens[b]);
+				int32_t len = pos + 1;
+				size_t qo = (size_t)idx * num_q_heads * head_dim;
+				size_t ko = (size_t)idx * num_kv_heads * head_dim;
+				if (pass == 0)
+					rc = oracle_append_rope(pool, num_pages, num_kv_heads, head_dim,
+								page_size, q + qo, k + ko, v + ko,
+								q_rot + qo, row, max_blocks, &len, &pos, 1,
+								num_q_heads, theta);
+				else
+					rc = oracle_gqa_decode(pool, num_pages, num_kv_heads, head_dim,
+							       page_size, q_rot + qo, row, max_blocks,
+							       &len, 1, num_q_heads, scale, out + qo);
+			}
+		}
+	}
+	return rc;
+}
+
 /*
  * Split-KV form (flash-decoding; not on the pages, defined by its closed
  * form): the tokens of each (b, i) row are cut into consecutive splits of
