@@ -209,6 +209,46 @@ int paged_decode_step(pkv_pool_t *pool, const void *q, const void *k, const void
                       int batch, int num_q_heads, float scale, int pages_per_split,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Device bytes of workspace paged_prefill needs for these sizes on the
+ * current device (0 for invalid sizes).
+ */
+size_t paged_prefill_workspace_bytes(int total_tokens, int num_q_heads, int num_kv_heads,
+                                     int max_blocks);
+
+/*
+ * Chunked causal prefill into the pool. ("Hours of YouTube …": prefill fills
+ * the prompt pages, the dense causal prefill item; RoPE per "手写LLM推理引擎…"
+ * section 3.2.) Sequence b holds start_pos[b] cached tokens and brings the
+ * chunk of tokens cu_tokens[b] .. cu_tokens[b+1]-1 (rows of q, k, v, q_rot and
+ * out) at positions start_pos[b], start_pos[b]+1, ...:
+ *   - every chunk token's k is rotated and stored, with its v, at its position
+ *     in its sequence's pages, with the bytes paged_kv_append_rope would store
+ *     for a decode token at that position;
+ *   - q_rot is its rotated q;
+ *   - out is the attention of each of its query heads over the sequence's
+ *     first start_pos[b] + t + 1 tokens (causal: the cached ones, the chunk's
+ *     earlier tokens and itself), as paged_gqa_decode computes it.
+ *   q            bf16 [total_tokens][num_q_heads][64];  k, v bf16 [total_tokens][num_kv_heads][64]
+ *   q_rot, out   fp32 [total_tokens][num_q_heads][64] out
+ *   block_tables int32 [batch][max_blocks], the pages of every token up to
+ *                start_pos[b] + chunk length assigned;  cu_tokens int32 [batch+1]
+ *                (cu_tokens[0] = 0, non-decreasing, cu_tokens[batch] = total_tokens);
+ *                start_pos int32 [batch] (>= 0)
+ *   workspace    device memory of at least paged_prefill_workspace_bytes(),
+ *                256-byte aligned, contents irrelevant
+ * Launches an expansion kernel, the append kernel and the decode (+ merge)
+ * kernels on `stream`: each chunk token is a one-token sequence of its own
+ * causal length. Tokens of a malformed chunk (cu_tokens decreasing, a
+ * negative start, or a position past max_blocks*16) are not stored, their rows
+ * are zeroed and PKV_ERR_SEQ_LEN is set.
+ */
+int paged_prefill(pkv_pool_t *pool, const void *q, const void *k, const void *v, float *q_rot,
+                  float *out, const int32_t *block_tables, int max_blocks,
+                  const int32_t *cu_tokens, const int32_t *start_pos, int batch, int total_tokens,
+                  int num_q_heads, double rope_theta, float scale, void *workspace,
+                  size_t workspace_bytes, void *stream);
+
 /* Bytes of the fixed device array paged_gqa_decode_no_alloc uses as workspace. */
 #define PKV_NO_ALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -40,6 +40,9 @@ _SIGNATURES = {
     "paged_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp,
                                _sz, _vp]),
     "paged_kv_split_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
+    "paged_prefill_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "paged_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _d, _f, _vp,
+                           _sz, _vp]),
     "pkv_get_error": (_i, [_vp, ctypes.POINTER(_i), _i]),
     "pkv_last_cuda_error": (_i, []),
     # include/pkv_sched.h (host only)
@@ -258,6 +261,38 @@ def paged_decode_step(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.T
         float(scale), pages_per_split, _dev(workspace, torch.uint8, "workspace", 1),
         workspace.numel(), _stream(stream))
     _check("paged_decode_step", rc)
+
+
+def paged_prefill_workspace_bytes(total_tokens: int, num_q_heads: int, num_kv_heads: int,
+                                  max_blocks: int) -> int:
+    return lib().paged_prefill_workspace_bytes(total_tokens, num_q_heads, num_kv_heads, max_blocks)
+
+
+def alloc_prefill_workspace(total_tokens: int, num_q_heads: int, num_kv_heads: int,
+                            max_blocks: int, device=None) -> torch.Tensor:
+    n = paged_prefill_workspace_bytes(total_tokens, num_q_heads, num_kv_heads, max_blocks)
+    if n == 0:
+        raise ValueError("invalid prefill sizes")
+    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def paged_prefill(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+                  q_rot: torch.Tensor, out: torch.Tensor, block_tables: torch.Tensor,
+                  cu_tokens: torch.Tensor, start_pos: torch.Tensor, rope_theta: float, scale: float,
+                  workspace: torch.Tensor, stream=None) -> None:
+    """Chunked causal prefill. q [T,Hq,64], k/v [T,Hkv,64] bf16; q_rot/out [T,Hq,64]
+    fp32 out; block_tables [B,max_blocks], cu_tokens [B+1], start_pos [B] int32."""
+    total, hq = q.shape[0], q.shape[1]
+    batch = block_tables.shape[0]
+    rc = lib().paged_prefill(
+        pool.handle, _dev(q, torch.bfloat16, "q", 3), _dev(k, torch.bfloat16, "k", 3),
+        _dev(v, torch.bfloat16, "v", 3), _dev(q_rot, torch.float32, "q_rot", 3),
+        _dev(out, torch.float32, "out", 3), _dev(block_tables, torch.int32, "block_tables", 2),
+        block_tables.shape[1], _dev(cu_tokens, torch.int32, "cu_tokens", 1),
+        _dev(start_pos, torch.int32, "start_pos", 1), batch, total, hq, float(rope_theta),
+        float(scale), _dev(workspace, torch.uint8, "workspace", 1), workspace.numel(),
+        _stream(stream))
+    _check("paged_prefill", rc)
 
 
 def decode_max_splits(max_blocks: int, pages_per_split: int) -> int:

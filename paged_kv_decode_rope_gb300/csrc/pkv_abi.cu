@@ -271,6 +271,68 @@ int paged_decode_step(pkv_pool_t* pool, const void* q, const void* k, const void
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
 
+size_t paged_prefill_workspace_bytes(int total_tokens, int num_q_heads, int num_kv_heads,
+                                     int max_blocks) {
+  if (total_tokens < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads ||
+      max_blocks < 1)
+    return 0;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess) return 0;
+  const int sms = pkv::device_sm_count(device);
+  if (sms < 1) return 0;
+  return pkv::prefill_workspace_bytes(total_tokens, num_q_heads, num_kv_heads, max_blocks, sms);
+}
+
+int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v, float* q_rot,
+                  float* out, const int32_t* block_tables, int max_blocks,
+                  const int32_t* cu_tokens, const int32_t* start_pos, int batch, int total_tokens,
+                  int num_q_heads, double rope_theta, float scale, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  if (!decode_shape_ok(pool, total_tokens, num_q_heads, max_blocks) || batch < 0 ||
+      total_tokens < 0 || !(rope_theta > 0.0) || !std::isfinite(rope_theta) ||
+      !std::isfinite(scale))
+    return -EINVAL;
+  if (total_tokens == 0) return 0;
+  if (batch < 1) return -EINVAL;
+  if (!q || !k || !v || !q_rot || !out || !block_tables || !cu_tokens || !start_pos || !workspace)
+    return -EINVAL;
+  if (!aligned16(q_rot) || !aligned16(out) || !aligned16(v) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return -EINVAL;
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int sms = pkv::device_sm_count(device);
+  const size_t need = paged_prefill_workspace_bytes(total_tokens, num_q_heads, pool->num_kv_heads,
+                                                    max_blocks);
+  if (sms < 1 || need == 0 || workspace_bytes < need) return -EINVAL;
+  pkv::PrefillLaunch a;
+  a.kv_map = &pool->kv_map;
+  a.pool = static_cast<const uint8_t*>(pool->storage);
+  a.num_pages = pool->num_pages;
+  a.num_kv_heads = pool->num_kv_heads;
+  a.q = static_cast<const uint16_t*>(q);
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.q_rot = q_rot;
+  a.out = out;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks;
+  a.cu_tokens = cu_tokens;
+  a.start_pos = start_pos;
+  a.batch = batch;
+  a.total_tokens = total_tokens;
+  a.num_q_heads = num_q_heads;
+  a.rope_theta = rope_theta;
+  a.scale = scale;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.sm_count = sms;
+  a.err = pool->d_err;
+  e = pkv::launch_prefill(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
 int paged_gqa_decode_partials(const pkv_pool_t* pool, const float* q_rot,
                               const int32_t* block_tables, int max_blocks,
                               const int32_t* seq_lens, int batch, int num_q_heads, float scale,

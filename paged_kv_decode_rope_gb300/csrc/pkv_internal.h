@@ -75,6 +75,37 @@ struct DecodeLaunch {
   float* q_rot_out;
 };
 
+// Chunked causal prefill (prefill.cu): every chunk token becomes a one-token
+// virtual sequence for the append and decode launches.
+struct PrefillLaunch {
+  const CUtensorMap* kv_map;
+  const uint8_t* pool;
+  long long num_pages;
+  int num_kv_heads;
+  const uint16_t* q;  // bf16 [total_tokens][num_q_heads][64]
+  const uint16_t* k;  // bf16 [total_tokens][num_kv_heads][64]
+  const uint16_t* v;
+  float* q_rot;       // fp32 [total_tokens][num_q_heads][64] out
+  float* out;         // fp32 [total_tokens][num_q_heads][64] out
+  const int32_t* block_tables;  // [batch][max_blocks]
+  int max_blocks;
+  const int32_t* cu_tokens;     // [batch + 1]
+  const int32_t* start_pos;     // [batch]
+  int batch;
+  int total_tokens;
+  int num_q_heads;
+  double rope_theta;
+  float scale;
+  void* workspace;
+  size_t workspace_bytes;
+  int sm_count;
+  int* err;
+};
+
+size_t prefill_workspace_bytes(int total_tokens, int num_q_heads, int num_kv_heads,
+                               int max_blocks, int sm_count);
+cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream);
+
 // Largest batch one decode launch serves (sequence lengths and page prefix sums
 // are staged in shared memory); larger batches are cut into several launches.
 constexpr int kDecodeBatchChunk = 2048;

@@ -1,0 +1,103 @@
+"""GPU chunked causal prefill (paged_prefill) against the oracle's prefill.
+
+Chunks of new tokens after cached prefixes (start 0: a fresh prompt), across
+page boundaries, several sequences per call, both model shapes; the pool must
+match bit for bit, q_rot and the outputs within the decode tolerances.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_rope_gb300 as pkv
+from tests.parity import assert_close, u16
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(starts, lens, hq=32, hkv=8, theta=500000.0, seed=0, max_blocks=None):
+    rng = np.random.default_rng(seed)
+    gen = torch.Generator().manual_seed(seed)
+    ends = [s + n for s, n in zip(starts, lens)]
+    mb = max_blocks or max(1, -(-max(ends) // 16))
+    need = sum(-(-e // 16) for e in ends)
+    num_pages = need + 7
+    page_elems = 2 * hkv * 16 * 64
+    pool = torch.randn(num_pages * page_elems, generator=gen).to(torch.bfloat16)
+    perm = rng.permutation(num_pages).astype(np.int32)
+    bt = np.full((len(starts), mb), -1, np.int32)
+    cur = 0
+    for b, e in enumerate(ends):
+        n = -(-e // 16)
+        bt[b, :n] = perm[cur:cur + n]
+        cur += n
+    total = int(sum(lens))
+    q = torch.randn(total, hq, 64, generator=gen).to(torch.bfloat16)
+    k = torch.randn(total, hkv, 64, generator=gen).to(torch.bfloat16)
+    v = torch.randn(total, hkv, 64, generator=gen).to(torch.bfloat16)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    st = np.asarray(starts, np.int32)
+    scale = 1.0 / 8.0
+
+    host = u16(pool).copy()
+    want_qrot, want = oracle.prefill(host, num_kv_heads=hkv, q=u16(q), k=u16(k), v=u16(v),
+                                     block_tables=bt, max_blocks=mb, cu_tokens=cu, start_pos=st,
+                                     num_q_heads=hq, theta=theta, scale=scale)
+
+    dev = torch.device("cuda")
+    dpool = pool.to(dev)
+    kp = pkv.kv_pool_create(dpool, hkv)
+    q_rot = torch.empty(total, hq, 64, device=dev)
+    out = torch.empty(total, hq, 64, device=dev)
+    ws = pkv.alloc_prefill_workspace(total, hq, hkv, mb, device=dev)
+    pkv.paged_prefill(kp, q.to(dev), k.to(dev), v.to(dev), q_rot, out, torch.from_numpy(bt).to(dev),
+                      torch.from_numpy(cu).to(dev), torch.from_numpy(st).to(dev), theta, scale, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_error(kp) == 0
+    got_pool = u16(dpool)
+    mism = np.flatnonzero(got_pool != host)
+    assert mism.size == 0, f"{mism.size} pool elements differ, first at {mism[:5]}"
+    np.testing.assert_allclose(q_rot.cpu().numpy(), want_qrot, rtol=1e-5, atol=2e-5)
+    assert_close(out.cpu().numpy(), want, f"prefill starts={starts} lens={lens}")
+    kp.close()
+
+
+def test_fresh_prompt():
+    _run([0], [37])
+
+
+def test_chunk_after_cached_prefix_across_pages():
+    _run([100], [50], seed=1)
+
+
+def test_several_sequences_one_token_chunk_included():
+    _run([0, 17, 300, 64], [16, 1, 45, 33], seed=2)
+
+
+def test_qwen_shape():
+    _run([5, 0], [40, 70], hq=14, hkv=2, theta=1e6, seed=3)
+
+
+def test_long_prompt_splits_over_warps():
+    _run([0], [600], seed=4)
+
+
+def test_malformed_chunk_is_flagged_and_zeroed():
+    dev = torch.device("cuda")
+    hkv, hq = 8, 32
+    pool = torch.zeros(8 * 2 * hkv * 16 * 64, dtype=torch.bfloat16, device=dev)
+    kp = pkv.kv_pool_create(pool, hkv)
+    q = torch.randn(4, hq, 64, device=dev).to(torch.bfloat16)
+    k = torch.randn(4, hkv, 64, device=dev).to(torch.bfloat16)
+    v = torch.randn(4, hkv, 64, device=dev).to(torch.bfloat16)
+    bt = torch.arange(2, dtype=torch.int32, device=dev).view(1, 2)
+    q_rot = torch.empty(4, hq, 64, device=dev)
+    out = torch.full((4, hq, 64), 7.0, device=dev)
+    ws = pkv.alloc_prefill_workspace(4, hq, hkv, 2, device=dev)
+    # start 30 + 4 tokens needs positions up to 33 > 2 pages * 16: the last two are malformed
+    pkv.paged_prefill(kp, q, k, v, q_rot, out, bt, torch.tensor([0, 4], dtype=torch.int32, device=dev),
+                      torch.tensor([30], dtype=torch.int32, device=dev), 500000.0, 0.125, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_error(kp, reset=True) & pkv.ERR_SEQ_LEN
+    assert (out[2:] == 0).all() and torch.isfinite(out[:2]).all() and (out[:2] != 7.0).any()
+    kp.close()
