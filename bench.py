@@ -466,7 +466,7 @@ def run_prefill(args, ws, rank, local) -> int:
     st = torch.zeros(nb, dtype=torch.int32, device=dev)
     q_rot = torch.empty(nl, total, hq, 64, device=dev)
     out = torch.empty(nl, total, hq, 64, device=dev)
-    wsp = pkv.alloc_prefill_workspace(total, hq, hkv, mb, device=dev)
+    wsp = pkv.alloc_prefill_workspace(total, nb, mb, device=dev)
 
     def step():
         for layer in range(nl):

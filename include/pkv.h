@@ -210,11 +210,11 @@ int paged_decode_step(pkv_pool_t *pool, const void *q, const void *k, const void
                       void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Device bytes of workspace paged_prefill needs for these sizes on the
- * current device (0 for invalid sizes).
+ * Device bytes of workspace paged_prefill needs for total_tokens chunk tokens
+ * over batch sequences with max_blocks-entry block tables (0 for invalid
+ * sizes: a negative count, batch < 1 or max_blocks < 1).
  */
-size_t paged_prefill_workspace_bytes(int total_tokens, int num_q_heads, int num_kv_heads,
-                                     int max_blocks);
+size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks);
 
 /*
  * Chunked causal prefill into the pool. ("Hours of YouTube …": prefill fills
@@ -237,11 +237,14 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int num_q_heads, int num_
  *                start_pos int32 [batch] (>= 0)
  *   workspace    device memory of at least paged_prefill_workspace_bytes(),
  *                256-byte aligned, contents irrelevant
- * Launches an expansion kernel, the append kernel and the decode (+ merge)
- * kernels on `stream`: each chunk token is a one-token sequence of its own
- * causal length. Tokens of a malformed chunk (cu_tokens decreasing, a
- * negative start, or a position past max_blocks*16) are not stored, their rows
- * are zeroed and PKV_ERR_SEQ_LEN is set.
+ * Launches four kernels on `stream`: an expansion of the chunk tokens, the
+ * append kernel (every chunk token stored as a decode token would be), a tile
+ * plan, and a flash-attention kernel on tensor cores, one CTA per (sequence,
+ * kv head, tile of 32 tokens for up to 4 query heads a kv head, 16 above)
+ * that streams the sequence's pages once per tile. Tokens of a malformed
+ * chunk (cu_tokens decreasing, a negative start, or a position past
+ * max_blocks*16) are not stored, their rows are zeroed and PKV_ERR_SEQ_LEN is
+ * set.
  */
 int paged_prefill(pkv_pool_t *pool, const void *q, const void *k, const void *v, float *q_rot,
                   float *out, const int32_t *block_tables, int max_blocks,

@@ -40,7 +40,7 @@ _SIGNATURES = {
     "paged_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp,
                                _sz, _vp]),
     "paged_kv_split_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
-    "paged_prefill_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "paged_prefill_workspace_bytes": (_sz, [_i, _i, _i]),
     "paged_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _d, _f, _vp,
                            _sz, _vp]),
     "pkv_get_error": (_i, [_vp, ctypes.POINTER(_i), _i]),
@@ -263,14 +263,13 @@ def paged_decode_step(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.T
     _check("paged_decode_step", rc)
 
 
-def paged_prefill_workspace_bytes(total_tokens: int, num_q_heads: int, num_kv_heads: int,
-                                  max_blocks: int) -> int:
-    return lib().paged_prefill_workspace_bytes(total_tokens, num_q_heads, num_kv_heads, max_blocks)
+def paged_prefill_workspace_bytes(total_tokens: int, batch: int, max_blocks: int) -> int:
+    return lib().paged_prefill_workspace_bytes(total_tokens, batch, max_blocks)
 
 
-def alloc_prefill_workspace(total_tokens: int, num_q_heads: int, num_kv_heads: int,
-                            max_blocks: int, device=None) -> torch.Tensor:
-    n = paged_prefill_workspace_bytes(total_tokens, num_q_heads, num_kv_heads, max_blocks)
+def alloc_prefill_workspace(total_tokens: int, batch: int, max_blocks: int,
+                            device=None) -> torch.Tensor:
+    n = paged_prefill_workspace_bytes(total_tokens, batch, max_blocks)
     if n == 0:
         raise ValueError("invalid prefill sizes")
     return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))

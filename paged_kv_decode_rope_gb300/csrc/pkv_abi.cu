@@ -271,16 +271,9 @@ int paged_decode_step(pkv_pool_t* pool, const void* q, const void* k, const void
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
 
-size_t paged_prefill_workspace_bytes(int total_tokens, int num_q_heads, int num_kv_heads,
-                                     int max_blocks) {
-  if (total_tokens < 0 || num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads ||
-      max_blocks < 1)
-    return 0;
-  int device = 0;
-  if (cudaGetDevice(&device) != cudaSuccess) return 0;
-  const int sms = pkv::device_sm_count(device);
-  if (sms < 1) return 0;
-  return pkv::prefill_workspace_bytes(total_tokens, num_q_heads, num_kv_heads, max_blocks, sms);
+size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks) {
+  if (total_tokens < 0 || batch < 1 || max_blocks < 1) return 0;
+  return pkv::prefill_workspace_bytes(total_tokens, batch, max_blocks);
 }
 
 int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v, float* q_rot,
@@ -303,8 +296,7 @@ int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v,
   cudaError_t e = cudaGetDevice(&device);
   if (e != cudaSuccess) return cuda_fail(e);
   const int sms = pkv::device_sm_count(device);
-  const size_t need = paged_prefill_workspace_bytes(total_tokens, num_q_heads, pool->num_kv_heads,
-                                                    max_blocks);
+  const size_t need = paged_prefill_workspace_bytes(total_tokens, batch, max_blocks);
   if (sms < 1 || need == 0 || workspace_bytes < need) return -EINVAL;
   pkv::PrefillLaunch a;
   a.kv_map = &pool->kv_map;

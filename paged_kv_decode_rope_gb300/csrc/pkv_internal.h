@@ -102,8 +102,7 @@ struct PrefillLaunch {
   int* err;
 };
 
-size_t prefill_workspace_bytes(int total_tokens, int num_q_heads, int num_kv_heads,
-                               int max_blocks, int sm_count);
+size_t prefill_workspace_bytes(int total_tokens, int batch, int max_blocks);
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream);
 
 // Largest batch one decode launch serves (sequence lengths and page prefix sums

@@ -49,7 +49,7 @@ def _run(starts, lens, hq=32, hkv=8, theta=500000.0, seed=0, max_blocks=None):
     kp = pkv.kv_pool_create(dpool, hkv)
     q_rot = torch.empty(total, hq, 64, device=dev)
     out = torch.empty(total, hq, 64, device=dev)
-    ws = pkv.alloc_prefill_workspace(total, hq, hkv, mb, device=dev)
+    ws = pkv.alloc_prefill_workspace(total, len(starts), mb, device=dev)
     pkv.paged_prefill(kp, q.to(dev), k.to(dev), v.to(dev), q_rot, out, torch.from_numpy(bt).to(dev),
                       torch.from_numpy(cu).to(dev), torch.from_numpy(st).to(dev), theta, scale, ws)
     torch.cuda.synchronize()
@@ -78,8 +78,17 @@ def test_qwen_shape():
     _run([5, 0], [40, 70], hq=14, hkv=2, theta=1e6, seed=3)
 
 
-def test_long_prompt_splits_over_warps():
+def test_long_prompt_many_tiles():
     _run([0], [600], seed=4)
+
+
+def test_tiles_after_a_prefix_ending_mid_page():
+    _run([100, 7], [70, 33], seed=6)
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (12, 4), (10, 2), (12, 2), (64, 8)])
+def test_every_group_size(hq, hkv):
+    _run([3, 40], [35, 20], hq=hq, hkv=hkv, seed=7 + hq)
 
 
 def test_malformed_chunk_is_flagged_and_zeroed():
@@ -93,7 +102,7 @@ def test_malformed_chunk_is_flagged_and_zeroed():
     bt = torch.arange(2, dtype=torch.int32, device=dev).view(1, 2)
     q_rot = torch.empty(4, hq, 64, device=dev)
     out = torch.full((4, hq, 64), 7.0, device=dev)
-    ws = pkv.alloc_prefill_workspace(4, hq, hkv, 2, device=dev)
+    ws = pkv.alloc_prefill_workspace(4, 1, 2, device=dev)
     # start 30 + 4 tokens needs positions up to 33 > 2 pages * 16: the last two are malformed
     pkv.paged_prefill(kp, q, k, v, q_rot, out, bt, torch.tensor([0, 4], dtype=torch.int32, device=dev),
                       torch.tensor([30], dtype=torch.int32, device=dev), 500000.0, 0.125, ws)
