@@ -130,8 +130,9 @@ size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_h
 
 /*
  * Paged GQA decode attention for one layer, split-KV with a log-sum-exp
- * merge (two kernel launches on `stream`: the decode, then the merge of the
- * segments it split). ("Hours of YouTube …", direct paged decode attention
+ * merge, in one kernel launch on `stream`: the kernel merges the pieces of
+ * the (sequence, kv head) segments it split, in shared memory where the
+ * pieces ran in one CTA and through the workspace where they did not. ("Hours of YouTube …", direct paged decode attention
  * item: each query head streams its sequence's cached pages and accumulates
  * softmax-weighted values online in FP32, with no gathered prefix and no
  * stored scores. The split-KV form and its merge are flash-decoding, not on
@@ -144,9 +145,13 @@ size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_h
  *                evenly over the persistent grid; > 0: cut the work into
  *                ranges of this many pages (used to force splits in tests).
  *   workspace    device memory of at least paged_gqa_decode_workspace_bytes(),
- *                256-byte aligned, contents irrelevant (every call writes each
- *                part it reads). Calls that share a workspace must not overlap
- *                on the GPU.
+ *                256-byte aligned, ZERO-FILLED before its first use. It holds
+ *                the partial results of segments split between CTAs, and a
+ *                zero word means "not written in this call"; every call puts
+ *                the words it wrote back to zero (also when it sets
+ *                PKV_ERR_TIMEOUT), so a workspace is zeroed once, when it is
+ *                allocated. Calls that share a workspace must not overlap on
+ *                the GPU.
  * Constraints: num_q_heads = g * num_kv_heads with 1 <= g <= PKV_MAX_GROUP.
  * Rows of a sequence with a bad length are written as zeros.
  */
@@ -272,8 +277,8 @@ int paged_prefill(pkv_pool_t *pool, const void *q, const void *k, const void *v,
  *   thousand sequences on a 152-SM GPU).
  *   The first call on each device looks up the array's device address (with
  *   that device current); make that first call before any stream capture.
- *   The array keeps the previous call's contents; nothing in it has to start
- *   at zero, because every call writes each part of it that it reads. All
+ *   The array is zero when the library loads, and every call leaves it zero
+ *   again (paged_gqa_decode's workspace contract). All
  *   calls share the one array: calls that overlap on the GPU (other streams,
  *   other threads) race and give wrong results; order them on one stream.
  */

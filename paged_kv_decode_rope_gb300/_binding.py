@@ -186,11 +186,13 @@ def paged_gqa_decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads:
 
 def alloc_decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, max_blocks: int,
                            pages_per_split: int = 0, device=None) -> torch.Tensor:
-    """A workspace buffer of the required size (its contents need no initialisation)."""
+    """A zero-filled workspace buffer of the required size (the decode reads a
+    zero word as "not written in this call" and leaves every word it wrote at
+    zero again)."""
     n = paged_gqa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, max_blocks, pages_per_split)
     if n == 0:
         raise ValueError("invalid decode sizes")
-    return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
 
 
 def paged_gqa_decode(pool: KVPool, q_rot: torch.Tensor, out: torch.Tensor,

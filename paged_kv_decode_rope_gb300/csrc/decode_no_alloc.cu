@@ -6,8 +6,8 @@
 // (a cudaMalloc there would synchronise the device and bypass the manager's
 // accounting), or a plugin that a runtime only hands its input and output
 // buffers. For them this entry point takes no workspace argument and never
-// allocates: the decode's scratch (per-(sequence, kv head) arrival counters
-// and the split pieces' partial results) lives in g_decode_scratch, a
+// allocates: the decode's scratch (the partial results of segments split
+// between CTAs, zero between calls) lives in g_decode_scratch, a
 // file-scope array that every GPU which loads this library holds until the
 // process exits.
 #include <cerrno>

@@ -37,10 +37,14 @@
 //    swizzle.
 //  * A (sequence, head) segment that lies inside one warp range is finished
 //    by that warp. A segment cut by range boundaries leaves one piece per
-//    range (unnormalised accumulator, max and sum) in a workspace slot, and a
-//    second small kernel merges the pieces by their log-sum-exp, one warp per
-//    segment. Publishing a piece is a handful of plain stores: no atomics, no
-//    fences, and nothing ever waits on another warp.
+//    range (unnormalised accumulator, max and sum). The pieces are merged by
+//    their log-sum-exp in the same kernel, after the CTA's warps have all
+//    finished their ranges: pieces within the CTA through shared memory, and
+//    a segment that crosses into a neighbouring CTA (at most one at each end
+//    of a CTA's ranges) through workspace slots whose words say whether they
+//    have been written in this call, the CTA that finds its neighbours'
+//    partials there merging. Nothing ever waits on another CTA, and no second
+//    kernel (with its launch and dependency hand-off) is needed.
 #include <atomic>
 #include <cmath>
 
@@ -109,8 +113,8 @@ struct DecodeParams {
   int hq;
   float qscale;  // scale * log2(e): scores live in the base-2 domain
   int pages_per_split;
-  int2* seg_info;  // [batch][hkv]: split segments' (2*first range + mid flag, piece count)
-  float* slots;
+  float* slots;  // [group][2]: a group's partial of the segment crossing its start (0) / end (1);
+                 // zero between calls
   float* o_part;
   float* lse_part;
   int32_t* num_splits;
@@ -138,7 +142,8 @@ size_t smem_bytes() {
   // +1 KiB so the K/V rings can start on a 1 KiB boundary (128-byte swizzle
   // atoms); the side rings follow them.
   return ring_offset_bytes() + 1024 +
-         static_cast<size_t>(Cfg<G>::kWarps) * Cfg<G>::kStages * (kHeadPageBytes + Cfg<G>::kSideBytes);
+         static_cast<size_t>(Cfg<G>::kWarps) * Cfg<G>::kStages * (kHeadPageBytes + Cfg<G>::kSideBytes) +
+         static_cast<size_t>(Cfg<G>::kWarps) * Cfg<G>::kSlotFloats * sizeof(float);
 }
 
 struct Cursor {
@@ -192,51 +197,145 @@ __device__ void scan_pages(const int* s_len, int* s_pre, int batch, int* s_warp)
   __syncthreads();
 }
 
-// Log-sum-exp merge of head g of one split (sequence, kv head) segment, from
-// the workspace slots the decode's warps wrote. Piece jp came from range
-// r0 + jp; piece 0 sits in slot 2 r0 + 1 when it was that range's last
-// segment rather than its first. Lane l owns dims 2l, 2l+1 and folds the
-// pieces into a running (max, sum, accumulator), eight pieces at a time whose
-// loads (max, sum and the lane's two accumulator values) are all in flight
-// together: one dependent round trip for up to eight pieces.
-template <int G>
-__device__ __forceinline__ void merge_head(const float* slots, float* out_row, int r0, bool r0_mid,
-                                           int pieces, int g, int lane) {
-  constexpr int kSF = Cfg<G>::kSlotFloats;
-  constexpr int kB = 8;
-  float mrun = -INFINITY, lrun = 0.f;
-  float2 arun = make_float2(0.f, 0.f);
-  for (int j0 = 0; j0 < pieces; j0 += kB) {
-    float mj[kB], lj[kB];
-    float2 aj[kB];
+// A piece of a split (sequence, kv head) segment, as one lane holds it: the
+// head g8 = lane / 4 and its dims 8d + 2 tig, +1 (d = 0..7), with the running
+// max (base-2 domain) and sum. fold() merges another piece into it.
+struct Piece {
+  float m, l;
+  float2 acc[8];
+  __device__ __forceinline__ void fold(float mb, float lb, const float2 (&ab)[8]) {
+    const float mn = fmaxf(m, mb);
+    if (mn == -INFINITY) return;  // neither side has seen a token
+    const float wa = fast_exp2(m - mn), wb = fast_exp2(mb - mn);
+    l = l * wa + lb * wb;
 #pragma unroll
-    for (int u = 0; u < kB; ++u) {
-      const int jp = j0 + u;
-      if (jp < pieces) {
-        const int slot = 2 * (r0 + jp) + ((jp == 0 && r0_mid) ? 1 : 0);
-        const float* sp = slots + static_cast<size_t>(slot) * kSF;
-        mj[u] = sp[G * kHeadDim + g];
-        lj[u] = sp[G * kHeadDim + G + g];
-        aj[u] = reinterpret_cast<const float2*>(sp + g * kHeadDim)[lane];
-      } else {
-        mj[u] = -INFINITY;
-        lj[u] = 0.f;
-        aj[u] = make_float2(0.f, 0.f);
-      }
+    for (int d = 0; d < 8; ++d) {
+      acc[d].x = acc[d].x * wa + ab[d].x * wb;
+      acc[d].y = acc[d].y * wa + ab[d].y * wb;
     }
+    m = mn;
+  }
+};
+
+// Slot layout (shared memory and the workspace): the accumulator as float2
+// [d][head][tig] (dims 8d + 2tig, +1 of each head: a warp's 64-bit accesses
+// for one d cover consecutive words, free of bank conflicts), then G maxima,
+// then G sums.
+template <int G>
+__device__ __forceinline__ void store_piece(float* sp, const Piece& pc, int g8, int tig) {
+  if (g8 >= G) return;
+  float2* acc = reinterpret_cast<float2*>(sp);
 #pragma unroll
-    for (int u = 0; u < kB; ++u) {
-      const float mn = fmaxf(mrun, mj[u]);
-      if (mn == -INFINITY) continue;  // no token seen yet on either side
-      const float wa = fast_exp2(mrun - mn), wb = fast_exp2(mj[u] - mn);
-      lrun = lrun * wa + lj[u] * wb;
-      arun.x = arun.x * wa + aj[u].x * wb;
-      arun.y = arun.y * wa + aj[u].y * wb;
-      mrun = mn;
+  for (int d = 0; d < 8; ++d) acc[(d * G + g8) * 4 + tig] = pc.acc[d];
+  if (tig == 0) {
+    sp[G * kHeadDim + g8] = pc.m;
+    sp[G * kHeadDim + G + g8] = pc.l;
+  }
+}
+
+// Fold the k slots at sp, sp + stride, ... (in that order) into pc, as one
+// log-sum-exp combination: the maxima first, then the weighted sums, so that
+// the loads of all k slots are in flight together.
+template <int G>
+__device__ __forceinline__ void fold_run(Piece& pc, const float* sp, int stride, int k, int g8,
+                                         int tig) {
+  if (k <= 0 || g8 >= G) return;
+  float mx = pc.m;
+  for (int j = 0; j < k; ++j) mx = fmaxf(mx, sp[j * stride + G * kHeadDim + g8]);
+  if (mx == -INFINITY) return;  // no piece has seen a token
+  const float w0 = fast_exp2(pc.m - mx);
+  pc.l *= w0;
+#pragma unroll
+  for (int d = 0; d < 8; ++d) {
+    pc.acc[d].x *= w0;
+    pc.acc[d].y *= w0;
+  }
+  for (int j = 0; j < k; ++j) {
+    const float* q = sp + j * stride;
+    const float wj = fast_exp2(q[G * kHeadDim + g8] - mx);
+    pc.l += wj * q[G * kHeadDim + G + g8];
+    const float2* acc = reinterpret_cast<const float2*>(q);
+#pragma unroll
+    for (int d = 0; d < 8; ++d) {
+      const float2 a = acc[(d * G + g8) * 4 + tig];
+      pc.acc[d].x += wj * a.x;
+      pc.acc[d].y += wj * a.y;
     }
   }
-  const float inv = lrun > 0.f ? 1.f / lrun : 0.f;
-  reinterpret_cast<float2*>(out_row)[lane] = make_float2(arun.x * inv, arun.y * inv);
+  pc.m = mx;
+}
+
+// Workspace partials of segments that cross a group boundary. A word holds
+// the float's bits plus one, so that 0 (the zero-filled workspace, or a slot
+// reset by its merger) means "not written in this call"; bits 0xFFFFFFFF, the
+// one pattern that would wrap to 0, is a NaN that arithmetic never produces.
+template <int G>
+__device__ __forceinline__ void publish_piece(float* sp, const Piece& pc, int g8, int tig) {
+  if (g8 >= G) return;
+  uint32_t* w = reinterpret_cast<uint32_t*>(sp);
+#pragma unroll
+  for (int d = 0; d < 8; ++d) {
+    const int i = 2 * ((d * G + g8) * 4 + tig);
+    w[i] = __float_as_uint(pc.acc[d].x) + 1u;
+    w[i + 1] = __float_as_uint(pc.acc[d].y) + 1u;
+  }
+  if (tig == 0) {
+    w[G * kHeadDim + g8] = __float_as_uint(pc.m) + 1u;
+    w[G * kHeadDim + G + g8] = __float_as_uint(pc.l) + 1u;
+  }
+}
+
+// Fold the partials of groups g_first .. g_last of a segment into `all`, in
+// group order whichever CTA does it (so the result does not depend on which
+// one does). Group grp's partial is `own`; the others are read from the
+// workspace through L2. Returns whether every one of those words had been
+// written (all lanes agree).
+template <int G>
+__device__ __forceinline__ bool gather_groups(Piece& all, const Piece& own, const float* slots,
+                                              int stride, int grp, int g_first, int g_last, int g8,
+                                              int tig) {
+  all.m = -INFINITY;
+  all.l = 0.f;
+#pragma unroll
+  for (int d = 0; d < 8; ++d) all.acc[d] = make_float2(0.f, 0.f);
+  bool complete = true;
+  if (g8 < G) {
+    for (int gg = g_first; gg <= g_last; ++gg) {
+      if (gg == grp) {
+        all.fold(own.m, own.l, own.acc);
+        continue;
+      }
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(
+          slots + static_cast<size_t>(2 * gg + (gg == g_first ? 1 : 0)) * stride);
+      uint32_t raw[18];
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        const uint2 v = __ldcg(reinterpret_cast<const uint2*>(w) + (d * G + g8) * 4 + tig);
+        raw[2 * d] = v.x;
+        raw[2 * d + 1] = v.y;
+      }
+      raw[16] = __ldcg(w + G * kHeadDim + g8);
+      raw[17] = __ldcg(w + G * kHeadDim + G + g8);
+      float2 ab[8];
+#pragma unroll
+      for (int d = 0; d < 8; ++d) {
+        complete = complete && raw[2 * d] != 0u && raw[2 * d + 1] != 0u;
+        ab[d] = make_float2(__uint_as_float(raw[2 * d] - 1u), __uint_as_float(raw[2 * d + 1] - 1u));
+      }
+      complete = complete && raw[16] != 0u && raw[17] != 0u;
+      all.fold(__uint_as_float(raw[16] - 1u), __uint_as_float(raw[17] - 1u), ab);
+    }
+  }
+  return __all_sync(kFull, complete);
+}
+
+template <int G>
+__device__ __forceinline__ void store_output(float* out_row0, const Piece& pc, int g8, int tig) {
+  if (g8 >= G) return;
+  const float inv = pc.l > 0.f ? 1.f / pc.l : 0.f;
+  float2* dst = reinterpret_cast<float2*>(out_row0 + g8 * kHeadDim);
+#pragma unroll
+  for (int d = 0; d < 8; ++d) dst[4 * d + tig] = make_float2(pc.acc[d].x * inv, pc.acc[d].y * inv);
 }
 
 // Step mode, first page of a piece: rotate the group's raw q rows at the
@@ -557,7 +656,6 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
       if (kPartials) {
         p.num_splits[idx] = 0;
       } else {
-        if (idx % G == 0) p.seg_info[idx / G] = make_int2(0, 0);  // nothing to merge
         if (kStep && p.q_rot_out) {
           float4* qo = reinterpret_cast<float4*>(p.q_rot_out + static_cast<size_t>(idx) * kHeadDim);
 #pragma unroll
@@ -572,10 +670,23 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
 
   if (n_items == 0) return;
 
-  for (int r = blockIdx.x * kW + warp; r < n_ranges && !failed; r += nwarps) {
-    int i0, i1;
-    range_bounds(r, i0, i1);
-    if (i0 >= i1) continue;
+  // Ranges come in groups of kW, one range per warp of a CTA: group grp covers
+  // ranges grp kW .. grp kW + kW - 1. A segment split over ranges of one group
+  // is merged in shared memory when the group ends; one that crosses a group
+  // boundary (at most one at each end) goes through the workspace, and the
+  // last group to arrive merges it.
+  float* s_slots = reinterpret_cast<float*>(
+      smem + (ring_base - smem_addr(smem)) +
+      kW * C::kStages * (kHeadPageBytes + C::kSideBytes));
+  __shared__ int s_first_bh[kW];  // a range's first piece, if it continues a segment: its segment
+  __shared__ bool s_has_head[kW];  // a range's last piece holds page 0 of a segment that goes on
+  __shared__ int2 s_cont_groups;   // groups of the first and last pages of warp 0's continued segment
+  const int n_groups = (n_ranges + kW - 1) / kW;
+  for (int grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
+    const int r = grp * kW + warp;
+    int i0 = 0, i1 = 0;
+    if (r < n_ranges) range_bounds(r, i0, i1);
+    if (i0 < i1 && !failed) {
     if (!pre_issued) describe(i0, i0, i1);
     cd_base = pd_base;
     cd_y = pd_y;
@@ -766,31 +877,127 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
             }
           }
         } else if (complete) {
-          if (lane == 0) p.seg_info[bh] = make_int2(0, 1);  // final output written here
           if (live) {
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             float2* dst = reinterpret_cast<float2*>(p.out + (row0 + g8) * kHeadDim);
 #pragma unroll
             for (int d = 0; d < 8; ++d) dst[4 * d + tig] = make_float2(of[d].x * inv, of[d].y * inv);
           }
-        } else {
-          // A piece of a split (sequence, head): leave its unnormalised
-          // accumulator, max and sum in the range's slot for the merge kernel;
-          // the piece holding page 0 records where the pieces are.
-          float* sp = p.slots + static_cast<size_t>(2 * r + (first_in_range ? 0 : 1)) * C::kSlotFloats;
-          if (live) {
-            float2* acc = reinterpret_cast<float2*>(sp + g8 * kHeadDim);
+        } else if (first_in_range) {
+          // A split piece that opens the range: its unnormalised accumulator,
+          // max and sum wait in this warp's shared-memory slot for the group's
+          // merge. (A split piece that closes the range stays in registers.)
+          Piece pc;
+          pc.m = mh;
+          pc.l = lsum;
 #pragma unroll
-            for (int d = 0; d < 8; ++d) acc[4 * d + tig] = of[d];
-            if (tig == 0) {
-              sp[G * kHeadDim + g8] = mh;
-              sp[G * kHeadDim + G + g8] = lsum;
-            }
-          }
-          if (start_pg == 0 && lane == 0)
-            p.seg_info[bh] = make_int2(2 * r + (first_in_range ? 0 : 1), pieces);
+          for (int d = 0; d < 8; ++d) pc.acc[d] = of[d];
+          store_piece<G>(s_slots + warp * C::kSlotFloats, pc, g8, tig);
         }
       }
+    }
+    }  // this warp's range
+
+    if (!kPartials) {
+      // Which pieces this warp merges follows from the range bounds alone (not
+      // from how far the warp got), so every arrival below happens even after
+      // a timeout and the workspace slots return to zero. Everything that does not
+      // need the other warps' pieces is worked out before the barrier.
+      int first_bh = -1, head_bh = -1;  // continued segment at i0; segment whose page 0 is here and that goes on
+      int head_gf = 0, head_gl = 0;     // groups of the head segment's first and last pages
+      auto groups_of = [&](int sg, int& gf, int& gl) {
+        const int b = sg / p.hkv;
+        const int np = s_pre[b + 1] - s_pre[b];
+        const int seg_start = p.hkv * s_pre[b] + (sg - b * p.hkv) * np;
+        gf = range_of(seg_start, sg) / kW;
+        gl = range_of(seg_start + np - 1, sg) / kW;
+      };
+      if (i0 < i1) {
+        const Cursor c0 = locate(i0, s_pre, s_len, p.batch, p.hkv);
+        if (c0.pg > 0) first_bh = c0.b * p.hkv + c0.h;
+        const Cursor cl = locate(i1 - 1, s_pre, s_len, p.batch, p.hkv);
+        if (i1 - 1 - cl.pg >= i0 && cl.pg < cl.np - 1) {
+          head_bh = cl.b * p.hkv + cl.h;
+          groups_of(head_bh, head_gf, head_gl);
+        }
+      }
+      if (lane == 0) {
+        s_first_bh[warp] = first_bh;
+        s_has_head[warp] = head_bh >= 0;
+        if (warp == 0 && first_bh >= 0) {
+          int gf, gl;
+          groups_of(first_bh, gf, gl);
+          s_cont_groups = make_int2(gf, gl);
+        }
+      }
+      __syncthreads();  // every slot and s_first_bh of the group are written
+
+      // Merge segment sg: pc holds its piece of range grp kW + w, and the
+      // pieces of the ranges after it in the group wait in their warps' slots.
+      auto merge_segment = [&](int sg, Piece& pc, int w, int g_first, int g_last) {
+        // the run of following warps whose first piece continues sg
+        const int w2 = w + 1 + lane;
+        const unsigned run = __ballot_sync(kFull, w2 < kW && s_first_bh[w2 < kW ? w2 : 0] == sg);
+        const int k = __ffs(~run) - 1;
+        fold_run<G>(pc, s_slots + (w + 1) * C::kSlotFloats, C::kSlotFloats, k, g8, tig);
+        float* out_row0 = p.out + static_cast<size_t>(sg) * G * kHeadDim;
+        if (g_first == g_last) {  // the whole segment lies in this group
+          store_output<G>(out_row0, pc, g8, tig);
+          return;
+        }
+        // The segment's other groups leave their partials in the workspace.
+        // A CTA that finds them all there merges at once (one round trip: the
+        // usual case for the CTA that finishes last). Otherwise it leaves its
+        // own partial, fences, and looks again; of the CTAs that look after
+        // their fence, the last one in the fences' order sees every partial,
+        // so some CTA always merges (two may, with identical results). The
+        // merger puts the segment's slots back to zero for the next call.
+        Piece all;
+        float* my_slot = p.slots + static_cast<size_t>(2 * grp + (grp == g_first ? 1 : 0)) * C::kSlotFloats;
+        bool done = gather_groups<G>(all, pc, p.slots, C::kSlotFloats, grp, g_first, g_last, g8, tig);
+        if (!done) {
+          publish_piece<G>(my_slot, pc, g8, tig);
+          __threadfence();
+          __syncwarp();
+          done = gather_groups<G>(all, pc, p.slots, C::kSlotFloats, grp, g_first, g_last, g8, tig);
+        }
+        if (!done) return;
+        store_output<G>(out_row0, all, g8, tig);
+        for (int gg = g_first; gg <= g_last; ++gg) {
+          float* q = p.slots + static_cast<size_t>(2 * gg + (gg == g_first ? 1 : 0)) * C::kSlotFloats;
+          for (int i = lane; i < C::kSlotFloats; i += 32) q[i] = 0.f;
+        }
+      };
+      // The segment continued from the previous group (its pieces open warp 0's
+      // range and maybe the next ones) is merged by the last warp with no
+      // segment of its own to merge, so that no warp merges two.
+      const int first_bh0 = s_first_bh[0];
+      int b_warp = 0;
+      for (int w2 = kW - 1; w2 > 0; --w2)
+        if (!s_has_head[w2]) {
+          b_warp = w2;
+          break;
+        }
+      if (first_bh0 >= 0 && warp == b_warp) {
+        Piece pc;
+        pc.m = -INFINITY;
+        pc.l = 0.f;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) pc.acc[d] = make_float2(0.f, 0.f);
+        fold_run<G>(pc, s_slots, C::kSlotFloats, 1, g8, tig);
+        const int2 gg = s_cont_groups;
+        merge_segment(first_bh0, pc, 0, gg.x, gg.y);
+      }
+      if (head_bh >= 0) {  // this range's last piece, still in registers
+        Piece pc;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) pc.acc[d] = make_float2(o[d][0] + o[d][2], o[d][1] + o[d][3]);
+        pc.l = l_run + __shfl_xor_sync(kFull, l_run, 1);
+        pc.l += __shfl_xor_sync(kFull, pc.l, 2);
+        pc.m = m_run;
+        merge_segment(head_bh, pc, warp, head_gf, head_gl);
+      }
+      __syncthreads();  // the slots are free for the next group
     }
   }
 
@@ -805,27 +1012,6 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   }
 }
 
-
-// Merge of the split (sequence, kv head) segments the decode left in the
-// workspace: one warp per (segment, query head of its group); segments the
-// decode finished itself are skipped.
-constexpr int kMergeWarps = 8;
-
-template <int G>
-__global__ void __launch_bounds__(kMergeWarps * 32)
-    merge_kernel(const int2* __restrict__ seg_info, const float* __restrict__ slots,
-                 float* __restrict__ out, int segments) {
-  const int lane = threadIdx.x & 31;
-  const int unit = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-  const int seg = unit / G, g = unit - seg * G;
-  grid_dependency_wait();  // the decode's stores
-  grid_launch_dependents();
-  if (seg >= segments) return;
-  const int2 info = seg_info[seg];
-  if (info.y < 2) return;
-  merge_head<G>(slots, out + (static_cast<size_t>(seg) * G + g) * kHeadDim, info.x >> 1,
-                info.x & 1, info.y, g, lane);
-}
 
 template <int G>
 struct Launcher {
@@ -854,9 +1040,9 @@ struct Launcher {
     return v;
   }
 
-  // Both kernels are launched with programmatic stream serialization: each
-  // may start (shared-memory set-up only) while its predecessor finishes, and
-  // waits for it before touching global memory.
+  // Launched with programmatic stream serialization: the kernel may start
+  // while its predecessor in the stream finishes (see the kernel for what it
+  // does before its dependency wait).
   static cudaError_t launch(const CUtensorMap& map, const DecodeParams& p, int grid,
                             cudaStream_t stream, int mode) {
     cudaLaunchAttribute attr[1];
@@ -869,15 +1055,7 @@ struct Launcher {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel(mode), map, p);
-    if (e != cudaSuccess || mode == kModePartials) return e;
-    const int segments = p.batch * p.hkv;
-    const int units = segments * G;
-    cfg.gridDim = dim3((units + kMergeWarps - 1) / kMergeWarps);
-    cfg.blockDim = dim3(kMergeWarps * 32);
-    cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, merge_kernel<G>, static_cast<const int2*>(p.seg_info),
-                              static_cast<const float*>(p.slots), p.out, segments);
+    return cudaLaunchKernelEx(&cfg, kernel(mode), map, p);
   }
 };
 
@@ -930,9 +1108,8 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int 
     const long long need = (items + pages_per_split - 1) / pages_per_split;
     if (need > ranges) ranges = need;
   }
-  const size_t info = ((static_cast<size_t>(batch) * num_kv_heads * sizeof(int2) + 255) / 256) * 256;
-  const size_t slots = static_cast<size_t>(2 * ranges) * slot_floats_for(group) * sizeof(float);
-  return info + slots;
+  // two partial slots per group of ranges (a group has one range per warp of a CTA)
+  return static_cast<size_t>(2 * ranges) * slot_floats_for(group) * sizeof(float);
 }
 
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
@@ -949,8 +1126,6 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
   const int sms = device_sm_count(device);
   if (sms < 1) return cudaErrorInvalidDevice;
   const int grid = sms * bps;
-  const size_t info_bytes =
-      ((static_cast<size_t>(a.batch) * a.num_kv_heads * sizeof(int2) + 255) / 256) * 256;
   const double log2e = 1.4426950408889634;
   for (int b0 = 0; b0 < a.batch; b0 += kDecodeBatchChunk) {
     const int nb = a.batch - b0 < kDecodeBatchChunk ? a.batch - b0 : kDecodeBatchChunk;
@@ -966,10 +1141,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
     p.hq = a.num_q_heads;
     p.qscale = static_cast<float>(static_cast<double>(a.scale) * log2e);
     p.pages_per_split = a.pages_per_split;
-    p.seg_info = partials ? nullptr
-                          : static_cast<int2*>(a.workspace) + static_cast<size_t>(b0) * a.num_kv_heads;
-    p.slots = partials ? nullptr
-                       : reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + info_bytes);
+    p.slots = partials ? nullptr : static_cast<float*>(a.workspace);
     const size_t row0 = static_cast<size_t>(b0) * a.num_q_heads;
     p.o_part = partials ? a.o_part + row0 * a.max_splits * kHeadDim : nullptr;
     p.lse_part = partials ? a.lse_part + row0 * a.max_splits : nullptr;
