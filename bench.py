@@ -262,7 +262,8 @@ def run_ours(args, ws, rank, local):
     pos = torch.from_numpy(wl.positions).to(dev)
     step = pkv.DecodeStep(pool, num_kv_heads=wl.num_kv_heads, num_q_heads=wl.num_q_heads,
                           num_layers=wl.num_layers, block_tables=bt, seq_lens=sl, positions=pos,
-                          rope_theta=wl.rope_theta, scale=wl.scale, pages_per_split=args.pages_per_split)
+                          rope_theta=wl.rope_theta, scale=wl.scale, pages_per_split=args.pages_per_split,
+                          fused_q_rot=False)
     stream = torch.cuda.current_stream()
     step_bytes = wl.kv_bytes_per_step()
     layer_bytes = wl.kv_bytes_per_layer()

@@ -343,27 +343,27 @@ __device__ __forceinline__ void store_output(float* out_row0, const Piece& pc, i
 // the sequence's cos/sin row (fp32 pairs) and then the raw q rows.
 // Thread (g8, tig) owns dims 16s + {2tig, 2tig+1, 8+2tig, 9+2tig} of head g8,
 // s = 0..3, so each rotate-half pair (d, d+32) is in one thread and it needs
-// cos/sin of the 8 frequencies j in {2tig, 2tig+1, 8+2tig, 9+2tig} + {0, 16}
-// (lane j reads cos_hi, sin_hi of frequency j, the fp32 roundings of the
-// fp64 values; shuffles hand them out). The rotation is fp32. The piece that holds page 0 also writes the rotated q (before
-// scaling) to q_rot_out.
+// cos/sin of the 8 frequencies j in {2tig, 2tig+1, 8+2tig, 9+2tig} + {0, 16}:
+// cos_hi and sin_hi (the fp32 roundings of the fp64 values) of each, read
+// straight from the table row (the lanes of one tig read the same 16 bytes).
+// The rotation is fp32. The piece that holds page 0 also writes the rotated
+// q (before scaling) to q_rot_out.
 template <int G>
 __device__ __forceinline__ void rope_query(const DecodeParams& p, uint32_t sS, int bh,
                                            bool write_qrot, int g8, int tig, int lane, float qs,
                                            uint32_t (&aq)[4][4]) {
-  const float cs = __uint_as_float(lds32(sS + 16 * lane));
-  const float sn = __uint_as_float(lds32(sS + 16 * lane + 8));
-  float cj[8], sj[8];  // j = (q & 1) + 2 tig + 8 (q >> 1), q = 0..7
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const int j = (q & 1) + 2 * tig + 8 * (q >> 1);
-    cj[q] = __shfl_sync(kFull, cs, j);
-    sj[q] = __shfl_sync(kFull, sn, j);
-  }
   if (g8 >= G) {
 #pragma unroll
     for (int s = 0; s < 4; ++s) aq[s][0] = aq[s][1] = aq[s][2] = aq[s][3] = 0u;
     return;
+  }
+  float cj[8], sj[8];  // j = (q & 1) + 2 tig + 8 (q >> 1), q = 0..7
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const int j = (q & 1) + 2 * tig + 8 * (q >> 1);
+    const float4 t = lds128f(sS + 16 * j);  // cos_hi, cos_lo, sin_hi, sin_lo
+    cj[q] = t.x;
+    sj[q] = t.z;
   }
   const uint32_t sQ = sS + kTrigBytes;
   // x[s][u]: dims 16s + 2tig + {0, 1} (u = 0, 1) and 16s + 8 + 2tig + {0, 1} (u = 2, 3)
@@ -681,11 +681,45 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   __shared__ int s_first_bh[kW];  // a range's first piece, if it continues a segment: its segment
   __shared__ bool s_has_head[kW];  // a range's last piece holds page 0 of a segment that goes on
   __shared__ int2 s_cont_groups;   // groups of the first and last pages of warp 0's continued segment
+  __shared__ int3 s_head[kW];      // a range's head segment and its first and last groups
   const int n_groups = (n_ranges + kW - 1) / kW;
+  // Which pieces a warp merges when the group ends follows from its range
+  // bounds alone (not from how far the warp got), so every merge below
+  // happens even after a timeout and the workspace slots return to zero.
+  // Lane 0 works it out when the range starts, while the first pages are on
+  // their way: the segment the range's first piece continues (if any), and
+  // the segment whose page 0 the range holds and that goes on past it.
+  auto groups_of = [&](int sg) {
+    const int b = sg / p.hkv;
+    const int np = s_pre[b + 1] - s_pre[b];
+    const int seg_start = p.hkv * s_pre[b] + (sg - b * p.hkv) * np;
+    return make_int2(range_of(seg_start, sg) / kW, range_of(seg_start + np - 1, sg) / kW);
+  };
+  auto plan_merges = [&](int i0, int i1) {
+    if (lane != 0) return;
+    int first_bh = -1;
+    int3 head = make_int3(-1, 0, 0);
+    if (i0 < i1) {
+      const Cursor c0 = locate(i0, s_pre, s_len, p.batch, p.hkv);
+      if (c0.pg > 0) first_bh = c0.b * p.hkv + c0.h;
+      const Cursor cl = locate(i1 - 1, s_pre, s_len, p.batch, p.hkv);
+      if (i1 - 1 - cl.pg >= i0 && cl.pg < cl.np - 1) {
+        head.x = cl.b * p.hkv + cl.h;
+        const int2 g = groups_of(head.x);
+        head.y = g.x;
+        head.z = g.y;
+      }
+    }
+    s_first_bh[warp] = first_bh;
+    s_has_head[warp] = head.x >= 0;
+    s_head[warp] = head;
+    if (warp == 0 && first_bh >= 0) s_cont_groups = groups_of(first_bh);
+  };
   for (int grp = blockIdx.x; grp < n_groups; grp += gridDim.x) {
     const int r = grp * kW + warp;
     int i0 = 0, i1 = 0;
     if (r < n_ranges) range_bounds(r, i0, i1);
+    if (!kPartials) plan_merges(i0, i1);
     if (i0 < i1 && !failed) {
     if (!pre_issued) describe(i0, i0, i1);
     cd_base = pd_base;
@@ -899,37 +933,6 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     }  // this warp's range
 
     if (!kPartials) {
-      // Which pieces this warp merges follows from the range bounds alone (not
-      // from how far the warp got), so every arrival below happens even after
-      // a timeout and the workspace slots return to zero. Everything that does not
-      // need the other warps' pieces is worked out before the barrier.
-      int first_bh = -1, head_bh = -1;  // continued segment at i0; segment whose page 0 is here and that goes on
-      int head_gf = 0, head_gl = 0;     // groups of the head segment's first and last pages
-      auto groups_of = [&](int sg, int& gf, int& gl) {
-        const int b = sg / p.hkv;
-        const int np = s_pre[b + 1] - s_pre[b];
-        const int seg_start = p.hkv * s_pre[b] + (sg - b * p.hkv) * np;
-        gf = range_of(seg_start, sg) / kW;
-        gl = range_of(seg_start + np - 1, sg) / kW;
-      };
-      if (i0 < i1) {
-        const Cursor c0 = locate(i0, s_pre, s_len, p.batch, p.hkv);
-        if (c0.pg > 0) first_bh = c0.b * p.hkv + c0.h;
-        const Cursor cl = locate(i1 - 1, s_pre, s_len, p.batch, p.hkv);
-        if (i1 - 1 - cl.pg >= i0 && cl.pg < cl.np - 1) {
-          head_bh = cl.b * p.hkv + cl.h;
-          groups_of(head_bh, head_gf, head_gl);
-        }
-      }
-      if (lane == 0) {
-        s_first_bh[warp] = first_bh;
-        s_has_head[warp] = head_bh >= 0;
-        if (warp == 0 && first_bh >= 0) {
-          int gf, gl;
-          groups_of(first_bh, gf, gl);
-          s_cont_groups = make_int2(gf, gl);
-        }
-      }
       __syncthreads();  // every slot and s_first_bh of the group are written
 
       // Merge segment sg: pc holds its piece of range grp kW + w, and the
@@ -945,18 +948,18 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
           store_output<G>(out_row0, pc, g8, tig);
           return;
         }
-        // The segment's other groups leave their partials in the workspace.
-        // A CTA that finds them all there merges at once (one round trip: the
-        // usual case for the CTA that finishes last). Otherwise it leaves its
-        // own partial, fences, and looks again; of the CTAs that look after
+        // Every group of the segment leaves its partial in the workspace. A
+        // CTA that then finds all the others' partials there merges at once
+        // (one round trip: the usual case for the CTA that finishes last).
+        // Otherwise it fences and looks again; of the CTAs that look after
         // their fence, the last one in the fences' order sees every partial,
         // so some CTA always merges (two may, with identical results). The
         // merger puts the segment's slots back to zero for the next call.
         Piece all;
         float* my_slot = p.slots + static_cast<size_t>(2 * grp + (grp == g_first ? 1 : 0)) * C::kSlotFloats;
+        publish_piece<G>(my_slot, pc, g8, tig);
         bool done = gather_groups<G>(all, pc, p.slots, C::kSlotFloats, grp, g_first, g_last, g8, tig);
         if (!done) {
-          publish_piece<G>(my_slot, pc, g8, tig);
           __threadfence();
           __syncwarp();
           done = gather_groups<G>(all, pc, p.slots, C::kSlotFloats, grp, g_first, g_last, g8, tig);
@@ -988,14 +991,15 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
         const int2 gg = s_cont_groups;
         merge_segment(first_bh0, pc, 0, gg.x, gg.y);
       }
-      if (head_bh >= 0) {  // this range's last piece, still in registers
+      const int3 head = s_head[warp];
+      if (head.x >= 0) {  // this range's last piece, still in registers
         Piece pc;
 #pragma unroll
         for (int d = 0; d < 8; ++d) pc.acc[d] = make_float2(o[d][0] + o[d][2], o[d][1] + o[d][3]);
         pc.l = l_run + __shfl_xor_sync(kFull, l_run, 1);
         pc.l += __shfl_xor_sync(kFull, pc.l, 2);
         pc.m = m_run;
-        merge_segment(head_bh, pc, warp, head_gf, head_gl);
+        merge_segment(head.x, pc, warp, head.y, head.z);
       }
       __syncthreads();  // the slots are free for the next group
     }

@@ -21,7 +21,7 @@ class DecodeStep:
     def __init__(self, pool_storage: torch.Tensor, *, num_kv_heads: int, num_q_heads: int,
                  num_layers: int, block_tables: torch.Tensor, seq_lens: torch.Tensor,
                  positions: torch.Tensor, rope_theta: float, scale: float,
-                 pages_per_split: int = 0):
+                 pages_per_split: int = 0, fused_q_rot: bool = True):
         dev = pool_storage.device
         self.num_layers = num_layers
         self.batch = int(seq_lens.shape[0])
@@ -30,6 +30,9 @@ class DecodeStep:
         self.rope_theta = float(rope_theta)
         self.scale = float(scale)
         self.pages_per_split = pages_per_split
+        # the fused step writes the rotated queries only when asked (the
+        # attention itself does not need them in memory)
+        self.fused_q_rot = fused_q_rot
         self.pool = B.kv_pool_create(pool_storage, num_kv_heads)
         self.block_tables = block_tables
         self.seq_lens = seq_lens
@@ -43,13 +46,13 @@ class DecodeStep:
         self.rope_cos_sin = B.alloc_rope_table(self.batch, device=dev)
 
     def launches_per_step(self, fused: bool = True) -> int:
-        """Kernels one step launches: per layer and batch chunk of 2048 a decode
-        and a merge, plus per layer the append kernel when not fused, or once
-        per step the cos/sin table when fused."""
+        """Kernels one step launches: per layer one decode per batch chunk of
+        2048, plus per layer the append kernel when not fused, or once per step
+        the cos/sin table when fused."""
         if not self.batch:
             return 0
         chunks = -(-self.batch // 2048)
-        return self.num_layers * (2 * chunks + (0 if fused else 1)) + (1 if fused else 0)
+        return self.num_layers * (chunks + (0 if fused else 1)) + (1 if fused else 0)
 
     def append(self, layer: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
         B.paged_kv_append_rope(self.pool, q[layer], k[layer], v[layer], self.q_rot[layer],
@@ -68,7 +71,8 @@ class DecodeStep:
                     stream=None) -> None:
         B.paged_decode_step(self.pool, q[layer], k[layer], v[layer], self.rope_cos_sin, self.out[layer],
                             self.block_tables[layer], self.seq_lens, self.scale, self.workspace,
-                            q_rot=self.q_rot[layer], pages_per_split=self.pages_per_split,
+                            q_rot=self.q_rot[layer] if self.fused_q_rot else None,
+                            pages_per_split=self.pages_per_split,
                             stream=stream)
 
     def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None,
