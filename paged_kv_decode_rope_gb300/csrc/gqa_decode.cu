@@ -55,12 +55,13 @@ namespace pkv {
 namespace {
 
 constexpr int kScanOffset = 512;           // scan scratch (16 ints) after the mbarriers
-constexpr int kHdrBytes = 1024;            // mbarriers (<= 32 warp-stages * 8 B) + scan scratch
+constexpr int kHdrBytes = 1024;            // mbarriers (<= 64 warp-stages * 8 B) + scan scratch
 constexpr int kMinRangePages = 4;          // smallest automatic range (fewer, cheaper merges)
 // Automatic partition weights: a page costs kPageUnits, and each (sequence,
 // kv head) segment adds kSegUnits for the fixed work of its pieces (query
 // rows, the new token, the result stores), about 3/4 of a page. Without it a
 // range of many short segments takes visibly longer than the others.
+constexpr int kSpareSms = 4;              // SMs left without a decode CTA (see launch_decode)
 constexpr int kPageUnits = 4;
 constexpr int kSegUnits = 3;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -87,13 +88,14 @@ constexpr int kIssueSide = 2;
 // the new token's raw k and v rows.
 constexpr int kTrigBytes = kHalfDim * 16;  // one sequence's row of the fp32 pair table
 
-// Warps per CTA and ring depth: small groups (little compute per page) hide
-// latency with more warps and double buffering; groups of 5-8 heads need the
-// registers of fewer warps and keep three stages in flight.
+// Warps per CTA and ring depth: three stages in flight per warp; groups of
+// up to 4 heads fit 12 warps in shared memory (rings, side rings and merge
+// slots), groups of 5-8 heads 10 (their registers). Measured against 16 x 2
+// and 14 x 2: 12 x 3 is 0.5 us a layer faster on the batch-64 step.
 template <int G>
 struct Cfg {
-  static constexpr int kWarps = G <= 4 ? 16 : 10;
-  static constexpr int kStages = G <= 4 ? 2 : 3;
+  static constexpr int kWarps = G <= 4 ? 12 : 10;
+  static constexpr int kStages = 3;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kQBytes = G * kHeadDim * 4;  // the group's fp32 query rows
   static constexpr int kStepSideBytes = kTrigBytes + G * kRowBytes + 2 * kRowBytes;
@@ -506,9 +508,12 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   const int pu = weighted ? kPageUnits : 1;
   const int su = weighted ? kSegUnits : 0;
   const int total_units = pu * n_items + su * n_seg;
-  const int cw = p.pages_per_split > 0
-                     ? p.pages_per_split
-                     : max(pu * kMinRangePages, (total_units + nwarps - 1) / nwarps);
+  // Short ranges cut latency when there is little work; once every warp
+  // would get a few pages anyway, ranges of at least twice that keep the
+  // number of pieces (and merges) down.
+  const int even = (total_units + nwarps - 1) / nwarps;
+  const int min_pages = even >= pu * kMinRangePages ? 2 * kMinRangePages : kMinRangePages;
+  const int cw = p.pages_per_split > 0 ? p.pages_per_split : max(pu * min_pages, even);
   const int n_ranges = (total_units + cw - 1) / cw;
   // First page item starting at or after unit u (n_items if none). Sequence b
   // starts at unit hkv (pu s_pre[b] + su b) and each of its segments spans
@@ -1129,7 +1134,11 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
   if (bps < 1) return cudaErrorInvalidConfiguration;
   const int sms = device_sm_count(device);
   if (sms < 1) return cudaErrorInvalidDevice;
-  const int grid = sms * bps;
+  // A few SMs get no decode CTA: CTAs are placed in block order as the
+  // previous kernel's CTAs leave their SMs, so the last ones would start
+  // late (their set-up runs while the memory system is busiest) and finish
+  // last; the page stream does not need every SM.
+  const int grid = sms * bps > kSpareSms ? sms * bps - kSpareSms : sms * bps;
   const double log2e = 1.4426950408889634;
   for (int b0 = 0; b0 < a.batch; b0 += kDecodeBatchChunk) {
     const int nb = a.batch - b0 < kDecodeBatchChunk ? a.batch - b0 : kDecodeBatchChunk;
