@@ -45,9 +45,9 @@ L2_BYTES = 129 * 10**6
 # the hash of the decode source it was taken on; reported only while the source
 # is unchanged.
 TRAFFIC = {
-    # workload -> (sha256 of gqa_decode.cu prefix, bytes per layer call: step kernel + merge kernel)
-    # profiles/gqa_decode_step_llama1b_b64_l16_u2048.md: 158.093 + 3.262 MB (step), 3.216 MB (merge)
-    "llama1b_b64_l16_u2048": ("68a987ae9f84ef2d", 164570624),
+    # workload -> (sha256 of gqa_decode.cu prefix, bytes per layer call: the step kernel)
+    # profiles/gqa_decode_step_llama1b_b64_l16_u2048.md: 158.242 MB read + 3.213 MB written
+    "llama1b_b64_l16_u2048": ("c82f6d914249a790", 161454592),
 }
 
 
@@ -378,7 +378,7 @@ def run_ours(args, ws, rank, local):
         "storage": "bf16 KV pages; new key rounded as fp64 rotation would round it; fp32 softmax and accumulation",
         "data": "synthetic (seeded; bf16 N(0,1) q/k/v and cache)", "config": _config(wl),
         "roofline": {"bound": "hbm",
-                     "kernel": "paged_decode_step call per layer: gqa_decode_kernel (step mode) + merge_kernel",
+                     "kernel": "paged_decode_step call per layer: gqa_decode_kernel (step mode, split pieces merged in the kernel)",
                      "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
