@@ -44,7 +44,8 @@ bool decode_shape_ok(const pkv_pool_t* pool, int batch, int num_q_heads, int max
 
 namespace pkv {
 
-cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, int num_kv_heads) {
+cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, int num_kv_heads,
+                          int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     void* fn = nullptr;
@@ -60,8 +61,9 @@ cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, 
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(PKV_HEAD_DIM),
                               static_cast<cuuint64_t>(num_pages) * num_kv_heads * 2 * PKV_PAGE_SIZE};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(PKV_HEAD_DIM) * 2};
-  // one box = 32 rows = one kv head's K and V rows of one page (4 KiB)
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(PKV_HEAD_DIM), 2 * PKV_PAGE_SIZE};
+  // a box of 32 rows = one kv head's K and V rows of one page (4 KiB); of 16
+  // rows = its K rows or its V rows
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(PKV_HEAD_DIM), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t elem[2] = {1, 1};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, storage, dims, strides, box, elem,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -104,7 +106,10 @@ int kv_pool_create(pkv_pool_t** pool, void* storage, size_t storage_bytes, int n
   if (!h) return -ENOMEM;
   int device = 0;
   cudaError_t e = cudaGetDevice(&device);
-  if (e == cudaSuccess) e = pkv::encode_kv_map(&h->kv_map, storage, static_cast<long long>(pages), num_kv_heads);
+  if (e == cudaSuccess)
+    e = pkv::encode_kv_map(&h->kv_map, storage, static_cast<long long>(pages), num_kv_heads, 2 * page_size);
+  if (e == cudaSuccess)
+    e = pkv::encode_kv_map(&h->kv16_map, storage, static_cast<long long>(pages), num_kv_heads, page_size);
   if (e != cudaSuccess) {
     delete h;
     return cuda_fail(e);
@@ -300,6 +305,7 @@ int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v,
   if (sms < 1 || need == 0 || workspace_bytes < need) return -EINVAL;
   pkv::PrefillLaunch a;
   a.kv_map = &pool->kv_map;
+  a.kv16_map = &pool->kv16_map;
   a.pool = static_cast<const uint8_t*>(pool->storage);
   a.num_pages = pool->num_pages;
   a.num_kv_heads = pool->num_kv_heads;

@@ -12,6 +12,8 @@ struct pkv_pool {
   // (one token's K or V of one kv head): [num_pages*num_kv_heads*2*16][64],
   // 32-row boxes (a kv head's K and V rows of one page), 128-byte swizzle.
   CUtensorMap kv_map;  // 64-byte aligned by its type
+  // the same tensor with 16-row boxes (a kv head's K rows, or V rows, of one page)
+  CUtensorMap kv16_map;
   void* storage;
   size_t storage_bytes;
   long long num_pages;
@@ -79,6 +81,7 @@ struct DecodeLaunch {
 // virtual sequence for the append and decode launches.
 struct PrefillLaunch {
   const CUtensorMap* kv_map;
+  const CUtensorMap* kv16_map;
   const uint8_t* pool;
   long long num_pages;
   int num_kv_heads;
@@ -128,7 +131,9 @@ int device_sm_count(int device);
 // Remember a CUDA failure for pkv_last_cuda_error() (calling thread).
 void record_cuda_error(cudaError_t e);
 
-// Encode the pool's TMA descriptor (see pkv_pool::kv_map).
-cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, int num_kv_heads);
+// Encode a TMA descriptor of the pool (see pkv_pool::kv_map) with boxes of
+// box_rows rows.
+cudaError_t encode_kv_map(CUtensorMap* map, void* storage, long long num_pages, int num_kv_heads,
+                          int box_rows);
 
 }  // namespace pkv

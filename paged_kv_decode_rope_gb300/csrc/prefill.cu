@@ -7,24 +7,21 @@
 // and appended like a decode token, and the queries of chunk token t attend
 // causally over the sequence's first start_pos[b] + t + 1 tokens.
 //
-// Three launches. (1) An expansion kernel turns every chunk token into a
+// Four launches. (1) An expansion kernel turns every chunk token into a
 // one-token "virtual sequence" (its causal length, its position, its
 // sequence's block table row). (2) The append kernel rotates and stores every
 // chunk token exactly as it does a decode token, and writes the rotated
-// queries. (3) A flash-attention kernel on tensor cores: one CTA per
-// (sequence, kv head, tile of query tokens) streams the sequence's pages up
-// to the tile's last position through a shared-memory ring (one TMA copy per
-// page) and every warp runs 16 (token, query head) rows of the tile against
-// each page: S = Q K^T and O += P V as m16n8k16 bf16 products with fp32
-// accumulation, the causal mask on the pages that hold the tile's positions,
-// and an online softmax per row. Q and P go in as bf16 plus a second product
-// with their bf16 rounding remainders, so both carry about 16 bits, as in the
-// decode. A tile plan (one CTA) lists the (sequence, first token) of every
-// tile.
-#include <cerrno>
+// queries. (3) A one-CTA plan lists the query tiles. (4) Flash attention on
+// the fifth-generation tensor cores: one CTA per (tile of up to 128 (token,
+// query head) rows, kv head) streams the sequence's pages up to the tile's
+// last position, four pages per step, through a TMA ring; tcgen05 MMAs with
+// fp32 accumulators in tensor memory compute S = Q K^T and O += P V, and one
+// thread per row runs the online softmax on its row of S.
+#include <atomic>
 #include <climits>
 
 #include "pkv_device.cuh"
+#include "tc05.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -62,16 +59,6 @@ __global__ void prefill_expand_kernel(const int32_t* __restrict__ block_tables, 
   for (int i = threadIdx.x; i < max_blocks; i += kExpandThreads) dst[i] = src[i];
 }
 
-// Query tokens per tile: 32 for groups of up to 4 query heads, 16 above,
-// so a CTA has 2G or G warps of 16 (token, head) rows each.
-template <int G>
-struct PrefillCfg {
-  static constexpr int kTokens = G <= 4 ? 32 : 16;
-  static constexpr int kRows = kTokens * G;
-  static constexpr int kWarps = kRows / 16;
-  static constexpr int kThreads = kWarps * 32;
-  static constexpr int kStages = 4;
-};
 constexpr int kPlanThreads = 1024;
 
 // Lists the tiles as {b, first chunk row, tokens, position of the first
@@ -120,20 +107,52 @@ struct PrefillAttnParams {
   int* err;
 };
 
-// Flash attention for one (tile, kv head): blockIdx.x = tile, blockIdx.y = kv head.
+// ---------------------------------------------------------------------------
+// Tensor-core (tcgen05) flash attention for one (tile, kv head).
+//
+// A tile is TcCfg<G>::kTokens chunk tokens x G query heads = up to 128 rows
+// (row R = token R / G, head R % G): the M = 128 of one tcgen05 MMA. Keys go
+// in steps of 64 (four pages). Per step:
+//   S = Q_hi K^T + Q_lo K^T    (tensor memory, 128 x 64 fp32)
+//   softmax warps: row R = tensor-memory lane R, one thread per row
+//   O += P_hi V + P_lo V       (tensor memory, 128 x 64 fp32)
+// Q and P enter as bf16 plus their bf16 rounding remainders (each about 16
+// bits), as in the decode. The softmax keeps a reference maximum per row and
+// moves it (rescaling the row of O in tensor memory) only when a score passes
+// it by more than kSlack in the base-2 domain, so P <= 2^kSlack; numerator
+// and denominator share the reference, so the result is the same softmax.
+// Warps 0-3 run the softmax and the epilogue, warp 4 issues the TMA copies
+// (each page's 16 K rows and 16 V rows into the stage's K and V tiles), and
+// one thread of warp 5 issues the MMAs. Every wait is bounded.
 template <int G>
-__global__ void __launch_bounds__(PrefillCfg<G>::kThreads)
-    prefill_attn_kernel(const __grid_constant__ CUtensorMap kv_map, const PrefillAttnParams p) {
-  using C = PrefillCfg<G>;
-  __shared__ __align__(1024) uint8_t ring[C::kStages][kHeadPageBytes];
-  __shared__ __align__(8) uint64_t full_bar[C::kStages], empty_bar[C::kStages];
+struct TcCfg {
+  static constexpr int kTokens = 128 / G;
+  static constexpr int kRows = kTokens * G;  // <= 128; rows past it are padding
+  static constexpr int kStages = 2;
+  static constexpr int kThreads = 192;
+  static constexpr uint32_t kTile = 128 * 128;  // a 128-row x 128-byte operand tile
+  static constexpr uint32_t kStep = 64 * 128;   // 64 K rows (or V rows) of one step
+  // dynamic shared memory: Q_hi, Q_lo, P_hi, P_lo, then per stage K and V
+  static constexpr uint32_t kQhi = 0, kQlo = kTile, kPhi = 2 * kTile, kPlo = 3 * kTile;
+  static constexpr uint32_t kStage0 = 4 * kTile;
+  static constexpr uint32_t kBytes = kStage0 + kStages * 2 * kStep;
+};
+constexpr float kSlack = 8.f;
+constexpr uint32_t kTmemCols = 128;  // S in columns 0-63, O in 64-127
+
+template <int G>
+__global__ void __launch_bounds__(TcCfg<G>::kThreads)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kv16_map, const PrefillAttnParams p) {
+  using C = TcCfg<G>;
+  extern __shared__ __align__(1024) uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t kv_full[C::kStages], kv_empty[C::kStages];
+  __shared__ __align__(8) uint64_t q_ready, s_full, p_full, o_done, drain;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_bad[C::kStages];  // pages of the step (bits 0-3) with a bad id
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g8 = lane >> 2, tig = lane & 3, mi = lane >> 3, ri = lane & 7;
-  if (static_cast<int>(blockIdx.x) >= *p.num_tiles) return;  // the grid is an upper bound
+  if (static_cast<int>(blockIdx.x) >= *p.num_tiles) return;
   const int4 tile = p.tiles[blockIdx.x];
   const int b = tile.x, row0 = tile.y, n_tok = tile.z, pos0 = tile.w, h = blockIdx.y;
-  // Tokens whose position does not fit the block table (the append flagged
-  // them) get zero rows; the rest of the tile is attended as usual.
   const long long room = static_cast<long long>(p.max_blocks) * kPage - pos0;
   const int n_ok = pos0 < 0 ? 0 : static_cast<int>(min(static_cast<long long>(n_tok), max(room, 0ll)));
   for (int e = n_ok * G * kHeadDim + tid; e < n_tok * G * kHeadDim; e += C::kThreads) {
@@ -143,223 +162,272 @@ __global__ void __launch_bounds__(PrefillCfg<G>::kThreads)
   if (n_ok <= 0) return;
   const int last_pos = pos0 + n_ok - 1;
   const int n_pages = last_pos / kPage + 1;
+  const int n_steps = (n_pages + 3) / 4;
   const int32_t* bt = p.block_tables + static_cast<size_t>(b) * p.max_blocks;
+  const uint32_t base = (smem_addr(dsmem) + 1023u) & ~1023u;
+  uint8_t* gbase = dsmem + (base - smem_addr(dsmem));
+  auto kst = [&](int st) { return base + C::kStage0 + st * 2 * C::kStep; };
+  auto vst = [&](int st) { return base + C::kStage0 + st * 2 * C::kStep + C::kStep; };
 
+  if (warp == 0) {
+    tmem_alloc(smem_addr(&s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
   if (tid == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(smem_addr(&full_bar[s]), 1);
-      mbar_init(smem_addr(&empty_bar[s]), C::kWarps);
+    for (int st = 0; st < C::kStages; ++st) {
+      mbar_init(smem_addr(&kv_full[st]), 1);
+      mbar_init(smem_addr(&kv_empty[st]), 1);
     }
+    mbar_init(smem_addr(&q_ready), 128);
+    mbar_init(smem_addr(&s_full), 1);
+    mbar_init(smem_addr(&p_full), 128);
+    mbar_init(smem_addr(&o_done), 1);
+    mbar_init(smem_addr(&drain), 1);
   }
   fence_mbar_init();
+  tc_fence_before();
   __syncthreads();
-
-  // thread 0 fills stage s with page pg (one 4 KiB box: 16 K rows, then 16 V rows)
-  int issued = 0;  // pages thread 0 has started copying
-  auto issue = [&](int pg, int s) {
-    ++issued;
-    const int page = bt[pg];
-    const uint32_t bar = smem_addr(&full_bar[s]);
-    if (page < 0 || static_cast<long long>(page) >= p.num_pages) {
-      atomicOr(p.err, PKV_ERR_PAGE_ID);
-      mbar_arrive(bar);  // nothing to wait for; the stage keeps stale rows
-      return;
-    }
-    mbar_arrive_expect_tx(bar, kHeadPageBytes);
-    // default L2 policy: the other tiles of the sequence read the same pages
-    tma_load_2d(smem_addr(ring[s]), &kv_map, 0, (page * p.hkv + h) * (2 * kPage), bar);
-  };
-  if (tid == 0)
-    for (int s = 0; s < C::kStages && s < n_pages; ++s) issue(s, s);
-
-  // This lane's two rows: R = 16 warp + g8 (+8) -> token R / G, query head h G + R % G.
-  int pos[2];
-  bool live[2];
-  uint32_t qh[4][4], ql[4][4];  // Q hi / lo as the A operand, per 16-dim k-step
-  {
-    float x[2][4][4];  // [row][k-step][c]: dims 16s + 2tig + {0,1}, 16s + 8 + 2tig + {0,1}
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const int R = 16 * warp + g8 + 8 * rr;
-      const int t = R / G, i = R - t * G;
-      live[rr] = t < n_ok;
-      pos[rr] = pos0 + min(t, n_ok - 1);  // rows past the tile copy its last position
-      const float* qr =
-          p.q_rot + (static_cast<size_t>(row0 + (live[rr] ? t : 0)) * p.hq + h * G + i) * kHeadDim;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const float2 a = *reinterpret_cast<const float2*>(qr + 16 * s + 2 * tig);
-        const float2 c = *reinterpret_cast<const float2*>(qr + 16 * s + 8 + 2 * tig);
-        x[rr][s][0] = a.x * p.qscale;
-        x[rr][s][1] = a.y * p.qscale;
-        x[rr][s][2] = c.x * p.qscale;
-        x[rr][s][3] = c.y * p.qscale;
-      }
-    }
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      // a0: row g8, dims 2tig..; a1: row g8+8; a2: row g8, dims 8+2tig..; a3: row g8+8
-      const uint32_t h0 = pack_bf16x2(x[0][s][0], x[0][s][1]), h1 = pack_bf16x2(x[1][s][0], x[1][s][1]);
-      const uint32_t h2 = pack_bf16x2(x[0][s][2], x[0][s][3]), h3 = pack_bf16x2(x[1][s][2], x[1][s][3]);
-      qh[s][0] = h0; qh[s][1] = h1; qh[s][2] = h2; qh[s][3] = h3;
-      const float2 f0 = bf16x2_to_float2(h0), f1 = bf16x2_to_float2(h1);
-      const float2 f2 = bf16x2_to_float2(h2), f3 = bf16x2_to_float2(h3);
-      ql[s][0] = pack_bf16x2(x[0][s][0] - f0.x, x[0][s][1] - f0.y);
-      ql[s][1] = pack_bf16x2(x[1][s][0] - f1.x, x[1][s][1] - f1.y);
-      ql[s][2] = pack_bf16x2(x[0][s][2] - f2.x, x[0][s][3] - f2.y);
-      ql[s][3] = pack_bf16x2(x[1][s][2] - f3.x, x[1][s][3] - f3.y);
-    }
-  }
-
-  float o[8][4];
-#pragma unroll
-  for (int d = 0; d < 8; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  int consumed = 0;  // pages whose copy this thread has seen land
+  tc_fence_after();
+  const uint32_t tmem = s_tmem, tS = tmem, tO = tmem + 64;
   bool failed = false;
 
-  for (int pg = 0; pg < n_pages; ++pg) {
-    const int s = pg % C::kStages;
-    const bool landed = mbar_wait_bounded(smem_addr(&full_bar[s]), (pg / C::kStages) & 1u);
-    if (!__all_sync(kFull, landed)) {
-      failed = true;
-      break;
+  if (warp == 4) {
+    // ---- TMA producer: step j's four pages into stage j % kStages ----
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < n_steps && !failed; ++j) {
+        const int st = j % C::kStages;
+        if (j >= C::kStages &&
+            !mbar_wait_bounded(smem_addr(&kv_empty[st]), ((j / C::kStages) - 1) & 1)) {
+          failed = true;
+          break;
+        }
+        int bad = 0, pages[4];
+        uint32_t bytes = 0;
+        for (int q = 0; q < 4; ++q) {
+          const int pg = 4 * j + q;
+          pages[q] = -1;
+          if (pg >= n_pages) continue;
+          const int page = bt[pg];
+          if (page < 0 || static_cast<long long>(page) >= p.num_pages) {
+            bad |= 1 << q;
+            continue;
+          }
+          pages[q] = page;
+          bytes += 2 * kHalfBytes;
+        }
+        if (bad) atomicOr(p.err, PKV_ERR_PAGE_ID);
+        s_bad[st] = bad;  // published by the arrival below
+        const uint32_t bar = smem_addr(&kv_full[st]);
+        mbar_arrive_expect_tx(bar, bytes);
+        for (int q = 0; q < 4; ++q) {
+          if (pages[q] < 0) continue;
+          const int y = (pages[q] * p.hkv + h) * (2 * kPage);
+          tma_load_2d(kst(st) + q * kHalfBytes, &kv16_map, 0, y, bar);
+          tma_load_2d(vst(st) + q * kHalfBytes, &kv16_map, 0, y + kPage, bar);
+        }
+        issued = j + 1;
+      }
+      // let the copies still in flight (at most the last kStages steps) land
+      // before shared memory goes away
+      if (failed)
+        for (int j = max(0, issued - C::kStages); j < issued; ++j)
+          mbar_wait_bounded(smem_addr(&kv_full[j % C::kStages]), (j / C::kStages) & 1);
     }
-    consumed = pg + 1;
-    const int page = bt[pg];
-    const bool bad = page < 0 || static_cast<long long>(page) >= p.num_pages;
-    if (!bad) {
-      const uint32_t sK = smem_addr(ring[s]), sV = sK + kHalfBytes;
-      // S = Q K^T (16 rows x 16 keys; n-tiles j: keys 8j..8j+7), Q as hi and lo products
-      uint32_t kb[2][4][2];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = q >> 1, s0 = 2 * (q & 1);
-        const int row = 8 * j + ri, chunk = 4 * (q & 1) + mi;
-        ldsm_x4(sK + row * kRowBytes + ((chunk ^ ri) << 4), kb[j][s0][0], kb[j][s0][1],
-                kb[j][s0 + 1][0], kb[j][s0 + 1][1]);
-      }
-      float sc[2][4];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          mma_bf16_16816(sc[j], qh[k], kb[j][k][0], kb[j][k][1]);
-          mma_bf16_16816(sc[j], ql[k], kb[j][k][0], kb[j][k][1]);
+  } else if (warp == 5) {
+    // ---- MMA issuer ----
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false);
+      constexpr uint32_t idPV = idesc_bf16_f32(128, 64, true);
+      const uint64_t dQhi = smem_desc_sw128(base + C::kQhi), dQlo = smem_desc_sw128(base + C::kQlo);
+      const uint64_t dPhi = smem_desc_sw128(base + C::kPhi), dPlo = smem_desc_sw128(base + C::kPlo);
+      if (!mbar_wait_bounded(smem_addr(&q_ready), 0)) failed = true;
+      for (int j = 0; j < n_steps && !failed; ++j) {
+        const int st = j % C::kStages;
+        if (!mbar_wait_bounded(smem_addr(&kv_full[st]), (j / C::kStages) & 1)) {
+          failed = true;
+          break;
         }
-      }
-      // causal mask: key position key0 + 8j + 2tig (+1) must not pass the row's position
-      const int key0 = pg * kPage;
-      if (key0 + kPage - 1 > min(pos[0], pos[1])) {
+        tc_fence_after();
+        const uint64_t dK = smem_desc_sw128(kst(st)), dV = smem_desc_sw128(vst(st));
+        // K-major tiles: a 16-element K step is 32 bytes along the swizzled
+        // row (+2 in the descriptor's 16-byte address units)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
+        for (int k = 0; k < 4; ++k) umma_bf16(tS, dQhi + 2 * k, dK + 2 * k, idS, k > 0);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (key0 + 8 * j + 2 * tig + (c & 1) > pos[c >> 1]) sc[j][c] = -INFINITY;
-      }
-      // online softmax per row (row g8: c = 0, 1; row g8 + 8: c = 2, 3); page 0
-      // holds key 0, which every row sees, so m_run is finite from then on
-      float pr[2][4];
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        float pm = fmaxf(fmaxf(sc[0][2 * rr], sc[0][2 * rr + 1]), fmaxf(sc[1][2 * rr], sc[1][2 * rr + 1]));
-        pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 1));
-        pm = fmaxf(pm, __shfl_xor_sync(kFull, pm, 2));
-        const float m_new = fmaxf(m_run[rr], pm);
-        const float alpha = m_new > m_run[rr] ? fast_exp2(m_run[rr] - m_new) : 1.f;
-        pr[rr][0] = fast_exp2(sc[0][2 * rr] - m_new);
-        pr[rr][1] = fast_exp2(sc[0][2 * rr + 1] - m_new);
-        pr[rr][2] = fast_exp2(sc[1][2 * rr] - m_new);
-        pr[rr][3] = fast_exp2(sc[1][2 * rr + 1] - m_new);
-        l_run[rr] = l_run[rr] * alpha + ((pr[rr][0] + pr[rr][1]) + (pr[rr][2] + pr[rr][3]));
-        m_run[rr] = m_new;
-#pragma unroll
-        for (int d = 0; d < 8; ++d) {
-          o[d][2 * rr] *= alpha;
-          o[d][2 * rr + 1] *= alpha;
+        for (int k = 0; k < 4; ++k) umma_bf16(tS, dQlo + 2 * k, dK + 2 * k, idS, true);
+        umma_commit(smem_addr(&s_full));
+        if (!mbar_wait_bounded(smem_addr(&p_full), j & 1)) {
+          failed = true;
+          break;
         }
-      }
-      // P as the A operand (a0: row g8, keys 2tig..; a1: row g8+8; a2, a3: keys 8+2tig..),
-      // once as bf16 and once as the bf16 remainder
-      uint32_t ph[4], pl[4];
-      {
-        const float pa[4][2] = {{pr[0][0], pr[0][1]}, {pr[1][0], pr[1][1]},
-                                {pr[0][2], pr[0][3]}, {pr[1][2], pr[1][3]}};
+        tc_fence_after();
+        // V is MN-major: a 16-key K step is 16 rows = 2048 bytes (+128)
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          ph[a] = pack_bf16x2(pa[a][0], pa[a][1]);
-          const float2 f = bf16x2_to_float2(ph[a]);
-          pl[a] = pack_bf16x2(pa[a][0] - f.x, pa[a][1] - f.y);
-        }
-      }
-      // O += P V (n-tiles d: dims 8d..8d+7), V fragments transposed by ldmatrix
-      uint32_t vb[8][2];
+        for (int k = 0; k < 4; ++k) umma_bf16(tO, dPhi + 2 * k, dV + 128 * k, idPV, j > 0 || k > 0);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int chunk = 2 * q + (mi >> 1), row = 8 * (mi & 1) + ri;
-        ldsm_x4_trans(sV + row * kRowBytes + ((chunk ^ ri) << 4), vb[2 * q][0], vb[2 * q][1],
-                      vb[2 * q + 1][0], vb[2 * q + 1][1]);
+        for (int k = 0; k < 4; ++k) umma_bf16(tO, dPlo + 2 * k, dV + 128 * k, idPV, true);
+        umma_commit(smem_addr(&kv_empty[st]));
+        umma_commit(smem_addr(&o_done));
       }
-      const int nv = last_pos - key0 + 1;  // slots holding keys of the tile
-      if (nv < kPage) {  // later slots were never written: keep their bits out of P V
-        const int t0 = 2 * tig;
-        const uint32_t m0 = (t0 < nv ? 0x0000ffffu : 0u) | (t0 + 1 < nv ? 0xffff0000u : 0u);
-        const uint32_t m1 = (t0 + 8 < nv ? 0x0000ffffu : 0u) | (t0 + 9 < nv ? 0xffff0000u : 0u);
-#pragma unroll
-        for (int d = 0; d < 8; ++d) {
-          vb[d][0] &= m0;
-          vb[d][1] &= m1;
-        }
-      }
-#pragma unroll
-      for (int d = 0; d < 8; ++d) {
-        mma_bf16_16816(o[d], ph, vb[d][0], vb[d][1]);
-        mma_bf16_16816(o[d], pl, vb[d][0], vb[d][1]);
+      if (failed) {  // let the MMAs already issued finish before the memory goes away
+        umma_commit(smem_addr(&drain));
+        mbar_wait_bounded(smem_addr(&drain), 0);
       }
     }
-    // Release the stage. Thread 0 refills the stage of the previous page, one
-    // page behind, so it rarely waits for the slower warps.
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty_bar[s]));
-    if (warp == 0) {
-      const int prev = pg - 1;
-      bool ok = true;
-      if (lane == 0 && prev >= 0 && prev + C::kStages < n_pages) {
-        const int ps = prev % C::kStages;
-        ok = mbar_wait_bounded(smem_addr(&empty_bar[ps]), (prev / C::kStages) & 1u);
-        if (ok) issue(prev + C::kStages, ps);
+  } else {
+    // ---- softmax and epilogue: thread tid owns row tid (tensor-memory lane tid) ----
+    const int r = tid;
+    const int t = r / G, gi = r - t * G;
+    const bool live = r < C::kRows && t < n_ok;
+    const int pos = pos0 + min(t, n_ok - 1);
+    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    // Q rows: scaled, as bf16 high part and remainder, 128-byte swizzled
+    {
+      float x[kHeadDim];
+      const float* qr = p.q_rot + (static_cast<size_t>(row0 + (live ? t : 0)) * p.hq + h * G + gi) * kHeadDim;
+#pragma unroll
+      for (int d = 0; d < kHeadDim; d += 4) {
+        const float4 v = live ? *reinterpret_cast<const float4*>(qr + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[d] = v.x * p.qscale;
+        x[d + 1] = v.y * p.qscale;
+        x[d + 2] = v.z * p.qscale;
+        x[d + 3] = v.w * p.qscale;
       }
-      if (!__shfl_sync(kFull, ok, 0)) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a0 = x[8 * c + 2 * e], a1 = x[8 * c + 2 * e + 1];
+          hi[e] = pack_bf16x2(a0, a1);
+          const float2 f = bf16x2_to_float2(hi[e]);
+          lo[e] = pack_bf16x2(a0 - f.x, a1 - f.y);
+        }
+        const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(gbase + C::kQhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(gbase + C::kQlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_addr(&q_ready));
+    }
+    float m_ref = -INFINITY, l_sum = 0.f;
+    for (int j = 0; j < n_steps; ++j) {
+      const int st = j % C::kStages;
+      const int k0 = 64 * j;
+      if (!mbar_wait_bounded(smem_addr(&s_full), j & 1)) {
         failed = true;
         break;
       }
+      tc_fence_after();
+      float sv[64];
+      {
+        float a[32], c[32];
+        tmem_ld32(tS + lane_addr, a);
+        tmem_ld32(tS + lane_addr + 32, c);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = a[i];
+          sv[32 + i] = c[i];
+        }
+      }
+      // the stage's copies have landed (the MMA saw them); this thread's own
+      // wait orders its reads of s_bad and its writes to the V tile after them
+      if (!mbar_wait_bounded(smem_addr(&kv_full[st]), (j / C::kStages) & 1)) failed = true;
+      const int bad = s_bad[st];
+      // keys past the row's position, and pages with a bad id, get no weight
+      if (k0 + 63 > pos || bad) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (k0 + i > pos || ((bad >> (i >> 4)) & 1)) sv[i] = -INFINITY;
+      }
+      float mx = sv[0];
+#pragma unroll
+      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, sv[i]);
+      if (mx > m_ref + kSlack) {
+        // move the reference up; O and l follow (O is complete: the MMAs of
+        // the previous step finished before this step's scores did)
+        if (j > 0 && m_ref != -INFINITY) {
+          const float alpha = fast_exp2(m_ref - mx);
+          l_sum *= alpha;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float o[32];
+            tmem_ld32(tO + lane_addr + 32 * half, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tmem_st32(tO + lane_addr + 32 * half, o);
+          }
+          tmem_wait_st();
+        }
+        m_ref = mx;
+      }
+      // P = exp2(S - m_ref), as bf16 high part and remainder, swizzled rows
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = m_ref == -INFINITY ? 0.f : fast_exp2(sv[8 * c + 2 * e] - m_ref);
+          const float p1 = m_ref == -INFINITY ? 0.f : fast_exp2(sv[8 * c + 2 * e + 1] - m_ref);
+          l_sum += p0 + p1;
+          hi[e] = pack_bf16x2(p0, p1);
+          const float2 f = bf16x2_to_float2(hi[e]);
+          lo[e] = pack_bf16x2(p0 - f.x, p1 - f.y);
+        }
+        const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(gbase + C::kPhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(gbase + C::kPlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+      // V rows that hold no key of the tile (past its last position, or of a
+      // page with a bad id) are zeroed, so that their bits cannot reach O
+      if (k0 + 63 > last_pos || bad) {
+        uint8_t* vrow = gbase + (vst(st) - base);
+        for (int idx = tid; idx < 64 * 8; idx += 128) {
+          const int key = idx >> 3;
+          if (k0 + key > last_pos || ((bad >> (key >> 4)) & 1))
+            *reinterpret_cast<uint4*>(vrow + key * 128 + (idx & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_addr(&p_full));
+    }
+    // epilogue: O / l for the live rows
+    if (!failed && mbar_wait_bounded(smem_addr(&o_done), (n_steps - 1) & 1)) {
+      tc_fence_after();
+      float o[64];
+      {
+        float a[32], c[32];
+        tmem_ld32(tO + lane_addr, a);
+        tmem_ld32(tO + lane_addr + 32, c);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          o[i] = a[i];
+          o[32 + i] = c[i];
+        }
+      }
+      if (live) {
+        const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        float* dst = p.out + (static_cast<size_t>(row0 + t) * p.hq + h * G + gi) * kHeadDim;
+#pragma unroll
+        for (int d = 0; d < kHeadDim; d += 4)
+          *reinterpret_cast<float4*>(dst + d) =
+              make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+      }
+    } else {
+      failed = true;
     }
   }
-
-  if (failed) {
-    // Report; the issuing thread then lets every copy it started land before
-    // the CTA's shared memory is released (a stage has one copy at a time).
-    if (lane == 0) atomicOr(p.err, PKV_ERR_TIMEOUT);
-    if (tid == 0) {
-      for (int pg = consumed; pg < issued; ++pg)
-        mbar_wait_bounded(smem_addr(&full_bar[pg % C::kStages]), (pg / C::kStages) & 1u);
-    }
-    return;
-  }
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    float l = l_run[rr] + __shfl_xor_sync(kFull, l_run[rr], 1);
-    l += __shfl_xor_sync(kFull, l, 2);
-    if (!live[rr]) continue;
-    const int R = 16 * warp + g8 + 8 * rr;
-    const int t = R / G, i = R - t * G;
-    float* dst = p.out + (static_cast<size_t>(row0 + t) * p.hq + h * G + i) * kHeadDim;
-    const float inv = 1.f / l;
-#pragma unroll
-    for (int d = 0; d < 8; ++d)
-      *reinterpret_cast<float2*>(dst + 8 * d + 2 * tig) =
-          make_float2(o[d][2 * rr] * inv, o[d][2 * rr + 1] * inv);
+  if (failed && lane == 0) atomicOr(p.err, PKV_ERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -390,7 +458,7 @@ PrefillLayout layout(int total_tokens, int batch, int max_blocks) {
 
 template <int G>
 cudaError_t launch_attn(const PrefillLaunch& a, const PrefillLayout& l, cudaStream_t stream) {
-  using C = PrefillCfg<G>;
+  using C = TcCfg<G>;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   int4* tiles = reinterpret_cast<int4*>(ws + l.tiles);
   int* count = reinterpret_cast<int*>(ws + l.count);
@@ -412,8 +480,15 @@ cudaError_t launch_attn(const PrefillLaunch& a, const PrefillLayout& l, cudaStre
   p.num_pages = a.num_pages;
   p.qscale = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   p.err = a.err;
+  const int smem = static_cast<int>(C::kBytes + 1024);  // + alignment to 1 KiB
+  static std::atomic<bool> attr_set[9];
+  if (!attr_set[G].load(std::memory_order_relaxed)) {
+    e = cudaFuncSetAttribute(prefill_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set[G].store(true, std::memory_order_relaxed);
+  }
   const dim3 grid(static_cast<unsigned>(grid_x), static_cast<unsigned>(a.num_kv_heads));
-  prefill_attn_kernel<G><<<grid, C::kThreads, 0, stream>>>(*a.kv_map, p);
+  prefill_tc_kernel<G><<<grid, C::kThreads, smem, stream>>>(*a.kv16_map, p);
   return cudaGetLastError();
 }
 
