@@ -112,18 +112,21 @@ struct PrefillAttnParams {
 //
 // A tile is TcCfg<G>::kTokens chunk tokens x G query heads = up to 128 rows
 // (row R = token R / G, head R % G): the M = 128 of one tcgen05 MMA. Keys go
-// in steps of 64 (four pages). Per step:
-//   S = Q_hi K^T + Q_lo K^T    (tensor memory, 128 x 64 fp32)
+// in steps of 64 (four pages). Per step j:
+//   S_j = Q_hi K_j^T + Q_lo K_j^T    (tensor memory, 128 x 64 fp32, two buffers)
 //   softmax warps: row R = tensor-memory lane R, one thread per row
-//   O += P_hi V + P_lo V       (tensor memory, 128 x 64 fp32)
+//   O += P_hi V_j + P_lo V_j         (tensor memory, 128 x 64 fp32)
 // Q and P enter as bf16 plus their bf16 rounding remainders (each about 16
 // bits), as in the decode. The softmax keeps a reference maximum per row and
 // moves it (rescaling the row of O in tensor memory) only when a score passes
 // it by more than kSlack in the base-2 domain, so P <= 2^kSlack; numerator
 // and denominator share the reference, so the result is the same softmax.
 // Warps 0-3 run the softmax and the epilogue, warp 4 issues the TMA copies
-// (each page's 16 K rows and 16 V rows into the stage's K and V tiles), and
-// one thread of warp 5 issues the MMAs. Every wait is bounded.
+// (each page's 16 K rows into the stage's K tile and its 16 V rows into the
+// V tile, with separate barriers so K of a later step can load as soon as
+// its stage's scores are done), and one thread of warp 5 issues the MMAs:
+// S_{j+1} goes out before P_j is ready, so the tensor core computes the next
+// scores while the softmax works on these. Every wait is bounded.
 template <int G>
 struct TcCfg {
   static constexpr int kTokens = 128 / G;
@@ -138,17 +141,30 @@ struct TcCfg {
   static constexpr uint32_t kBytes = kStage0 + kStages * 2 * kStep;
 };
 constexpr float kSlack = 8.f;
-constexpr uint32_t kTmemCols = 128;  // S in columns 0-63, O in 64-127
+constexpr uint32_t kTmemCols = 256;  // S buffers in columns 0-63 and 64-127, O in 128-191
+
+// Bits 0-3: which of step j's four pages have a bad page id.
+__device__ __forceinline__ int bad_pages(const int32_t* bt, int j, int n_pages, long long num_pages) {
+  int bad = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int pg = 4 * j + q;
+    if (pg >= n_pages) continue;
+    const int page = bt[pg];
+    if (page < 0 || static_cast<long long>(page) >= num_pages) bad |= 1 << q;
+  }
+  return bad;
+}
 
 template <int G>
 __global__ void __launch_bounds__(TcCfg<G>::kThreads)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv16_map, const PrefillAttnParams p) {
   using C = TcCfg<G>;
   extern __shared__ __align__(1024) uint8_t dsmem[];
-  __shared__ __align__(8) uint64_t kv_full[C::kStages], kv_empty[C::kStages];
-  __shared__ __align__(8) uint64_t q_ready, s_full, p_full, o_done, drain;
+  __shared__ __align__(8) uint64_t k_full[C::kStages], k_empty[C::kStages];
+  __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
+  __shared__ __align__(8) uint64_t s_full[2], q_ready, p_full, pv_done, drain;
   __shared__ uint32_t s_tmem;
-  __shared__ int s_bad[C::kStages];  // pages of the step (bits 0-3) with a bad id
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (static_cast<int>(blockIdx.x) >= *p.num_tiles) return;
   const int4 tile = p.tiles[blockIdx.x];
@@ -175,64 +191,79 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
   }
   if (tid == 0) {
     for (int st = 0; st < C::kStages; ++st) {
-      mbar_init(smem_addr(&kv_full[st]), 1);
-      mbar_init(smem_addr(&kv_empty[st]), 1);
+      mbar_init(smem_addr(&k_full[st]), 1);
+      mbar_init(smem_addr(&k_empty[st]), 1);
+      mbar_init(smem_addr(&v_full[st]), 1);
+      mbar_init(smem_addr(&v_empty[st]), 1);
     }
+    mbar_init(smem_addr(&s_full[0]), 1);
+    mbar_init(smem_addr(&s_full[1]), 1);
     mbar_init(smem_addr(&q_ready), 128);
-    mbar_init(smem_addr(&s_full), 1);
     mbar_init(smem_addr(&p_full), 128);
-    mbar_init(smem_addr(&o_done), 1);
+    mbar_init(smem_addr(&pv_done), 1);
     mbar_init(smem_addr(&drain), 1);
   }
   fence_mbar_init();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem, tS = tmem, tO = tmem + 64;
+  const uint32_t tmem = s_tmem, tO = tmem + 128;
+  auto tS = [&](int j) { return tmem + 64 * (j & 1); };
   bool failed = false;
 
   if (warp == 4) {
     // ---- TMA producer: step j's four pages into stage j % kStages ----
     if (lane == 0) {
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n_steps && !failed; ++j) {
-        const int st = j % C::kStages;
-        if (j >= C::kStages &&
-            !mbar_wait_bounded(smem_addr(&kv_empty[st]), ((j / C::kStages) - 1) & 1)) {
-          failed = true;
-          break;
-        }
-        int bad = 0, pages[4];
+        const int st = j % C::kStages, use = j / C::kStages;
+        int pages[4];
         uint32_t bytes = 0;
+        int bad = 0;
         for (int q = 0; q < 4; ++q) {
           const int pg = 4 * j + q;
           pages[q] = -1;
           if (pg >= n_pages) continue;
           const int page = bt[pg];
           if (page < 0 || static_cast<long long>(page) >= p.num_pages) {
-            bad |= 1 << q;
+            bad = 1;
             continue;
           }
           pages[q] = page;
-          bytes += 2 * kHalfBytes;
+          bytes += kHalfBytes;
         }
         if (bad) atomicOr(p.err, PKV_ERR_PAGE_ID);
-        s_bad[st] = bad;  // published by the arrival below
-        const uint32_t bar = smem_addr(&kv_full[st]);
-        mbar_arrive_expect_tx(bar, bytes);
-        for (int q = 0; q < 4; ++q) {
-          if (pages[q] < 0) continue;
-          const int y = (pages[q] * p.hkv + h) * (2 * kPage);
-          tma_load_2d(kst(st) + q * kHalfBytes, &kv16_map, 0, y, bar);
-          tma_load_2d(vst(st) + q * kHalfBytes, &kv16_map, 0, y + kPage, bar);
+        // K tile: free once the stage's scores are done
+        if (use > 0 && !mbar_wait_bounded(smem_addr(&k_empty[st]), (use - 1) & 1)) {
+          failed = true;
+          break;
         }
-        issued = j + 1;
+        mbar_arrive_expect_tx(smem_addr(&k_full[st]), bytes);
+        for (int q = 0; q < 4; ++q)
+          if (pages[q] >= 0)
+            tma_load_2d(kst(st) + q * kHalfBytes, &kv16_map, 0, (pages[q] * p.hkv + h) * (2 * kPage),
+                        smem_addr(&k_full[st]));
+        k_issued = j + 1;
+        // V tile: free once the stage's P V product is done
+        if (use > 0 && !mbar_wait_bounded(smem_addr(&v_empty[st]), (use - 1) & 1)) {
+          failed = true;
+          break;
+        }
+        mbar_arrive_expect_tx(smem_addr(&v_full[st]), bytes);
+        for (int q = 0; q < 4; ++q)
+          if (pages[q] >= 0)
+            tma_load_2d(vst(st) + q * kHalfBytes, &kv16_map, 0,
+                        (pages[q] * p.hkv + h) * (2 * kPage) + kPage, smem_addr(&v_full[st]));
+        v_issued = j + 1;
       }
-      // let the copies still in flight (at most the last kStages steps) land
+      // let the copies still in flight (the last kStages steps at most) land
       // before shared memory goes away
-      if (failed)
-        for (int j = max(0, issued - C::kStages); j < issued; ++j)
-          mbar_wait_bounded(smem_addr(&kv_full[j % C::kStages]), (j / C::kStages) & 1);
+      if (failed) {
+        for (int j = max(0, k_issued - C::kStages); j < k_issued; ++j)
+          mbar_wait_bounded(smem_addr(&k_full[j % C::kStages]), (j / C::kStages) & 1);
+        for (int j = max(0, v_issued - C::kStages); j < v_issued; ++j)
+          mbar_wait_bounded(smem_addr(&v_full[j % C::kStages]), (j / C::kStages) & 1);
+      }
     }
   } else if (warp == 5) {
     // ---- MMA issuer ----
@@ -241,34 +272,43 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
       constexpr uint32_t idPV = idesc_bf16_f32(128, 64, true);
       const uint64_t dQhi = smem_desc_sw128(base + C::kQhi), dQlo = smem_desc_sw128(base + C::kQlo);
       const uint64_t dPhi = smem_desc_sw128(base + C::kPhi), dPlo = smem_desc_sw128(base + C::kPlo);
-      if (!mbar_wait_bounded(smem_addr(&q_ready), 0)) failed = true;
-      for (int j = 0; j < n_steps && !failed; ++j) {
+      // S_j into buffer j % 2 (its previous scores, S_{j-2}, were read before P_{j-2} was ready)
+      auto issue_s = [&](int j) -> bool {
         const int st = j % C::kStages;
-        if (!mbar_wait_bounded(smem_addr(&kv_full[st]), (j / C::kStages) & 1)) {
-          failed = true;
-          break;
-        }
+        if (!mbar_wait_bounded(smem_addr(&k_full[st]), (j / C::kStages) & 1)) return false;
         tc_fence_after();
-        const uint64_t dK = smem_desc_sw128(kst(st)), dV = smem_desc_sw128(vst(st));
+        const uint64_t dK = smem_desc_sw128(kst(st));
         // K-major tiles: a 16-element K step is 32 bytes along the swizzled
         // row (+2 in the descriptor's 16-byte address units)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16(tS, dQhi + 2 * k, dK + 2 * k, idS, k > 0);
+        for (int k = 0; k < 4; ++k) umma_bf16(tS(j), dQhi + 2 * k, dK + 2 * k, idS, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16(tS, dQlo + 2 * k, dK + 2 * k, idS, true);
-        umma_commit(smem_addr(&s_full));
-        if (!mbar_wait_bounded(smem_addr(&p_full), j & 1)) {
+        for (int k = 0; k < 4; ++k) umma_bf16(tS(j), dQlo + 2 * k, dK + 2 * k, idS, true);
+        umma_commit(smem_addr(&k_empty[st]));
+        umma_commit(smem_addr(&s_full[j & 1]));
+        return true;
+      };
+      if (!mbar_wait_bounded(smem_addr(&q_ready), 0) || !issue_s(0)) failed = true;
+      for (int j = 0; j < n_steps && !failed; ++j) {
+        const int st = j % C::kStages;
+        if (j + 1 < n_steps && !issue_s(j + 1)) {
+          failed = true;
+          break;
+        }
+        if (!mbar_wait_bounded(smem_addr(&p_full), j & 1) ||
+            !mbar_wait_bounded(smem_addr(&v_full[st]), (j / C::kStages) & 1)) {
           failed = true;
           break;
         }
         tc_fence_after();
+        const uint64_t dV = smem_desc_sw128(vst(st));
         // V is MN-major: a 16-key K step is 16 rows = 2048 bytes (+128)
 #pragma unroll
         for (int k = 0; k < 4; ++k) umma_bf16(tO, dPhi + 2 * k, dV + 128 * k, idPV, j > 0 || k > 0);
 #pragma unroll
         for (int k = 0; k < 4; ++k) umma_bf16(tO, dPlo + 2 * k, dV + 128 * k, idPV, true);
-        umma_commit(smem_addr(&kv_empty[st]));
-        umma_commit(smem_addr(&o_done));
+        umma_commit(smem_addr(&v_empty[st]));
+        umma_commit(smem_addr(&pv_done));
       }
       if (failed) {  // let the MMAs already issued finish before the memory goes away
         umma_commit(smem_addr(&drain));
@@ -312,10 +352,13 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
       mbar_arrive(smem_addr(&q_ready));
     }
     float m_ref = -INFINITY, l_sum = 0.f;
+    int bad_next = bad_pages(bt, 0, n_pages, p.num_pages);
     for (int j = 0; j < n_steps; ++j) {
       const int st = j % C::kStages;
       const int k0 = 64 * j;
-      if (!mbar_wait_bounded(smem_addr(&s_full), j & 1)) {
+      const int bad = bad_next;
+      if (j + 1 < n_steps) bad_next = bad_pages(bt, j + 1, n_pages, p.num_pages);
+      if (!mbar_wait_bounded(smem_addr(&s_full[j & 1]), (j >> 1) & 1)) {
         failed = true;
         break;
       }
@@ -323,8 +366,8 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
       float sv[64];
       {
         float a[32], c[32];
-        tmem_ld32(tS + lane_addr, a);
-        tmem_ld32(tS + lane_addr + 32, c);
+        tmem_ld32(tS(j) + lane_addr, a);
+        tmem_ld32(tS(j) + lane_addr + 32, c);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -332,10 +375,6 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
           sv[32 + i] = c[i];
         }
       }
-      // the stage's copies have landed (the MMA saw them); this thread's own
-      // wait orders its reads of s_bad and its writes to the V tile after them
-      if (!mbar_wait_bounded(smem_addr(&kv_full[st]), (j / C::kStages) & 1)) failed = true;
-      const int bad = s_bad[st];
       // keys past the row's position, and pages with a bad id, get no weight
       if (k0 + 63 > pos || bad) {
 #pragma unroll
@@ -345,10 +384,12 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
       float mx = sv[0];
 #pragma unroll
       for (int i = 1; i < 64; ++i) mx = fmaxf(mx, sv[i]);
+      // O and the P tile belong to P_{j-1} V_{j-1} until it completes
+      if (j > 0 && !mbar_wait_bounded(smem_addr(&pv_done), (j - 1) & 1)) failed = true;
       if (mx > m_ref + kSlack) {
-        // move the reference up; O and l follow (O is complete: the MMAs of
-        // the previous step finished before this step's scores did)
+        // move the reference up; O and l follow
         if (j > 0 && m_ref != -INFINITY) {
+          tc_fence_after();
           const float alpha = fast_exp2(m_ref - mx);
           l_sum *= alpha;
 #pragma unroll
@@ -382,8 +423,10 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
         *reinterpret_cast<uint4*>(gbase + C::kPlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       // V rows that hold no key of the tile (past its last position, or of a
-      // page with a bad id) are zeroed, so that their bits cannot reach O
+      // page with a bad id) are zeroed once the stage's V copies have landed,
+      // so that their bits cannot reach O
       if (k0 + 63 > last_pos || bad) {
+        if (!mbar_wait_bounded(smem_addr(&v_full[st]), (j / C::kStages) & 1)) failed = true;
         uint8_t* vrow = gbase + (vst(st) - base);
         for (int idx = tid; idx < 64 * 8; idx += 128) {
           const int key = idx >> 3;
@@ -396,7 +439,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
       mbar_arrive(smem_addr(&p_full));
     }
     // epilogue: O / l for the live rows
-    if (!failed && mbar_wait_bounded(smem_addr(&o_done), (n_steps - 1) & 1)) {
+    if (!failed && mbar_wait_bounded(smem_addr(&pv_done), (n_steps - 1) & 1)) {
       tc_fence_after();
       float o[64];
       {
