@@ -242,13 +242,15 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks
  *                start_pos int32 [batch] (>= 0)
  *   workspace    device memory of at least paged_prefill_workspace_bytes(),
  *                256-byte aligned, contents irrelevant
- * Launches four kernels on `stream`: an expansion of the chunk tokens, the
- * append kernel (every chunk token stored as a decode token would be), a tile
- * plan, and a flash-attention kernel on tensor cores, one CTA per (sequence,
- * kv head, tile of 32 tokens for up to 4 query heads a kv head, 16 above)
- * that streams the sequence's pages once per tile. Tokens of a malformed
- * chunk (cu_tokens decreasing, a negative start, or a position past
- * max_blocks*16) are not stored, their rows are zeroed and PKV_ERR_SEQ_LEN is
+ * Launches five kernels on `stream`: an expansion of the chunk tokens (each
+ * token's sequence and position), the RoPE table of their positions (as
+ * paged_rope_cos_sin), the append (every chunk token stored as a decode
+ * token would be, with the same certified key rounding), a tile plan, and a
+ * flash-attention kernel on the tcgen05 tensor cores, one CTA per (sequence,
+ * kv head, tile of up to 128 (token, query head) rows) that streams the
+ * sequence's pages once per tile. Tokens of a malformed chunk (cu_tokens
+ * decreasing, a negative start, or a position past max_blocks*16) are not
+ * stored, their rows are zeroed and PKV_ERR_SEQ_LEN is
  * set.
  */
 int paged_prefill(pkv_pool_t *pool, const void *q, const void *k, const void *v, float *q_rot,

@@ -27,18 +27,17 @@
 namespace pkv {
 namespace {
 
-constexpr int kExpandThreads = 128;
+constexpr int kExpandThreads = 256;
+constexpr int kHalfDim = kHeadDim / 2;
 
-// One CTA per chunk token: find its sequence by bisection over cu_tokens,
-// then write its length (0 when the sequence's chunk is malformed: the
-// append and decode then flag it and zero its rows), its position, and a
-// copy of its sequence's block table row.
-__global__ void prefill_expand_kernel(const int32_t* __restrict__ block_tables, int max_blocks,
-                                      const int32_t* __restrict__ cu_tokens,
+// One thread per chunk token: find its sequence by bisection over cu_tokens
+// and write it (-1 when the sequence's chunk is malformed: a decreasing
+// cu_tokens, a negative start, or a position past max_blocks*16) and its
+// position (0 when malformed).
+__global__ void prefill_expand_kernel(int max_blocks, const int32_t* __restrict__ cu_tokens,
                                       const int32_t* __restrict__ start_pos, int batch, int total,
-                                      int32_t* __restrict__ tok_tables, int32_t* __restrict__ tok_lens,
-                                      int32_t* __restrict__ tok_pos) {
-  const int idx = blockIdx.x;
+                                      int32_t* __restrict__ tok_seq, int32_t* __restrict__ tok_pos) {
+  const int idx = blockIdx.x * kExpandThreads + threadIdx.x;
   if (idx >= total) return;
   int lo = 0, hi = batch - 1;  // largest b with cu_tokens[b] <= idx
   while (lo < hi) {
@@ -50,13 +49,73 @@ __global__ void prefill_expand_kernel(const int32_t* __restrict__ block_tables, 
   const long long pos = static_cast<long long>(start_pos[b]) + (idx - c0);
   const bool ok = c0 <= idx && idx < c1 && start_pos[b] >= 0 &&
                   pos + 1 <= static_cast<long long>(max_blocks) * kPage;
-  if (threadIdx.x == 0) {
-    tok_lens[idx] = ok ? static_cast<int32_t>(pos + 1) : 0;
-    tok_pos[idx] = ok ? static_cast<int32_t>(pos) : 0;
+  tok_seq[idx] = ok ? b : -1;
+  tok_pos[idx] = ok ? static_cast<int32_t>(pos) : 0;
+}
+
+// One CTA per chunk token: its rotated query (fp32, from the fp32 cos/sin of
+// the rope table), its key rotated and rounded to bf16 exactly as fp64
+// arithmetic rounds it (the certified fp32 double-word path, fp64 from the
+// table where it cannot certify: the bytes the decode append stores), and
+// its value, both stored at its position in its sequence's pages.
+constexpr int kAppendThreads = 128;
+__global__ void __launch_bounds__(kAppendThreads)
+    prefill_append_kernel(uint16_t* __restrict__ pool, long long num_pages, int hkv, int hq,
+                          const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                          const uint16_t* __restrict__ v, float* __restrict__ q_rot,
+                          const int32_t* __restrict__ block_tables, int max_blocks,
+                          const int32_t* __restrict__ tok_seq, const int32_t* __restrict__ tok_pos,
+                          const float4* __restrict__ rope_ff, const double2* __restrict__ rope_dd,
+                          int* __restrict__ err) {
+  __shared__ float4 cs[kHalfDim];
+  const int tkn = blockIdx.x, tid = threadIdx.x;
+  if (tid < kHalfDim) cs[tid] = rope_ff[static_cast<size_t>(tkn) * kHalfDim + tid];
+  __syncthreads();
+  const uint16_t* qb = q + static_cast<size_t>(tkn) * hq * kHeadDim;
+  float* qo = q_rot + static_cast<size_t>(tkn) * hq * kHeadDim;
+  for (int idx = tid; idx < hq * kHalfDim; idx += kAppendThreads) {
+    const int head = idx / kHalfDim, j = idx - head * kHalfDim;
+    const float x0 = __uint_as_float(static_cast<uint32_t>(qb[head * kHeadDim + j]) << 16);
+    const float x1 = __uint_as_float(static_cast<uint32_t>(qb[head * kHeadDim + j + kHalfDim]) << 16);
+    qo[head * kHeadDim + j] = x0 * cs[j].x - x1 * cs[j].z;
+    qo[head * kHeadDim + j + kHalfDim] = x1 * cs[j].x + x0 * cs[j].z;
   }
-  const int32_t* src = block_tables + static_cast<size_t>(b) * max_blocks;
-  int32_t* dst = tok_tables + static_cast<size_t>(idx) * max_blocks;
-  for (int i = threadIdx.x; i < max_blocks; i += kExpandThreads) dst[i] = src[i];
+  const int b = tok_seq[tkn];
+  if (b < 0) {
+    if (tid == 0) atomicOr(err, PKV_ERR_SEQ_LEN);
+    return;
+  }
+  const int pos = tok_pos[tkn];
+  const long long page = block_tables[static_cast<size_t>(b) * max_blocks + pos / kPage];
+  if (page < 0 || page >= num_pages) {
+    if (tid == 0) atomicOr(err, PKV_ERR_PAGE_ID);
+    return;
+  }
+  const int slot = pos % kPage;
+  uint16_t* page_base = pool + static_cast<size_t>(page) * hkv * (kHeadPageBytes / 2);
+  const uint16_t* kb = k + static_cast<size_t>(tkn) * hkv * kHeadDim;
+  for (int idx = tid; idx < hkv * kHalfDim; idx += kAppendThreads) {
+    const int hh = idx / kHalfDim, j = idx - hh * kHalfDim;
+    const uint16_t k0 = kb[hh * kHeadDim + j], k1 = kb[hh * kHeadDim + j + kHalfDim];
+    const float x0 = __uint_as_float(static_cast<uint32_t>(k0) << 16);
+    const float x1 = __uint_as_float(static_cast<uint32_t>(k1) << 16);
+    const float4 c = cs[j];
+    uint16_t y0, y1;
+    if (!(rotated_bf16_fast(x0, x1, c.x, c.y, c.z, c.w, y0) &&
+          rotated_bf16_fast(x1, -x0, c.x, c.y, c.z, c.w, y1))) {
+      const double2 cd = rope_dd[static_cast<size_t>(tkn) * kHalfDim + j];
+      rotate_key_pair(k0, k1, cd.x, cd.y, y0, y1);
+    }
+    uint16_t* krow = page_base + (hh * 2 + 0) * (kHalfBytes / 2) + slot * kHeadDim;
+    krow[j] = y0;
+    krow[j + kHalfDim] = y1;
+  }
+  const uint4* vb = reinterpret_cast<const uint4*>(v + static_cast<size_t>(tkn) * hkv * kHeadDim);
+  for (int idx = tid; idx < hkv * (kRowBytes / 16); idx += kAppendThreads) {
+    const int hh = idx / (kRowBytes / 16), c = idx - hh * (kRowBytes / 16);
+    uint4* vrow = reinterpret_cast<uint4*>(page_base + (hh * 2 + 1) * (kHalfBytes / 2) + slot * kHeadDim);
+    vrow[c] = vb[hh * (kRowBytes / 16) + c];
+  }
 }
 
 constexpr int kPlanThreads = 1024;
@@ -476,10 +535,10 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
 
 size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
-// Workspace: the expanded per-token tables, lengths and positions the append
-// kernel reads, then the tile list and its count.
+// Workspace: each chunk token's sequence and position, the rope table of the
+// chunk tokens (fp32 pairs, then fp64), then the tile list and its count.
 struct PrefillLayout {
-  size_t tables, lens, pos, tiles, count, total;
+  size_t seq, pos, rope, tiles, count, total;
 };
 
 // An upper bound on the tiles of any split of total_tokens over the batch
@@ -489,11 +548,12 @@ size_t max_tiles(int total_tokens, int batch) {
 }
 
 PrefillLayout layout(int total_tokens, int batch, int max_blocks) {
+  (void)max_blocks;
   PrefillLayout l;
-  l.tables = 0;
-  l.lens = l.tables + align256(sizeof(int32_t) * static_cast<size_t>(total_tokens) * max_blocks);
-  l.pos = l.lens + align256(sizeof(int32_t) * static_cast<size_t>(total_tokens));
-  l.tiles = l.pos + align256(sizeof(int32_t) * static_cast<size_t>(total_tokens));
+  l.seq = 0;
+  l.pos = l.seq + align256(sizeof(int32_t) * static_cast<size_t>(total_tokens));
+  l.rope = l.pos + align256(sizeof(int32_t) * static_cast<size_t>(total_tokens));
+  l.tiles = l.rope + align256(static_cast<size_t>(total_tokens) * kHalfDim * (sizeof(float4) + sizeof(double2)));
   l.count = l.tiles + align256(sizeof(int4) * max_tiles(total_tokens, batch));
   l.total = l.count + 256;
   return l;
@@ -545,32 +605,25 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream) {
   if (a.total_tokens == 0) return cudaSuccess;
   const PrefillLayout l = layout(a.total_tokens, a.batch, a.max_blocks);
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  int32_t* tok_tables = reinterpret_cast<int32_t*>(ws + l.tables);
-  int32_t* tok_lens = reinterpret_cast<int32_t*>(ws + l.lens);
+  int32_t* tok_seq = reinterpret_cast<int32_t*>(ws + l.seq);
   int32_t* tok_pos = reinterpret_cast<int32_t*>(ws + l.pos);
-  prefill_expand_kernel<<<a.total_tokens, kExpandThreads, 0, stream>>>(
-      a.block_tables, a.max_blocks, a.cu_tokens, a.start_pos, a.batch, a.total_tokens, tok_tables,
-      tok_lens, tok_pos);
+  void* rope = ws + l.rope;
+  prefill_expand_kernel<<<(a.total_tokens + kExpandThreads - 1) / kExpandThreads, kExpandThreads, 0,
+                          stream>>>(a.max_blocks, a.cu_tokens, a.start_pos, a.batch, a.total_tokens,
+                                    tok_seq, tok_pos);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-
-  AppendLaunch ap;
-  ap.pool = const_cast<uint16_t*>(reinterpret_cast<const uint16_t*>(a.pool));
-  ap.num_pages = a.num_pages;
-  ap.num_kv_heads = a.num_kv_heads;
-  ap.q = a.q;
-  ap.k = a.k;
-  ap.v = a.v;
-  ap.q_rot = a.q_rot;
-  ap.block_tables = tok_tables;
-  ap.max_blocks = a.max_blocks;
-  ap.seq_lens = tok_lens;
-  ap.positions = tok_pos;
-  ap.batch = a.total_tokens;
-  ap.num_q_heads = a.num_q_heads;
-  ap.rope_theta = a.rope_theta;
-  ap.err = a.err;
-  e = launch_append_rope(ap, stream);
+  // cos/sin of every chunk token's position: fp32 pairs, then fp64
+  e = launch_rope_cos_sin(tok_pos, a.total_tokens, a.rope_theta, rope, stream);
+  if (e != cudaSuccess) return e;
+  const float4* rope_ff = static_cast<const float4*>(rope);
+  const double2* rope_dd =
+      reinterpret_cast<const double2*>(rope_ff + static_cast<size_t>(a.total_tokens) * kHalfDim);
+  prefill_append_kernel<<<a.total_tokens, kAppendThreads, 0, stream>>>(
+      const_cast<uint16_t*>(reinterpret_cast<const uint16_t*>(a.pool)), a.num_pages, a.num_kv_heads,
+      a.num_q_heads, a.q, a.k, a.v, a.q_rot, a.block_tables, a.max_blocks, tok_seq, tok_pos, rope_ff,
+      rope_dd, a.err);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
   switch (a.num_q_heads / a.num_kv_heads) {
