@@ -440,9 +440,15 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
         for (int i = 0; i < 64; ++i)
           if (k0 + i > pos || ((bad >> (i >> 4)) & 1)) sv[i] = -INFINITY;
       }
-      float mx = sv[0];
+      // row maximum as a tree (short dependency chains)
+      float mt[16];
 #pragma unroll
-      for (int i = 1; i < 64; ++i) mx = fmaxf(mx, sv[i]);
+      for (int i = 0; i < 16; ++i) mt[i] = fmaxf(fmaxf(sv[4 * i], sv[4 * i + 1]), fmaxf(sv[4 * i + 2], sv[4 * i + 3]));
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) mt[i] = fmaxf(mt[i], mt[i + w]);
+      const float mx = mt[0];
       // O and the P tile belong to P_{j-1} V_{j-1} until it completes
       if (j > 0 && !mbar_wait_bounded(smem_addr(&pv_done), (j - 1) & 1)) failed = true;
       if (mx > m_ref + kSlack) {
@@ -465,14 +471,17 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
         m_ref = mx;
       }
       // P = exp2(S - m_ref), as bf16 high part and remainder, swizzled rows
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // all scores -inf: P = 0
+      float lp[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t hi[4], lo[4];
+        lp[c] = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = m_ref == -INFINITY ? 0.f : fast_exp2(sv[8 * c + 2 * e] - m_ref);
-          const float p1 = m_ref == -INFINITY ? 0.f : fast_exp2(sv[8 * c + 2 * e + 1] - m_ref);
-          l_sum += p0 + p1;
+          const float p0 = fast_exp2(sv[8 * c + 2 * e] - m_use);
+          const float p1 = fast_exp2(sv[8 * c + 2 * e + 1] - m_use);
+          lp[c] += p0 + p1;
           hi[e] = pack_bf16x2(p0, p1);
           const float2 f = bf16x2_to_float2(hi[e]);
           lo[e] = pack_bf16x2(p0 - f.x, p1 - f.y);
@@ -481,6 +490,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
         *reinterpret_cast<uint4*>(gbase + C::kPhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(gbase + C::kPlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
+      l_sum += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
       // V rows that hold no key of the tile (past its last position, or of a
       // page with a bad id) are zeroed once the stage's V copies have landed,
       // so that their bits cannot reach O
