@@ -180,10 +180,13 @@ struct PrefillAttnParams {
 // moves it (rescaling the row of O in tensor memory) only when a score passes
 // it by more than kSlack in the base-2 domain, so P <= 2^kSlack; numerator
 // and denominator share the reference, so the result is the same softmax.
-// Warps 0-3 run the softmax and the epilogue, warp 4 issues the TMA copies
+// Warps 0-7 run the softmax and the epilogue, two threads per row (warps w
+// and w + 4 share tensor-memory lanes 32 (w % 4) ..; one takes columns 0-31,
+// the other 32-63, and they exchange row maxima and sums through shared
+// memory), warp 8 issues the TMA copies
 // (each page's 16 K rows into the stage's K tile and its 16 V rows into the
 // V tile, with separate barriers so K of a later step can load as soon as
-// its stage's scores are done), and one thread of warp 5 issues the MMAs:
+// its stage's scores are done), and one thread of warp 9 issues the MMAs:
 // S_{j+1} goes out before P_j is ready, so the tensor core computes the next
 // scores while the softmax works on these. Every wait is bounded.
 template <int G>
@@ -191,7 +194,8 @@ struct TcCfg {
   static constexpr int kTokens = 128 / G;
   static constexpr int kRows = kTokens * G;  // <= 128; rows past it are padding
   static constexpr int kStages = 2;
-  static constexpr int kThreads = 192;
+  static constexpr int kSoftmaxThreads = 256;
+  static constexpr int kThreads = kSoftmaxThreads + 64;
   static constexpr uint32_t kTile = 128 * 128;  // a 128-row x 128-byte operand tile
   static constexpr uint32_t kStep = 64 * 128;   // 64 K rows (or V rows) of one step
   // dynamic shared memory: Q_hi, Q_lo, P_hi, P_lo, then per stage K and V
@@ -216,7 +220,7 @@ __device__ __forceinline__ int bad_pages(const int32_t* bt, int j, int n_pages, 
 }
 
 template <int G>
-__global__ void __launch_bounds__(TcCfg<G>::kThreads)
+__global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv16_map, const PrefillAttnParams p) {
   using C = TcCfg<G>;
   extern __shared__ __align__(1024) uint8_t dsmem[];
@@ -224,6 +228,8 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
   __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
   __shared__ __align__(8) uint64_t s_full[2], q_ready, p_full, pv_done, drain;
   __shared__ uint32_t s_tmem;
+  __shared__ float s_xchg[2][2][128];  // [step parity][column half][row]: row maxima
+  __shared__ float s_lsum[2][128];     // [column half][row]: the halves' sums
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (static_cast<int>(blockIdx.x) >= *p.num_tiles) return;
   const int4 tile = p.tiles[blockIdx.x];
@@ -257,8 +263,8 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
     }
     mbar_init(smem_addr(&s_full[0]), 1);
     mbar_init(smem_addr(&s_full[1]), 1);
-    mbar_init(smem_addr(&q_ready), 128);
-    mbar_init(smem_addr(&p_full), 128);
+    mbar_init(smem_addr(&q_ready), C::kSoftmaxThreads);
+    mbar_init(smem_addr(&p_full), C::kSoftmaxThreads);
     mbar_init(smem_addr(&pv_done), 1);
     mbar_init(smem_addr(&drain), 1);
   }
@@ -270,7 +276,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
   auto tS = [&](int j) { return tmem + 64 * (j & 1); };
   bool failed = false;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---- TMA producer: step j's four pages into stage j % kStages ----
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;
@@ -324,7 +330,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
           mbar_wait_bounded(smem_addr(&v_full[j % C::kStages]), (j / C::kStages) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---- MMA issuer ----
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 64, false);
@@ -375,18 +381,20 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
       }
     }
   } else {
-    // ---- softmax and epilogue: thread tid owns row tid (tensor-memory lane tid) ----
-    const int r = tid;
+    // ---- softmax and epilogue: row r = tid % 128 (tensor-memory lane r), column half hf ----
+    const int r = tid & 127, hf = tid >> 7;
     const int t = r / G, gi = r - t * G;
     const bool live = r < C::kRows && t < n_ok;
     const int pos = pos0 + min(t, n_ok - 1);
-    const uint32_t lane_addr = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    auto pair_sync = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     // Q rows: scaled, as bf16 high part and remainder, 128-byte swizzled
+    // (this thread: dims 32 hf .. 32 hf + 31, chunks 4 hf .. 4 hf + 3)
     {
-      float x[kHeadDim];
-      const float* qr = p.q_rot + (static_cast<size_t>(row0 + (live ? t : 0)) * p.hq + h * G + gi) * kHeadDim;
+      float x[32];
+      const float* qr = p.q_rot + (static_cast<size_t>(row0 + (live ? t : 0)) * p.hq + h * G + gi) * kHeadDim + 32 * hf;
 #pragma unroll
-      for (int d = 0; d < kHeadDim; d += 4) {
+      for (int d = 0; d < 32; d += 4) {
         const float4 v = live ? *reinterpret_cast<const float4*>(qr + d) : make_float4(0.f, 0.f, 0.f, 0.f);
         x[d] = v.x * p.qscale;
         x[d + 1] = v.y * p.qscale;
@@ -394,11 +402,12 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
         x[d + 3] = v.w * p.qscale;
       }
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * hf + cc;
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float a0 = x[8 * c + 2 * e], a1 = x[8 * c + 2 * e + 1];
+          const float a0 = x[8 * cc + 2 * e], a1 = x[8 * cc + 2 * e + 1];
           hi[e] = pack_bf16x2(a0, a1);
           const float2 f = bf16x2_to_float2(hi[e]);
           lo[e] = pack_bf16x2(a0 - f.x, a1 - f.y);
@@ -414,74 +423,62 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
     int bad_next = bad_pages(bt, 0, n_pages, p.num_pages);
     for (int j = 0; j < n_steps; ++j) {
       const int st = j % C::kStages;
-      const int k0 = 64 * j;
+      const int k0 = 64 * j + 32 * hf;  // key position of this thread's first column
       const int bad = bad_next;
       if (j + 1 < n_steps) bad_next = bad_pages(bt, j + 1, n_pages, p.num_pages);
-      if (!mbar_wait_bounded(smem_addr(&s_full[j & 1]), (j >> 1) & 1)) {
-        failed = true;
-        break;
-      }
+      if (!mbar_wait_bounded(smem_addr(&s_full[j & 1]), (j >> 1) & 1)) failed = true;
       tc_fence_after();
-      float sv[64];
-      {
-        float a[32], c[32];
-        tmem_ld32(tS(j) + lane_addr, a);
-        tmem_ld32(tS(j) + lane_addr + 32, c);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          sv[i] = a[i];
-          sv[32 + i] = c[i];
-        }
-      }
+      float sv[32];
+      tmem_ld32(tS(j) + lane_addr + 32 * hf, sv);
+      tmem_wait_ld();
       // keys past the row's position, and pages with a bad id, get no weight
-      if (k0 + 63 > pos || bad) {
+      if (k0 + 31 > pos || bad) {
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (k0 + i > pos || ((bad >> (i >> 4)) & 1)) sv[i] = -INFINITY;
+        for (int i = 0; i < 32; ++i)
+          if (k0 + i > pos || ((bad >> (2 * hf + (i >> 4))) & 1)) sv[i] = -INFINITY;
       }
-      // row maximum as a tree (short dependency chains)
-      float mt[16];
+      float mt[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) mt[i] = fmaxf(fmaxf(sv[4 * i], sv[4 * i + 1]), fmaxf(sv[4 * i + 2], sv[4 * i + 3]));
+      for (int i = 0; i < 8; ++i) mt[i] = fmaxf(fmaxf(sv[4 * i], sv[4 * i + 1]), fmaxf(sv[4 * i + 2], sv[4 * i + 3]));
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
+      for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
         for (int i = 0; i < w; ++i) mt[i] = fmaxf(mt[i], mt[i + w]);
-      const float mx = mt[0];
+      // the row's maximum: this half's and the partner thread's
+      s_xchg[j & 1][hf][r] = mt[0];
+      pair_sync();
+      const float mx = fmaxf(mt[0], s_xchg[j & 1][hf ^ 1][r]);
       // O and the P tile belong to P_{j-1} V_{j-1} until it completes
       if (j > 0 && !mbar_wait_bounded(smem_addr(&pv_done), (j - 1) & 1)) failed = true;
       if (mx > m_ref + kSlack) {
-        // move the reference up; O and l follow
+        // move the reference up; O (this thread's half of the columns) and l follow
         if (j > 0 && m_ref != -INFINITY) {
           tc_fence_after();
           const float alpha = fast_exp2(m_ref - mx);
           l_sum *= alpha;
+          float o[32];
+          tmem_ld32(tO + lane_addr + 32 * hf, o);
+          tmem_wait_ld();
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float o[32];
-            tmem_ld32(tO + lane_addr + 32 * half, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tmem_st32(tO + lane_addr + 32 * half, o);
-          }
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tmem_st32(tO + lane_addr + 32 * hf, o);
           tmem_wait_st();
         }
         m_ref = mx;
       }
       // P = exp2(S - m_ref), as bf16 high part and remainder, swizzled rows
       const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // all scores -inf: P = 0
-      float lp[8];
+      float lp[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int cc = 0; cc < 4; ++cc) {
+        const int c = 4 * hf + cc;
         uint32_t hi[4], lo[4];
-        lp[c] = 0.f;
+        lp[cc] = 0.f;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(sv[8 * c + 2 * e] - m_use);
-          const float p1 = fast_exp2(sv[8 * c + 2 * e + 1] - m_use);
-          lp[c] += p0 + p1;
+          const float p0 = fast_exp2(sv[8 * cc + 2 * e] - m_use);
+          const float p1 = fast_exp2(sv[8 * cc + 2 * e + 1] - m_use);
+          lp[cc] += p0 + p1;
           hi[e] = pack_bf16x2(p0, p1);
           const float2 f = bf16x2_to_float2(hi[e]);
           lo[e] = pack_bf16x2(p0 - f.x, p1 - f.y);
@@ -490,16 +487,16 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
         *reinterpret_cast<uint4*>(gbase + C::kPhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(gbase + C::kPlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      l_sum += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
+      l_sum += (lp[0] + lp[1]) + (lp[2] + lp[3]);
       // V rows that hold no key of the tile (past its last position, or of a
       // page with a bad id) are zeroed once the stage's V copies have landed,
       // so that their bits cannot reach O
-      if (k0 + 63 > last_pos || bad) {
+      if (64 * j + 63 > last_pos || bad) {
         if (!mbar_wait_bounded(smem_addr(&v_full[st]), (j / C::kStages) & 1)) failed = true;
         uint8_t* vrow = gbase + (vst(st) - base);
-        for (int idx = tid; idx < 64 * 8; idx += 128) {
+        for (int idx = tid; idx < 64 * 8; idx += C::kSoftmaxThreads) {
           const int key = idx >> 3;
-          if (k0 + key > last_pos || ((bad >> (key >> 4)) & 1))
+          if (64 * j + key > last_pos || ((bad >> (key >> 4)) & 1))
             *reinterpret_cast<uint4*>(vrow + key * 128 + (idx & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
@@ -507,26 +504,20 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads)
       tc_fence_before();
       mbar_arrive(smem_addr(&p_full));
     }
-    // epilogue: O / l for the live rows
+    // epilogue: O / l for the live rows, l being the sum of both halves' sums
+    s_lsum[hf][r] = l_sum;
+    pair_sync();
+    const float l_row = l_sum + s_lsum[hf ^ 1][r];
     if (!failed && mbar_wait_bounded(smem_addr(&pv_done), (n_steps - 1) & 1)) {
       tc_fence_after();
-      float o[64];
-      {
-        float a[32], c[32];
-        tmem_ld32(tO + lane_addr, a);
-        tmem_ld32(tO + lane_addr + 32, c);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          o[i] = a[i];
-          o[32 + i] = c[i];
-        }
-      }
+      float o[32];
+      tmem_ld32(tO + lane_addr + 32 * hf, o);
+      tmem_wait_ld();
       if (live) {
-        const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-        float* dst = p.out + (static_cast<size_t>(row0 + t) * p.hq + h * G + gi) * kHeadDim;
+        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+        float* dst = p.out + (static_cast<size_t>(row0 + t) * p.hq + h * G + gi) * kHeadDim + 32 * hf;
 #pragma unroll
-        for (int d = 0; d < kHeadDim; d += 4)
+        for (int d = 0; d < 32; d += 4)
           *reinterpret_cast<float4*>(dst + d) =
               make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
       }
