@@ -174,7 +174,7 @@ struct PrefillAttnParams {
 // in steps of 64 (four pages). Per step j:
 //   S_j = Q_hi K_j^T + Q_lo K_j^T    (tensor memory, 128 x 64 fp32, two buffers)
 //   softmax warps: row R = tensor-memory lane R, one thread per row
-//   O += P_hi V_j + P_lo V_j         (tensor memory, 128 x 64 fp32)
+//   O += P_hi V_j + P_lo V_j         (tensor memory, 128 x 64 fp32; P in tensor memory)
 // Q and P enter as bf16 plus their bf16 rounding remainders (each about 16
 // bits), as in the decode. The softmax keeps a reference maximum per row and
 // moves it (rescaling the row of O in tensor memory) only when a score passes
@@ -193,18 +193,20 @@ template <int G>
 struct TcCfg {
   static constexpr int kTokens = 128 / G;
   static constexpr int kRows = kTokens * G;  // <= 128; rows past it are padding
-  static constexpr int kStages = 2;
+  static constexpr int kStages = 4;
   static constexpr int kSoftmaxThreads = 256;
   static constexpr int kThreads = kSoftmaxThreads + 64;
   static constexpr uint32_t kTile = 128 * 128;  // a 128-row x 128-byte operand tile
   static constexpr uint32_t kStep = 64 * 128;   // 64 K rows (or V rows) of one step
-  // dynamic shared memory: Q_hi, Q_lo, P_hi, P_lo, then per stage K and V
-  static constexpr uint32_t kQhi = 0, kQlo = kTile, kPhi = 2 * kTile, kPlo = 3 * kTile;
-  static constexpr uint32_t kStage0 = 4 * kTile;
+  // dynamic shared memory: Q_hi, Q_lo, then per stage K and V
+  static constexpr uint32_t kQhi = 0, kQlo = kTile;
+  static constexpr uint32_t kStage0 = 2 * kTile;
   static constexpr uint32_t kBytes = kStage0 + kStages * 2 * kStep;
 };
 constexpr float kSlack = 8.f;
-constexpr uint32_t kTmemCols = 256;  // S buffers in columns 0-63 and 64-127, O in 128-191
+// tensor memory: S buffers in columns 0-63 and 64-127, O in 128-191, P_hi in
+// 192-223 and P_lo in 224-255 (two bf16 keys per column)
+constexpr uint32_t kTmemCols = 256;
 
 // Bits 0-3: which of step j's four pages have a bad page id.
 __device__ __forceinline__ int bad_pages(const int32_t* bt, int j, int n_pages, long long num_pages) {
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem, tO = tmem + 128;
+  const uint32_t tmem = s_tmem, tO = tmem + 128, tPhi = tmem + 192, tPlo = tmem + 224;
   auto tS = [&](int j) { return tmem + 64 * (j & 1); };
   bool failed = false;
 
@@ -336,7 +338,6 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       constexpr uint32_t idS = idesc_bf16_f32(128, 64, false);
       constexpr uint32_t idPV = idesc_bf16_f32(128, 64, true);
       const uint64_t dQhi = smem_desc_sw128(base + C::kQhi), dQlo = smem_desc_sw128(base + C::kQlo);
-      const uint64_t dPhi = smem_desc_sw128(base + C::kPhi), dPlo = smem_desc_sw128(base + C::kPlo);
       // S_j into buffer j % 2 (its previous scores, S_{j-2}, were read before P_{j-2} was ready)
       auto issue_s = [&](int j) -> bool {
         const int st = j % C::kStages;
@@ -367,11 +368,12 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         }
         tc_fence_after();
         const uint64_t dV = smem_desc_sw128(vst(st));
-        // V is MN-major: a 16-key K step is 16 rows = 2048 bytes (+128)
+        // P from tensor memory (a 16-key K step is 8 columns); V is MN-major:
+        // a 16-key K step is 16 rows = 2048 bytes (+128)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16(tO, dPhi + 2 * k, dV + 128 * k, idPV, j > 0 || k > 0);
+        for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tPhi + 8 * k, dV + 128 * k, idPV, j > 0 || k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16(tO, dPlo + 2 * k, dV + 128 * k, idPV, true);
+        for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tPlo + 8 * k, dV + 128 * k, idPV, true);
         umma_commit(smem_addr(&v_empty[st]));
         umma_commit(smem_addr(&pv_done));
       }
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       s_xchg[j & 1][hf][r] = mt[0];
       pair_sync();
       const float mx = fmaxf(mt[0], s_xchg[j & 1][hf ^ 1][r]);
-      // O and the P tile belong to P_{j-1} V_{j-1} until it completes
+      // O and P belong to P_{j-1} V_{j-1} until it completes
       if (j > 0 && !mbar_wait_bounded(smem_addr(&pv_done), (j - 1) & 1)) failed = true;
       if (mx > m_ref + kSlack) {
         // move the reference up; O (this thread's half of the columns) and l follow
@@ -466,27 +468,23 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         }
         m_ref = mx;
       }
-      // P = exp2(S - m_ref), as bf16 high part and remainder, swizzled rows
+      // P = exp2(S - m_ref) as bf16 high part and remainder, into tensor
+      // memory: this thread's 32 keys are columns 16 hf .. 16 hf + 15
       const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // all scores -inf: P = 0
-      float lp[4];
+      float lp[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int c = 4 * hf + cc;
-        uint32_t hi[4], lo[4];
-        lp[cc] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(sv[8 * cc + 2 * e] - m_use);
-          const float p1 = fast_exp2(sv[8 * cc + 2 * e + 1] - m_use);
-          lp[cc] += p0 + p1;
-          hi[e] = pack_bf16x2(p0, p1);
-          const float2 f = bf16x2_to_float2(hi[e]);
-          lo[e] = pack_bf16x2(p0 - f.x, p1 - f.y);
-        }
-        const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(gbase + C::kPhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(gbase + C::kPlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      for (int e = 0; e < 16; ++e) {
+        const float p0 = fast_exp2(sv[2 * e] - m_use);
+        const float p1 = fast_exp2(sv[2 * e + 1] - m_use);
+        lp[e & 3] += p0 + p1;
+        hi[e] = pack_bf16x2(p0, p1);
+        const float2 f = bf16x2_to_float2(hi[e]);
+        lo[e] = pack_bf16x2(p0 - f.x, p1 - f.y);
       }
+      tmem_st16u(tPhi + lane_addr + 16 * hf, hi);
+      tmem_st16u(tPlo + lane_addr + 16 * hf, lo);
+      tmem_wait_st();
       l_sum += (lp[0] + lp[1]) + (lp[2] + lp[3]);
       // V rows that hold no key of the tile (past its last position, or of a
       // page with a bad id) are zeroed once the stage's V copies have landed,
