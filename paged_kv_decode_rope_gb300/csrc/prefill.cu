@@ -208,19 +208,6 @@ constexpr float kSlack = 8.f;
 // 192-223 and P_lo in 224-255 (two bf16 keys per column)
 constexpr uint32_t kTmemCols = 256;
 
-// Bits 0-3: which of step j's four pages have a bad page id.
-__device__ __forceinline__ int bad_pages(const int32_t* bt, int j, int n_pages, long long num_pages) {
-  int bad = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int pg = 4 * j + q;
-    if (pg >= n_pages) continue;
-    const int page = bt[pg];
-    if (page < 0 || static_cast<long long>(page) >= num_pages) bad |= 1 << q;
-  }
-  return bad;
-}
-
 template <int G>
 __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv16_map, const PrefillAttnParams p) {
@@ -279,58 +266,73 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   bool failed = false;
 
   if (warp == 8) {
-    // ---- TMA producer: step j's four pages into stage j % kStages ----
-    if (lane == 0) {
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_steps && !failed; ++j) {
-        const int st = j % C::kStages, use = j / C::kStages;
-        int pages[4];
-        uint32_t bytes = 0;
-        int bad = 0;
-        for (int q = 0; q < 4; ++q) {
-          const int pg = 4 * j + q;
-          pages[q] = -1;
-          if (pg >= n_pages) continue;
-          const int page = bt[pg];
-          if (page < 0 || static_cast<long long>(page) >= p.num_pages) {
-            bad = 1;
-            continue;
-          }
-          pages[q] = page;
-          bytes += kHalfBytes;
+    // ---- TMA producer: step j's four pages into stage j % kStages. The
+    // warp reads the page ids 32 at a time (lane i: page 32 m + i), the next
+    // 32 while it issues the current ones, so no step waits for a block-table
+    // load; lane 0 issues the copies. ----
+    int k_issued = 0, v_issued = 0;
+    int pid = lane < n_pages ? bt[lane] : -1;
+    int pid_next = 32 + lane < n_pages ? bt[32 + lane] : -1;
+    for (int j = 0; j < n_steps && !failed; ++j) {
+      const int st = j % C::kStages, use = j / C::kStages;
+      if (j > 0 && (j & 7) == 0) {  // the next 32 pages
+        pid = pid_next;
+        const int nxt = 4 * j + 32 + lane;
+        pid_next = nxt < n_pages ? bt[nxt] : -1;
+      }
+      int pages[4];
+      uint32_t bytes = 0;
+      int bad = 0;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int pg = 4 * j + q;
+        const int page = __shfl_sync(kFull, pid, (4 * j + q) & 31);
+        pages[q] = -1;
+        if (pg >= n_pages) continue;
+        if (page < 0 || static_cast<long long>(page) >= p.num_pages) {
+          bad = 1;
+          continue;
         }
-        if (bad) atomicOr(p.err, PKV_ERR_PAGE_ID);
-        // K tile: free once the stage's scores are done
-        if (use > 0 && !mbar_wait_bounded(smem_addr(&k_empty[st]), (use - 1) & 1)) {
-          failed = true;
-          break;
-        }
+        pages[q] = page;
+        bytes += kHalfBytes;
+      }
+      if (bad && lane == 0) atomicOr(p.err, PKV_ERR_PAGE_ID);
+      // K tile: free once the stage's scores are done
+      if (use > 0 && !mbar_wait_bounded(smem_addr(&k_empty[st]), (use - 1) & 1)) failed = true;
+      if (__any_sync(kFull, failed)) {
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
         mbar_arrive_expect_tx(smem_addr(&k_full[st]), bytes);
         for (int q = 0; q < 4; ++q)
           if (pages[q] >= 0)
             tma_load_2d(kst(st) + q * kHalfBytes, &kv16_map, 0, (pages[q] * p.hkv + h) * (2 * kPage),
                         smem_addr(&k_full[st]));
-        k_issued = j + 1;
-        // V tile: free once the stage's P V product is done
-        if (use > 0 && !mbar_wait_bounded(smem_addr(&v_empty[st]), (use - 1) & 1)) {
-          failed = true;
-          break;
-        }
+      }
+      k_issued = j + 1;
+      // V tile: free once the stage's P V product is done
+      if (use > 0 && !mbar_wait_bounded(smem_addr(&v_empty[st]), (use - 1) & 1)) failed = true;
+      if (__any_sync(kFull, failed)) {
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
         mbar_arrive_expect_tx(smem_addr(&v_full[st]), bytes);
         for (int q = 0; q < 4; ++q)
           if (pages[q] >= 0)
             tma_load_2d(vst(st) + q * kHalfBytes, &kv16_map, 0,
                         (pages[q] * p.hkv + h) * (2 * kPage) + kPage, smem_addr(&v_full[st]));
-        v_issued = j + 1;
       }
-      // let the copies still in flight (the last kStages steps at most) land
-      // before shared memory goes away
-      if (failed) {
-        for (int j = max(0, k_issued - C::kStages); j < k_issued; ++j)
-          mbar_wait_bounded(smem_addr(&k_full[j % C::kStages]), (j / C::kStages) & 1);
-        for (int j = max(0, v_issued - C::kStages); j < v_issued; ++j)
-          mbar_wait_bounded(smem_addr(&v_full[j % C::kStages]), (j / C::kStages) & 1);
-      }
+      v_issued = j + 1;
+    }
+    // let the copies still in flight (the last kStages steps at most) land
+    // before shared memory goes away
+    if (failed && lane == 0) {
+      for (int j = max(0, k_issued - C::kStages); j < k_issued; ++j)
+        mbar_wait_bounded(smem_addr(&k_full[j % C::kStages]), (j / C::kStages) & 1);
+      for (int j = max(0, v_issued - C::kStages); j < v_issued; ++j)
+        mbar_wait_bounded(smem_addr(&v_full[j % C::kStages]), (j / C::kStages) & 1);
     }
   } else if (warp == 9) {
     // ---- MMA issuer ----
@@ -422,12 +424,23 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       mbar_arrive(smem_addr(&q_ready));
     }
     float m_ref = -INFINITY, l_sum = 0.f;
-    int bad_next = bad_pages(bt, 0, n_pages, p.num_pages);
+    // which pages have a bad id: bit i of bad_win for page 32 m + i, from the
+    // warp's window of page ids (lane i reads page 32 m + i), the next window
+    // loaded while this one is used
+    auto bad_bits = [&](int m) {
+      const int pg = 32 * m + lane;
+      const int page = pg < n_pages ? bt[pg] : 0;
+      return __ballot_sync(kFull, pg < n_pages && (page < 0 || static_cast<long long>(page) >= p.num_pages));
+    };
+    uint32_t bad_win = bad_bits(0), bad_nextwin = n_pages > 32 ? bad_bits(1) : 0u;
     for (int j = 0; j < n_steps; ++j) {
       const int st = j % C::kStages;
       const int k0 = 64 * j + 32 * hf;  // key position of this thread's first column
-      const int bad = bad_next;
-      if (j + 1 < n_steps) bad_next = bad_pages(bt, j + 1, n_pages, p.num_pages);
+      if (j > 0 && (j & 7) == 0) {
+        bad_win = bad_nextwin;
+        bad_nextwin = 32 * (j / 8 + 1) < n_pages ? bad_bits(j / 8 + 1) : 0u;
+      }
+      const int bad = static_cast<int>((bad_win >> ((4 * j) & 31)) & 0xFu);
       if (!mbar_wait_bounded(smem_addr(&s_full[j & 1]), (j >> 1) & 1)) failed = true;
       tc_fence_after();
       float sv[32];
