@@ -110,3 +110,27 @@ def test_malformed_chunk_is_flagged_and_zeroed():
     assert pkv.pkv_get_error(kp, reset=True) & pkv.ERR_SEQ_LEN
     assert (out[2:] == 0).all() and torch.isfinite(out[:2]).all() and (out[:2] != 7.0).any()
     kp.close()
+
+
+def test_bad_page_id_is_flagged_and_masked():
+    """A block-table entry outside the pool: the page is neither written nor
+    read (its keys get no weight), the error bit is set, outputs stay finite."""
+    dev = torch.device("cuda")
+    hkv, hq = 8, 32
+    gen = torch.Generator().manual_seed(9)
+    pool = torch.randn(16 * 2 * hkv * 16 * 64, generator=gen).to(torch.bfloat16).to(dev)
+    kp = pkv.kv_pool_create(pool, hkv)
+    t = 70
+    q = torch.randn(t, hq, 64, generator=gen).to(torch.bfloat16).to(dev)
+    k = torch.randn(t, hkv, 64, generator=gen).to(torch.bfloat16).to(dev)
+    v = torch.randn(t, hkv, 64, generator=gen).to(torch.bfloat16).to(dev)
+    bt = torch.tensor([[3, 7, 99, 1, 5]], dtype=torch.int32, device=dev)  # page 2 of 5 is bad
+    q_rot = torch.empty(t, hq, 64, device=dev)
+    out = torch.empty(t, hq, 64, device=dev)
+    ws = pkv.alloc_prefill_workspace(t, 1, 5, device=dev)
+    pkv.paged_prefill(kp, q, k, v, q_rot, out, bt, torch.tensor([0, t], dtype=torch.int32, device=dev),
+                      torch.tensor([0], dtype=torch.int32, device=dev), 500000.0, 0.125, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_error(kp, reset=True) & pkv.ERR_PAGE_ID
+    assert torch.isfinite(out).all()
+    kp.close()
