@@ -468,11 +468,13 @@ def run_prefill(args, ws, rank, local) -> int:
     q_rot = torch.empty(nl, total, hq, 64, device=dev)
     out = torch.empty(nl, total, hq, 64, device=dev)
     wsp = pkv.alloc_prefill_workspace(total, nb, mb, device=dev)
+    rope = pkv.alloc_prefill_rope_table(total, device=dev)
 
-    def step():
+    def step():  # the RoPE table once per pass (same positions in every layer), then every layer
+        pkv.paged_prefill_rope_table(cu, st, total, mb, theta, rope)
         for layer in range(nl):
             pkv.paged_prefill(kp, q[layer], k[layer], v[layer], q_rot[layer], out[layer], bt[layer],
-                              cu, st, theta, 0.125, wsp)
+                              cu, st, theta, 0.125, wsp, rope_table=rope)
 
     for _ in range(2):
         step()

@@ -240,9 +240,11 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks
  *                start_pos[b] + chunk length assigned;  cu_tokens int32 [batch+1]
  *                (cu_tokens[0] = 0, non-decreasing, cu_tokens[batch] = total_tokens);
  *                start_pos int32 [batch] (>= 0)
+ *   rope_table   from paged_prefill_rope_table for these chunks, or NULL (then
+ *                the call builds it in the workspace)
  *   workspace    device memory of at least paged_prefill_workspace_bytes(),
  *                256-byte aligned, contents irrelevant
- * Launches five kernels on `stream`: an expansion of the chunk tokens (each
+ * Launches five kernels on `stream` (four with a rope_table): an expansion of the chunk tokens (each
  * token's sequence and position), the RoPE table of their positions (as
  * paged_rope_cos_sin), the append (every chunk token stored as a decode
  * token would be, with the same certified key rounding), a tile plan, and a
@@ -256,8 +258,20 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks
 int paged_prefill(pkv_pool_t *pool, const void *q, const void *k, const void *v, float *q_rot,
                   float *out, const int32_t *block_tables, int max_blocks,
                   const int32_t *cu_tokens, const int32_t *start_pos, int batch, int total_tokens,
-                  int num_q_heads, double rope_theta, float scale, void *workspace,
-                  size_t workspace_bytes, void *stream);
+                  int num_q_heads, double rope_theta, float scale, const void *rope_table,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The RoPE table of a prefill call's chunk tokens, to be built once and
+ * handed to every layer's paged_prefill (the positions are the same in every
+ * layer). Token t (rows in cu_tokens order) of sequence b sits at position
+ * start_pos[b] + (t - cu_tokens[b]); a token of a malformed chunk gets
+ * position 0. Layout: as paged_rope_cos_sin with batch = total_tokens, i.e.
+ * PKV_ROPE_TABLE_BYTES(total_tokens) bytes, 16-byte aligned.
+ */
+int paged_prefill_rope_table(const int32_t *cu_tokens, const int32_t *start_pos, int batch,
+                             int total_tokens, int max_blocks, double rope_theta, void *table,
+                             void *stream);
 
 /* Bytes of the fixed device array paged_gqa_decode_no_alloc uses as workspace. */
 #define PKV_NO_ALLOC_SCRATCH_BYTES (8u << 20)

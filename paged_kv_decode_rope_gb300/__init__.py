@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     KVPool,
     PkvError,
     alloc_decode_workspace,
+    alloc_prefill_rope_table,
     alloc_prefill_workspace,
     alloc_rope_table,
     decode_max_splits,
@@ -36,6 +37,7 @@ from ._binding import (  # noqa: F401
     paged_kv_append_rope,
     paged_kv_split_combine,
     paged_prefill,
+    paged_prefill_rope_table,
     paged_prefill_workspace_bytes,
     paged_rope_cos_sin,
     pkv_get_error,

@@ -42,7 +42,8 @@ _SIGNATURES = {
     "paged_kv_split_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "paged_prefill_workspace_bytes": (_sz, [_i, _i, _i]),
     "paged_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _d, _f, _vp,
-                           _sz, _vp]),
+                           _vp, _sz, _vp]),
+    "paged_prefill_rope_table": (_i, [_vp, _vp, _i, _i, _i, _d, _vp, _vp]),
     "pkv_get_error": (_i, [_vp, ctypes.POINTER(_i), _i]),
     "pkv_last_cuda_error": (_i, []),
     # include/pkv_sched.h (host only)
@@ -277,12 +278,30 @@ def alloc_prefill_workspace(total_tokens: int, batch: int, max_blocks: int,
     return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
 
 
+def alloc_prefill_rope_table(total_tokens: int, device=None) -> torch.Tensor:
+    return torch.empty(max(total_tokens, 1) * ROPE_TABLE_BYTES_PER_SEQ, dtype=torch.uint8,
+                       device=device or torch.device("cuda"))
+
+
+def paged_prefill_rope_table(cu_tokens: torch.Tensor, start_pos: torch.Tensor, total_tokens: int,
+                             max_blocks: int, rope_theta: float, table: torch.Tensor,
+                             stream=None) -> None:
+    """The chunk tokens' RoPE table, built once and handed to every layer's paged_prefill."""
+    batch = start_pos.shape[0]
+    rc = lib().paged_prefill_rope_table(
+        _dev(cu_tokens, torch.int32, "cu_tokens", 1), _dev(start_pos, torch.int32, "start_pos", 1),
+        batch, total_tokens, max_blocks, float(rope_theta), _dev(table, torch.uint8, "table", 1),
+        _stream(stream))
+    _check("paged_prefill_rope_table", rc)
+
+
 def paged_prefill(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                   q_rot: torch.Tensor, out: torch.Tensor, block_tables: torch.Tensor,
                   cu_tokens: torch.Tensor, start_pos: torch.Tensor, rope_theta: float, scale: float,
-                  workspace: torch.Tensor, stream=None) -> None:
+                  workspace: torch.Tensor, stream=None, rope_table: torch.Tensor | None = None) -> None:
     """Chunked causal prefill. q [T,Hq,64], k/v [T,Hkv,64] bf16; q_rot/out [T,Hq,64]
-    fp32 out; block_tables [B,max_blocks], cu_tokens [B+1], start_pos [B] int32."""
+    fp32 out; block_tables [B,max_blocks], cu_tokens [B+1], start_pos [B] int32;
+    rope_table from paged_prefill_rope_table (built once for all layers) or None."""
     total, hq = q.shape[0], q.shape[1]
     batch = block_tables.shape[0]
     rc = lib().paged_prefill(
@@ -291,8 +310,8 @@ def paged_prefill(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
         _dev(out, torch.float32, "out", 3), _dev(block_tables, torch.int32, "block_tables", 2),
         block_tables.shape[1], _dev(cu_tokens, torch.int32, "cu_tokens", 1),
         _dev(start_pos, torch.int32, "start_pos", 1), batch, total, hq, float(rope_theta),
-        float(scale), _dev(workspace, torch.uint8, "workspace", 1), workspace.numel(),
-        _stream(stream))
+        float(scale), None if rope_table is None else _dev(rope_table, torch.uint8, "rope_table", 1),
+        _dev(workspace, torch.uint8, "workspace", 1), workspace.numel(), _stream(stream))
     _check("paged_prefill", rc)
 
 

@@ -281,11 +281,25 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks
   return pkv::prefill_workspace_bytes(total_tokens, batch, max_blocks);
 }
 
+int paged_prefill_rope_table(const int32_t* cu_tokens, const int32_t* start_pos, int batch,
+                             int total_tokens, int max_blocks, double rope_theta, void* table,
+                             void* stream) {
+  if (batch < 0 || total_tokens < 0 || max_blocks < 1 || !(rope_theta > 0.0) ||
+      !std::isfinite(rope_theta))
+    return -EINVAL;
+  if (total_tokens == 0) return 0;
+  if (batch < 1 || !cu_tokens || !start_pos || !table || !aligned16(table)) return -EINVAL;
+  const cudaError_t e = pkv::launch_prefill_rope_table(cu_tokens, start_pos, batch, total_tokens,
+                                                       max_blocks, rope_theta, table,
+                                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
 int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v, float* q_rot,
                   float* out, const int32_t* block_tables, int max_blocks,
                   const int32_t* cu_tokens, const int32_t* start_pos, int batch, int total_tokens,
-                  int num_q_heads, double rope_theta, float scale, void* workspace,
-                  size_t workspace_bytes, void* stream) {
+                  int num_q_heads, double rope_theta, float scale, const void* rope_table,
+                  void* workspace, size_t workspace_bytes, void* stream) {
   if (!decode_shape_ok(pool, total_tokens, num_q_heads, max_blocks) || batch < 0 ||
       total_tokens < 0 || !(rope_theta > 0.0) || !std::isfinite(rope_theta) ||
       !std::isfinite(scale))
@@ -294,7 +308,7 @@ int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v,
   if (batch < 1) return -EINVAL;
   if (!q || !k || !v || !q_rot || !out || !block_tables || !cu_tokens || !start_pos || !workspace)
     return -EINVAL;
-  if (!aligned16(q_rot) || !aligned16(out) || !aligned16(v) ||
+  if (!aligned16(q_rot) || !aligned16(out) || !aligned16(v) || !aligned16(rope_table) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return -EINVAL;
   int device = 0;
@@ -323,6 +337,7 @@ int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v,
   a.num_q_heads = num_q_heads;
   a.rope_theta = rope_theta;
   a.scale = scale;
+  a.rope_table = rope_table;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.sm_count = sms;

@@ -99,6 +99,7 @@ struct PrefillLaunch {
   int num_q_heads;
   double rope_theta;
   float scale;
+  const void* rope_table;  // the chunk tokens' RoPE table, or null: built in the workspace
   void* workspace;
   size_t workspace_bytes;
   int sm_count;
@@ -106,6 +107,9 @@ struct PrefillLaunch {
 };
 
 size_t prefill_workspace_bytes(int total_tokens, int batch, int max_blocks);
+cudaError_t launch_prefill_rope_table(const int32_t* cu_tokens, const int32_t* start_pos, int batch,
+                                      int total_tokens, int max_blocks, double rope_theta, void* table,
+                                      cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream);
 
 // Largest batch one decode launch serves (sequence lengths and page prefix sums

@@ -30,6 +30,23 @@ namespace {
 constexpr int kExpandThreads = 256;
 constexpr int kHalfDim = kHeadDim / 2;
 
+// The position of chunk token idx (its sequence found by bisection over
+// cu_tokens), or -1 for a token of a malformed chunk.
+__device__ __forceinline__ long long chunk_position(const int32_t* cu_tokens, const int32_t* start_pos,
+                                                    int batch, int max_blocks, int idx, int* seq) {
+  int lo = 0, hi = batch - 1;  // largest b with cu_tokens[b] <= idx
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu_tokens[mid] <= idx) lo = mid; else hi = mid - 1;
+  }
+  const int c0 = cu_tokens[lo], c1 = cu_tokens[lo + 1];
+  const long long pos = static_cast<long long>(start_pos[lo]) + (idx - c0);
+  *seq = lo;
+  const bool ok = c0 <= idx && idx < c1 && start_pos[lo] >= 0 &&
+                  pos + 1 <= static_cast<long long>(max_blocks) * kPage;
+  return ok ? pos : -1;
+}
+
 // One thread per chunk token: find its sequence by bisection over cu_tokens
 // and write it (-1 when the sequence's chunk is malformed: a decreasing
 // cu_tokens, a negative start, or a position past max_blocks*16) and its
@@ -39,18 +56,35 @@ __global__ void prefill_expand_kernel(int max_blocks, const int32_t* __restrict_
                                       int32_t* __restrict__ tok_seq, int32_t* __restrict__ tok_pos) {
   const int idx = blockIdx.x * kExpandThreads + threadIdx.x;
   if (idx >= total) return;
-  int lo = 0, hi = batch - 1;  // largest b with cu_tokens[b] <= idx
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cu_tokens[mid] <= idx) lo = mid; else hi = mid - 1;
-  }
-  const int b = lo;
-  const int c0 = cu_tokens[b], c1 = cu_tokens[b + 1];
-  const long long pos = static_cast<long long>(start_pos[b]) + (idx - c0);
-  const bool ok = c0 <= idx && idx < c1 && start_pos[b] >= 0 &&
-                  pos + 1 <= static_cast<long long>(max_blocks) * kPage;
-  tok_seq[idx] = ok ? b : -1;
-  tok_pos[idx] = ok ? static_cast<int32_t>(pos) : 0;
+  int b;
+  const long long pos = chunk_position(cu_tokens, start_pos, batch, max_blocks, idx, &b);
+  tok_seq[idx] = pos >= 0 ? b : -1;
+  tok_pos[idx] = pos >= 0 ? static_cast<int32_t>(pos) : 0;
+}
+
+struct PrefillInvFreq {
+  double v[kHalfDim];  // theta^(-2j/64), from the C library's pow on the host
+};
+
+// One thread per (chunk token, frequency): cos and sin of its position times
+// inv_freq_j in fp64 (position 0 for a token of a malformed chunk), stored as
+// fp32 pairs {hi, lo} and in fp64: the layout of paged_rope_cos_sin's table.
+__global__ void prefill_rope_kernel(const int32_t* __restrict__ cu_tokens,
+                                    const int32_t* __restrict__ start_pos, int batch, int total,
+                                    int max_blocks, const PrefillInvFreq inv,
+                                    float4* __restrict__ pairs, double2* __restrict__ full) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= total * kHalfDim) return;
+  const int tkn = idx / kHalfDim, j = idx - tkn * kHalfDim;
+  int seq;
+  const long long pos = chunk_position(cu_tokens, start_pos, batch, max_blocks, tkn, &seq);
+  const double angle = __dmul_rn(static_cast<double>(pos < 0 ? 0 : pos), inv.v[j]);
+  double sn, cs;
+  sincos(angle, &sn, &cs);
+  const float ch = __double2float_rn(cs), sh = __double2float_rn(sn);
+  pairs[idx] = make_float4(ch, __double2float_rn(__dsub_rn(cs, static_cast<double>(ch))), sh,
+                           __double2float_rn(__dsub_rn(sn, static_cast<double>(sh))));
+  full[idx] = make_double2(cs, sn);
 }
 
 // One CTA per chunk token: its rotated query (fp32, from the fp32 cos/sin of
@@ -609,6 +643,21 @@ cudaError_t launch_attn(const PrefillLaunch& a, const PrefillLayout& l, cudaStre
 
 }  // namespace
 
+cudaError_t launch_prefill_rope_table(const int32_t* cu_tokens, const int32_t* start_pos, int batch,
+                                      int total_tokens, int max_blocks, double rope_theta, void* table,
+                                      cudaStream_t stream) {
+  if (total_tokens == 0) return cudaSuccess;
+  PrefillInvFreq inv;
+  for (int j = 0; j < kHalfDim; ++j)
+    inv.v[j] = std::pow(rope_theta, -(2.0 * j) / static_cast<double>(kHeadDim));
+  const int n = total_tokens * kHalfDim;
+  float4* pairs = static_cast<float4*>(table);
+  double2* full = reinterpret_cast<double2*>(pairs + n);
+  prefill_rope_kernel<<<(n + 255) / 256, 256, 0, stream>>>(cu_tokens, start_pos, batch, total_tokens,
+                                                            max_blocks, inv, pairs, full);
+  return cudaGetLastError();
+}
+
 size_t prefill_workspace_bytes(int total_tokens, int batch, int max_blocks) {
   return layout(total_tokens, batch, max_blocks).total;
 }
@@ -625,9 +674,14 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream) {
                                     tok_seq, tok_pos);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // cos/sin of every chunk token's position: fp32 pairs, then fp64
-  e = launch_rope_cos_sin(tok_pos, a.total_tokens, a.rope_theta, rope, stream);
-  if (e != cudaSuccess) return e;
+  // cos/sin of every chunk token's position (fp32 pairs, then fp64): the
+  // caller's table (built once for all layers), else one in the workspace
+  if (a.rope_table) {
+    rope = const_cast<void*>(a.rope_table);
+  } else {
+    e = launch_rope_cos_sin(tok_pos, a.total_tokens, a.rope_theta, rope, stream);
+    if (e != cudaSuccess) return e;
+  }
   const float4* rope_ff = static_cast<const float4*>(rope);
   const double2* rope_dd =
       reinterpret_cast<const double2*>(rope_ff + static_cast<size_t>(a.total_tokens) * kHalfDim);

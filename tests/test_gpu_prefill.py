@@ -15,7 +15,7 @@ from tests.parity import assert_close, u16
 pytestmark = pytest.mark.gpu
 
 
-def _run(starts, lens, hq=32, hkv=8, theta=500000.0, seed=0, max_blocks=None):
+def _run(starts, lens, hq=32, hkv=8, theta=500000.0, seed=0, max_blocks=None, table=False):
     rng = np.random.default_rng(seed)
     gen = torch.Generator().manual_seed(seed)
     ends = [s + n for s, n in zip(starts, lens)]
@@ -50,8 +50,13 @@ def _run(starts, lens, hq=32, hkv=8, theta=500000.0, seed=0, max_blocks=None):
     q_rot = torch.empty(total, hq, 64, device=dev)
     out = torch.empty(total, hq, 64, device=dev)
     ws = pkv.alloc_prefill_workspace(total, len(starts), mb, device=dev)
+    d_cu, d_st = torch.from_numpy(cu).to(dev), torch.from_numpy(st).to(dev)
+    rope = None
+    if table:  # the table built once, as for all the layers of a pass
+        rope = pkv.alloc_prefill_rope_table(total, device=dev)
+        pkv.paged_prefill_rope_table(d_cu, d_st, total, mb, theta, rope)
     pkv.paged_prefill(kp, q.to(dev), k.to(dev), v.to(dev), q_rot, out, torch.from_numpy(bt).to(dev),
-                      torch.from_numpy(cu).to(dev), torch.from_numpy(st).to(dev), theta, scale, ws)
+                      d_cu, d_st, theta, scale, ws, rope_table=rope)
     torch.cuda.synchronize()
     assert pkv.pkv_get_error(kp) == 0
     got_pool = u16(dpool)
@@ -84,6 +89,11 @@ def test_long_prompt_many_tiles():
 
 def test_tiles_after_a_prefix_ending_mid_page():
     _run([100, 7], [70, 33], seed=6)
+
+
+def test_prebuilt_rope_table():
+    _run([0, 17, 300, 64], [16, 1, 45, 33], seed=10, table=True)
+    _run([5, 0], [40, 70], hq=14, hkv=2, theta=1e6, seed=11, table=True)
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (12, 4), (10, 2), (12, 2), (64, 8)])
