@@ -10,7 +10,6 @@ whole pool bit for bit at the end (pages reused after release included).
 """
 import numpy as np
 import pytest
-import torch
 
 import oracle
 import workloads
