@@ -405,8 +405,9 @@ def run_ours(args, ws, rank, local):
 
 
 def run_trace(args, ws, rank, local) -> int:
-    """A continuous-batching decode trace (page scheduler + fused decode steps),
-    Llama-3.2-1B shape, 16 layers, 2.5 GiB pool. Prints one JSON line of its own."""
+    """A continuous-batching trace (page scheduler, paged prefill of the admitted
+    prompts, fused decode steps), Llama-3.2-1B shape, 16 layers, 2.5 GiB pool.
+    Prints one JSON line of its own."""
     import paged_kv_decode_rope_gb300 as pkv  # noqa: F401  (loads the library)
     from paged_kv_decode_rope_gb300.build import build
     from paged_kv_decode_rope_gb300.trace import DecodeTrace
@@ -416,7 +417,7 @@ def run_trace(args, ws, rank, local) -> int:
                                     new_range=(32, 256), early_stop_frac=0.3)
     tr = DecodeTrace(reqs, num_pages=81920, num_layers=16, num_q_heads=32, num_kv_heads=8,
                      rope_theta=500000.0, seed=args.seed + 1000 * rank, max_batch=256,
-                     device=torch.device("cuda", local), device_inputs=True)
+                     device=torch.device("cuda", local), device_inputs=True, prefill_tokens=8192)
     st = tr.run()
     tr.close()
     ms = _barrier_max(st["device_ms"], ws)
@@ -430,12 +431,18 @@ def run_trace(args, ws, rank, local) -> int:
                 "device_ms": round(st["device_ms"], 2), "wall_s": round(st["wall_s"], 2),
                 "wall_tokens_per_s": round(st["decode_tokens"] / st["wall_s"], 1),
                 "completed": st["completed"], "sched": st["sched"],
+                "prefill": {"calls": st["prefill_calls"], "prompt_tokens": st["prompt_tokens"],
+                            "device_ms": round(st["prefill_ms"], 2),
+                            "tokens_per_s": round(st["prompt_tokens"] / (st["prefill_ms"] / 1e3), 1)},
                 "config": {"requests": args.trace, "prompt": "U[64,1024]", "max_new": "U[32,256]",
                            "early_stop": 0.3, "layers": 16, "q_heads": 32, "kv_heads": 8,
-                           "pool_pages": 81920, "batching": "continuous"},
+                           "pool_pages": 81920, "batching": "continuous",
+                           "prefill_call_tokens": 8192},
                 "data": "synthetic (seeded)",
                 "timing": "CUDA events around each step's RoPE table and per-layer fused decode "
-                          "calls, summed; wall time includes host scheduling and input copies"}
+                          "calls, summed (prefill: around each call's RoPE table and per-layer "
+                          "paged_prefill calls); wall time includes host scheduling, input "
+                          "draws and copies"}
         print(json.dumps(line), flush=True)
     return 0
 

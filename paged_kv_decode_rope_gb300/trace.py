@@ -1,13 +1,17 @@
 """Multi-step decode traces: continuous batching over the shared page pool.
 
 A PageScheduler admits requests under their page budgets and hands out pages
-lazily; every step runs the fused decode step (RoPE, append, paged GQA decode)
-through the C ABI for the active batch, whose sequences grow by one token per
-step and cross page boundaries as they go. This is the batched decode loop of
-"Hours of YouTube and 85 handtyped pages of notes on LLM Inference – Start
-here" (continuous batching item) around this library's kernels; prefill is not
-part of the library, so a request's prompt slots are filled with the seeded
-K/V a prefill would have left (workloads.trace_prompt_kv).
+lazily. The requests admitted in one pass are prefilled together through the
+C ABI (paged_prefill: their prompts' keys rotated and stored in their pages,
+causal attention over the prompt), in calls of at most prefill_tokens chunk
+tokens, a long prompt split into chunks over several calls. Then every step
+runs the fused decode step (RoPE, append, paged GQA decode) for the active
+batch, whose sequences grow by one token per step and cross page boundaries
+as they go. This is the batched engine loop of "Hours of YouTube and 85
+handtyped pages of notes on LLM Inference – Start here" (continuous batching
+and dense causal prefill items) around this library's kernels; the model's
+projections are not part of the library, so every prompt and step token
+brings seeded q/k/v (workloads.trace_prompt_qkv, workloads.trace_step_qkv).
 
 Per request: after its prefill it holds prompt_len tokens and has produced its
 first token; each decode step processes the newest token (appending it at its
@@ -27,11 +31,33 @@ from . import _binding as B
 from .sched import PageScheduler
 
 
+def pack_prefill_chunks(requests, prompt_lens, budget: int):
+    """Chunks (request, start, length) of the prompts, packed in order into calls
+    of at most budget tokens. A prompt that does not fit the rest of a call
+    continues in the next one, so a call never holds two chunks of one request
+    (a chunk's attention reads the pages its earlier chunks stored)."""
+    if budget < 1:
+        raise ValueError("budget must be positive")
+    calls, cur, room = [], [], budget
+    for r, n_tok in zip(requests, prompt_lens):
+        start, left = 0, int(n_tok)
+        while left > 0:
+            n = min(left, room)
+            cur.append((r, start, n))
+            start, left, room = start + n, left - n, room - n
+            if room == 0:
+                calls.append(cur)
+                cur, room = [], budget
+    if cur:
+        calls.append(cur)
+    return calls
+
+
 class DecodeTrace:
     def __init__(self, requests, *, num_pages: int, num_layers: int, num_q_heads: int,
                  num_kv_heads: int, rope_theta: float, seed: int = 0, context_len: int = 2048,
                  static_batching: bool = False, max_batch: int = 256, device="cuda",
-                 device_inputs: bool = False):
+                 device_inputs: bool = False, prefill_tokens: int = 8192):
         self.requests = list(requests)
         self.num_layers, self.hq, self.hkv = num_layers, num_q_heads, num_kv_heads
         self.rope_theta, self.seed = float(rope_theta), seed
@@ -55,31 +81,76 @@ class DecodeTrace:
         self.tokens = 0      # decode tokens processed
         self.kv_bytes = 0    # KV bytes the decode steps read (valid tokens)
         self.device_ms = 0.0
+        self.prefill_tokens = int(prefill_tokens)
+        if self.prefill_tokens < 1:
+            raise ValueError("prefill_tokens must be positive")
+        self.prefill_calls = 0
+        self.prompt_tokens = 0
+        self.prefill_ms = 0.0
         # device_inputs: draw each step's q/k/v on the GPU in one call (for
         # timing); otherwise per (request, step) on the host (reproducible
         # whatever the batch, for parity checks)
         self.device_inputs = device_inputs
         self._gen = torch.Generator(device=self.device)
         self._gen.manual_seed(seed)
+        self._prompts = {}   # request index -> its prompt q/k/v (host inputs)
 
     # -- host side -----------------------------------------------------------
-    def _fill_prompt(self, r: int) -> None:
-        """The K/V a prefill leaves in request r's prompt slots, written into its pages."""
-        req = self.requests[r]
-        kv = workloads.trace_prompt_kv(self.seed, r, self.num_layers, self.hkv, req.prompt_len)
-        view = self.pool.view(-1, self.hkv, 2, B.PAGE_SIZE, B.HEAD_DIM)
-        t = torch.arange(req.prompt_len)
+    def _prompt_qkv(self, r: int):
+        if r not in self._prompts:
+            req = self.requests[r]
+            self._prompts[r] = workloads.trace_prompt_qkv(self.seed, r, self.num_layers, self.hq,
+                                                          self.hkv, req.prompt_len)
+        return self._prompts[r]
+
+    def run_prefill(self, chunks, on_prefill=None) -> None:
+        """One paged_prefill per layer over the chunks [(request, start, length)]."""
+        dev = self.device
+        nb = len(chunks)
+        lens = np.array([c[2] for c in chunks], dtype=np.int32)
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        start = np.array([c[1] for c in chunks], dtype=np.int32)
+        total = int(cu[-1])
+        bt = np.stack([self.rows[c[0]] for c in chunks], axis=1)  # [L][B][max_blocks]
+        if self.device_inputs:
+            def draw(h):
+                return torch.randn((self.num_layers, total, h, B.HEAD_DIM), generator=self._gen,
+                                   device=dev).to(torch.bfloat16)
+            q, k, v = draw(self.hq), draw(self.hkv), draw(self.hkv)
+        else:
+            parts = [self._prompt_qkv(r) for r, _, _ in chunks]
+            q, k, v = (torch.cat([p[i][:, s:s + n] for p, (_, s, n) in zip(parts, chunks)], dim=1)
+                       .to(dev) for i in range(3))
+        d_cu = torch.from_numpy(cu).to(dev)
+        d_start = torch.from_numpy(start).to(dev)
+        d_bt = torch.from_numpy(np.ascontiguousarray(bt)).to(dev)
+        q_rot = torch.empty(self.num_layers, total, self.hq, B.HEAD_DIM, dtype=torch.float32,
+                            device=dev)
+        out = torch.empty_like(q_rot)
+        ws = B.alloc_prefill_workspace(total, nb, self.max_blocks, device=dev)
+        table = B.alloc_prefill_rope_table(total, device=dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        B.paged_prefill_rope_table(d_cu, d_start, total, self.max_blocks, self.rope_theta, table)
         for layer in range(self.num_layers):
-            pages = torch.from_numpy(self.rows[r][layer][(t // B.PAGE_SIZE).numpy()].astype(np.int64))
-            src = kv[layer].permute(2, 0, 1, 3).to(self.device)  # [P][Hkv][2][64]
-            view[pages.to(self.device), :, :, (t % B.PAGE_SIZE).to(self.device)] = src
+            B.paged_prefill(self.kvpool, q[layer], k[layer], v[layer], q_rot[layer], out[layer],
+                            d_bt[layer], d_cu, d_start, self.rope_theta, self.scale, ws,
+                            rope_table=table)
+        e1.record()
+        torch.cuda.synchronize()
+        self.prefill_ms += e0.elapsed_time(e1)
+        self.prefill_calls += 1
+        self.prompt_tokens += total
+        if on_prefill is not None:
+            on_prefill(chunks, (cu, start, bt, q, k, v), q_rot, out)
 
     def _refresh_rows(self, r: int) -> None:
         self.rows[r] = self.sched.block_rows(self.ids[r], self.max_blocks)
 
-    def admit(self, on_admit=None) -> list[int]:
+    def admit(self, on_admit=None, on_prefill=None) -> list[int]:
         """Submit what is waiting (once) and admit under the budgets; prefill the
-        admitted. on_admit(r, rows) sees each admitted request's page rows."""
+        admitted. on_admit(r, rows) sees each admitted request's page rows,
+        on_prefill(chunks, inputs, q_rot, out) every prefill call."""
         for r in self.waiting:
             if r not in self.ids:
                 req = self.requests[r]
@@ -88,12 +159,16 @@ class DecodeTrace:
         admitted = [by_id[i] for i in self.sched.admit()]
         for r in admitted:
             self.waiting.remove(r)
-            req = self.requests[r]
-            self.sched.grow(self.ids[r], req.prompt_len)
+            self.sched.grow(self.ids[r], self.requests[r].prompt_len)
             self._refresh_rows(r)
-            self._fill_prompt(r)
             if on_admit is not None:
                 on_admit(r, self.rows[r])
+        lens = [self.requests[r].prompt_len for r in admitted]
+        for chunks in pack_prefill_chunks(admitted, lens, self.prefill_tokens):
+            self.run_prefill(chunks, on_prefill)
+        for r in admitted:
+            req = self.requests[r]
+            self._prompts.pop(r, None)
             self.state[r] = [req.prompt_len, 1, 0]
             if req.stop_after <= 1:  # its only token came from the prefill
                 self._finish(r)
@@ -166,12 +241,14 @@ class DecodeTrace:
         self.tokens += len(batch)
         self.steps += 1
 
-    def run(self, on_step=None, on_admit=None, max_steps: int = 1_000_000) -> dict:
+    def run(self, on_step=None, on_admit=None, on_prefill=None,
+            max_steps: int = 1_000_000) -> dict:
         """Drive the trace to completion. on_step(batch, inputs, out) sees every
-        step, on_admit(r, rows) every admission."""
+        decode step, on_admit(r, rows) every admission, on_prefill(chunks,
+        inputs, q_rot, out) every prefill call."""
         t0 = time.perf_counter()
         while (self.waiting or self.state) and self.steps < max_steps:
-            self.admit(on_admit)
+            self.admit(on_admit, on_prefill)
             batch = self.batch()
             if not batch:
                 if self.waiting and not self.state:
@@ -190,6 +267,8 @@ class DecodeTrace:
             raise RuntimeError("device error flags set during the trace")
         return {"steps": self.steps, "decode_tokens": self.tokens, "kv_bytes": self.kv_bytes,
                 "device_ms": self.device_ms, "wall_s": wall, "completed": len(self.done),
+                "prefill_calls": self.prefill_calls, "prompt_tokens": self.prompt_tokens,
+                "prefill_ms": self.prefill_ms,
                 "sched": self.sched.stats()}
 
     def close(self) -> None:

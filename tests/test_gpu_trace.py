@@ -1,12 +1,14 @@
 """A multi-step continuous-batching decode trace against the oracle.
 
 The page scheduler admits requests under their budgets (a small pool forces
-waits) and hands out pages lazily; every decode step runs the fused step
-through the C ABI for the active batch, whose sequences cross page
-boundaries. The test mirrors the trace on a host copy of the pool with the
-oracle (the prompt slots filled from the same seeded K/V, then each step's
-append and decode), checks every step's output within the tolerance, and the
-whole pool bit for bit at the end (pages reused after release included).
+waits) and hands out pages lazily; the admitted prompts are prefilled through
+the C ABI (in calls of a bounded token count, long prompts split into chunks
+over several calls), then every decode step runs the fused step for the
+active batch, whose sequences cross page boundaries. The test mirrors the
+trace on a host copy of the pool with the oracle (each prefill call, then each
+step's append and decode), checks every prefill and step output within the
+tolerance, and the whole pool bit for bit at the end (pages reused after
+release included).
 """
 import numpy as np
 import pytest
@@ -18,8 +20,8 @@ from tests.parity import assert_close, u16
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("static", [False, True])
-def test_trace_matches_oracle_step_by_step(static):
+@pytest.mark.parametrize("static,prefill_tokens", [(False, 8192), (True, 8192), (False, 48)])
+def test_trace_matches_oracle_step_by_step(static, prefill_tokens):
     from paged_kv_decode_rope_gb300.trace import DecodeTrace
     hq, hkv, nl, theta, seed = 32, 8, 2, 500000.0, 4
     reqs = [workloads.TraceRequest(p, m, s) for p, m, s in
@@ -27,17 +29,25 @@ def test_trace_matches_oracle_step_by_step(static):
              (64, 1, 1), (200, 30, 12)]]
     # 64 pages = 2 layers x 32: budgets of 4..15 pages per layer, so requests wait
     tr = DecodeTrace(reqs, num_pages=64, num_layers=nl, num_q_heads=hq, num_kv_heads=hkv,
-                     rope_theta=theta, seed=seed, static_batching=static, max_batch=8)
+                     rope_theta=theta, seed=seed, static_batching=static, max_batch=8,
+                     prefill_tokens=prefill_tokens)
     page_elems = 2 * hkv * 16 * 64
     host = np.zeros(64 * page_elems, dtype=np.uint16)
-    view = host.reshape(64, hkv, 2, 16, 64)
-    checked = {"steps": 0, "worst": 0.0}
+    checked = {"steps": 0, "worst": 0.0, "calls": 0, "split": 0}
 
-    def on_admit(r, rows):
-        kv = u16(workloads.trace_prompt_kv(seed, r, nl, hkv, reqs[r].prompt_len))  # [L][Hkv][2][P][64]
+    def on_prefill(chunks, inputs, q_rot, out):
+        cu, start, bt, q, k, v = inputs
+        checked["split"] += sum(1 for c in chunks if c[1] > 0)
+        got_qrot, got = q_rot.cpu().numpy(), out.cpu().numpy()
         for layer in range(nl):
-            for t in range(reqs[r].prompt_len):
-                view[rows[layer][t // 16], :, :, t % 16] = kv[layer][:, :, t]
+            want_qrot, want = oracle.prefill(host, num_kv_heads=hkv, q=u16(q[layer]), k=u16(k[layer]),
+                                             v=u16(v[layer]), block_tables=bt[layer],
+                                             max_blocks=bt.shape[-1], cu_tokens=cu, start_pos=start,
+                                             num_q_heads=hq, theta=theta, scale=1.0 / 8.0)
+            np.testing.assert_allclose(got_qrot[layer], want_qrot, rtol=1e-5, atol=2e-5)
+            checked["worst"] = max(checked["worst"],
+                                   assert_close(got[layer], want, f"prefill {checked['calls']} layer {layer}"))
+        checked["calls"] += 1
 
     def on_step(batch, inputs, out):
         pos, seq_lens, bt, q, k, v = inputs
@@ -54,13 +64,17 @@ def test_trace_matches_oracle_step_by_step(static):
                                    assert_close(got[layer], want, f"step {checked['steps']} layer {layer}"))
         checked["steps"] += 1
 
-    stats = tr.run(on_step=on_step, on_admit=on_admit)
+    stats = tr.run(on_step=on_step, on_prefill=on_prefill)
     assert stats["completed"] == len(reqs)
     sched = stats["sched"]
     assert sched["admission_waits"] > 0 and sched["free_pages"] == 64 and sched["active"] == 0
     assert sched["largest_batch"] <= 8 and sched["peak_assigned_pages"] <= 64
     # every decode step processed one token of every active request
     assert stats["decode_tokens"] == sum(r.stop_after - 1 for r in reqs)
+    assert stats["prompt_tokens"] == sum(r.prompt_len for r in reqs)
+    assert stats["prefill_calls"] == checked["calls"] >= 1
+    if prefill_tokens < max(r.prompt_len for r in reqs):
+        assert checked["split"] > 0  # some prompt continued in a later call
     got_pool = u16(tr.pool)
     mism = np.flatnonzero(got_pool != host)
     assert mism.size == 0, f"{mism.size} pool elements differ, first at {mism[:5]}"

@@ -173,3 +173,28 @@ def test_c_names_are_bound():
     assert pkv.pkv_sched_stats(h)["largest_batch"] == 3
     pkv.pkv_sched_finish(h, rid)
     pkv.pkv_sched_destroy(h)
+
+
+def test_prefill_chunk_packing():
+    from paged_kv_decode_rope_gb300.trace import pack_prefill_chunks
+    calls = pack_prefill_chunks([0, 1, 2], [5, 100, 3], 48)
+    assert calls == [[(0, 0, 5), (1, 0, 43)], [(1, 43, 48)], [(1, 91, 9), (2, 0, 3)]]
+    assert pack_prefill_chunks([0, 1], [48, 48], 48) == [[(0, 0, 48)], [(1, 0, 48)]]
+    assert pack_prefill_chunks([0, 1], [0, 7], 8) == [[(1, 0, 7)]]
+    assert pack_prefill_chunks([], [], 8) == []
+    with pytest.raises(ValueError):
+        pack_prefill_chunks([0], [4], 0)
+    rng = np.random.default_rng(7)
+    for _ in range(200):
+        n = int(rng.integers(1, 12))
+        lens = rng.integers(0, 300, size=n).tolist()
+        budget = int(rng.integers(1, 400))
+        calls = pack_prefill_chunks(list(range(n)), lens, budget)
+        for call in calls:
+            assert 1 <= sum(c[2] for c in call) <= budget
+            assert len({c[0] for c in call}) == len(call)  # one chunk per request per call
+        assert all(sum(c[2] for c in call) == budget for call in calls[:-1])
+        for r in range(n):  # every prompt covered once, in order
+            pieces = [c for call in calls for c in call if c[0] == r]
+            assert [p[1] for p in pieces] == list(np.cumsum([0] + [p[2] for p in pieces])[:-1])
+            assert sum(p[2] for p in pieces) == lens[r]

@@ -276,8 +276,8 @@ def make(name: str, seed: int = 0, device="cpu", sentinel: bool = False,
 @dataclasses.dataclass
 class TraceRequest:
     """One request of a synthetic trace: prompt_len cached tokens after its
-    (stand-in) prefill, at most max_new generated tokens, and the number it
-    actually generates before stopping (<= max_new; early stop when smaller)."""
+    prefill, at most max_new generated tokens, and the number it actually
+    generates before stopping (<= max_new; early stop when smaller)."""
     prompt_len: int
     max_new: int
     stop_after: int
@@ -297,13 +297,17 @@ def trace_requests(n: int, seed: int, prompt_range=(1, 512), new_range=(1, 256),
     return out
 
 
-def trace_prompt_kv(seed: int, request: int, num_layers: int, num_kv_heads: int,
-                    prompt_len: int) -> torch.Tensor:
-    """The K/V a request's prefill leaves in its prompt slots: bf16 N(0,1)
-    [num_layers][num_kv_heads][2 (K, V)][prompt_len][64], on the CPU."""
+def trace_prompt_qkv(seed: int, request: int, num_layers: int, num_q_heads: int,
+                     num_kv_heads: int, prompt_len: int):
+    """A request's prompt as its prefill sees it: q [num_layers][prompt_len][Hq][64]
+    and k, v [num_layers][prompt_len][Hkv][64], bf16 N(0,1), on the CPU;
+    independent of which other requests share the prefill call."""
     gen = torch.Generator()
     gen.manual_seed(hash((seed, request, 0x9E)) & 0x7FFFFFFF)
-    return _bf16_normal(gen, (num_layers, num_kv_heads, 2, prompt_len, HEAD_DIM), "cpu")
+    q = _bf16_normal(gen, (num_layers, prompt_len, num_q_heads, HEAD_DIM), "cpu")
+    k = _bf16_normal(gen, (num_layers, prompt_len, num_kv_heads, HEAD_DIM), "cpu")
+    v = _bf16_normal(gen, (num_layers, prompt_len, num_kv_heads, HEAD_DIM), "cpu")
+    return q, k, v
 
 
 def trace_step_qkv(seed: int, request: int, step: int, num_layers: int, num_q_heads: int,
