@@ -67,7 +67,7 @@ extern "C" {
 /* Bits of the pool's device error word. */
 #define PKV_ERR_SEQ_LEN 0x1  /* seq_lens[b] < 1 or > max_blocks*16: sequence skipped, its output rows zeroed */
 #define PKV_ERR_PAGE_ID 0x2  /* block-table entry outside [0, num_pages): that page skipped */
-#define PKV_ERR_TIMEOUT 0x4  /* a bounded wait for a shared-memory copy gave up; results incomplete */
+#define PKV_ERR_TIMEOUT 0x4  /* a bounded wait (a copy into shared memory, or another CTA's partial) gave up; results incomplete */
 #define PKV_ERR_SPLITS  0x8  /* a row needed more than max_splits partial results: row skipped */
 
 typedef struct pkv_pool pkv_pool_t;
@@ -148,10 +148,11 @@ size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_h
  *                256-byte aligned, ZERO-FILLED before its first use. It holds
  *                the partial results of segments split between CTAs, and a
  *                zero word means "not written in this call"; every call puts
- *                the words it wrote back to zero (also when it sets
- *                PKV_ERR_TIMEOUT), so a workspace is zeroed once, when it is
- *                allocated. Calls that share a workspace must not overlap on
- *                the GPU.
+ *                the words it wrote back to zero, so a workspace is zeroed
+ *                once, when it is allocated. (After a call that set
+ *                PKV_ERR_TIMEOUT, zero it again: a CTA that gave up waiting
+ *                for a neighbour's partial leaves its slots as they are.)
+ *                Calls that share a workspace must not overlap on the GPU.
  * Constraints: num_q_heads = g * num_kv_heads with 1 <= g <= PKV_MAX_GROUP.
  * Rows of a sequence with a bad length are written as zeros.
  */

@@ -42,9 +42,11 @@
 //    finished their ranges: pieces within the CTA through shared memory, and
 //    a segment that crosses into a neighbouring CTA (at most one at each end
 //    of a CTA's ranges) through workspace slots whose words say whether they
-//    have been written in this call, the CTA that finds its neighbours'
-//    partials there merging. Nothing ever waits on another CTA, and no second
-//    kernel (with its launch and dependency hand-off) is needed.
+//    have been written in this call: the CTA holding the segment's last
+//    pages waits (bounded) until its neighbours' partials are all there and
+//    merges them, the others publish and go on. A CTA only waits for CTAs of
+//    earlier groups, and no second kernel (with its launch and dependency
+//    hand-off) is needed.
 #include <atomic>
 #include <cmath>
 
@@ -57,6 +59,10 @@ namespace {
 constexpr int kScanOffset = 512;           // scan scratch (16 ints) after the mbarriers
 constexpr int kHdrBytes = 1024;            // mbarriers (<= 64 warp-stages * 8 B) + scan scratch
 constexpr int kMinRangePages = 4;          // smallest automatic range (fewer, cheaper merges)
+// Looks of a merger at its neighbours' partials before it gives up and
+// reports PKV_ERR_TIMEOUT (a look is one round trip to L2, about a
+// microsecond: this is a second or more, where a partial comes in a few).
+constexpr uint32_t kMergeLooks = 1u << 20;
 // Automatic partition weights: a page costs kPageUnits, and each (sequence,
 // kv head) segment adds kSegUnits for the fixed work of its pieces (query
 // rows, the new token, the result stores), about 3/4 of a page. Without it a
@@ -328,6 +334,64 @@ __device__ __forceinline__ bool gather_groups(Piece& all, const Piece& own, cons
       all.fold(__uint_as_float(raw[16] - 1u), __uint_as_float(raw[17] - 1u), ab);
     }
   }
+  return __all_sync(kFull, complete);
+}
+
+// The first look of a CTA that has published its partial: the same fold as
+// gather_groups, but the other groups' slots are first copied into shared
+// memory at `stage` (this warp's page ring, idle once its range is done) by
+// 16-byte asynchronous copies that are all in flight together, so that the
+// look costs one round trip to L2 whatever the number of groups. Up to
+// kStageSlots slots fit; a segment over more groups is looked at in batches.
+// Only a word-by-word read: every word is either zero or its final value,
+// so a look never folds a half-written partial.
+template <int G>
+__device__ __forceinline__ bool gather_groups_staged(Piece& all, const Piece& own,
+                                                     const float* slots, uint32_t stage, int grp,
+                                                     int g_first, int g_last, int g8, int tig,
+                                                     int lane) {
+  using C = Cfg<G>;
+  constexpr int kChunks = C::kSlotFloats / 4;
+  constexpr int kStageSlots = C::kStages * kHeadPageBytes / (C::kSlotFloats * 4);
+  static_assert(kStageSlots >= 2, "the page ring holds at least two slots");
+  all.m = -INFINITY;
+  all.l = 0.f;
+#pragma unroll
+  for (int d = 0; d < 8; ++d) all.acc[d] = make_float2(0.f, 0.f);
+  bool complete = true;
+  for (int g0 = g_first; g0 <= g_last; g0 += kStageSlots) {
+    const int g1 = min(g_last, g0 + kStageSlots - 1);
+    for (int gg = g0; gg <= g1; ++gg) {
+      if (gg == grp) continue;
+      const float* src = slots + static_cast<size_t>(2 * gg + (gg == g_first ? 1 : 0)) * C::kSlotFloats;
+      const uint32_t dst = stage + static_cast<uint32_t>((gg - g0) * C::kSlotFloats * 4);
+      for (int c = lane; c < kChunks; c += 32) cp_async16(dst + 16 * c, src + 4 * c);
+    }
+    cp_async_wait_all();
+    __syncwarp();
+    if (g8 < G) {
+      for (int gg = g0; gg <= g1; ++gg) {
+        if (gg == grp) {
+          all.fold(own.m, own.l, own.acc);
+          continue;
+        }
+        const uint32_t w = stage + static_cast<uint32_t>((gg - g0) * C::kSlotFloats * 4);
+        float2 ab[8];
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+          const uint2 v = lds64u(w + 8 * ((d * G + g8) * 4 + tig));
+          complete = complete && v.x != 0u && v.y != 0u;
+          ab[d] = make_float2(__uint_as_float(v.x - 1u), __uint_as_float(v.y - 1u));
+        }
+        const uint32_t mw = lds32(w + 4 * (G * kHeadDim + g8));
+        const uint32_t lw = lds32(w + 4 * (G * kHeadDim + G + g8));
+        complete = complete && mw != 0u && lw != 0u;
+        all.fold(__uint_as_float(mw - 1u), __uint_as_float(lw - 1u), ab);
+      }
+    }
+    __syncwarp();  // the stage is read before the next batch lands in it
+  }
+  fence_proxy_async_smem();  // the ring's next page copies come after these writes
   return __all_sync(kFull, complete);
 }
 
@@ -679,7 +743,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   // ranges grp kW .. grp kW + kW - 1. A segment split over ranges of one group
   // is merged in shared memory when the group ends; one that crosses a group
   // boundary (at most one at each end) goes through the workspace, and the
-  // last group to arrive merges it.
+  // CTA of its last group merges it.
   float* s_slots = reinterpret_cast<float*>(
       smem + (ring_base - smem_addr(smem)) +
       kW * C::kStages * (kHeadPageBytes + C::kSideBytes));
@@ -953,25 +1017,43 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
           store_output<G>(out_row0, pc, g8, tig);
           return;
         }
-        // Every group of the segment leaves its partial in the workspace. A
-        // CTA that then finds all the others' partials there merges at once
-        // (one round trip: the usual case for the CTA that finishes last).
-        // Otherwise it fences and looks again; of the CTAs that look after
-        // their fence, the last one in the fences' order sees every partial,
-        // so some CTA always merges (two may, with identical results). The
-        // merger puts the segment's slots back to zero for the next call.
+        // The CTA of the segment's last group merges it; the CTAs of its other
+        // groups leave their partials in the workspace and move on without
+        // waiting. Every word of a partial says by itself whether it has been
+        // written, so the merger needs no fence: it looks until every word
+        // is there, folds the partials in group order and puts the slots back
+        // to zero for the next call. A CTA only ever waits for groups before
+        // its own, so the wait ends; it is bounded all the same.
+        if (grp != g_last) {
+          publish_piece<G>(p.slots + static_cast<size_t>(2 * grp + (grp == g_first ? 1 : 0)) *
+                                         C::kSlotFloats,
+                           pc, g8, tig);
+          return;
+        }
         Piece all;
-        float* my_slot = p.slots + static_cast<size_t>(2 * grp + (grp == g_first ? 1 : 0)) * C::kSlotFloats;
-        publish_piece<G>(my_slot, pc, g8, tig);
-        bool done = gather_groups<G>(all, pc, p.slots, C::kSlotFloats, grp, g_first, g_last, g8, tig);
-        if (!done) {
-          __threadfence();
-          __syncwarp();
+        bool done = false;
+        for (uint32_t look = 0; look < kMergeLooks && !done; ++look) {
+          // Two or more other groups: stage them, so that their round trips
+          // overlap (not in a warp that timed out: page copies may still land
+          // in its ring). Only groups of 5-8 heads: their few KV heads make
+          // segments long enough to span three or more CTAs, and their kernel
+          // has the registers to spare; in the register-capped kernel of 1-4
+          // heads the extra code cost 0.2 us per layer where it never ran.
+          if constexpr (G > 4) {
+            if (g_last - g_first >= 2 && !failed) {
+              done = gather_groups_staged<G>(all, pc, p.slots, ring0, grp, g_first, g_last, g8,
+                                             tig, lane);
+              continue;
+            }
+          }
           done = gather_groups<G>(all, pc, p.slots, C::kSlotFloats, grp, g_first, g_last, g8, tig);
         }
-        if (!done) return;
+        if (!done) {  // a partial never came: leave the slots, report
+          if (lane == 0) atomicOr(p.err, PKV_ERR_TIMEOUT);
+          return;
+        }
         store_output<G>(out_row0, all, g8, tig);
-        for (int gg = g_first; gg <= g_last; ++gg) {
+        for (int gg = g_first; gg < g_last; ++gg) {
           float* q = p.slots + static_cast<size_t>(2 * gg + (gg == g_first ? 1 : 0)) * C::kSlotFloats;
           for (int i = lane; i < C::kSlotFloats; i += 32) q[i] = 0.f;
         }
