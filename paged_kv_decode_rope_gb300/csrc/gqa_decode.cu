@@ -65,11 +65,13 @@ constexpr int kMinRangePages = 4;          // smallest automatic range (fewer, c
 constexpr uint32_t kMergeLooks = 1u << 20;
 // Automatic partition weights: a page costs kPageUnits, and each (sequence,
 // kv head) segment adds kSegUnits for the fixed work of its pieces (query
-// rows, the new token, the result stores), about 3/4 of a page. Without it a
-// range of many short segments takes visibly longer than the others.
+// rows, the new token, the merges and result stores), about 1 1/4 pages
+// (measured: 3 to 8 units tried; 5 was best on the skewed batch, 30.8 -> 30.2
+// us per layer, and neutral elsewhere). Without it a range of many short
+// segments takes visibly longer than the others.
 constexpr int kSpareSms = 4;              // SMs left without a decode CTA (see launch_decode)
 constexpr int kPageUnits = 4;
-constexpr int kSegUnits = 3;
+constexpr int kSegUnits = 5;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kHalfDim = kHeadDim / 2;
 

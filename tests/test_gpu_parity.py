@@ -78,6 +78,16 @@ def test_qwen_shape_long_context():
     full_check(wl)
 
 
+@pytest.mark.parametrize("hq,hkv", [(32, 8), (10, 2), (14, 2), (16, 2)])
+def test_segment_over_many_ctas(hq, hkv):
+    # one-page ranges: each head's 188 pages span about 19 CTAs, so the CTA of
+    # the last one waits for 18 partials (for 5-8 heads staged in shared
+    # memory in several batches, more than its page ring holds at once)
+    wl = workloads.build("span", batch=2, num_layers=1, num_q_heads=hq, num_kv_heads=hkv,
+                         cached_lens=[2999, 40], rope_theta=1e6, seed=hq + 7, sentinel=True)
+    full_check(wl, pages_per_split=1)
+
+
 @pytest.mark.parametrize("pps", [1, 2, 7, 64])
 def test_split_invariance(pps):
     wl = workloads.make("llama1b_b8_l16_u512", seed=2, sentinel=True)
