@@ -92,30 +92,34 @@ class DecodeStep:
                       copy_streams=None) -> None:
         """One step with its inputs in pinned host memory, layer-pipelined.
 
-        host_in / dev_in map "q", "k", "v" ([NL,...] bf16), "block_tables",
-        "seq_lens" and "positions" to pinned host tensors and their device
-        copies (dev_in's tables, lengths and positions must be the tensors
-        this step was built with). The step (fused path) runs on the current
-        stream. copy_streams[0] copies the per-step tables and layer 0's
-        q/k/v, then the first half of the remaining layers' q/k/v, then the
-        rest; the step waits for each group just before the first layer that
-        needs it (three waits, so the chain of decode launches keeps its
-        programmatic overlap elsewhere). copy_streams[1] copies each layer's
-        output back to host_out as soon as that layer is done. The current
-        stream finally waits for both copy streams.
+        host_in / dev_in map "q", "k", "v" ([NL,...] bf16), "block_tables"
+        ([NL,...] int32), "seq_lens" and "positions" to pinned host tensors and
+        their device copies (dev_in's tables, lengths and positions must be the
+        tensors this step was built with). The step (fused path) runs on the
+        current stream. copy_streams[0] copies the layers' block tables and
+        q/k/v in three groups: layer 0 (with the lengths and positions), the
+        next three layers (they land while layer 0 runs), then the rest (while
+        layers 0-3 run). The step waits for each group just before its first
+        layer. Each such wait costs the chain of decode launches its
+        programmatic overlap at that layer, several microseconds, so the
+        groups are few; more, smaller ones (1, 1, 2, 4, ... layers) were 5-13
+        us per step slower on batch 64 and the Qwen shape. copy_streams[1]
+        copies each layer's output back to host_out as soon as that layer is
+        done. The current stream finally waits for both copy streams.
         """
         cur = torch.cuda.current_stream()
         cs_in, cs_out = copy_streams or (torch.cuda.Stream(), torch.cuda.Stream())
         nl = self.num_layers
         cs_in.wait_stream(cur)
         cs_out.wait_stream(cur)
-        half = 1 + (nl - 1 + 1) // 2
-        groups = [g for g in ((0, 1), (1, min(half, nl)), (min(half, nl), nl)) if g[0] < g[1]]
+        groups = [g for g in ((0, 1), (1, min(4, nl)), (min(4, nl), nl)) if g[0] < g[1]]
         ready = []
         with torch.cuda.stream(cs_in):
-            for key in ("block_tables", "seq_lens", "positions"):
-                dev_in[key].copy_(host_in[key], non_blocking=True)
             for lo, hi in groups:
+                dev_in["block_tables"][lo:hi].copy_(host_in["block_tables"][lo:hi], non_blocking=True)
+                if lo == 0:
+                    for key in ("seq_lens", "positions"):
+                        dev_in[key].copy_(host_in[key], non_blocking=True)
                 for key in ("q", "k", "v"):
                     dev_in[key][lo:hi].copy_(host_in[key][lo:hi], non_blocking=True)
                 ev = torch.cuda.Event()
