@@ -144,6 +144,10 @@ size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_h
  *   pages_per_split  0: balance all (sequence, kv head, page) work items
  *                evenly over the persistent grid; > 0: cut the work into
  *                ranges of this many pages (used to force splits in tests).
+ *                Small values can give a CTA several rounds of ranges; a
+ *                CTA that merges a split segment then waits for CTAs of an
+ *                earlier round, so run such calls with the GPU to itself
+ *                (otherwise the bounded wait may end in PKV_ERR_TIMEOUT).
  *   workspace    device memory of at least paged_gqa_decode_workspace_bytes(),
  *                256-byte aligned, ZERO-FILLED before its first use. It holds
  *                the partial results of segments split between CTAs, and a
