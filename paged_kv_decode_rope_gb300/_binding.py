@@ -111,6 +111,20 @@ def _dev(t: torch.Tensor, dtype: torch.dtype, name: str, ndim: int | None = None
     return t.data_ptr()
 
 
+def _shape(t: torch.Tensor, want: tuple, name: str) -> tuple:
+    """Check t's shape against `want` (an int per dimension, None for any
+    size) before any pointer reaches the library: the C ABI sees bare
+    pointers, so a tensor of the wrong size would be read or written out of
+    bounds on the device. Returns the shape."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    got = tuple(t.shape)
+    if len(got) != len(want) or any(w is not None and g != w for g, w in zip(got, want)):
+        spec = "[" + ", ".join("*" if w is None else str(w) for w in want) + "]"
+        raise ValueError(f"{name} must have shape {spec}, got {list(got)}")
+    return got
+
+
 class KVPool:
     """A page pool over caller storage (the handle of kv_pool_create)."""
 
@@ -169,7 +183,13 @@ def paged_kv_append_rope(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torc
                          positions: torch.Tensor, rope_theta: float, stream=None) -> None:
     """q [B,Hq,64] bf16, k/v [B,Hkv,64] bf16, q_rot [B,Hq,64] fp32 out,
     block_tables [B,max_blocks] int32, seq_lens/positions [B] int32."""
-    batch, hq = q.shape[0], q.shape[1]
+    batch, hq, _ = _shape(q, (None, None, HEAD_DIM), "q")
+    for t, name in ((k, "k"), (v, "v")):
+        _shape(t, (batch, pool.num_kv_heads, HEAD_DIM), name)
+    _shape(q_rot, (batch, hq, HEAD_DIM), "q_rot")
+    _shape(block_tables, (batch, None), "block_tables")
+    _shape(seq_lens, (batch,), "seq_lens")
+    _shape(positions, (batch,), "positions")
     rc = lib().paged_kv_append_rope(
         pool.handle, _dev(q, torch.bfloat16, "q", 3), _dev(k, torch.bfloat16, "k", 3),
         _dev(v, torch.bfloat16, "v", 3), _dev(q_rot, torch.float32, "q_rot", 3),
@@ -196,11 +216,19 @@ def alloc_decode_workspace(batch: int, num_q_heads: int, num_kv_heads: int, max_
     return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
 
 
+def _decode_shapes(q_rot, out, block_tables, seq_lens) -> tuple:
+    batch, hq, _ = _shape(q_rot, (None, None, HEAD_DIM), "q_rot")
+    _shape(out, (batch, hq, HEAD_DIM), "out")
+    _shape(block_tables, (batch, None), "block_tables")
+    _shape(seq_lens, (batch,), "seq_lens")
+    return batch, hq
+
+
 def paged_gqa_decode(pool: KVPool, q_rot: torch.Tensor, out: torch.Tensor,
                      block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
                      workspace: torch.Tensor, pages_per_split: int = 0, stream=None) -> None:
     """q_rot/out [B,Hq,64] fp32; workspace from alloc_decode_workspace()."""
-    batch, hq = q_rot.shape[0], q_rot.shape[1]
+    batch, hq = _decode_shapes(q_rot, out, block_tables, seq_lens)
     rc = lib().paged_gqa_decode(
         pool.handle, _dev(q_rot, torch.float32, "q_rot", 3), _dev(out, torch.float32, "out", 3),
         _dev(block_tables, torch.int32, "block_tables", 2), block_tables.shape[1],
@@ -215,7 +243,7 @@ def paged_gqa_decode_no_alloc(pool: KVPool, q_rot: torch.Tensor, out: torch.Tens
     """paged_gqa_decode without a workspace: for callers that cannot allocate
     device memory, the library's fixed scratch array serves instead. Calls
     that overlap on the GPU share that array and race."""
-    batch, hq = q_rot.shape[0], q_rot.shape[1]
+    batch, hq = _decode_shapes(q_rot, out, block_tables, seq_lens)
     rc = lib().paged_gqa_decode_no_alloc(
         pool.handle, _dev(q_rot, torch.float32, "q_rot", 3), _dev(out, torch.float32, "out", 3),
         _dev(block_tables, torch.int32, "block_tables", 2), block_tables.shape[1],
@@ -235,7 +263,7 @@ def paged_rope_cos_sin(positions: torch.Tensor, rope_theta: float, table: torch.
     """positions [B] int32 -> the step's RoPE table (uint8 [B*1024], from
     alloc_rope_table): float32 [B,32,4] {cos_hi, cos_lo, sin_hi, sin_lo}, then
     float64 [B,32,2] {cos, sin}."""
-    batch = positions.shape[0]
+    (batch,) = _shape(positions, (None,), "positions")
     if table.numel() < batch * ROPE_TABLE_BYTES_PER_SEQ:
         raise ValueError("rope table too small")
     rc = lib().paged_rope_cos_sin(_dev(positions, torch.int32, "positions", 1), batch,
@@ -252,7 +280,14 @@ def paged_decode_step(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.T
     """One layer's whole step (RoPE + append + decode) in one call.
     q [B,Hq,64], k/v [B,Hkv,64] bf16; rope_table from paged_rope_cos_sin for
     these B sequences; out [B,Hq,64] fp32; q_rot optional fp32 out."""
-    batch, hq = q.shape[0], q.shape[1]
+    batch, hq, _ = _shape(q, (None, None, HEAD_DIM), "q")
+    for t, name in ((k, "k"), (v, "v")):
+        _shape(t, (batch, pool.num_kv_heads, HEAD_DIM), name)
+    _shape(out, (batch, hq, HEAD_DIM), "out")
+    if q_rot is not None:
+        _shape(q_rot, (batch, hq, HEAD_DIM), "q_rot")
+    _shape(block_tables, (batch, None), "block_tables")
+    _shape(seq_lens, (batch,), "seq_lens")
     if rope_table.numel() < batch * ROPE_TABLE_BYTES_PER_SEQ:
         raise ValueError("rope table too small")
     rc = lib().paged_decode_step(
@@ -287,7 +322,10 @@ def paged_prefill_rope_table(cu_tokens: torch.Tensor, start_pos: torch.Tensor, t
                              max_blocks: int, rope_theta: float, table: torch.Tensor,
                              stream=None) -> None:
     """The chunk tokens' RoPE table, built once and handed to every layer's paged_prefill."""
-    batch = start_pos.shape[0]
+    (batch,) = _shape(start_pos, (None,), "start_pos")
+    _shape(cu_tokens, (batch + 1,), "cu_tokens")
+    if table.numel() < max(total_tokens, 1) * ROPE_TABLE_BYTES_PER_SEQ:
+        raise ValueError("rope table too small")
     rc = lib().paged_prefill_rope_table(
         _dev(cu_tokens, torch.int32, "cu_tokens", 1), _dev(start_pos, torch.int32, "start_pos", 1),
         batch, total_tokens, max_blocks, float(rope_theta), _dev(table, torch.uint8, "table", 1),
@@ -302,8 +340,16 @@ def paged_prefill(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
     """Chunked causal prefill. q [T,Hq,64], k/v [T,Hkv,64] bf16; q_rot/out [T,Hq,64]
     fp32 out; block_tables [B,max_blocks], cu_tokens [B+1], start_pos [B] int32;
     rope_table from paged_prefill_rope_table (built once for all layers) or None."""
-    total, hq = q.shape[0], q.shape[1]
-    batch = block_tables.shape[0]
+    total, hq, _ = _shape(q, (None, None, HEAD_DIM), "q")
+    for t, name in ((k, "k"), (v, "v")):
+        _shape(t, (total, pool.num_kv_heads, HEAD_DIM), name)
+    _shape(q_rot, (total, hq, HEAD_DIM), "q_rot")
+    _shape(out, (total, hq, HEAD_DIM), "out")
+    batch, _ = _shape(block_tables, (None, None), "block_tables")
+    _shape(cu_tokens, (batch + 1,), "cu_tokens")
+    _shape(start_pos, (batch,), "start_pos")
+    if rope_table is not None and rope_table.numel() < max(total, 1) * ROPE_TABLE_BYTES_PER_SEQ:
+        raise ValueError("rope table too small")
     rc = lib().paged_prefill(
         pool.handle, _dev(q, torch.bfloat16, "q", 3), _dev(k, torch.bfloat16, "k", 3),
         _dev(v, torch.bfloat16, "v", 3), _dev(q_rot, torch.float32, "q_rot", 3),
@@ -324,7 +370,12 @@ def paged_gqa_decode_partials(pool: KVPool, q_rot: torch.Tensor, block_tables: t
                               o_part: torch.Tensor, lse_part: torch.Tensor,
                               num_splits: torch.Tensor, stream=None) -> None:
     """o_part [B*Hq, S, 64] fp32, lse_part [B*Hq, S] fp32, num_splits [B*Hq] int32 (outputs)."""
-    batch, hq = q_rot.shape[0], q_rot.shape[1]
+    batch, hq, _ = _shape(q_rot, (None, None, HEAD_DIM), "q_rot")
+    _shape(block_tables, (batch, None), "block_tables")
+    _shape(seq_lens, (batch,), "seq_lens")
+    _, max_splits, _ = _shape(o_part, (batch * hq, None, HEAD_DIM), "o_part")
+    _shape(lse_part, (batch * hq, max_splits), "lse_part")
+    _shape(num_splits, (batch * hq,), "num_splits")
     rc = lib().paged_gqa_decode_partials(
         pool.handle, _dev(q_rot, torch.float32, "q_rot", 3),
         _dev(block_tables, torch.int32, "block_tables", 2), block_tables.shape[1],
@@ -336,8 +387,13 @@ def paged_gqa_decode_partials(pool: KVPool, q_rot: torch.Tensor, block_tables: t
 
 def paged_kv_split_combine(o_part: torch.Tensor, lse_part: torch.Tensor, num_splits: torch.Tensor,
                            out: torch.Tensor, stream=None) -> None:
-    """o_part [rows, S, D], lse_part [rows, S], num_splits [rows] -> out [rows, D]."""
-    rows, max_splits, head_dim = o_part.shape
+    """o_part [rows, S, D], lse_part [rows, S], num_splits [rows] -> out [rows, D]
+    (any shape of rows * D elements)."""
+    rows, max_splits, head_dim = _shape(o_part, (None, None, None), "o_part")
+    _shape(lse_part, (rows, max_splits), "lse_part")
+    _shape(num_splits, (rows,), "num_splits")
+    if out.numel() != rows * head_dim:
+        raise ValueError(f"out must hold rows * D = {rows * head_dim} elements, got {out.numel()}")
     rc = lib().paged_kv_split_combine(
         _dev(o_part, torch.float32, "o_part", 3), _dev(lse_part, torch.float32, "lse_part", 2),
         _dev(num_splits, torch.int32, "num_splits", 1), _dev(out, torch.float32, "out"),

@@ -102,3 +102,85 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(B, "LIBRARY", str(tmp_path / "libpkv.so"))
     with pytest.raises(RuntimeError, match="not built"):
         B.lib()
+
+
+def test_binding_rejects_mismatched_shapes_before_the_library():
+    """The C ABI takes bare pointers, so the binding checks that the tensors
+    agree in shape (batch, head counts, head_dim 64) before any pointer is
+    passed: a mismatch would otherwise be read out of bounds on the device."""
+    import torch
+
+    import paged_kv_decode_rope_gb300._binding as B
+    pool = B.KVPool(0, None, 8)  # shapes only: the checks run before the handle is used
+    bf, f32, i32 = torch.bfloat16, torch.float32, torch.int32
+    q, k, v = torch.zeros(4, 32, 64, dtype=bf), torch.zeros(4, 8, 64, dtype=bf), torch.zeros(4, 8, 64, dtype=bf)
+    qr, out = torch.zeros(4, 32, 64, dtype=f32), torch.zeros(4, 32, 64, dtype=f32)
+    bt, sl, pos = torch.zeros(4, 16, dtype=i32), torch.ones(4, dtype=i32), torch.zeros(4, dtype=i32)
+    ws, table = torch.zeros(1024, dtype=torch.uint8), torch.zeros(4 * 1024, dtype=torch.uint8)
+    bad = {
+        "k": torch.zeros(4, 4, 64, dtype=bf),        # not the pool's kv heads
+        "v": torch.zeros(3, 8, 64, dtype=bf),        # batch
+        "q": torch.zeros(4, 32, 32, dtype=bf),       # head_dim
+        "q_rot": torch.zeros(4, 16, 64, dtype=f32),  # heads
+        "block_tables": torch.zeros(5, 16, dtype=i32),
+        "seq_lens": torch.ones(3, dtype=i32),
+        "positions": torch.zeros(5, dtype=i32),
+    }
+
+    def append(**kw):
+        a = dict(q=q, k=k, v=v, q_rot=qr, block_tables=bt, seq_lens=sl, positions=pos)
+        a.update(kw)
+        B.paged_kv_append_rope(pool, a["q"], a["k"], a["v"], a["q_rot"], a["block_tables"],
+                               a["seq_lens"], a["positions"], 500000.0)
+
+    for name, t in bad.items():
+        with pytest.raises(ValueError, match=f"{name} must have shape"):
+            append(**{name: t})
+
+    def step(**kw):
+        a = dict(q=q, k=k, v=v, out=out, block_tables=bt, seq_lens=sl)
+        a.update(kw)
+        B.paged_decode_step(pool, a["q"], a["k"], a["v"], table, a["out"], a["block_tables"],
+                            a["seq_lens"], 0.125, ws)
+
+    for name in ("k", "v", "q", "block_tables", "seq_lens"):
+        with pytest.raises(ValueError, match=f"{name} must have shape"):
+            step(**{name: bad[name]})
+    with pytest.raises(ValueError, match="out must have shape"):
+        step(out=torch.zeros(4, 32, 63, dtype=f32))
+    with pytest.raises(ValueError, match="out must have shape"):
+        B.paged_gqa_decode(pool, qr, torch.zeros(4, 31, 64, dtype=f32), bt, sl, 0.125, ws)
+    with pytest.raises(ValueError, match="seq_lens must have shape"):
+        B.paged_gqa_decode_no_alloc(pool, qr, out, bt, torch.ones(2, dtype=i32), 0.125)
+    with pytest.raises(ValueError, match="positions must have shape"):
+        B.paged_rope_cos_sin(torch.zeros(4, 1, dtype=i32), 1e4, table)
+    # prefill: T tokens over B sequences
+    pq, pk = torch.zeros(10, 32, 64, dtype=bf), torch.zeros(10, 8, 64, dtype=bf)
+    pqr, pout = torch.zeros(10, 32, 64, dtype=f32), torch.zeros(10, 32, 64, dtype=f32)
+    pbt, cu, st = torch.zeros(2, 16, dtype=i32), torch.tensor([0, 4, 10], dtype=i32), torch.zeros(2, dtype=i32)
+    with pytest.raises(ValueError, match="cu_tokens must have shape"):
+        B.paged_prefill(pool, pq, pk, pk, pqr, pout, pbt, cu[:2], st, 1e4, 0.125, ws)
+    with pytest.raises(ValueError, match="k must have shape"):
+        B.paged_prefill(pool, pq, pk[:9], pk, pqr, pout, pbt, cu, st, 1e4, 0.125, ws)
+    with pytest.raises(ValueError, match="rope table too small"):
+        B.paged_prefill(pool, pq, pk, pk, pqr, pout, pbt, cu, st, 1e4, 0.125, ws,
+                        rope_table=torch.zeros(1024, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="start_pos must have shape"):
+        B.paged_prefill_rope_table(cu, torch.zeros(2, 1, dtype=i32), 10, 16, 1e4,
+                                   torch.zeros(10 * 1024, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="cu_tokens must have shape"):
+        B.paged_prefill_rope_table(cu, torch.zeros(3, dtype=i32), 10, 16, 1e4,
+                                   torch.zeros(10 * 1024, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="rope table too small"):
+        B.paged_prefill_rope_table(cu, st, 10, 16, 1e4, torch.zeros(9 * 1024, dtype=torch.uint8))
+    # split results and their merge
+    rows = 4 * 32
+    with pytest.raises(ValueError, match="o_part must have shape"):
+        B.paged_gqa_decode_partials(pool, qr, bt, sl, 0.125, 1, torch.zeros(rows - 1, 3, 64),
+                                    torch.zeros(rows - 1, 3), torch.zeros(rows - 1, dtype=i32))
+    with pytest.raises(ValueError, match="lse_part must have shape"):
+        B.paged_kv_split_combine(torch.zeros(5, 3, 64), torch.zeros(5, 2), torch.zeros(5, dtype=i32),
+                                 torch.zeros(5, 64))
+    with pytest.raises(ValueError, match="out must hold"):
+        B.paged_kv_split_combine(torch.zeros(5, 3, 64), torch.zeros(5, 3), torch.zeros(5, dtype=i32),
+                                 torch.zeros(5, 63))

@@ -91,7 +91,7 @@ def test_host_side_rejections():
         pkv.paged_gqa_decode(st.pool, st.q_rot[0], st.out[0], st.block_tables[0], st.seq_lens,
                              0.125, st.workspace[:64])
     with pytest.raises(pkv.PkvError, match="EINVAL"):   # group 16 > 8
-        q16 = torch.zeros(4, 128, 64, device="cuda")
+        q16 = torch.zeros(st.seq_lens.shape[0], 128, 64, device="cuda")
         pkv.paged_gqa_decode(st.pool, q16, q16.clone(), st.block_tables[0], st.seq_lens, 0.125,
                              st.workspace)
     with pytest.raises(pkv.PkvError, match="EINVAL"):   # theta
