@@ -48,7 +48,7 @@ TRAFFIC = {
     # workload -> (sha256 of gqa_decode.cu prefix, bytes per layer call: the step kernel)
     # profiles/gqa_decode_step_llama1b_b64_l16_u2048.md: 158.246 MB read + 2.838 MB written
     "llama1b_b64_l16_u2048": ("6c2f42d9114cc786", 161083904),
-    # same file, Qwen2.5-0.5B section: 47.004 MB read + 0.063 MB written
+    # profiles/gqa_decode_step_qwen05b_b32_l24_u1024_4096.md: 47.004 MB read + 0.063 MB written
     "qwen05b_b32_l24_u1024_4096": ("6c2f42d9114cc786", 47067136),
 }
 
