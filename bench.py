@@ -104,24 +104,39 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        rows = []
         try:
             with open(self.path) as f:
-                for line in f:
-                    parts = [p.strip() for p in line.split(",")]
-                    if len(parts) >= 9:
-                        rows.append(parts)
+                lines = f.readlines()
             os.unlink(self.path)
         except Exception:
             return None
-        if not rows:
+        return summarise_clocks(lines)
+
+
+def summarise_clocks(lines) -> dict | None:
+    """Median SM clock, the largest max clock and every throttle reason seen
+    Active, from nvidia-smi CSV lines in ClockSampler.FIELDS order (no header,
+    no units). None when no line parses."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) >= 9:
+            rows.append(parts)
+    if not rows:
+        return None
+
+    def num(x):
+        try:
+            return float(x)
+        except ValueError:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+
+    sm = [v for v in (num(r[1]) for r in rows) if v is not None]
+    mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(rows)}
 
 
 def _dist():

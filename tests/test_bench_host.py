@@ -1,0 +1,32 @@
+"""Host-side helpers of the benchmark (no GPU): the clock-sample summary that
+decides whether a run saw throttling."""
+import bench
+
+
+def test_clock_summary_median_max_and_reasons():
+    lines = [
+        "0, 2070, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+        "0, 1980, 2070, 1300.2, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n",
+        "0, 2055, 2070, 1250.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n",
+    ]
+    got = bench.summarise_clocks(lines)
+    assert got == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_clock_summary_reports_every_slowdown_kind():
+    lines = [
+        "0, 1500, 2070, 1400, 0x8, Active, Not Active, Not Active, Not Active",
+        "0, 1400, 2070, 1400, 0x48, Not Active, Active, Active, Not Active",
+    ]
+    got = bench.summarise_clocks(lines)
+    assert got["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+    assert got["sm_mhz"] == 1450.0
+
+
+def test_clock_summary_skips_unparsable_values_and_short_lines():
+    lines = ["", "garbage", "0, [N/A], 2070, 10, 0x0, Not Active, Not Active, Not Active, Not Active",
+             "0, 2070, [N/A], 10, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    got = bench.summarise_clocks(lines)
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 2}
+    assert bench.summarise_clocks([]) is None
+    assert bench.summarise_clocks(["a, b"]) is None
