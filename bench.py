@@ -108,9 +108,9 @@ class ClockSampler:
             with open(self.path) as f:
                 lines = f.readlines()
             os.unlink(self.path)
+            return summarise_clocks(lines)
         except Exception:
             return None
-        return summarise_clocks(lines)
 
 
 def summarise_clocks(lines) -> dict | None:
