@@ -17,6 +17,13 @@ import torch
 from . import _binding as B
 
 
+def host_copy_groups(num_layers: int) -> list[tuple[int, int]]:
+    """Layer ranges [lo, hi) whose inputs DecodeStep.run_from_host copies
+    together: layer 0, layers 1-3, the rest (empty ranges dropped)."""
+    nl = num_layers
+    return [g for g in ((0, 1), (1, min(4, nl)), (min(4, nl), nl)) if g[0] < g[1]]
+
+
 class DecodeStep:
     def __init__(self, pool_storage: torch.Tensor, *, num_kv_heads: int, num_q_heads: int,
                  num_layers: int, block_tables: torch.Tensor, seq_lens: torch.Tensor,
@@ -112,7 +119,7 @@ class DecodeStep:
         nl = self.num_layers
         cs_in.wait_stream(cur)
         cs_out.wait_stream(cur)
-        groups = [g for g in ((0, 1), (1, min(4, nl)), (min(4, nl), nl)) if g[0] < g[1]]
+        groups = host_copy_groups(nl)
         ready = []
         with torch.cuda.stream(cs_in):
             for lo, hi in groups:

@@ -1,5 +1,6 @@
-"""Host-side helpers of the benchmark (no GPU): the clock-sample summary that
-decides whether a run saw throttling."""
+"""Host-side helpers of the benchmark and the end-to-end step (no GPU): the
+clock-sample summary that decides whether a run saw throttling, and the
+layer groups whose inputs the host path copies together."""
 import bench
 
 
@@ -30,3 +31,16 @@ def test_clock_summary_skips_unparsable_values_and_short_lines():
     assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 2}
     assert bench.summarise_clocks([]) is None
     assert bench.summarise_clocks(["a, b"]) is None
+
+
+def test_host_copy_groups_cover_every_layer_once_in_three_waits_at_most():
+    from paged_kv_decode_rope_gb300.step import host_copy_groups
+    assert host_copy_groups(1) == [(0, 1)]
+    assert host_copy_groups(2) == [(0, 1), (1, 2)]
+    assert host_copy_groups(4) == [(0, 1), (1, 4)]
+    assert host_copy_groups(16) == [(0, 1), (1, 4), (4, 16)]
+    assert host_copy_groups(24) == [(0, 1), (1, 4), (4, 24)]
+    for nl in range(1, 40):
+        g = host_copy_groups(nl)
+        assert g[0] == (0, 1) and len(g) <= 3
+        assert [lo for lo, _ in g[1:]] == [hi for _, hi in g[:-1]] and g[-1][1] == nl
