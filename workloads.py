@@ -133,9 +133,10 @@ def _sentinel_unused(pool: torch.Tensor, wl_shape, block_tables: np.ndarray,
             if t.size:
                 used[block_tables[layer, b, t // PAGE_SIZE], t % PAGE_SIZE] = True
     unused = torch.from_numpy(~used).to(pool.device)
-    sentinel = torch.tensor(SENTINEL_BF16, dtype=torch.int16).view(torch.bfloat16).to(pool.device)
+    # written as 16-bit integers: a bf16 assignment may canonicalise the NaN
+    bits = pool.view(torch.int16).view(num_pages, hkv, 2, PAGE_SIZE, HEAD_DIM)
     mask = unused[:, None, None, :, None].expand_as(view)
-    view[mask] = sentinel
+    bits[mask] = SENTINEL_BF16
 
 
 def build(name: str, *, batch: int, num_layers: int, num_q_heads: int, num_kv_heads: int,
