@@ -7,16 +7,17 @@
 // and appended like a decode token, and the queries of chunk token t attend
 // causally over the sequence's first start_pos[b] + t + 1 tokens.
 //
-// Four launches. (1) An expansion kernel turns every chunk token into a
-// one-token "virtual sequence" (its causal length, its position, its
-// sequence's block table row). (2) The append kernel rotates and stores every
-// chunk token exactly as it does a decode token, and writes the rotated
-// queries. (3) A one-CTA plan lists the query tiles. (4) Flash attention on
-// the fifth-generation tensor cores: one CTA per (tile of up to 128 (token,
-// query head) rows, kv head) streams the sequence's pages up to the tile's
-// last position, four pages per step, through a TMA ring; tcgen05 MMAs with
-// fp32 accumulators in tensor memory compute S = Q K^T and O += P V, and one
-// thread per row runs the online softmax on its row of S.
+// Five launches (four when the caller hands in the chunk tokens' RoPE
+// table). (1) An expansion kernel gives every chunk token its sequence and
+// position. (2) The RoPE table of those positions, unless given. (3) The
+// append kernel rotates and stores every chunk token exactly as a decode
+// token would be stored, and writes the rotated queries. (4) A one-CTA plan
+// lists the query tiles. (5) Flash attention on the fifth-generation tensor
+// cores: one CTA per (tile of up to 128 (token, query head) rows, kv head)
+// streams the sequence's pages up to the tile's last position, four pages
+// per step, through a TMA ring; tcgen05 MMAs with fp32 accumulators in tensor
+// memory compute S = Q K^T and O += P V, and two threads per row (32 columns
+// each) run the online softmax on its row of S.
 #include <atomic>
 #include <climits>
 
