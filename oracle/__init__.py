@@ -1,7 +1,7 @@
 """fp64 CPU oracle for the paged-KV decode step (test infrastructure).
 
-Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
-leg may import this package. It wraps the plain C oracle in ``pkv_oracle.c``
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU legs (the
+CPU baseline and ``--impl reference``) may import this package. It wraps the plain C oracle in ``pkv_oracle.c``
 (built on first use) with numpy marshalling; it shares no code with the CUDA
 library and never imports it.
 """

@@ -2,7 +2,8 @@
  * pkv_oracle.c -- reference oracle for the batched paged-KV decode step.
  *
  * TEST INFRASTRUCTURE ONLY. Only the test suite, the package smoke check and
- * the benchmark's CPU-baseline leg load this file's library. The CUDA library
+ * the benchmark's CPU legs (the CPU baseline and the reference arm) load this
+ * file's library. The CUDA library
  * never links it, calls it or includes anything from it, and this file includes
  * nothing from the CUDA library.
  *
