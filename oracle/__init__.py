@@ -81,8 +81,11 @@ def _check(rc: int, what: str) -> None:
 
 
 def bf16_to_double(bits) -> np.ndarray:
+    """Exact widening (the bf16 bits are the top half of a float32); NaN
+    encodings stay NaN (the cast of a signalling NaN is not an error here)."""
     bits = _u16(bits)
-    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
 def bf16_from_double(x) -> np.ndarray:
