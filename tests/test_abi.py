@@ -184,3 +184,23 @@ def test_binding_rejects_mismatched_shapes_before_the_library():
     with pytest.raises(ValueError, match="out must hold"):
         B.paged_kv_split_combine(torch.zeros(5, 3, 64), torch.zeros(5, 3), torch.zeros(5, dtype=i32),
                                  torch.zeros(5, 63))
+
+
+def test_binding_constants_match_the_header():
+    """The Python binding's copies of the header's constants (sizes it
+    allocates and checks, error bits it decodes) equal the macros."""
+    import paged_kv_decode_rope_gb300._binding as B
+    text = open(HEADERS[0], encoding="utf-8").read()
+
+    def macro(name):
+        m = re.search(rf"#define {name}\s+(\S+)", text)
+        assert m, name
+        return int(m.group(1), 0)
+
+    assert B.HEAD_DIM == macro("PKV_HEAD_DIM")
+    assert B.PAGE_SIZE == macro("PKV_PAGE_SIZE")
+    assert B.MAX_GROUP == macro("PKV_MAX_GROUP")
+    assert (B.ERR_SEQ_LEN, B.ERR_PAGE_ID, B.ERR_TIMEOUT, B.ERR_SPLITS) == tuple(
+        macro(f"PKV_ERR_{n}") for n in ("SEQ_LEN", "PAGE_ID", "TIMEOUT", "SPLITS"))
+    m = re.search(r"#define PKV_ROPE_TABLE_BYTES\(batch\) \(\(size_t\)\(batch\) \* (\d+)u\)", text)
+    assert m and int(m.group(1)) == B.ROPE_TABLE_BYTES_PER_SEQ
