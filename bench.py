@@ -67,6 +67,31 @@ def _peaks() -> tuple[float, str]:
         return 6800.0, "fallback"
 
 
+def _tensor_peak(sustained: bool = True) -> tuple[float, str]:
+    """Dense bf16 TFLOP/s: the measured cuBLAS rate (sustained for a kernel
+    timed inside a long loop, burst for one timed alone), else the fallback."""
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)[key]), "measured"
+    except Exception:
+        return (1700.0 if sustained else 1900.0), "fallback"
+
+
+def prefill_roofline(pairs: float, ms: float, peak: float, source: str) -> dict:
+    """The prefill pass's roofline: causal attention is a dense contraction,
+    bound by the bf16 tensor cores. Algorithmic flops are 2 products x 2 x 64
+    per (query head, visible key) pair; the kernel's hi/lo operand split and
+    the masked halves of diagonal steps are work on top of that, not counted."""
+    achieved = pairs * 4 * 64 / (ms / 1e3) / 1e12
+    return {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05), with the pass's append",
+            "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "peak_source": f"{source} (MEASURED_PEAKS.json bf16_tflops_sustained, cuBLAS bf16)"
+                           if source == "measured" else "fallback (1.7 PFLOP/s sustained)",
+            "flops_per_pass": pairs * 4 * 64}
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a region."""
 
@@ -528,6 +553,7 @@ def run_prefill(args, ws, rank, local) -> int:
                 "higher_is_better": True, "ms_per_pass": round(ms, 4), "steps": args.steps,
                 "warmup": args.warmup,
                 "attention_tflops": round(pairs * 4 * 64 / (ms / 1e3) / 1e12, 2),
+                "roofline": prefill_roofline(pairs, ms, *_tensor_peak(sustained=True)),
                 "config": {"sequences": nb, "prompt_tokens": t, "layers": nl, "q_heads": hq,
                            "kv_heads": hkv, "start": 0},
                 "data": "synthetic (seeded)",

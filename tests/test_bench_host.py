@@ -44,3 +44,15 @@ def test_host_copy_groups_cover_every_layer_once_in_three_waits_at_most():
         g = host_copy_groups(nl)
         assert g[0] == (0, 1) and len(g) <= 3
         assert [lo for lo, _ in g[1:]] == [hi for _, hi in g[:-1]] and g[-1][1] == nl
+
+
+def test_prefill_roofline_counts_algorithmic_flops_against_the_tensor_peak():
+    # 4 prompts x 2048 tokens, 32 query heads, 16 layers, 4.47 ms per pass
+    pairs = 4 * 2048 * 2049 / 2 * 32 * 16
+    r = bench.prefill_roofline(pairs, 4.47, 1710.2, "measured")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["traffic"] is None
+    assert abs(r["achieved"] - pairs * 256 / 4.47e-3 / 1e12) < 0.01
+    assert abs(r["achieved"] - 246.3) < 0.5          # the figure the docs quote for this case
+    assert abs(r["frac"] - r["achieved"] / 1710.2) < 1e-4
+    peak, src = bench._tensor_peak()
+    assert peak > 0 and src in ("measured", "fallback")
