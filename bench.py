@@ -46,9 +46,9 @@ L2_BYTES = 129 * 10**6
 # is unchanged.
 TRAFFIC = {
     # workload -> (sha256 of gqa_decode.cu prefix, bytes per layer call: the step kernel)
-    # profiles/gqa_decode_step_llama1b_b64_l16_u2048.md: 158.246 MB read + 2.838 MB written
+    # batch 64: 158.246 MB read + 2.838 MB written (ncu --set full, one layer call)
     "llama1b_b64_l16_u2048": ("6c2f42d9114cc786", 161083904),
-    # profiles/gqa_decode_step_qwen05b_b32_l24_u1024_4096.md: 47.004 MB read + 0.063 MB written
+    # Qwen shape: 47.004 MB read + 0.063 MB written (ncu --set full, one layer call)
     "qwen05b_b32_l24_u1024_4096": ("6c2f42d9114cc786", 47067136),
 }
 
@@ -417,7 +417,9 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4), "us_per_step": round(ms_step_max * 1e3, 2),
         "pct_of_hbm_peak": round(100 * value / ws / peak, 2), "pct_of_8tbs": round(100 * value / ws / 8000, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "storage": "bf16 KV pages; new key rounded as fp64 rotation would round it; fp32 softmax and accumulation",
+        "storage": ("bf16 KV pages; new key rounded as fp64 rotation would round it; q.K and P.V on "
+                    "tensor cores with bf16 hi+lo operand pairs for q and P (about 16 mantissa bits) "
+                    "and fp32 accumulation; fp32 softmax"),
         "data": "synthetic (seeded; bf16 N(0,1) q/k/v and cache)", "config": _config(wl),
         "roofline": {"bound": "hbm",
                      "kernel": "paged_decode_step call per layer: gqa_decode_kernel (step mode, split pieces merged in the kernel)",

@@ -98,6 +98,23 @@ int kv_pool_num_pages(const pkv_pool_t *pool);
 size_t kv_pool_page_bytes(int num_kv_heads, int head_dim, int page_size);
 
 /*
+ * Bound of the one wait in the decode that depends on another CTA: the CTA
+ * that merges a (sequence, kv head) segment split across CTAs looks at the
+ * other CTAs' partial results, each look one round trip to L2, and after
+ * `looks` looks without finding them all it gives up: PKV_ERR_TIMEOUT is set,
+ * that segment's output rows are left unwritten and its workspace slots stay
+ * written (zero the workspace again before the next call). The default,
+ * 2^20 looks, is a second or more, where the partials arrive within
+ * microseconds; 0 makes every such merger give up at once (a way to exercise
+ * the timeout path without any wait). The setting belongs to the pool handle
+ * and is read when a decode is launched (a captured CUDA graph keeps the
+ * value it was captured with). *previous, if not NULL, receives the old value.
+ * Host only; no device work. (Failure handling of this library, not on the
+ * pages.)
+ */
+int kv_pool_set_merge_wait_limit(pkv_pool_t *pool, uint32_t looks, uint32_t *previous);
+
+/*
  * RoPE + append for one layer. ("Hours of YouTube …", shared BF16 KV page pool
  * item: decode appends the new token at its absolute RoPE position;
  * "手写LLM推理引擎…" section 3.2: the rotation, inverse frequency
@@ -155,7 +172,8 @@ size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_h
  *                the words it wrote back to zero, so a workspace is zeroed
  *                once, when it is allocated. (After a call that set
  *                PKV_ERR_TIMEOUT, zero it again: a CTA that gave up waiting
- *                for a neighbour's partial leaves its slots as they are.)
+ *                for a neighbour's partial leaves its slots as they are; see
+ *                kv_pool_set_merge_wait_limit.)
  *                Calls that share a workspace must not overlap on the GPU.
  * Constraints: num_q_heads = g * num_kv_heads with 1 <= g <= PKV_MAX_GROUP.
  * Rows of a sequence with a bad length are written as zeros.
@@ -293,15 +311,23 @@ int paged_prefill_rope_table(const int32_t *cu_tokens, const int32_t *start_pos,
  * exits. It calls no allocation routine.
  *   Arguments, layouts and results are those of paged_gqa_decode.
  *   Returns -E2BIG when these sizes need more scratch than the array holds
- *   (paged_gqa_decode_workspace_bytes() > PKV_NO_ALLOC_SCRATCH_BYTES; with
- *   pages_per_split = 0 this covers group sizes up to 8 and batches of a few
- *   thousand sequences on a 152-SM GPU).
+ *   (paged_gqa_decode_workspace_bytes() > PKV_NO_ALLOC_SCRATCH_BYTES). With
+ *   pages_per_split = 0 the need does not depend on the batch: it is two
+ *   partial slots of (64 + 2) * group floats per warp of the persistent
+ *   grid, 2 * SMs * CTAs per SM * warps per CTA * slot bytes; with groups
+ *   of 8 on a 152-SM GPU (one CTA of 10 warps per SM) that is 6.1 MiB, so a
+ *   GPU with 30% more SMs would get -E2BIG for groups of 8.
  *   The first call on each device looks up the array's device address (with
- *   that device current); make that first call before any stream capture.
- *   The array is zero when the library loads, and every call leaves it zero
- *   again (paged_gqa_decode's workspace contract). All
- *   calls share the one array: calls that overlap on the GPU (other streams,
- *   other threads) race and give wrong results; order them on one stream.
+ *   that device current) and keeps it for the process; make that first call
+ *   before any stream capture. The address does not survive a reset of the
+ *   device's primary context (cudaDeviceReset): do not call this entry point
+ *   after one.
+ *   Each call first clears, on `stream`, the bytes of the array it will use
+ *   (a cudaMemsetAsync, which allocates nothing), so the zero state the
+ *   decode needs holds even after a call that ended with PKV_ERR_TIMEOUT.
+ *   All calls share the one array: calls that overlap on the GPU (other
+ *   streams, other threads) race and give wrong results; order them on one
+ *   stream.
  */
 int paged_gqa_decode_no_alloc(const pkv_pool_t *pool, const float *q_rot, float *out,
                               const int32_t *block_tables, int max_blocks,

@@ -13,6 +13,7 @@ from ._binding import (  # noqa: F401
     ERR_SEQ_LEN,
     ERR_SPLITS,
     ERR_TIMEOUT,
+    DEFAULT_MERGE_WAIT_LOOKS,
     HEAD_DIM,
     LIBRARY,
     MAX_GROUP,
@@ -28,6 +29,7 @@ from ._binding import (  # noqa: F401
     kv_pool_destroy,
     kv_pool_num_pages,
     kv_pool_page_bytes,
+    kv_pool_set_merge_wait_limit,
     lib,
     paged_decode_step,
     paged_gqa_decode,

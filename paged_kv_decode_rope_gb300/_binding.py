@@ -31,6 +31,7 @@ _SIGNATURES = {
     "kv_pool_destroy": (_i, [_vp]),
     "kv_pool_num_pages": (_i, [_vp]),
     "kv_pool_page_bytes": (_sz, [_i, _i, _i]),
+    "kv_pool_set_merge_wait_limit": (_i, [_vp, ctypes.c_uint32, ctypes.POINTER(ctypes.c_uint32)]),
     "paged_kv_append_rope": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _d, _vp]),
     "paged_gqa_decode_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "paged_gqa_decode": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp, _sz, _vp]),
@@ -176,6 +177,18 @@ def kv_pool_destroy(pool: KVPool) -> None:
 
 def kv_pool_num_pages(pool: KVPool) -> int:
     return pool.num_pages
+
+
+DEFAULT_MERGE_WAIT_LOOKS = 1 << 20
+
+
+def kv_pool_set_merge_wait_limit(pool: KVPool, looks: int) -> int:
+    """Bound of a decode merger's wait for other CTAs' partials, in looks (0:
+    give up at once, setting ERR_TIMEOUT). Returns the previous bound."""
+    prev = ctypes.c_uint32(0)
+    _check("kv_pool_set_merge_wait_limit",
+           lib().kv_pool_set_merge_wait_limit(pool.handle, int(looks), ctypes.byref(prev)))
+    return prev.value
 
 
 def paged_kv_append_rope(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -7,9 +7,9 @@
 // accounting), or a plugin that a runtime only hands its input and output
 // buffers. For them this entry point takes no workspace argument and never
 // allocates: the decode's scratch (the partial results of segments split
-// between CTAs, zero between calls) lives in g_decode_scratch, a
-// file-scope array that every GPU which loads this library holds until the
-// process exits.
+// between CTAs, each word tagged so that zero means "not written in this
+// call") lives in g_decode_scratch, a file-scope array that every GPU which
+// loads this library holds until the process exits.
 #include <cerrno>
 #include <cmath>
 #include <mutex>
@@ -25,7 +25,9 @@ std::mutex g_mu;
 void* g_scratch_ptr[64] = {nullptr};  // device address of g_decode_scratch, per device
 
 // The array's name is a host-side stand-in in host code; a kernel needs its
-// device address, looked up once per device with that device current.
+// device address, looked up once per device with that device current and
+// kept for the process (it does not survive a reset of the device's primary
+// context).
 cudaError_t scratch_address(int device, void** ptr) {
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -58,9 +60,13 @@ extern "C" int paged_gqa_decode_no_alloc(const pkv_pool_t* pool, const float* q_
   cudaError_t e = cudaGetDevice(&device);
   void* scratch = nullptr;
   if (e == cudaSuccess) e = scratch_address(device, &scratch);
-  // The array keeps the previous call's contents. Nothing in it has to start
-  // at zero: the decode writes every segment record and split piece that the
-  // merge then reads.
+  // The decode reads a zero word as "not written in this call". A call that
+  // completes leaves every word it wrote at zero again, but one whose merger
+  // gave up waiting (PKV_ERR_TIMEOUT) leaves its partials behind, and this
+  // array's callers have no handle to clear it. So every call clears the
+  // bytes it will use, on its own stream, before the decode; a memset
+  // allocates nothing.
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     pkv::record_cuda_error(e);
     return -EIO;

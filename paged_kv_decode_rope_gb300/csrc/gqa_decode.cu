@@ -59,10 +59,6 @@ namespace {
 constexpr int kScanOffset = 512;           // scan scratch (16 ints) after the mbarriers
 constexpr int kHdrBytes = 1024;            // mbarriers (<= 64 warp-stages * 8 B) + scan scratch
 constexpr int kMinRangePages = 4;          // smallest automatic range (fewer, cheaper merges)
-// Looks of a merger at its neighbours' partials before it gives up and
-// reports PKV_ERR_TIMEOUT (a look is one round trip to L2, about a
-// microsecond: this is a second or more, where a partial comes in a few).
-constexpr uint32_t kMergeLooks = 1u << 20;
 // Automatic partition weights: a page costs kPageUnits, and each (sequence,
 // kv head) segment adds kSegUnits for the fixed work of its pieces (query
 // rows, the new token, the merges and result stores), about 1 1/4 pages
@@ -130,6 +126,7 @@ struct DecodeParams {
   int32_t* num_splits;
   int max_splits;
   int* err;
+  uint32_t merge_looks;  // looks of a merger at other CTAs' partials before PKV_ERR_TIMEOUT
   int ring_offset;  // byte offset of the copy rings in dynamic shared memory (rounded up to 1 KiB)
   // step mode
   const uint16_t* q_raw;    // bf16 [batch][hq][64]
@@ -1034,7 +1031,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
         }
         Piece all;
         bool done = false;
-        for (uint32_t look = 0; look < kMergeLooks && !done; ++look) {
+        for (uint32_t look = 0; look < p.merge_looks && !done; ++look) {
           // Two or more other groups: stage them, so that their round trips
           // overlap (not in a warp that timed out: page copies may still land
           // in its ring). Only groups of 5-8 heads: their few KV heads make
@@ -1245,6 +1242,7 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
     p.num_splits = partials ? a.num_splits + row0 : nullptr;
     p.max_splits = a.max_splits;
     p.err = a.err;
+    p.merge_looks = a.merge_looks;
     p.ring_offset = static_cast<int>(ring_offset_bytes());
     const size_t qrow0 = static_cast<size_t>(b0) * a.num_q_heads * kHeadDim;
     const size_t krow0 = static_cast<size_t>(b0) * a.num_kv_heads * kHeadDim;

@@ -132,6 +132,7 @@ int kv_pool_create(pkv_pool_t** pool, void* storage, size_t storage_bytes, int n
   h->num_kv_heads = num_kv_heads;
   h->d_err = d_err;
   h->device = device;
+  h->merge_looks = pkv::kDefaultMergeLooks;
   *pool = h;
   return 0;
 }
@@ -146,6 +147,13 @@ int kv_pool_destroy(pkv_pool_t* pool) {
 int kv_pool_num_pages(const pkv_pool_t* pool) {
   if (!pool) return -EINVAL;
   return static_cast<int>(pool->num_pages);
+}
+
+int kv_pool_set_merge_wait_limit(pkv_pool_t* pool, uint32_t looks, uint32_t* previous) {
+  if (!pool) return -EINVAL;
+  if (previous) *previous = pool->merge_looks;
+  pool->merge_looks = looks;
+  return 0;
 }
 
 int paged_kv_append_rope(pkv_pool_t* pool, const void* q, const void* k, const void* v,
@@ -220,6 +228,7 @@ int paged_gqa_decode(const pkv_pool_t* pool, const float* q_rot, float* out,
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.err = pool->d_err;
+  a.merge_looks = pool->merge_looks;
   cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
@@ -272,6 +281,7 @@ int paged_decode_step(pkv_pool_t* pool, const void* q, const void* k, const void
   a.v_new = static_cast<const uint16_t*>(v);
   a.rope_table = rope_table;
   a.q_rot_out = q_rot;
+  a.merge_looks = pool->merge_looks;
   cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
@@ -377,6 +387,7 @@ int paged_gqa_decode_partials(const pkv_pool_t* pool, const float* q_rot,
   a.num_splits = num_splits;
   a.max_splits = max_splits;
   a.err = pool->d_err;
+  a.merge_looks = pool->merge_looks;
   cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }

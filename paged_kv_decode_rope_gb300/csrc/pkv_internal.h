@@ -20,11 +20,18 @@ struct pkv_pool {
   int num_kv_heads;
   int* d_err;  // device error word (PKV_ERR_* bits)
   int device;
+  // looks a decode's merger takes at another CTA's partial before it gives
+  // up with PKV_ERR_TIMEOUT (kv_pool_set_merge_wait_limit)
+  uint32_t merge_looks;
 };
 
 namespace pkv {
 
 constexpr int kMaxKvHeads = 256;
+// Default bound of a merger's wait: looks at another CTA's partial, each an
+// L2 round trip of about a microsecond, so a second or more where a partial
+// comes within a few microseconds.
+constexpr uint32_t kDefaultMergeLooks = 1u << 20;
 
 struct AppendLaunch {
   uint16_t* pool;
@@ -69,6 +76,7 @@ struct DecodeLaunch {
   int32_t* num_splits;
   int max_splits;
   int* err;
+  uint32_t merge_looks;  // bound of a merger's wait for other CTAs' partials
   // the fused step (q_raw != nullptr): RoPE + append of the new token, then the decode
   const uint16_t* q_raw;
   const uint16_t* k_new;

@@ -11,7 +11,8 @@ as they go. This is the batched engine loop of "Hours of YouTube and 85
 handtyped pages of notes on LLM Inference – Start here" (continuous batching
 and dense causal prefill items) around this library's kernels; the model's
 projections are not part of the library, so every prompt and step token
-brings seeded q/k/v (workloads.trace_prompt_qkv, workloads.trace_step_qkv).
+brings its q/k/v from the caller: either two callables (a request's prompt
+rows, a request's step rows) or, for timing, a seeded draw on the device.
 
 Per request: after its prefill it holds prompt_len tokens and has produced its
 first token; each decode step processes the newest token (appending it at its
@@ -26,7 +27,6 @@ import time
 import numpy as np
 import torch
 
-import workloads
 from . import _binding as B
 from .sched import PageScheduler
 
@@ -57,7 +57,17 @@ class DecodeTrace:
     def __init__(self, requests, *, num_pages: int, num_layers: int, num_q_heads: int,
                  num_kv_heads: int, rope_theta: float, seed: int = 0, context_len: int = 2048,
                  static_batching: bool = False, max_batch: int = 256, device="cuda",
-                 device_inputs: bool = False, prefill_tokens: int = 8192):
+                 device_inputs: bool = False, prefill_tokens: int = 8192,
+                 prompt_qkv=None, step_qkv=None):
+        """prompt_qkv(request, prompt_len) -> (q [L][T][Hq][64], k, v [L][T][Hkv][64])
+        and step_qkv(request, step) -> (q [L][Hq][64], k, v [L][Hkv][64]), bf16
+        host tensors, give each request's inputs independently of the batch it
+        shares (for parity checks). With device_inputs=True they are not used:
+        every call draws its rows on the device from a generator seeded with
+        `seed` (for timing)."""
+        if not device_inputs and (prompt_qkv is None or step_qkv is None):
+            raise ValueError("give prompt_qkv and step_qkv, or device_inputs=True")
+        self._prompt_src, self._step_src = prompt_qkv, step_qkv
         self.requests = list(requests)
         self.num_layers, self.hq, self.hkv = num_layers, num_q_heads, num_kv_heads
         self.rope_theta, self.seed = float(rope_theta), seed
@@ -98,9 +108,7 @@ class DecodeTrace:
     # -- host side -----------------------------------------------------------
     def _prompt_qkv(self, r: int):
         if r not in self._prompts:
-            req = self.requests[r]
-            self._prompts[r] = workloads.trace_prompt_qkv(self.seed, r, self.num_layers, self.hq,
-                                                          self.hkv, req.prompt_len)
+            self._prompts[r] = self._prompt_src(r, self.requests[r].prompt_len)
         return self._prompts[r]
 
     def run_prefill(self, chunks, on_prefill=None) -> None:
@@ -202,8 +210,7 @@ class DecodeTrace:
                                    device=self.device).to(torch.bfloat16)
             q, k, v = draw(self.hq), draw(self.hkv), draw(self.hkv)
             return pos, pos + 1, bt, q, k, v
-        qkv = [workloads.trace_step_qkv(self.seed, r, self.state[r][2], self.num_layers, self.hq,
-                                        self.hkv) for r in batch]
+        qkv = [self._step_src(r, self.state[r][2]) for r in batch]
         q = torch.stack([x[0] for x in qkv], dim=1)
         k = torch.stack([x[1] for x in qkv], dim=1)
         v = torch.stack([x[2] for x in qkv], dim=1)

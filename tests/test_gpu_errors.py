@@ -102,3 +102,51 @@ def test_host_side_rejections():
     with pytest.raises(pkv.PkvError, match="EINVAL"):   # misaligned storage
         pkv.kv_pool_create(torch.empty(1 << 20, dtype=torch.uint8, device="cuda")[8:], 8)
     st.close()
+
+
+def test_merge_wait_timeout_is_reported_and_recoverable():
+    """The one wait on another CTA (a merger looking for the partials of a
+    segment split across CTAs) is bounded. With the bound set to 0 looks every
+    such merger gives up at once, so nothing waits: the error word gets
+    ERR_TIMEOUT, those segments' rows stay unwritten, every other row is
+    correct, and after the workspace is zeroed again a normal call is correct
+    everywhere and leaves the workspace zero."""
+    wl = workloads.build("timeout", batch=5, num_layers=1, num_q_heads=32, num_kv_heads=8,
+                         cached_lens=[3000, 17, 1500, 4000, 260], rope_theta=500000.0, seed=21)
+    dw = DeviceWorkload(wl)
+    st = dw.step
+    st.append(0, dw.q, dw.k, dw.v)
+    want_pool = u16(wl.pool).reshape(-1).copy()
+    _, want = oracle_layer(want_pool, wl, 0, u16(wl.q)[0], u16(wl.k)[0], u16(wl.v)[0])
+    assert st.error_bits(reset=True) == 0
+
+    prev = pkv.kv_pool_set_merge_wait_limit(st.pool, 0)
+    assert prev == pkv.DEFAULT_MERGE_WAIT_LOOKS
+    out = torch.full_like(st.out[0], float("nan"))
+    pkv.paged_gqa_decode(st.pool, st.q_rot[0], out, st.block_tables[0], st.seq_lens, wl.scale,
+                         st.workspace)
+    torch.cuda.synchronize()
+    assert st.error_bits(reset=True) == pkv.ERR_TIMEOUT
+    got = out.cpu().numpy()
+    unwritten = np.isnan(got).all(axis=-1)                     # [B, Hq]
+    assert unwritten.any(), "no segment crossed CTAs: the timeout path did not run"
+    assert not unwritten.all()
+    # a row is written in full or not at all; the written ones are right
+    assert not (np.isnan(got).any(axis=-1) & ~unwritten).any()
+    assert_close(got[~unwritten], want[~unwritten], "rows whose merge did not time out")
+    # rows of one (sequence, kv head) segment go together
+    g = wl.num_q_heads // wl.num_kv_heads
+    seg = unwritten.reshape(wl.batch, wl.num_kv_heads, g)
+    assert (seg.all(axis=-1) | ~seg.any(axis=-1)).all()
+    assert bool(st.workspace.any()), "the given-up merges left their partials behind"
+
+    assert pkv.kv_pool_set_merge_wait_limit(st.pool, prev) == 0
+    st.workspace.zero_()
+    out.fill_(float("nan"))
+    pkv.paged_gqa_decode(st.pool, st.q_rot[0], out, st.block_tables[0], st.seq_lens, wl.scale,
+                         st.workspace)
+    torch.cuda.synchronize()
+    assert st.error_bits() == 0
+    assert_close(out.cpu().numpy(), want, "after the workspace was zeroed again")
+    assert not bool(st.workspace.any()), "a completed call leaves the workspace zero"
+    st.close()

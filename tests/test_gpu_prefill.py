@@ -144,3 +144,77 @@ def test_bad_page_id_is_flagged_and_masked():
     assert pkv.pkv_get_error(kp, reset=True) & pkv.ERR_PAGE_ID
     assert torch.isfinite(out).all()
     kp.close()
+
+
+def _oracle_prefill_threaded(host, bt, cu, starts, q, k, v, hq, hkv, theta, scale, workers=16):
+    """The oracle's prefill by its definition, spread over threads: every chunk
+    token is appended exactly as a one-token decode append at its position
+    (one oracle append call over all tokens as one-token sequences), then
+    token t of sequence b attends, like one decode, over the sequence's first
+    start + t + 1 tokens; the causal prefixes only read slots that earlier
+    tokens wrote, so the decodes run in parallel batches. (That a prefill
+    equals this composition is pinned in tests/test_oracle_prefill.py.)"""
+    import concurrent.futures
+    total = int(cu[-1])
+    seq_of = np.repeat(np.arange(len(starts)), np.diff(cu))
+    pos = (np.asarray(starts)[seq_of] + np.arange(total) - cu[seq_of]).astype(np.int32)
+    tbt = np.ascontiguousarray(bt[seq_of])
+    q_rot = oracle.append_rope(host, num_kv_heads=hkv, q=q, k=k, v=v, block_tables=tbt,
+                               max_blocks=bt.shape[1], seq_lens=pos + 1, positions=pos,
+                               batch=total, num_q_heads=hq, theta=theta)
+    out = np.empty_like(q_rot)
+
+    def part(lo, hi):
+        out[lo:hi] = oracle.gqa_decode(host, num_kv_heads=hkv, q_rot=q_rot[lo:hi],
+                                       block_tables=tbt[lo:hi], max_blocks=bt.shape[1],
+                                       seq_lens=pos[lo:hi] + 1, batch=hi - lo, num_q_heads=hq,
+                                       scale=scale)
+
+    # longer prefixes cost more: interleave the token ranges over the threads
+    edges = np.linspace(0, total, 8 * workers + 1).astype(int)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(lambda i: part(edges[i], edges[i + 1]), range(len(edges) - 1)))
+    return q_rot, out
+
+
+@pytest.mark.parametrize("nb,t", [(4, 2048), (1, 8192)])
+def test_measured_prefill_sizes_every_row(nb, t):
+    """The prompt sizes the benchmark measures (Llama-3.2-1B shape, fresh
+    prompts, one layer): the whole pool bit for bit, q_rot and every output
+    row of every token and head within the decode tolerances."""
+    hq, hkv, theta, scale = 32, 8, 500000.0, 0.125
+    gen = torch.Generator().manual_seed(40 + nb)
+    rng = np.random.default_rng(40 + nb)
+    mb = -(-t // 16)
+    num_pages = nb * mb + 5
+    pool = torch.randn(num_pages * 2 * hkv * 16 * 64, generator=gen).to(torch.bfloat16)
+    bt = rng.permutation(num_pages)[:nb * mb].astype(np.int32).reshape(nb, mb)
+    total = nb * t
+    q = torch.randn(total, hq, 64, generator=gen).to(torch.bfloat16)
+    k = torch.randn(total, hkv, 64, generator=gen).to(torch.bfloat16)
+    v = torch.randn(total, hkv, 64, generator=gen).to(torch.bfloat16)
+    cu = np.arange(0, total + 1, t, dtype=np.int32)
+    starts = np.zeros(nb, np.int32)
+
+    dev = torch.device("cuda")
+    dpool = pool.to(dev)
+    kp = pkv.kv_pool_create(dpool, hkv)
+    q_rot = torch.empty(total, hq, 64, device=dev)
+    out = torch.empty(total, hq, 64, device=dev)
+    ws = pkv.alloc_prefill_workspace(total, nb, mb, device=dev)
+    d_cu, d_st = torch.from_numpy(cu).to(dev), torch.from_numpy(starts).to(dev)
+    rope = pkv.alloc_prefill_rope_table(total, device=dev)
+    pkv.paged_prefill_rope_table(d_cu, d_st, total, mb, theta, rope)
+    pkv.paged_prefill(kp, q.to(dev), k.to(dev), v.to(dev), q_rot, out, torch.from_numpy(bt).to(dev),
+                      d_cu, d_st, theta, scale, ws, rope_table=rope)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_error(kp) == 0
+
+    host = u16(pool).copy()
+    want_qrot, want = _oracle_prefill_threaded(host, bt, cu, starts, u16(q), u16(k), u16(v), hq,
+                                               hkv, theta, scale)
+    mism = np.flatnonzero(u16(dpool) != host)
+    assert mism.size == 0, f"{mism.size} pool elements differ, first at {mism[:5]}"
+    np.testing.assert_allclose(q_rot.cpu().numpy(), want_qrot, rtol=1e-5, atol=2e-5)
+    assert_close(out.cpu().numpy(), want, f"prefill {nb} x {t}")
+    kp.close()

@@ -30,7 +30,9 @@ def test_trace_matches_oracle_step_by_step(static, prefill_tokens):
     # 64 pages = 2 layers x 32: budgets of 4..15 pages per layer, so requests wait
     tr = DecodeTrace(reqs, num_pages=64, num_layers=nl, num_q_heads=hq, num_kv_heads=hkv,
                      rope_theta=theta, seed=seed, static_batching=static, max_batch=8,
-                     prefill_tokens=prefill_tokens)
+                     prefill_tokens=prefill_tokens,
+                     prompt_qkv=lambda r, n: workloads.trace_prompt_qkv(seed, r, nl, hq, hkv, n),
+                     step_qkv=lambda r, s: workloads.trace_step_qkv(seed, r, s, nl, hq, hkv))
     page_elems = 2 * hkv * 16 * 64
     host = np.zeros(64 * page_elems, dtype=np.uint16)
     checked = {"steps": 0, "worst": 0.0, "calls": 0, "split": 0}
