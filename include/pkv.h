@@ -126,8 +126,10 @@ int kv_pool_set_merge_wait_limit(pkv_pool_t *pool, uint32_t looks, uint32_t *pre
  *   seq_lens      int32 [batch], length after the append (>= 1)
  *   positions     int32 [batch], RoPE position of the new token
  *   rope_theta    RoPE base (> 0, finite)
- * The rotated key is computed in fp64 and rounded once to bf16 (nearest,
- * ties to even); v is copied bit for bit. q_rot is fp32, not rounded to bf16.
+ * The stored key is the bf16 rounding (nearest, ties to even) of the fp64
+ * rotation by the correctly rounded fp64 cos and sin of the angle (as in
+ * paged_rope_cos_sin): two rounded products and one rounded sum or
+ * difference. v is copied bit for bit. q_rot is fp32, not rounded to bf16.
  * A sequence with a bad length or page id gets its q_rot written but nothing
  * stored in the pool (error bit set). batch == 0 is a no-op.
  * num_q_heads must be a multiple of the pool's num_kv_heads.
@@ -188,8 +190,12 @@ int paged_gqa_decode(const pkv_pool_t *pool, const float *q_rot, float *out,
 
 /*
  * RoPE angles of a decode step: for each sequence b and frequency j < 32,
- * cos and sin of positions[b] * rope_theta^(-2j/64) in fp64 (the product
- * rounded once, then the CUDA math library's fp64 sincos). ("手写LLM推理引擎…"
+ * cos and sin of positions[b] * rope_theta^(-2j/64) in fp64: the product
+ * rounded once to fp64, then its cos and sin correctly rounded to fp64 (the
+ * fp64 values nearest to the true ones, evaluated in double-double with a
+ * rounding test; every angle of positions below 2^17 at bases 1e4, 5e5 and
+ * 1e6 is decided, and elsewhere an undecided value, of probability about
+ * 2^-37, is within half an ulp plus 2^-90 relative). ("手写LLM推理引擎…"
  * section 3.2 precomputes such a cos/sin table once instead of per use.)
  * The positions are the same in every layer, so one table serves all the
  * layers of a step. Layout of the PKV_ROPE_TABLE_BYTES(batch) bytes:

@@ -38,7 +38,9 @@ def lib():
             L.oracle_rope_inv_freq.argtypes = [_c_double, _c_int, _c_int]
             L.oracle_rope_inv_freq.restype = _c_double
             L.oracle_rope_rotate_many.argtypes = [_f64p, _f64p, _c_long, _c_int, _i32p, _c_double]
-            L.oracle_rope_rotate_many.restype = None
+            L.oracle_rope_rotate_many.restype = _c_int
+            L.oracle_cos_sin_many.argtypes = [_f64p, _f64p, _f64p, _c_long]
+            L.oracle_cos_sin_many.restype = _c_long
             L.oracle_append_rope.argtypes = [_u16p, _c_long, _c_int, _c_int, _c_int, _u16p, _u16p,
                                              _u16p, _f64p, _i32p, _c_int, _i32p, _i32p, _c_int,
                                              _c_int, _c_double]
@@ -104,8 +106,26 @@ def rope_rotate(x, positions, theta: float) -> np.ndarray:
     x = _f64(x)
     n, d = x.shape
     y = np.empty_like(x)
-    lib().oracle_rope_rotate_many(x, y, n, d, _i32(positions).reshape(n), float(theta))
+    _check(lib().oracle_rope_rotate_many(x, y, n, d, _i32(positions).reshape(n), float(theta)),
+           "rope_rotate (cos/sin not decidable)")
     return y
+
+
+def cos_sin(angles) -> tuple[np.ndarray, np.ndarray, int]:
+    """Correctly rounded fp64 cos and sin of fp64 angles; also returns how many
+    values the rounding test could not decide (0 expected)."""
+    a = _f64(angles)
+    c = np.empty_like(a)
+    s = np.empty_like(a)
+    bad = lib().oracle_cos_sin_many(a.reshape(-1), c.reshape(-1), s.reshape(-1), a.size)
+    return c, s, int(bad)
+
+
+def rope_angles(positions, theta: float, head_dim: int = 64) -> np.ndarray:
+    """The fp64 angles fl(pos * inv_freq_j), [n][head_dim/2], as the rotation forms them."""
+    inv = rope_inv_freq(theta, head_dim)
+    pos = np.asarray(positions, dtype=np.float64).reshape(-1, 1)
+    return pos * inv[None, :]  # one rounded fp64 product per element
 
 
 def append_rope(pool_u16: np.ndarray, *, num_kv_heads: int, q, k, v, block_tables, max_blocks: int,

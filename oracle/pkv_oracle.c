@@ -97,6 +97,147 @@ void oracle_bf16_from_double_array(const double *x, uint16_t *out, long n)
 		out[i] = oracle_bf16_from_double(x[i]);
 }
 
+/*
+ * cos and sin of an fp64 angle, correctly rounded to fp64: the fp64 numbers
+ * nearest to the true values. [P2] section 3.2 rotates by cos and sin of the
+ * angle m theta_j; the stored key is the bf16 rounding of an fp64 rotation by
+ * them, so they are fixed by this definition rather than by whichever math
+ * library is linked.
+ *
+ * Method, in double-double arithmetic (a value is hi + lo, about 106 bits):
+ *  - reduction: k = nearest integer to a * 2/pi, r = a - k pi/2 with pi/2 as
+ *    the sum of four doubles (each the double nearest to what the previous
+ *    ones leave over, pi/2 to about 2^-216), every product k * part exact
+ *    (two-product by FMA), the differences summed in double-double;
+ *  - Taylor series at |r| <= pi/4 (plus a few ulps), nested:
+ *    sin r = r (1 - r^2/(2*3) (1 - r^2/(4*5) (...))),
+ *    cos r = 1 - r^2/(1*2) (1 - r^2/(3*4) (...)), 16 factors each, every
+ *    step in double-double (division by the integer (2n)(2n+1) or
+ *    (2n-1)(2n) done in double-double);
+ *  - quadrant k mod 4 picks +-sin r / +-cos r;
+ *  - rounding test: the double-double result is within 2^-92 of the true
+ *    value relative (plus k 2^-130 absolute for the reduction); if a midpoint
+ *    between neighbouring doubles lies that close, the rounding cannot be
+ *    decided and the function returns -1 (0 otherwise).
+ */
+typedef struct {
+	double hi, lo;
+} ddouble;
+
+static ddouble dd_sum(double a, double b)  /* a + b exactly (Knuth) */
+{
+	double s = a + b;
+	double bb = s - a;
+	double e = (a - (s - bb)) + (b - bb);
+	ddouble r = { s, e };
+	return r;
+}
+
+static ddouble dd_quick(double a, double b)  /* a + b exactly, |a| >= |b| (Dekker) */
+{
+	double s = a + b;
+	ddouble r = { s, b - (s - a) };
+	return r;
+}
+
+static ddouble dd_prod(double a, double b)  /* a * b exactly */
+{
+	double p = a * b;
+	ddouble r = { p, fma(a, b, -p) };
+	return r;
+}
+
+static ddouble dd_plus(ddouble x, ddouble y)
+{
+	ddouble s = dd_sum(x.hi, y.hi);
+	ddouble t = dd_sum(x.lo, y.lo);
+	s = dd_quick(s.hi, s.lo + t.hi);
+	return dd_quick(s.hi, s.lo + t.lo);
+}
+
+static ddouble dd_times(ddouble x, ddouble y)
+{
+	ddouble p = dd_prod(x.hi, y.hi);
+	return dd_quick(p.hi, p.lo + (x.hi * y.lo + x.lo * y.hi));
+}
+
+static ddouble dd_over(ddouble x, double d)  /* x / d */
+{
+	double q1 = x.hi / d;
+	ddouble p = dd_prod(q1, d);
+	double rem = ((x.hi - p.hi) - p.lo) + x.lo;
+	return dd_quick(q1, rem / d);
+}
+
+/* 1 - x, for |x| < 1 */
+static ddouble dd_one_minus(ddouble x)
+{
+	ddouble s = dd_sum(1.0, -x.hi);
+	return dd_quick(s.hi, s.lo - x.lo);
+}
+
+/* Whether x.hi is the double nearest to every real within eps of x. */
+static int dd_decided(ddouble x, double eps)
+{
+	if (x.hi == 0.0)
+		return x.lo == 0.0 && eps == 0.0;
+	int e;
+	frexp(x.hi, &e);                 /* |x.hi| in [2^(e-1), 2^e) */
+	double ulp = ldexp(1.0, e - 53);
+	double m = fabs(x.hi);
+	int inward = (x.lo < 0.0) == (x.hi > 0.0);
+	double half = (inward && m == ldexp(1.0, e - 1)) ? ulp / 4 : ulp / 2;
+	return fabs(x.lo) + eps < half;
+}
+
+int oracle_cos_sin(double a, double *c, double *s)
+{
+	static const double pio2[4] = {
+		0x1.921fb54442d18p+0, 0x1.1a62633145c07p-54,
+		-0x1.f1976b7ed8fbcp-110, 0x1.4cf98e804177dp-164,
+	};
+	if (!isfinite(a) || fabs(a) >= 0x1p52) {
+		*c = *s = NAN;
+		return -2;
+	}
+	int neg = signbit(a) != 0;
+	double x = fabs(a);
+	double k = nearbyint(x * 0x1.45f306dc9c883p-1);  /* 2/pi rounded */
+	ddouble r = { x, 0.0 };
+	for (int i = 0; i < 4; i++) {
+		ddouble p = dd_prod(k, pio2[i]);
+		p.hi = -p.hi;
+		p.lo = -p.lo;
+		r = dd_plus(r, p);
+	}
+	ddouble z = dd_times(r, r);
+	ddouble ts = { 1.0, 0.0 }, tc = { 1.0, 0.0 };
+	for (int n = 16; n >= 1; n--) {
+		ts = dd_one_minus(dd_over(dd_times(z, ts), (double)((2 * n) * (2 * n + 1))));
+		tc = dd_one_minus(dd_over(dd_times(z, tc), (double)((2 * n - 1) * (2 * n))));
+	}
+	ddouble sr = dd_times(r, ts), cr = tc;
+	ddouble cv, sv;
+	switch ((long long)k & 3) {
+	case 0: cv = cr; sv = sr; break;
+	case 1: cv = sr; cv.hi = -cv.hi; cv.lo = -cv.lo; sv = cr; break;
+	case 2: cv = cr; cv.hi = -cv.hi; cv.lo = -cv.lo; sv = sr; sv.hi = -sv.hi; sv.lo = -sv.lo; break;
+	default: cv = sr; sv = cr; sv.hi = -sv.hi; sv.lo = -sv.lo; break;
+	}
+	if (neg) {
+		sv.hi = -sv.hi;
+		sv.lo = -sv.lo;
+	}
+	*c = cv.hi;
+	*s = sv.hi;
+	if (x == 0.0)
+		return 0;                    /* cos 0 = 1 and sin 0 = 0 exactly */
+	double abs_err = k * 0x1p-130;       /* the reduction is exact when k = 0 */
+	int ok = dd_decided(cv, fabs(cv.hi) * 0x1p-92 + abs_err) &&
+		 dd_decided(sv, fabs(sv.hi) * 0x1p-92 + abs_err);
+	return ok ? 0 : -1;
+}
+
 /* [P2] section 3.2, cos/sin precompute: inverse frequency base^(-2j/dim). */
 double oracle_rope_inv_freq(double theta, int j, int head_dim)
 {
@@ -108,13 +249,15 @@ double oracle_rope_inv_freq(double theta, int j, int head_dim)
  *   y_j       = x_j * cos - x_{j+D/2} * sin
  *   y_{j+D/2} = x_{j+D/2} * cos + x_j * sin
  * Each product and each sum is one fp64 rounding (no fused multiply-add). */
-void oracle_rope_rotate(const double *x, double *y, int head_dim, long pos, double theta)
+int oracle_rope_rotate(const double *x, double *y, int head_dim, long pos, double theta)
 {
 	int half = head_dim / 2;
+	int rc = 0;
 	for (int j = 0; j < half; j++) {
 		double angle = (double)pos * oracle_rope_inv_freq(theta, j, head_dim);
-		double c = cos(angle);
-		double s = sin(angle);
+		double c, s;
+		if (oracle_cos_sin(angle, &c, &s) != 0)
+			rc = -4;             /* cos/sin not decidable: the caller reports it */
 		double a = x[j];
 		double b = x[j + half];
 		double ac = a * c;
@@ -124,14 +267,29 @@ void oracle_rope_rotate(const double *x, double *y, int head_dim, long pos, doub
 		y[j] = ac - bs;
 		y[j + half] = bc + as;
 	}
+	return rc;
 }
 
-/* Rotate n vectors of length head_dim, vector i at position pos[i]. */
-void oracle_rope_rotate_many(const double *x, double *y, long n, int head_dim,
-			     const int32_t *pos, double theta)
+/* Rotate n vectors of length head_dim, vector i at position pos[i]. Returns
+ * 0, or -4 when some cos/sin could not be rounded with certainty. */
+int oracle_rope_rotate_many(const double *x, double *y, long n, int head_dim,
+			    const int32_t *pos, double theta)
 {
+	int rc = 0;
 	for (long i = 0; i < n; i++)
-		oracle_rope_rotate(x + i * head_dim, y + i * head_dim, head_dim, pos[i], theta);
+		if (oracle_rope_rotate(x + i * head_dim, y + i * head_dim, head_dim, pos[i], theta))
+			rc = -4;
+	return rc;
+}
+
+/* cos and sin of n angles (oracle_cos_sin); returns the number undecided. */
+long oracle_cos_sin_many(const double *a, double *c, double *s, long n)
+{
+	long bad = 0;
+	for (long i = 0; i < n; i++)
+		if (oracle_cos_sin(a[i], c + i, s + i) != 0)
+			bad++;
+	return bad;
 }
 
 static size_t pool_offset(long page, int h, int kind, int slot, int d,
@@ -148,8 +306,8 @@ static size_t pool_offset(long page, int h, int kind, int slot, int d,
  *
  * q, k, v are bf16 bits, [B][Hq][D], [B][Hkv][D], [B][Hkv][D]. The rotated
  * query goes to q_rot (fp64, [B][Hq][D]). Returns 0, or -1 for a bad length,
- * -2 for a bad page id, -3 for a bad shape (nothing after the failing sequence
- * is written).
+ * -2 for a bad page id, -3 for a bad shape, -4 when a cos/sin could not be
+ * rounded with certainty (nothing after the failing sequence is written).
  */
 int oracle_append_rope(uint16_t *pool, long num_pages, int num_kv_heads, int head_dim,
 		       int page_size, const uint16_t *q, const uint16_t *k, const uint16_t *v,
@@ -175,7 +333,8 @@ int oracle_append_rope(uint16_t *pool, long num_pages, int num_kv_heads, int hea
 			const uint16_t *vh = v + ((size_t)b * num_kv_heads + h) * head_dim;
 			for (int d = 0; d < head_dim; d++)
 				in[d] = oracle_bf16_to_double(kh[d]);
-			oracle_rope_rotate(in, out, head_dim, pos, theta);
+			if (oracle_rope_rotate(in, out, head_dim, pos, theta))
+				return -4;
 			for (int d = 0; d < head_dim; d++) {
 				pool[pool_offset(page, h, 0, slot, d, num_kv_heads, head_dim, page_size)] =
 					oracle_bf16_from_double(out[d]);
@@ -186,8 +345,9 @@ int oracle_append_rope(uint16_t *pool, long num_pages, int num_kv_heads, int hea
 			const uint16_t *qh = q + ((size_t)b * num_q_heads + i) * head_dim;
 			for (int d = 0; d < head_dim; d++)
 				in[d] = oracle_bf16_to_double(qh[d]);
-			oracle_rope_rotate(in, q_rot + ((size_t)b * num_q_heads + i) * head_dim,
-					   head_dim, pos, theta);
+			if (oracle_rope_rotate(in, q_rot + ((size_t)b * num_q_heads + i) * head_dim,
+					       head_dim, pos, theta))
+				return -4;
 		}
 	}
 	return 0;

@@ -9,16 +9,20 @@
 // y_{j'} = x_{j'} cos + x_j sin with theta_j = base^(-2j/D), read with
 // rotate-half pairing j' = j + D/2.
 //
-// One CTA per sequence. 32 threads evaluate the 32 angles' cos/sin in fp64;
-// the key is rotated in fp64 with explicitly rounded products and sums (no
-// contraction) and rounded once to bf16, so the stored bytes are reproducible
-// bit for bit. The query is rotated in fp32 and kept in fp32. Values are
-// copied verbatim. The whole kernel moves B*(Hq+2*Hkv)*128 bytes: it is
-// launch-latency bound, not bandwidth bound.
+// One CTA per sequence. 64 threads evaluate the 32 angles' cos and sin,
+// correctly rounded to fp64 (rope_cr.cuh). The key is rotated and rounded to
+// bf16 exactly as fp64 arithmetic on those values rounds it (two rounded
+// products, one rounded difference, then one rounding to bf16): by the
+// certified fp32 double-word path the fused decode step uses, with the fp64
+// rotation where that path cannot certify, so the stored bytes are the same
+// bit for bit whichever entry point appends. The query is rotated in fp32 and
+// kept in fp32. Values are copied verbatim. The whole kernel moves
+// B*(Hq+2*Hkv)*128 bytes: it is launch-latency bound, not bandwidth bound.
 #include <cmath>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
+#include "rope_cr.cuh"
 
 namespace pkv {
 namespace {
@@ -45,35 +49,37 @@ struct AppendParams {
   int hq;
   int* err;
   double inv_freq[kHalf];
+  RopeSeriesCoef coef;
 };
 
 __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const AppendParams p) {
-  __shared__ double cos_d[kHalf], sin_d[kHalf];
-  __shared__ float cos_f[kHalf], sin_f[kHalf];
+  __shared__ double cs_d[kHalf][2];  // {cos, sin}, correctly rounded fp64
+  __shared__ float cs_f[kHalf][4];   // {cos_hi, cos_lo, sin_hi, sin_lo}
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   const int n = p.seq_lens[b];
   const int pos = p.positions[b];
-  if (tid < kHalf) {
-    const double angle = __dmul_rn(static_cast<double>(pos), p.inv_freq[tid]);
-    double s, c;
-    sincos(angle, &s, &c);
-    cos_d[tid] = c;
-    sin_d[tid] = s;
-    cos_f[tid] = static_cast<float>(c);
-    sin_f[tid] = static_cast<float>(s);
+  if (tid < 2 * kHalf) {  // thread 2j: cos of angle j, 2j + 1: its sin
+    const int j = tid >> 1, w = tid & 1;
+    bool certain;
+    const double val = rope_cos_or_sin_cr(__dmul_rn(static_cast<double>(pos), p.inv_freq[j]), w != 0,
+                                          p.coef, &certain);
+    const float hi = __double2float_rn(val);
+    cs_d[j][w] = val;
+    cs_f[j][2 * w] = hi;
+    cs_f[j][2 * w + 1] = __double2float_rn(__dsub_rn(val, static_cast<double>(hi)));
   }
   __syncthreads();
 
-  // Rotated query, fp32, [Hq][64].
+  // Rotated query, fp32, [Hq][64], from the fp32 roundings of cos and sin.
   const uint16_t* qb = p.q + static_cast<size_t>(b) * p.hq * kHeadDim;
   float* qo = p.q_rot + static_cast<size_t>(b) * p.hq * kHeadDim;
   for (int idx = tid; idx < p.hq * kHalf; idx += kAppendThreads) {
     const int head = idx / kHalf, j = idx % kHalf;
     const float x0 = __uint_as_float(static_cast<uint32_t>(qb[head * kHeadDim + j]) << 16);
     const float x1 = __uint_as_float(static_cast<uint32_t>(qb[head * kHeadDim + j + kHalf]) << 16);
-    qo[head * kHeadDim + j] = x0 * cos_f[j] - x1 * sin_f[j];
-    qo[head * kHeadDim + j + kHalf] = x1 * cos_f[j] + x0 * sin_f[j];
+    qo[head * kHeadDim + j] = x0 * cs_f[j][0] - x1 * cs_f[j][2];
+    qo[head * kHeadDim + j + kHalf] = x1 * cs_f[j][0] + x0 * cs_f[j][2];
   }
 
   // Destination slot of the new token.
@@ -91,12 +97,18 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   const int slot = t % kPage;
   uint16_t* page_base = p.pool + static_cast<size_t>(page) * p.hkv * (kHeadPageBytes / 2);
 
-  // Rotated key: fp64, explicit roundings, one rounding to bf16.
+  // Rotated key, rounded once to bf16 as the fp64 rotation rounds it.
   const uint16_t* kb = p.k + static_cast<size_t>(b) * p.hkv * kHeadDim;
   for (int idx = tid; idx < p.hkv * kHalf; idx += kAppendThreads) {
     const int h = idx / kHalf, j = idx % kHalf;
+    const uint16_t k0 = kb[h * kHeadDim + j], k1 = kb[h * kHeadDim + j + kHalf];
+    const float x0 = __uint_as_float(static_cast<uint32_t>(k0) << 16);
+    const float x1 = __uint_as_float(static_cast<uint32_t>(k1) << 16);
+    const float* c = cs_f[j];
     uint16_t y0, y1;
-    rotate_key_pair(kb[h * kHeadDim + j], kb[h * kHeadDim + j + kHalf], cos_d[j], sin_d[j], y0, y1);
+    if (!(rotated_bf16_fast(x0, x1, c[0], c[1], c[2], c[3], y0) &&
+          rotated_bf16_fast(x1, -x0, c[0], c[1], c[2], c[3], y1)))
+      rotate_key_pair(k0, k1, cs_d[j][0], cs_d[j][1], y0, y1);
     uint16_t* krow = page_base + (h * 2 + 0) * (kHalfBytes / 2) + slot * kHeadDim;
     krow[j] = y0;
     krow[j + kHalf] = y1;
@@ -110,27 +122,45 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   }
 }
 
-// One thread per (sequence, frequency): cos and sin of pos * inv_freq_j in
-// fp64 (the values the append kernel forms for its rotation), stored twice:
-// as fp32 pairs {hi, lo} (hi = the fp64 value rounded to fp32, lo = the
-// remainder rounded to fp32, so hi + lo is within 2^-48 of it) for the fused
-// step's fp32 paths, and in fp64 for its rare fp64 fallback.
-__global__ void rope_cos_sin_kernel(const int32_t* __restrict__ positions, int batch,
-                                    const InvFreq inv, float4* __restrict__ pairs,
-                                    double2* __restrict__ full) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= batch * kHalf) return;
-  const int b = idx / kHalf, j = idx % kHalf;
-  const double angle = __dmul_rn(static_cast<double>(positions[b]), inv.v[j]);
-  double s, c;
-  sincos(angle, &s, &c);
-  const float ch = __double2float_rn(c), sh = __double2float_rn(s);
-  pairs[idx] = make_float4(ch, __double2float_rn(__dsub_rn(c, static_cast<double>(ch))), sh,
-                           __double2float_rn(__dsub_rn(s, static_cast<double>(sh))));
-  full[idx] = make_double2(c, s);
+// Two threads per (sequence, frequency), one for the cos and one for the sin
+// of pos * inv_freq_j, correctly rounded to fp64 (the values the append
+// kernel forms for its rotation), stored twice: as fp32 pairs {hi, lo} (hi =
+// the fp64 value rounded to fp32, lo = the remainder rounded to fp32, so
+// hi + lo is within 2^-48 of it) for the fused step's fp32 paths, and in fp64
+// for its rare fp64 fallback. One warp of 32 (sequence, frequency, cos|sin)
+// values per 32 threads: fp64 throughput on this part is low, so the values
+// are spread over as many SMs as the batch allows.
+constexpr int kTableThreads = 64;
+__global__ void __launch_bounds__(kTableThreads)
+    rope_cos_sin_kernel(const int32_t* __restrict__ positions, int batch, const InvFreq inv,
+                        const RopeSeriesCoef coef, float2* __restrict__ pairs,
+                        double* __restrict__ full) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;  // 2 (b 32 + j) + (0: cos, 1: sin)
+  if (idx >= batch * 2 * kHalf) return;
+  const int bj = idx >> 1, b = bj / kHalf, j = bj - b * kHalf;
+  bool certain;
+  const double val = rope_cos_or_sin_cr(__dmul_rn(static_cast<double>(positions[b]), inv.v[j]),
+                                        (idx & 1) != 0, coef, &certain);
+  const float hi = __double2float_rn(val);
+  pairs[idx] = make_float2(hi, __double2float_rn(__dsub_rn(val, static_cast<double>(hi))));
+  full[idx] = val;
 }
 
 }  // namespace
+
+RopeSeriesCoef rope_series_coef() {
+  RopeSeriesCoef c;
+  for (int n = 0; n < 16; ++n) {
+    // n = 0 is unused; 1/((2n-1)(2n)) and 1/((2n)(2n+1)) for n >= 1
+    const double dc = n ? static_cast<double>((2 * n - 1) * (2 * n)) : 1.0;
+    const double ds = n ? static_cast<double>((2 * n) * (2 * n + 1)) : 1.0;
+    c.cos_hi[n] = 1.0 / dc;
+    c.cos_lo[n] = std::fma(-c.cos_hi[n], dc, 1.0) / dc;
+    c.sin_hi[n] = 1.0 / ds;
+    c.sin_lo[n] = std::fma(-c.sin_hi[n], ds, 1.0) / ds;
+  }
+  return c;
+}
 
 cudaError_t launch_rope_cos_sin(const int32_t* positions, int batch, double rope_theta,
                                 void* table, cudaStream_t stream) {
@@ -138,10 +168,11 @@ cudaError_t launch_rope_cos_sin(const int32_t* positions, int batch, double rope
   InvFreq inv;
   for (int j = 0; j < kHalf; ++j)
     inv.v[j] = std::pow(rope_theta, -(2.0 * j) / static_cast<double>(kHeadDim));
-  const int n = batch * kHalf;
-  float4* pairs = static_cast<float4*>(table);
-  double2* full = reinterpret_cast<double2*>(pairs + n);
-  rope_cos_sin_kernel<<<(n + 255) / 256, 256, 0, stream>>>(positions, batch, inv, pairs, full);
+  const int n = batch * 2 * kHalf;
+  float2* pairs = static_cast<float2*>(table);
+  double* full = reinterpret_cast<double*>(pairs + n);
+  rope_cos_sin_kernel<<<(n + kTableThreads - 1) / kTableThreads, kTableThreads, 0, stream>>>(
+      positions, batch, inv, rope_series_coef(), pairs, full);
   return cudaGetLastError();
 }
 
@@ -164,9 +195,10 @@ cudaError_t launch_append_rope(const AppendLaunch& a, cudaStream_t stream) {
   // Step 1 of the rotation, the 32 inverse frequencies base^(-2j/64), is a
   // launch constant: it is evaluated once here with the C library's pow and
   // passed by value; each kernel thread then forms its angle pos * inv_freq_j
-  // (one rounded product) and its cos/sin in fp64.
+  // (one rounded product) and its correctly rounded fp64 cos or sin.
   for (int j = 0; j < kHalf; ++j)
     p.inv_freq[j] = std::pow(a.rope_theta, -(2.0 * j) / static_cast<double>(kHeadDim));
+  p.coef = rope_series_coef();
   append_rope_kernel<<<a.batch, kAppendThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }

@@ -24,6 +24,7 @@
 #include "pkv_device.cuh"
 #include "tc05.cuh"
 #include "pkv_internal.h"
+#include "rope_cr.cuh"
 
 namespace pkv {
 namespace {
@@ -67,25 +68,27 @@ struct PrefillInvFreq {
   double v[kHalfDim];  // theta^(-2j/64), from the C library's pow on the host
 };
 
-// One thread per (chunk token, frequency): cos and sin of its position times
-// inv_freq_j in fp64 (position 0 for a token of a malformed chunk), stored as
-// fp32 pairs {hi, lo} and in fp64: the layout of paged_rope_cos_sin's table.
-__global__ void prefill_rope_kernel(const int32_t* __restrict__ cu_tokens,
-                                    const int32_t* __restrict__ start_pos, int batch, int total,
-                                    int max_blocks, const PrefillInvFreq inv,
-                                    float4* __restrict__ pairs, double2* __restrict__ full) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= total * kHalfDim) return;
-  const int tkn = idx / kHalfDim, j = idx - tkn * kHalfDim;
+// Two threads per (chunk token, frequency), one for the cos and one for the
+// sin of its position times inv_freq_j, correctly rounded to fp64 (position 0
+// for a token of a malformed chunk), stored as fp32 pairs {hi, lo} and in
+// fp64: the layout of paged_rope_cos_sin's table.
+constexpr int kRopeThreads = 64;
+__global__ void __launch_bounds__(kRopeThreads)
+    prefill_rope_kernel(const int32_t* __restrict__ cu_tokens,
+                        const int32_t* __restrict__ start_pos, int batch, int total,
+                        int max_blocks, const PrefillInvFreq inv, const RopeSeriesCoef coef,
+                        float2* __restrict__ pairs, double* __restrict__ full) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;  // 2 (token 32 + j) + (0: cos, 1: sin)
+  if (idx >= total * 2 * kHalfDim) return;
+  const int tj = idx >> 1, tkn = tj / kHalfDim, j = tj - tkn * kHalfDim;
   int seq;
   const long long pos = chunk_position(cu_tokens, start_pos, batch, max_blocks, tkn, &seq);
   const double angle = __dmul_rn(static_cast<double>(pos < 0 ? 0 : pos), inv.v[j]);
-  double sn, cs;
-  sincos(angle, &sn, &cs);
-  const float ch = __double2float_rn(cs), sh = __double2float_rn(sn);
-  pairs[idx] = make_float4(ch, __double2float_rn(__dsub_rn(cs, static_cast<double>(ch))), sh,
-                           __double2float_rn(__dsub_rn(sn, static_cast<double>(sh))));
-  full[idx] = make_double2(cs, sn);
+  bool certain;
+  const double val = rope_cos_or_sin_cr(angle, (idx & 1) != 0, coef, &certain);
+  const float hi = __double2float_rn(val);
+  pairs[idx] = make_float2(hi, __double2float_rn(__dsub_rn(val, static_cast<double>(hi))));
+  full[idx] = val;
 }
 
 // One CTA per chunk token: its rotated query (fp32, from the fp32 cos/sin of
@@ -651,11 +654,11 @@ cudaError_t launch_prefill_rope_table(const int32_t* cu_tokens, const int32_t* s
   PrefillInvFreq inv;
   for (int j = 0; j < kHalfDim; ++j)
     inv.v[j] = std::pow(rope_theta, -(2.0 * j) / static_cast<double>(kHeadDim));
-  const int n = total_tokens * kHalfDim;
-  float4* pairs = static_cast<float4*>(table);
-  double2* full = reinterpret_cast<double2*>(pairs + n);
-  prefill_rope_kernel<<<(n + 255) / 256, 256, 0, stream>>>(cu_tokens, start_pos, batch, total_tokens,
-                                                            max_blocks, inv, pairs, full);
+  const int n = total_tokens * 2 * kHalfDim;
+  float2* pairs = static_cast<float2*>(table);
+  double* full = reinterpret_cast<double*>(pairs + n);
+  prefill_rope_kernel<<<(n + kRopeThreads - 1) / kRopeThreads, kRopeThreads, 0, stream>>>(
+      cu_tokens, start_pos, batch, total_tokens, max_blocks, inv, rope_series_coef(), pairs, full);
   return cudaGetLastError();
 }
 

@@ -108,3 +108,78 @@ def test_rotation_direction():
     assert y[0] == pytest.approx(math.cos(1.0), abs=1e-16)
     assert y[4] == pytest.approx(math.sin(1.0), abs=1e-16)
     assert np.count_nonzero(y) == 2
+
+
+def _cr_reference(angles):
+    """cos and sin of each fp64 angle in 200-bit arithmetic, rounded to the
+    nearest fp64 value (mpmath; an independent evaluation)."""
+    mpmath = pytest.importorskip("mpmath")
+    from mpmath.libmp import round_nearest, to_float
+    c, s = [], []
+    with mpmath.workprec(200):
+        for a in angles:
+            x = mpmath.mpf(float(a))
+            c.append(to_float(mpmath.cos(x)._mpf_, rnd=round_nearest))
+            s.append(to_float(mpmath.sin(x)._mpf_, rnd=round_nearest))
+    return np.array(c), np.array(s)
+
+
+def _rope_sample_angles():
+    """RoPE angles fl(pos * inv_j) at the three bases in use: every frequency
+    at a spread of positions (small, page-sized, the context caps, far beyond
+    them, up to the largest int32), plus random doubles and the doubles
+    nearest to multiples of pi/2 (the reductions with most cancellation)."""
+    rng = np.random.default_rng(5)
+    pos = np.unique(np.concatenate([np.arange(0, 40), [63, 64, 1000, 2047, 2048, 4095, 4096,
+                                                       65535, 131071, 1 << 20, 12345678,
+                                                       2**31 - 1],
+                                    rng.integers(0, 1 << 17, 150)]))
+    ang = [oracle.rope_angles(pos, th).reshape(-1) for th in (1e4, 5e5, 1e6)]
+    k = np.arange(1, 4000, dtype=np.float64)
+    near = k * (math.pi / 2)
+    return np.concatenate(ang + [rng.uniform(0, 2**17, 3000), near, np.nextafter(near, 0)])
+
+
+def test_cos_sin_are_correctly_rounded():
+    """The oracle's fp64 cos and sin are the fp64 values nearest to the true
+    ones (checked against a 200-bit evaluation), and every rounding was
+    decided."""
+    a = _rope_sample_angles()
+    c, s, undecided = oracle.cos_sin(a)
+    assert undecided == 0
+    want_c, want_s = _cr_reference(a)
+    assert np.array_equal(c, want_c), int((c != want_c).sum())
+    assert np.array_equal(s, want_s), int((s != want_s).sum())
+
+
+def test_cos_sin_special_values_and_symmetry():
+    c, s, bad = oracle.cos_sin(np.array([0.0, -0.0]))
+    assert bad == 0 and np.all(c == 1.0) and np.all(s == 0.0)
+    assert not np.signbit(s[0]) and np.signbit(s[1])       # sin(+0) = +0, sin(-0) = -0
+    rng = np.random.default_rng(6)
+    a = rng.uniform(0, 1e5, 2000)
+    c1, s1, _ = oracle.cos_sin(a)
+    c2, s2, _ = oracle.cos_sin(-a)
+    assert np.array_equal(c1, c2) and np.array_equal(s1, -s2)  # cos even, sin odd
+
+
+def test_cos_sin_within_one_ulp_of_the_c_library():
+    """The C library's cos and sin are not correctly rounded everywhere but
+    are within one ulp: a sanity bound on the oracle's values."""
+    a = _rope_sample_angles()
+    c, s, _ = oracle.cos_sin(a)
+    lc = np.array([math.cos(x) for x in a])
+    ls = np.array([math.sin(x) for x in a])
+    for got, ref in ((c, lc), (s, ls)):
+        ulp = np.spacing(np.abs(ref))
+        assert np.all(np.abs(got - ref) <= ulp)
+
+
+def test_cos_sin_decided_over_the_whole_rope_domain():
+    """Every angle fl(pos * inv_j) for positions below 2^17 and every
+    frequency at bases 1e4, 5e5 and 1e6 (12.6 million values each of cos and
+    sin) is decided by the oracle's rounding test, so the pool's bit-exact key
+    bytes are defined everywhere the workloads reach."""
+    for th in (1e4, 5e5, 1e6):
+        _, _, undecided = oracle.cos_sin(oracle.rope_angles(np.arange(1 << 17), th))
+        assert undecided == 0, th
