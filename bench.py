@@ -45,12 +45,10 @@ L2_BYTES = 129 * 10**6
 # the hash of the decode source it was taken on; reported only while the source
 # is unchanged.
 TRAFFIC = {
-    # workload -> (sha256 of gqa_decode.cu prefix, bytes per layer call: the step kernel)
-    # batch 64: 158.246 MB read + 2.838 MB written (ncu --set full, one layer call)
-    "llama1b_b64_l16_u2048": ("6c2f42d9114cc786", 161083904),
-    # Qwen shape: 47.004 MB read + 0.063 MB written (ncu --set full, one layer call)
-    "qwen05b_b32_l24_u1024_4096": ("6c2f42d9114cc786", 47067136),
+    # (workload, seed) -> (sha256 prefix of gqa_decode.cu, read + write bytes per layer call)
 }
+# The other workloads the 70% target names, timed as sub-records of the default line.
+SUB_WORKLOADS = ["llama1b_b256_l16_skew", "qwen05b_b32_l24_u1024_4096"]
 
 
 def _decode_source_hash() -> str:
@@ -289,6 +287,103 @@ def run_reference(args, ws, rank):
     return 0
 
 
+def _timed_step(pkv, wl, dev, args, ws) -> tuple[dict, object]:
+    """Device time of one whole step of ``wl``: warm-up, one CUDA graph of the
+    step (every layer's fused call), W untimed replays, then K replays timed
+    with CUDA events between a barrier and a synchronize; the max over ranks.
+    Workloads whose step reads less than 4x L2 get an L2 flush (a write of
+    2x L2) before every timed replay. Returns the figures and the step."""
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    sl = torch.from_numpy(wl.seq_lens).to(dev)
+    pos = torch.from_numpy(wl.positions).to(dev)
+    step = pkv.DecodeStep(wl.pool, num_kv_heads=wl.num_kv_heads, num_q_heads=wl.num_q_heads,
+                          num_layers=wl.num_layers, block_tables=bt, seq_lens=sl, positions=pos,
+                          rope_theta=wl.rope_theta, scale=wl.scale, pages_per_split=args.pages_per_split,
+                          fused_q_rot=False)
+    stream = torch.cuda.current_stream()
+    step_bytes = wl.kv_bytes_per_step()
+    flush = None
+    if step_bytes <= 4 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):  # eager warm-up (first calls cache kernel attributes)
+        step.run(wl.q, wl.k, wl.v)
+    torch.cuda.synchronize()
+    assert step.error_bits() == 0, "device error flags set during warm-up"
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run(wl.q, wl.k, wl.v)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for s in range(args.steps):
+            flush.fill_(float(s))
+            evs[s][0].record(stream)
+            graph.replay()
+            evs[s][1].record(stream)
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+    _barrier(ws)
+    ms_max = _barrier_max(ms, ws)
+    total_bytes = _barrier_sum(float(step_bytes), ws)
+    assert step.error_bits() == 0, "device error flags set during the timed steps"
+    del graph
+    return {"ms": ms_max, "value": total_bytes / (ms_max / 1e3) / 1e9, "kv_bytes_per_step": step_bytes,
+            "layer_bytes": wl.kv_bytes_per_layer(), "layers": wl.num_layers,
+            "launches": step.launches_per_step() * args.steps, "flush": flush is not None,
+            "seq_len_mean": round(float(wl.seq_lens.mean()), 1)}, step
+
+
+def _seed_sweep(pkv, name, seeds, dev, args, ws, rank) -> list[dict]:
+    """_timed_step of workload ``name`` at each seed (rank r adds 1000 r)."""
+    runs = []
+    for sd in seeds:
+        wl = workloads.make(name, seed=sd + 1000 * rank, device=dev, layers=args.layers)
+        r, step = _timed_step(pkv, wl, dev, args, ws)
+        r["seed"] = sd
+        runs.append(r)
+        step.close()
+        del wl, step
+        torch.cuda.empty_cache()
+    return runs
+
+
+def _median_run(runs: list[dict]) -> dict:
+    return sorted(runs, key=lambda r: r["value"])[len(runs) // 2]
+
+
+def _roofline(r: dict, name: str, seed: int, peak: float, peak_kind: str, steps: int) -> dict:
+    """The decode kernel's roofline from a _timed_step result: algorithmic K/V
+    bytes of one layer call over the mean layer-call time in graph replays."""
+    dec_avg_s = r["ms"] / r["layers"] / 1e3
+    achieved = r["layer_bytes"] / dec_avg_s / 1e9
+    h = _decode_source_hash()
+    traffic = None
+    if (name, seed) in TRAFFIC and TRAFFIC[(name, seed)][0] == h:
+        traffic = TRAFFIC[(name, seed)][1]
+    return {"bound": "hbm",
+            "kernel": "paged_decode_step call per layer: gqa_decode_kernel (step mode, split pieces merged in the kernel)",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
+            "bytes_per_launch": r["layer_bytes"], "launch_us_mean": round(dec_avg_s * 1e6, 2),
+            "timing": f"CUDA events around {steps} replays of a graph of the step's {r['layers']} "
+                      "paged_decode_step calls (inter-kernel gaps included)",
+            "decode_source": h}
+
+
 def run_ours(args, ws, rank, local):
     import paged_kv_decode_rope_gb300 as pkv
     from paged_kv_decode_rope_gb300.build import build
@@ -297,8 +392,26 @@ def run_ours(args, ws, rank, local):
     build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = workloads.make(args.workload, seed=args.seed + 1000 * rank, device=dev, layers=args.layers)
-    pool = wl.pool  # appended into in place; the append is idempotent across steps
+    peak, peak_kind = _peaks()
+    seeds = [args.seed + i for i in range(max(1, args.seeds))]
+    sub_names = [n for n in SUB_WORKLOADS if n != args.workload] \
+        if args.workload == DEFAULT_WORKLOAD and not args.layers and not args.no_sub else []
+
+    # Device-timed steps: the workload at every seed, then the other named
+    # workloads of the target, with the SM clocks sampled throughout.
+    clocks = ClockSampler(local)
+    clocks.start()
+    t_wall = time.perf_counter()
+    runs = _seed_sweep(pkv, args.workload, seeds, dev, args, ws, rank)
+    sub_runs = {name: _seed_sweep(pkv, name, seeds, dev, args, ws, rank) for name in sub_names}
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    head = _median_run(runs)
+    value, ms_step_max = head["value"], head["ms"]
+
+    # The median seed's workload again, for the end-to-end figure and the CPU baseline.
+    wl = workloads.make(args.workload, seed=head["seed"] + 1000 * rank, device=dev, layers=args.layers)
+    pool = wl.pool
     bt = torch.from_numpy(wl.block_tables).to(dev)
     sl = torch.from_numpy(wl.seq_lens).to(dev)
     pos = torch.from_numpy(wl.positions).to(dev)
@@ -307,59 +420,8 @@ def run_ours(args, ws, rank, local):
                           rope_theta=wl.rope_theta, scale=wl.scale, pages_per_split=args.pages_per_split,
                           fused_q_rot=False)
     stream = torch.cuda.current_stream()
-    step_bytes = wl.kv_bytes_per_step()
-    layer_bytes = wl.kv_bytes_per_layer()
-    flush = None
-    if step_bytes <= 4 * L2_BYTES:
-        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-
-    # Eager warm-up (first calls cache kernel attributes), then capture one step
-    # (all layers: append + decode) and the decode launches alone as CUDA graphs.
-    for _ in range(3):
-        step.run(wl.q, wl.k, wl.v)
-    torch.cuda.synchronize()
-    assert step.error_bits() == 0, "device error flags set during warm-up"
-    nl = wl.num_layers
-    g_step = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_step):
-        step.run(wl.q, wl.k, wl.v)
-    for _ in range(args.warmup):
-        g_step.replay()
-    torch.cuda.synchronize()
-
-    def timed(graph, steps):
-        """Device ms per replay; with a flush buffer, L2 is flushed before each replay."""
-        if flush is None:
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(steps):
-                graph.replay()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            return e0.elapsed_time(e1) / steps
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(steps)]
-        for s in range(steps):
-            flush.fill_(float(s))
-            evs[s][0].record(stream)
-            graph.replay()
-            evs[s][1].record(stream)
-        torch.cuda.synchronize()
-        return sum(a.elapsed_time(b) for a, b in evs) / steps
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    _barrier(ws)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter()
-    ms_per_step = timed(g_step, args.steps)
-    wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
-    _barrier(ws)
-    ms_step_max = _barrier_max(ms_per_step, ws)
-    total_bytes = _barrier_sum(float(step_bytes), ws)
-    value = total_bytes / (ms_step_max / 1e3) / 1e9
-    assert step.error_bits() == 0, "device error flags set during the timed steps"
+    total_bytes = _barrier_sum(float(wl.kv_bytes_per_step()), ws)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if head["flush"] else None
 
     # end to end: host buffers in pinned memory; per step copy q/k/v, tables,
     # lengths and positions in, run the step through the C ABI, copy outputs out.
@@ -405,13 +467,25 @@ def run_ours(args, ws, rank, local):
     e2e_ms = _barrier_max(e0.elapsed_time(e1) / e2e_steps, ws)
     e2e_value = total_bytes / (e2e_ms / 1e3) / 1e9
 
-    peak, peak_kind = _peaks()
-    dec_avg_s = ms_per_step / nl / 1e3  # one layer's paged_decode_step call
-    achieved = layer_bytes / dec_avg_s / 1e9
-    h = _decode_source_hash()
-    traffic = None
-    if wl.name in TRAFFIC and TRAFFIC[wl.name][0] == h:
-        traffic = TRAFFIC[wl.name][1]
+    def record(r, name):
+        return {"value": round(r["value"], 2), "unit": "GB/s", "us_per_step": round(r["ms"] * 1e3, 2),
+                "pct_of_hbm_peak": round(100 * r["value"] / ws / peak, 2),
+                "pct_of_8tbs": round(100 * r["value"] / ws / 8000, 2), "seed": r["seed"],
+                "kv_bytes_per_step": r["kv_bytes_per_step"], "seq_len_mean": r["seq_len_mean"],
+                "roofline_frac": _roofline(r, name, r["seed"], peak, peak_kind, args.steps)["frac"]}
+
+    def sweep(rs, name):
+        return {"median_of_seeds": [r["seed"] for r in rs],
+                "per_seed": [{"seed": r["seed"], "value": round(r["value"], 2),
+                              "us_per_step": round(r["ms"] * 1e3, 2),
+                              "seq_len_mean": r["seq_len_mean"]} for r in rs]}
+
+    sub = {}
+    for name, rs in sub_runs.items():
+        m = _median_run(rs)
+        sub[name] = {**record(m, name), **sweep(rs, name),
+                     "roofline": _roofline(m, name, m["seed"], peak, peak_kind, args.steps),
+                     "clocks": "the line's clocks (sampled across every device-timed step)"}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step_max, 4), "us_per_step": round(ms_step_max * 1e3, 2),
@@ -420,26 +494,24 @@ def run_ours(args, ws, rank, local):
         "storage": ("bf16 KV pages; new key rounded as fp64 rotation would round it; q.K and P.V on "
                     "tensor cores with bf16 hi+lo operand pairs for q and P (about 16 mantissa bits) "
                     "and fp32 accumulation; fp32 softmax"),
-        "data": "synthetic (seeded; bf16 N(0,1) q/k/v and cache)", "config": _config(wl),
-        "roofline": {"bound": "hbm",
-                     "kernel": "paged_decode_step call per layer: gqa_decode_kernel (step mode, split pieces merged in the kernel)",
-                     "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)",
-                     "bytes_per_launch": layer_bytes, "launch_us_mean": round(dec_avg_s * 1e6, 2),
-                     "timing": f"CUDA events around {args.steps} replays of a graph of the step's {nl} "
-                               "paged_decode_step calls (inter-kernel gaps included)",
-                     "decode_source": h},
+        "data": "synthetic (seeded; bf16 N(0,1) q/k/v and cache)",
+        "config": {**_config(wl), "seed": head["seed"],
+                   "headline": f"median over seeds {seeds[0]}..{seeds[-1]} of the per-seed GB/s; "
+                               "us_per_step, roofline and config are the median seed's"},
+        "seeds": sweep(runs, args.workload),
+        "roofline": _roofline(head, args.workload, head["seed"], peak, peak_kind, args.steps),
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                 "timing": "CUDA events around replays of a CUDA graph of DecodeStep.run_from_host: "
                           "pinned host -> device copies of block tables, lengths, positions and each "
                           "layer's q/k/v, the step through the C ABI, device -> pinned host copy of "
                           "each layer's output; copies on two copy streams, layer-pipelined"},
-        "gpu_launches": step.launches_per_step() * args.steps,
-        "timing": "CUDA events around K replays of a CUDA graph of one whole step",
+        "gpu_launches": head["launches"],
+        "timing": "CUDA events around K replays of a CUDA graph of one whole step, per seed",
         "clocks": clk, "wall_s_timed": round(wall, 3),
     }
+    if sub:
+        line["workloads"] = sub
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, pool)
     if rank == 0:
@@ -519,13 +591,12 @@ def run_prefill(args, ws, rank, local) -> int:
     q_rot = torch.empty(nl, total, hq, 64, device=dev)
     out = torch.empty(nl, total, hq, 64, device=dev)
     wsp = pkv.alloc_prefill_workspace(total, nb, mb, device=dev)
-    rope = pkv.alloc_prefill_rope_table(total, device=dev)
+    rope = pkv.build_rope_table(theta, mb * 16, device=dev)  # once per model, like its weights
 
-    def step():  # the RoPE table once per pass (same positions in every layer), then every layer
-        pkv.paged_prefill_rope_table(cu, st, total, mb, theta, rope)
+    def step():  # every layer's prefill of the prompts
         for layer in range(nl):
             pkv.paged_prefill(kp, q[layer], k[layer], v[layer], q_rot[layer], out[layer], bt[layer],
-                              cu, st, theta, 0.125, wsp, rope_table=rope)
+                              cu, st, rope, 0.125, wsp)
 
     for _ in range(2):
         step()
@@ -571,6 +642,10 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--seeds", type=int, default=5,
+                    help="time the workload at this many seeds (seed, seed+1, ...); the line's value is the median")
+    ap.add_argument("--no-sub", action="store_true",
+                    help="skip the sub-records of the other target workloads")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--pages-per-split", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -69,6 +69,7 @@ extern "C" {
 #define PKV_ERR_PAGE_ID 0x2  /* block-table entry outside [0, num_pages): that page skipped */
 #define PKV_ERR_TIMEOUT 0x4  /* a bounded wait (a copy into shared memory, or another CTA's partial) gave up; results incomplete */
 #define PKV_ERR_SPLITS  0x8  /* a row needed more than max_splits partial results: row skipped */
+#define PKV_ERR_POSITION 0x10 /* a RoPE position outside the RoPE table's rows: token skipped, its rows zeroed */
 
 typedef struct pkv_pool pkv_pool_t;
 
@@ -185,29 +186,40 @@ int paged_gqa_decode(const pkv_pool_t *pool, const float *q_rot, float *out,
                      int batch, int num_q_heads, float scale, int pages_per_split,
                      void *workspace, size_t workspace_bytes, void *stream);
 
-/* Bytes of the RoPE table of a step with `batch` sequences. */
-#define PKV_ROPE_TABLE_BYTES(batch) ((size_t)(batch) * 1024u)
+/* Bytes of a RoPE table of `rows` rows. */
+#define PKV_ROPE_TABLE_BYTES(rows) ((size_t)(rows) * 1024u)
 
 /*
- * RoPE angles of a decode step: for each sequence b and frequency j < 32,
- * cos and sin of positions[b] * rope_theta^(-2j/64) in fp64: the product
- * rounded once to fp64, then its cos and sin correctly rounded to fp64 (the
- * fp64 values nearest to the true ones, evaluated in double-double with a
- * rounding test; every angle of positions below 2^17 at bases 1e4, 5e5 and
- * 1e6 is decided, and elsewhere an undecided value, of probability about
- * 2^-37, is within half an ulp plus 2^-90 relative). ("手写LLM推理引擎…"
- * section 3.2 precomputes such a cos/sin table once instead of per use.)
- * The positions are the same in every layer, so one table serves all the
- * layers of a step. Layout of the PKV_ROPE_TABLE_BYTES(batch) bytes:
- *   float[batch][32][4]  {cos_hi, cos_lo, sin_hi, sin_lo}: cos_hi = cos
- *                        rounded to fp32, cos_lo = (cos - cos_hi) rounded to
- *                        fp32 (so cos_hi + cos_lo is within 2^-48 |cos|), the
- *                        same for sin; then
- *   double[batch][32][2] {cos, sin}.
- *   positions  int32 [batch];  table  out, 16-byte aligned
+ * RoPE cos/sin table: row r holds, for each frequency j < 32, the cos and sin
+ * of the angle positions[r] * rope_theta^(-2j/64): the product rounded once
+ * to fp64, then its cos and sin correctly rounded to fp64 (the fp64 values
+ * nearest to the true ones, evaluated in double-double with a rounding test;
+ * every angle of positions below 2^17 at bases 1e4, 5e5 and 1e6 is decided,
+ * and elsewhere an undecided value, of probability about 2^-37, is within
+ * half an ulp plus 2^-90 relative). Layout of the PKV_ROPE_TABLE_BYTES(rows)
+ * bytes:
+ *   float[rows][32][4]  {cos_hi, cos_lo, sin_hi, sin_lo}: cos_hi = cos
+ *                       rounded to fp32, cos_lo = (cos - cos_hi) rounded to
+ *                       fp32 (so cos_hi + cos_lo is within 2^-48 |cos|), the
+ *                       same for sin; then
+ *   double[rows][32][2] {cos, sin}.
+ *   positions  int32 [rows];  table  out, 16-byte aligned
+ * The evaluation is a chain of about 200 dependent fp64 operations per value,
+ * which on this GPU takes about 13 us whatever the number of rows: the table
+ * is meant to be built once (paged_rope_table_build), not per step.
  */
-int paged_rope_cos_sin(const int32_t *positions, int batch, double rope_theta, void *table,
+int paged_rope_cos_sin(const int32_t *positions, int rows, double rope_theta, void *table,
                        void *stream);
+
+/*
+ * The RoPE table of every position 0 .. num_positions - 1 (row p = position p),
+ * as paged_rope_cos_sin builds it. ("手写LLM推理引擎…" section 3.2 precomputes
+ * the cos/sin of every position up to the context length once, instead of
+ * per use.) paged_decode_step and paged_prefill read the row of each token's
+ * position from it. table: PKV_ROPE_TABLE_BYTES(num_positions) bytes,
+ * 16-byte aligned. num_positions >= 1.
+ */
+int paged_rope_table_build(double rope_theta, int num_positions, void *table, void *stream);
 
 /*
  * The whole decode step of one layer in one call: paged_kv_append_rope
@@ -220,28 +232,32 @@ int paged_rope_cos_sin(const int32_t *positions, int batch, double rope_theta, v
  * rounded to bf16 exactly as fp64 arithmetic on the same fp64 cos/sin rounds
  * it), and each warp rotates the query rows it uses (in fp32).
  *   q            bf16 [batch][num_q_heads][64];  k, v bf16 [batch][num_kv_heads][64]
- *   rope_table   from paged_rope_cos_sin for this step's positions (same batch)
+ *   rope_table   a RoPE table of rope_positions rows, row p for position p
+ *                (paged_rope_table_build), built once for the model's theta
+ *   positions    int32 [batch], RoPE position of each new token; a position
+ *                outside [0, rope_positions) skips the sequence (nothing
+ *                appended, its rows zeroed) and sets PKV_ERR_POSITION
  *   q_rot        fp32 [batch][num_q_heads][64] out, or NULL: the rotated query
- *                (rows of sequences with a bad length are zeroed)
+ *                (rows of sequences with a bad length or position are zeroed)
  *   out          fp32 [batch][num_q_heads][64]
  *   other arguments as for paged_gqa_decode; the workspace is sized by
  *   paged_gqa_decode_workspace_bytes().
  * A sequence whose new-token page id is bad gets no append and no attention
  * over that page (error bit set).
  * Launch order: the kernels are launched with programmatic dependent launch.
- * This call reads seq_lens, block_tables and the pool's existing pages before
- * it waits for the kernel that precedes it in `stream`. That kernel must
- * therefore not write them if it lets its dependents start early
+ * This call reads seq_lens, positions, block_tables and the pool's existing
+ * pages before it waits for the kernel that precedes it in `stream`. That
+ * kernel must therefore not write them if it lets its dependents start early
  * (griddepcontrol.launch_dependents / cudaTriggerProgrammaticLaunchCompletion).
  * A kernel that does not trigger early, a memcpy, or this library's own
  * kernels (which never write another layer's pages) are fine. q, k, v, the
  * RoPE table and all outputs are accessed only after that wait.
  */
 int paged_decode_step(pkv_pool_t *pool, const void *q, const void *k, const void *v,
-                      const void *rope_table, float *q_rot, float *out,
-                      const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
-                      int batch, int num_q_heads, float scale, int pages_per_split,
-                      void *workspace, size_t workspace_bytes, void *stream);
+                      const void *rope_table, int rope_positions, const int32_t *positions,
+                      float *q_rot, float *out, const int32_t *block_tables, int max_blocks,
+                      const int32_t *seq_lens, int batch, int num_q_heads, float scale,
+                      int pages_per_split, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Device bytes of workspace paged_prefill needs for total_tokens chunk tokens
@@ -269,38 +285,27 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks
  *                start_pos[b] + chunk length assigned;  cu_tokens int32 [batch+1]
  *                (cu_tokens[0] = 0, non-decreasing, cu_tokens[batch] = total_tokens);
  *                start_pos int32 [batch] (>= 0)
- *   rope_table   from paged_prefill_rope_table for these chunks, or NULL (then
- *                the call builds it in the workspace)
+ *   rope_table   a RoPE table of rope_positions rows, row p for position p
+ *                (paged_rope_table_build), built once for the model's theta
  *   workspace    device memory of at least paged_prefill_workspace_bytes(),
  *                256-byte aligned, contents irrelevant
- * Launches five kernels on `stream` (four with a rope_table): an expansion of the chunk tokens (each
- * token's sequence and position), the RoPE table of their positions (as
- * paged_rope_cos_sin), the append (every chunk token stored as a decode
- * token would be, with the same certified key rounding), a tile plan, and a
+ * Launches four kernels on `stream`: an expansion of the chunk tokens (each
+ * token's sequence and position), the append (every chunk token stored as a
+ * decode token would be, with the same certified key rounding, the cos and
+ * sin read from the table row of its position), a tile plan, and a
  * flash-attention kernel on the tcgen05 tensor cores, one CTA per (sequence,
  * kv head, tile of up to 128 (token, query head) rows) that streams the
  * sequence's pages once per tile. Tokens of a malformed chunk (cu_tokens
  * decreasing, a negative start, or a position past max_blocks*16) are not
- * stored, their rows are zeroed and PKV_ERR_SEQ_LEN is
- * set.
+ * stored, their rows are zeroed and PKV_ERR_SEQ_LEN is set; tokens at a
+ * position past the table's rows are treated the same way with
+ * PKV_ERR_POSITION.
  */
 int paged_prefill(pkv_pool_t *pool, const void *q, const void *k, const void *v, float *q_rot,
                   float *out, const int32_t *block_tables, int max_blocks,
                   const int32_t *cu_tokens, const int32_t *start_pos, int batch, int total_tokens,
-                  int num_q_heads, double rope_theta, float scale, const void *rope_table,
+                  int num_q_heads, const void *rope_table, int rope_positions, float scale,
                   void *workspace, size_t workspace_bytes, void *stream);
-
-/*
- * The RoPE table of a prefill call's chunk tokens, to be built once and
- * handed to every layer's paged_prefill (the positions are the same in every
- * layer). Token t (rows in cu_tokens order) of sequence b sits at position
- * start_pos[b] + (t - cu_tokens[b]); a token of a malformed chunk gets
- * position 0. Layout: as paged_rope_cos_sin with batch = total_tokens, i.e.
- * PKV_ROPE_TABLE_BYTES(total_tokens) bytes, 16-byte aligned.
- */
-int paged_prefill_rope_table(const int32_t *cu_tokens, const int32_t *start_pos, int batch,
-                             int total_tokens, int max_blocks, double rope_theta, void *table,
-                             void *stream);
 
 /* Bytes of the fixed device array paged_gqa_decode_no_alloc uses as workspace. */
 #define PKV_NO_ALLOC_SCRATCH_BYTES (8u << 20)

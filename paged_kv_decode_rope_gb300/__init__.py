@@ -10,6 +10,7 @@ is the thin Python binding with the same names; it only marshals arguments.
 """
 from ._binding import (  # noqa: F401
     ERR_PAGE_ID,
+    ERR_POSITION,
     ERR_SEQ_LEN,
     ERR_SPLITS,
     ERR_TIMEOUT,
@@ -21,9 +22,9 @@ from ._binding import (  # noqa: F401
     KVPool,
     PkvError,
     alloc_decode_workspace,
-    alloc_prefill_rope_table,
     alloc_prefill_workspace,
     alloc_rope_table,
+    build_rope_table,
     decode_max_splits,
     kv_pool_create,
     kv_pool_destroy,
@@ -39,9 +40,10 @@ from ._binding import (  # noqa: F401
     paged_kv_append_rope,
     paged_kv_split_combine,
     paged_prefill,
-    paged_prefill_rope_table,
     paged_prefill_workspace_bytes,
     paged_rope_cos_sin,
+    paged_rope_table_build,
+    rope_table_rows,
     pkv_get_error,
     pkv_last_cuda_error,
 )

@@ -18,8 +18,8 @@ LIBRARY = os.path.join(_HERE, "libpkv.so")
 HEAD_DIM = 64
 PAGE_SIZE = 16
 MAX_GROUP = 8
-ROPE_TABLE_BYTES_PER_SEQ = 1024  # PKV_ROPE_TABLE_BYTES(1)
-ERR_SEQ_LEN, ERR_PAGE_ID, ERR_TIMEOUT, ERR_SPLITS = 0x1, 0x2, 0x4, 0x8
+ROPE_TABLE_BYTES_PER_ROW = 1024  # PKV_ROPE_TABLE_BYTES(1)
+ERR_SEQ_LEN, ERR_PAGE_ID, ERR_TIMEOUT, ERR_SPLITS, ERR_POSITION = 0x1, 0x2, 0x4, 0x8, 0x10
 
 _lib = None
 _lock = threading.Lock()
@@ -38,13 +38,13 @@ _SIGNATURES = {
     "paged_gqa_decode_partials": (_i, [_vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp, _vp, _vp, _i, _vp]),
     "paged_gqa_decode_no_alloc": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp]),
     "paged_rope_cos_sin": (_i, [_vp, _i, _d, _vp, _vp]),
-    "paged_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp,
-                               _sz, _vp]),
+    "paged_rope_table_build": (_i, [_d, _i, _vp, _vp]),
+    "paged_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f,
+                               _i, _vp, _sz, _vp]),
     "paged_kv_split_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
     "paged_prefill_workspace_bytes": (_sz, [_i, _i, _i]),
-    "paged_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _d, _f, _vp,
+    "paged_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _vp, _i, _f,
                            _vp, _sz, _vp]),
-    "paged_prefill_rope_table": (_i, [_vp, _vp, _i, _i, _i, _d, _vp, _vp]),
     "pkv_get_error": (_i, [_vp, ctypes.POINTER(_i), _i]),
     "pkv_last_cuda_error": (_i, []),
     # include/pkv_sched.h (host only)
@@ -265,34 +265,57 @@ def paged_gqa_decode_no_alloc(pool: KVPool, q_rot: torch.Tensor, out: torch.Tens
     _check("paged_gqa_decode_no_alloc", rc)
 
 
-def alloc_rope_table(batch: int, device=None) -> torch.Tensor:
-    """A buffer for paged_rope_cos_sin's table of ``batch`` sequences."""
-    return torch.empty(batch * ROPE_TABLE_BYTES_PER_SEQ, dtype=torch.uint8,
+def alloc_rope_table(rows: int, device=None) -> torch.Tensor:
+    """A buffer for a RoPE table of ``rows`` rows (PKV_ROPE_TABLE_BYTES)."""
+    return torch.empty(rows * ROPE_TABLE_BYTES_PER_ROW, dtype=torch.uint8,
                        device=device or torch.device("cuda"))
+
+
+def rope_table_rows(table: torch.Tensor) -> int:
+    return table.numel() // ROPE_TABLE_BYTES_PER_ROW
 
 
 def paged_rope_cos_sin(positions: torch.Tensor, rope_theta: float, table: torch.Tensor,
                        stream=None) -> None:
-    """positions [B] int32 -> the step's RoPE table (uint8 [B*1024], from
-    alloc_rope_table): float32 [B,32,4] {cos_hi, cos_lo, sin_hi, sin_lo}, then
-    float64 [B,32,2] {cos, sin}."""
-    (batch,) = _shape(positions, (None,), "positions")
-    if table.numel() < batch * ROPE_TABLE_BYTES_PER_SEQ:
+    """positions [R] int32 -> a RoPE table of R rows (uint8 [R*1024], from
+    alloc_rope_table), row r for positions[r]: float32 [R,32,4] {cos_hi,
+    cos_lo, sin_hi, sin_lo}, then float64 [R,32,2] {cos, sin}."""
+    (rows,) = _shape(positions, (None,), "positions")
+    if table.numel() < rows * ROPE_TABLE_BYTES_PER_ROW:
         raise ValueError("rope table too small")
-    rc = lib().paged_rope_cos_sin(_dev(positions, torch.int32, "positions", 1), batch,
+    rc = lib().paged_rope_cos_sin(_dev(positions, torch.int32, "positions", 1), rows,
                                   float(rope_theta), _dev(table, torch.uint8, "table", 1),
                                   _stream(stream))
     _check("paged_rope_cos_sin", rc)
 
 
+def paged_rope_table_build(rope_theta: float, num_positions: int, table: torch.Tensor,
+                           stream=None) -> None:
+    """The RoPE table of positions 0 .. num_positions-1 (row p = position p)."""
+    if table.numel() < num_positions * ROPE_TABLE_BYTES_PER_ROW:
+        raise ValueError("rope table too small")
+    rc = lib().paged_rope_table_build(float(rope_theta), int(num_positions),
+                                      _dev(table, torch.uint8, "table", 1), _stream(stream))
+    _check("paged_rope_table_build", rc)
+
+
+def build_rope_table(rope_theta: float, num_positions: int, device=None, stream=None) -> torch.Tensor:
+    """Allocate and build the RoPE table of positions 0 .. num_positions-1, once
+    per model (the decode step and the prefill read the row of each position)."""
+    table = alloc_rope_table(num_positions, device=device)
+    paged_rope_table_build(rope_theta, num_positions, table, stream)
+    return table
+
+
 def paged_decode_step(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
-                      rope_table: torch.Tensor, out: torch.Tensor, block_tables: torch.Tensor,
-                      seq_lens: torch.Tensor, scale: float, workspace: torch.Tensor,
-                      q_rot: torch.Tensor | None = None, pages_per_split: int = 0,
-                      stream=None) -> None:
+                      rope_table: torch.Tensor, positions: torch.Tensor, out: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                      workspace: torch.Tensor, q_rot: torch.Tensor | None = None,
+                      pages_per_split: int = 0, stream=None) -> None:
     """One layer's whole step (RoPE + append + decode) in one call.
-    q [B,Hq,64], k/v [B,Hkv,64] bf16; rope_table from paged_rope_cos_sin for
-    these B sequences; out [B,Hq,64] fp32; q_rot optional fp32 out."""
+    q [B,Hq,64], k/v [B,Hkv,64] bf16; rope_table a position table
+    (build_rope_table), positions [B] int32 rows of it; out [B,Hq,64] fp32;
+    q_rot optional fp32 out."""
     batch, hq, _ = _shape(q, (None, None, HEAD_DIM), "q")
     for t, name in ((k, "k"), (v, "v")):
         _shape(t, (batch, pool.num_kv_heads, HEAD_DIM), name)
@@ -301,11 +324,12 @@ def paged_decode_step(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.T
         _shape(q_rot, (batch, hq, HEAD_DIM), "q_rot")
     _shape(block_tables, (batch, None), "block_tables")
     _shape(seq_lens, (batch,), "seq_lens")
-    if rope_table.numel() < batch * ROPE_TABLE_BYTES_PER_SEQ:
-        raise ValueError("rope table too small")
+    _shape(positions, (batch,), "positions")
+    rows = rope_table_rows(rope_table)
     rc = lib().paged_decode_step(
         pool.handle, _dev(q, torch.bfloat16, "q", 3), _dev(k, torch.bfloat16, "k", 3),
-        _dev(v, torch.bfloat16, "v", 3), _dev(rope_table, torch.uint8, "rope_table", 1),
+        _dev(v, torch.bfloat16, "v", 3), _dev(rope_table, torch.uint8, "rope_table", 1), rows,
+        _dev(positions, torch.int32, "positions", 1),
         None if q_rot is None else _dev(q_rot, torch.float32, "q_rot", 3),
         _dev(out, torch.float32, "out", 3), _dev(block_tables, torch.int32, "block_tables", 2),
         block_tables.shape[1], _dev(seq_lens, torch.int32, "seq_lens", 1), batch, hq,
@@ -326,33 +350,13 @@ def alloc_prefill_workspace(total_tokens: int, batch: int, max_blocks: int,
     return torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda"))
 
 
-def alloc_prefill_rope_table(total_tokens: int, device=None) -> torch.Tensor:
-    return torch.empty(max(total_tokens, 1) * ROPE_TABLE_BYTES_PER_SEQ, dtype=torch.uint8,
-                       device=device or torch.device("cuda"))
-
-
-def paged_prefill_rope_table(cu_tokens: torch.Tensor, start_pos: torch.Tensor, total_tokens: int,
-                             max_blocks: int, rope_theta: float, table: torch.Tensor,
-                             stream=None) -> None:
-    """The chunk tokens' RoPE table, built once and handed to every layer's paged_prefill."""
-    (batch,) = _shape(start_pos, (None,), "start_pos")
-    _shape(cu_tokens, (batch + 1,), "cu_tokens")
-    if table.numel() < max(total_tokens, 1) * ROPE_TABLE_BYTES_PER_SEQ:
-        raise ValueError("rope table too small")
-    rc = lib().paged_prefill_rope_table(
-        _dev(cu_tokens, torch.int32, "cu_tokens", 1), _dev(start_pos, torch.int32, "start_pos", 1),
-        batch, total_tokens, max_blocks, float(rope_theta), _dev(table, torch.uint8, "table", 1),
-        _stream(stream))
-    _check("paged_prefill_rope_table", rc)
-
-
 def paged_prefill(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                   q_rot: torch.Tensor, out: torch.Tensor, block_tables: torch.Tensor,
-                  cu_tokens: torch.Tensor, start_pos: torch.Tensor, rope_theta: float, scale: float,
-                  workspace: torch.Tensor, stream=None, rope_table: torch.Tensor | None = None) -> None:
+                  cu_tokens: torch.Tensor, start_pos: torch.Tensor, rope_table: torch.Tensor,
+                  scale: float, workspace: torch.Tensor, stream=None) -> None:
     """Chunked causal prefill. q [T,Hq,64], k/v [T,Hkv,64] bf16; q_rot/out [T,Hq,64]
     fp32 out; block_tables [B,max_blocks], cu_tokens [B+1], start_pos [B] int32;
-    rope_table from paged_prefill_rope_table (built once for all layers) or None."""
+    rope_table a position table (build_rope_table)."""
     total, hq, _ = _shape(q, (None, None, HEAD_DIM), "q")
     for t, name in ((k, "k"), (v, "v")):
         _shape(t, (total, pool.num_kv_heads, HEAD_DIM), name)
@@ -361,15 +365,13 @@ def paged_prefill(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tenso
     batch, _ = _shape(block_tables, (None, None), "block_tables")
     _shape(cu_tokens, (batch + 1,), "cu_tokens")
     _shape(start_pos, (batch,), "start_pos")
-    if rope_table is not None and rope_table.numel() < max(total, 1) * ROPE_TABLE_BYTES_PER_SEQ:
-        raise ValueError("rope table too small")
     rc = lib().paged_prefill(
         pool.handle, _dev(q, torch.bfloat16, "q", 3), _dev(k, torch.bfloat16, "k", 3),
         _dev(v, torch.bfloat16, "v", 3), _dev(q_rot, torch.float32, "q_rot", 3),
         _dev(out, torch.float32, "out", 3), _dev(block_tables, torch.int32, "block_tables", 2),
         block_tables.shape[1], _dev(cu_tokens, torch.int32, "cu_tokens", 1),
-        _dev(start_pos, torch.int32, "start_pos", 1), batch, total, hq, float(rope_theta),
-        float(scale), None if rope_table is None else _dev(rope_table, torch.uint8, "rope_table", 1),
+        _dev(start_pos, torch.int32, "start_pos", 1), batch, total, hq,
+        _dev(rope_table, torch.uint8, "rope_table", 1), rope_table_rows(rope_table), float(scale),
         _dev(workspace, torch.uint8, "workspace", 1), workspace.numel(), _stream(stream))
     _check("paged_prefill", rc)
 

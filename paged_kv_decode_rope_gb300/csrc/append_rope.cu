@@ -122,14 +122,14 @@ __global__ void __launch_bounds__(kAppendThreads) append_rope_kernel(const Appen
   }
 }
 
-// Two threads per (sequence, frequency), one for the cos and one for the sin
-// of pos * inv_freq_j, correctly rounded to fp64 (the values the append
-// kernel forms for its rotation), stored twice: as fp32 pairs {hi, lo} (hi =
-// the fp64 value rounded to fp32, lo = the remainder rounded to fp32, so
-// hi + lo is within 2^-48 of it) for the fused step's fp32 paths, and in fp64
-// for its rare fp64 fallback. One warp of 32 (sequence, frequency, cos|sin)
-// values per 32 threads: fp64 throughput on this part is low, so the values
-// are spread over as many SMs as the batch allows.
+// Two threads per (row, frequency), one for the cos and one for the sin of
+// pos * inv_freq_j (pos = positions[row], or the row itself), correctly
+// rounded to fp64 (the values the append kernel forms for its rotation),
+// stored twice: as fp32 pairs {hi, lo} (hi = the fp64 value rounded to fp32,
+// lo = the remainder rounded to fp32, so hi + lo is within 2^-48 of it) for
+// the fp32 paths of the fused step and the prefill, and in fp64 for their
+// rare fp64 fallback. Small blocks spread the values over as many SMs as the
+// rows allow: each value is a long chain of dependent fp64 operations.
 constexpr int kTableThreads = 64;
 __global__ void __launch_bounds__(kTableThreads)
     rope_cos_sin_kernel(const int32_t* __restrict__ positions, int batch, const InvFreq inv,
@@ -138,8 +138,9 @@ __global__ void __launch_bounds__(kTableThreads)
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;  // 2 (b 32 + j) + (0: cos, 1: sin)
   if (idx >= batch * 2 * kHalf) return;
   const int bj = idx >> 1, b = bj / kHalf, j = bj - b * kHalf;
+  const int pos = positions ? positions[b] : b;
   bool certain;
-  const double val = rope_cos_or_sin_cr(__dmul_rn(static_cast<double>(positions[b]), inv.v[j]),
+  const double val = rope_cos_or_sin_cr(__dmul_rn(static_cast<double>(pos), inv.v[j]),
                                         (idx & 1) != 0, coef, &certain);
   const float hi = __double2float_rn(val);
   pairs[idx] = make_float2(hi, __double2float_rn(__dsub_rn(val, static_cast<double>(hi))));
@@ -165,6 +166,7 @@ RopeSeriesCoef rope_series_coef() {
 cudaError_t launch_rope_cos_sin(const int32_t* positions, int batch, double rope_theta,
                                 void* table, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
+  if (static_cast<long long>(batch) * 2 * kHalf >= (1ll << 31)) return cudaErrorInvalidValue;
   InvFreq inv;
   for (int j = 0; j < kHalf; ++j)
     inv.v[j] = std::pow(rope_theta, -(2.0 * j) / static_cast<double>(kHeadDim));

@@ -132,8 +132,10 @@ struct DecodeParams {
   const uint16_t* q_raw;    // bf16 [batch][hq][64]
   const uint16_t* k_new;    // bf16 [batch][hkv][64]
   const uint16_t* v_new;    // bf16 [batch][hkv][64]
-  const float4* rope_ff;    // [batch][32] {cos_hi, cos_lo, sin_hi, sin_lo} (fp32 pairs)
-  const double2* rope_dd;   // [batch][32] {cos, sin} in fp64
+  const float4* rope_ff;    // [rope_positions][32] {cos_hi, cos_lo, sin_hi, sin_lo} (fp32 pairs)
+  const double2* rope_dd;   // [rope_positions][32] {cos, sin} in fp64
+  const int32_t* positions; // [batch] RoPE position of each new token
+  int rope_positions;
   float* q_rot_out;         // fp32 [batch][hq][64] or null
   uint8_t* pool_w;          // the pool's bytes, for the new token's rows
 };
@@ -480,7 +482,7 @@ __device__ __forceinline__ void rope_query(const DecodeParams& p, uint32_t sS, i
 // cos/sin row, then G raw q rows, then raw k and v.
 template <int G>
 __device__ __forceinline__ void append_new_token(const DecodeParams& p, uint32_t sK, uint32_t sV,
-                                                 uint32_t sS, int b, int y, int row, int lane) {
+                                                 uint32_t sS, int pos, int y, int row, int lane) {
   const int j = lane;
   const float4 cs = lds128f(sS + 16 * j);  // cos_hi, cos_lo, sin_hi, sin_lo
   const uint32_t sKV = sS + kTrigBytes + G * kRowBytes;
@@ -491,7 +493,7 @@ __device__ __forceinline__ void append_new_token(const DecodeParams& p, uint32_t
   const bool fast = rotated_bf16_fast(x0, x1, cs.x, cs.y, cs.z, cs.w, y0) &&
                     rotated_bf16_fast(x1, -x0, cs.x, cs.y, cs.z, cs.w, y1);
   if (!fast) {
-    const double2 cd = p.rope_dd[static_cast<size_t>(b) * kHalfDim + j];
+    const double2 cd = p.rope_dd[static_cast<size_t>(pos) * kHalfDim + j];
     rotate_key_pair(k0, k1, cd.x, cd.y, y0, y1);
   }
   const uint32_t v01 = lds32(sKV + kRowBytes + 4 * j);
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   int* s_warp = reinterpret_cast<int*>(smem + kScanOffset);
   int* s_len = reinterpret_cast<int*>(smem + kHdrBytes);
   int* s_pre = s_len + p.batch;
-  __shared__ int s_bad_len;
+  __shared__ int s_bad;  // PKV_ERR_SEQ_LEN / PKV_ERR_POSITION of sequences skipped here
   const uint32_t bar0 = smem_addr(smem) + warp * C::kStages * 8;
   const uint32_t ring_base = (smem_addr(smem) + p.ring_offset + 1023u) & ~1023u;
   const uint32_t ring0 = ring_base + warp * C::kStages * kHeadPageBytes;
@@ -538,7 +540,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   // tables and the first pages of each warp's range, which the previous
   // kernel must not write (see paged_decode_step); the step's query and new
   // token rows and all of its stores come after the wait.
-  if (tid == 0) s_bad_len = 0;
+  if (tid == 0) s_bad = 0;
   if (lane == 0)
     for (int s = 0; s < C::kStages; ++s) mbar_init(bar0 + 8 * s, 1);
   fence_mbar_init();
@@ -548,9 +550,14 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   const int cap = p.max_blocks * kPage;
   for (int b = tid; b < p.batch; b += kT) {
     int n = p.seq_lens[b];
-    if (n < 1 || n > cap) {
+    int bad = (n < 1 || n > cap) ? PKV_ERR_SEQ_LEN : 0;
+    if (kStep) {
+      const int pos = p.positions[b];
+      if (pos < 0 || pos >= p.rope_positions) bad |= PKV_ERR_POSITION;
+    }
+    if (bad) {
       n = 0;
-      s_bad_len = 1;
+      atomicOr(&s_bad, bad);
     }
     s_len[b] = n;
   }
@@ -610,10 +617,11 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   //        a piece (6) | bad page (7) | last page of the sequence (8) |
   //        page index within the sequence (9+)
   //   bh   sequence * hkv + kv head
+  //   pos  step mode: the sequence's RoPE position (its row of the table)
   // The producer (copy issue) runs at most kStages items ahead of the consumer,
   // hence at most one batch ahead; the consumer keeps its own copy.
-  int pd_base = 0, pd_y = -1, pd_meta = 0, pd_bh = 0;
-  int cd_base = 0, cd_y = -1, cd_meta = 0, cd_bh = 0;
+  int pd_base = 0, pd_y = -1, pd_meta = 0, pd_bh = 0, pd_pos = 0;
+  int cd_base = 0, cd_y = -1, cd_meta = 0, cd_bh = 0, cd_pos = 0;
 
   auto describe = [&](int base, int i0, int i1) {
     pd_base = base;
@@ -625,6 +633,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     if (item < i1) {
       const Cursor ci = locate(item, s_pre, s_len, p.batch, p.hkv);
       const int page = __ldg(p.block_tables + static_cast<size_t>(ci.b) * p.max_blocks + ci.pg);
+      if (kStep) pd_pos = __ldg(p.positions + ci.b);  // checked with the lengths
       const int nv = min(kPage, ci.len - ci.pg * kPage);
       const int first = (item == i0 || ci.pg == 0) ? 1 : 0;
       const int last = (item == i1 - 1 || ci.pg == ci.np - 1) ? 1 : 0;
@@ -647,6 +656,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     const int y = __shfl_sync(kFull, pd_y, t);
     const int meta = __shfl_sync(kFull, pd_meta, t);
     const int bh = __shfl_sync(kFull, pd_bh, t);
+    const int pos = kStep ? __shfl_sync(kFull, pd_pos, t) : 0;
     if (lane == 0) {
       const bool first = (meta >> 5) & 1;
       const uint32_t bar = bar0 + 8 * st;
@@ -676,7 +686,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
           // the sequence's cos/sin row; the group's raw q rows on a piece's
           // first page; the new token's raw k and v rows on the sequence's last
           if (first || seg_last)
-            bulk_g2s(side, p.rope_ff + static_cast<size_t>(bh / p.hkv) * kHalfDim, kTrigBytes, bar);
+            bulk_g2s(side, p.rope_ff + static_cast<size_t>(pos) * kHalfDim, kTrigBytes, bar);
           if (first)
             bulk_g2s(side + kTrigBytes, p.q_raw + static_cast<size_t>(bh) * G * kHeadDim,
                      G * kRowBytes, bar);
@@ -716,8 +726,8 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     grid_dependency_wait();
   }
 
-  if (s_bad_len) {  // rows of invalid sequences: zero output (or zero split count)
-    if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, PKV_ERR_SEQ_LEN);
+  if (s_bad) {  // rows of invalid sequences: zero output (or zero split count)
+    if (blockIdx.x == 0 && tid == 0) atomicOr(p.err, s_bad);
     const int rows = p.batch * p.hq;
     for (int idx = blockIdx.x * kT + tid; idx < rows; idx += gridDim.x * kT) {
       if (s_len[idx / p.hq] != 0) continue;
@@ -794,6 +804,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
     cd_y = pd_y;
     cd_meta = pd_meta;
     cd_bh = pd_bh;
+    cd_pos = pd_pos;
     {
       int st = stage;
       for (int k = 0; k < C::kStages && i0 + k < i1; ++k) {
@@ -816,6 +827,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
         cd_y = pd_y;
         cd_meta = pd_meta;
         cd_bh = pd_bh;
+        cd_pos = pd_pos;
       }
       const int t = i - cd_base;
       const int meta = __shfl_sync(kFull, cd_meta, t);
@@ -860,7 +872,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
         // key, put K and V into the stage (the copy brought the stale slot)
         // and into the pool.
         const int y = __shfl_sync(kFull, cd_y, t);
-        append_new_token<G>(p, sK, sV, sS, __shfl_sync(kFull, cd_bh, t) / p.hkv, y, nv - 1, lane);
+        append_new_token<G>(p, sK, sV, sS, __shfl_sync(kFull, cd_pos, t), y, nv - 1, lane);
         __syncwarp();
       }
       if (!bad) {
@@ -1249,13 +1261,14 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
     p.q_raw = step ? a.q_raw + qrow0 : nullptr;
     p.k_new = step ? a.k_new + krow0 : nullptr;
     p.v_new = step ? a.v_new + krow0 : nullptr;
-    // the fp32 pair table, then the fp64 table (see launch_rope_cos_sin)
-    p.rope_ff = step ? static_cast<const float4*>(a.rope_table) + static_cast<size_t>(b0) * kHalfDim
-                     : nullptr;
+    // the fp32 pair rows, then the fp64 rows (see launch_rope_cos_sin), one
+    // row per position
+    p.rope_ff = step ? static_cast<const float4*>(a.rope_table) : nullptr;
     p.rope_dd = step ? reinterpret_cast<const double2*>(static_cast<const float4*>(a.rope_table) +
-                                                        static_cast<size_t>(a.batch) * kHalfDim) +
-                           static_cast<size_t>(b0) * kHalfDim
+                                                        static_cast<size_t>(a.rope_positions) * kHalfDim)
                      : nullptr;
+    p.positions = step ? a.positions + b0 : nullptr;
+    p.rope_positions = a.rope_positions;
     p.q_rot_out = (step && a.q_rot_out) ? a.q_rot_out + qrow0 : nullptr;
     p.pool_w = const_cast<uint8_t*>(a.pool);
     e = launch_group(group, *a.kv_map, p, grid, stream, mode);

@@ -233,26 +233,38 @@ int paged_gqa_decode(const pkv_pool_t* pool, const float* q_rot, float* out,
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
 
-int paged_rope_cos_sin(const int32_t* positions, int batch, double rope_theta, void* table,
+int paged_rope_cos_sin(const int32_t* positions, int rows, double rope_theta, void* table,
                        void* stream) {
-  if (batch < 0 || !(rope_theta > 0.0) || !std::isfinite(rope_theta)) return -EINVAL;
-  if (batch == 0) return 0;
+  if (rows < 0 || rows >= (1 << 24) || !(rope_theta > 0.0) || !std::isfinite(rope_theta))
+    return -EINVAL;
+  if (rows == 0) return 0;
   if (!positions || !table || !aligned16(table)) return -EINVAL;
-  cudaError_t e = pkv::launch_rope_cos_sin(positions, batch, rope_theta, table,
+  cudaError_t e = pkv::launch_rope_cos_sin(positions, rows, rope_theta, table,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
+int paged_rope_table_build(double rope_theta, int num_positions, void* table, void* stream) {
+  if (num_positions < 1 || num_positions >= (1 << 24) || !(rope_theta > 0.0) ||
+      !std::isfinite(rope_theta))
+    return -EINVAL;
+  if (!table || !aligned16(table)) return -EINVAL;
+  cudaError_t e = pkv::launch_rope_cos_sin(nullptr, num_positions, rope_theta, table,
                                            static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
 
 int paged_decode_step(pkv_pool_t* pool, const void* q, const void* k, const void* v,
-                      const void* rope_table, float* q_rot, float* out, const int32_t* block_tables,
-                      int max_blocks, const int32_t* seq_lens, int batch, int num_q_heads,
-                      float scale, int pages_per_split, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+                      const void* rope_table, int rope_positions, const int32_t* positions,
+                      float* q_rot, float* out, const int32_t* block_tables, int max_blocks,
+                      const int32_t* seq_lens, int batch, int num_q_heads, float scale,
+                      int pages_per_split, void* workspace, size_t workspace_bytes, void* stream) {
   if (!decode_shape_ok(pool, batch, num_q_heads, max_blocks) || pages_per_split < 0 ||
-      !std::isfinite(scale))
+      !std::isfinite(scale) || rope_positions < 1 || rope_positions >= (1 << 24))
     return -EINVAL;
   if (batch == 0) return 0;
-  if (!q || !k || !v || !rope_table || !out || !block_tables || !seq_lens || !workspace)
+  if (!q || !k || !v || !rope_table || !positions || !out || !block_tables || !seq_lens ||
+      !workspace)
     return -EINVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rope_table) || !aligned16(out) ||
       (q_rot && !aligned16(q_rot)) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -280,6 +292,8 @@ int paged_decode_step(pkv_pool_t* pool, const void* q, const void* k, const void
   a.k_new = static_cast<const uint16_t*>(k);
   a.v_new = static_cast<const uint16_t*>(v);
   a.rope_table = rope_table;
+  a.rope_positions = rope_positions;
+  a.positions = positions;
   a.q_rot_out = q_rot;
   a.merge_looks = pool->merge_looks;
   cudaError_t e = pkv::launch_decode(a, static_cast<cudaStream_t>(stream));
@@ -291,32 +305,19 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks
   return pkv::prefill_workspace_bytes(total_tokens, batch, max_blocks);
 }
 
-int paged_prefill_rope_table(const int32_t* cu_tokens, const int32_t* start_pos, int batch,
-                             int total_tokens, int max_blocks, double rope_theta, void* table,
-                             void* stream) {
-  if (batch < 0 || total_tokens < 0 || max_blocks < 1 || !(rope_theta > 0.0) ||
-      !std::isfinite(rope_theta))
-    return -EINVAL;
-  if (total_tokens == 0) return 0;
-  if (batch < 1 || !cu_tokens || !start_pos || !table || !aligned16(table)) return -EINVAL;
-  const cudaError_t e = pkv::launch_prefill_rope_table(cu_tokens, start_pos, batch, total_tokens,
-                                                       max_blocks, rope_theta, table,
-                                                       static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? 0 : cuda_fail(e);
-}
-
 int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v, float* q_rot,
                   float* out, const int32_t* block_tables, int max_blocks,
                   const int32_t* cu_tokens, const int32_t* start_pos, int batch, int total_tokens,
-                  int num_q_heads, double rope_theta, float scale, const void* rope_table,
+                  int num_q_heads, const void* rope_table, int rope_positions, float scale,
                   void* workspace, size_t workspace_bytes, void* stream) {
   if (!decode_shape_ok(pool, total_tokens, num_q_heads, max_blocks) || batch < 0 ||
-      total_tokens < 0 || !(rope_theta > 0.0) || !std::isfinite(rope_theta) ||
-      !std::isfinite(scale))
+      total_tokens < 0 || !std::isfinite(scale) || rope_positions < 1 ||
+      rope_positions >= (1 << 24))
     return -EINVAL;
   if (total_tokens == 0) return 0;
   if (batch < 1) return -EINVAL;
-  if (!q || !k || !v || !q_rot || !out || !block_tables || !cu_tokens || !start_pos || !workspace)
+  if (!q || !k || !v || !q_rot || !out || !block_tables || !cu_tokens || !start_pos ||
+      !rope_table || !workspace)
     return -EINVAL;
   if (!aligned16(q_rot) || !aligned16(out) || !aligned16(v) || !aligned16(rope_table) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -345,9 +346,9 @@ int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v,
   a.batch = batch;
   a.total_tokens = total_tokens;
   a.num_q_heads = num_q_heads;
-  a.rope_theta = rope_theta;
   a.scale = scale;
   a.rope_table = rope_table;
+  a.rope_positions = rope_positions;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.sm_count = sms;

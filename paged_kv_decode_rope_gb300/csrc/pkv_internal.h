@@ -81,7 +81,9 @@ struct DecodeLaunch {
   const uint16_t* q_raw;
   const uint16_t* k_new;
   const uint16_t* v_new;
-  const void* rope_table;  // from launch_rope_cos_sin for this batch
+  const void* rope_table;   // RoPE table of rope_positions rows, row p = position p
+  int rope_positions;
+  const int32_t* positions;  // [batch] RoPE position of each new token
   float* q_rot_out;
 };
 
@@ -105,9 +107,9 @@ struct PrefillLaunch {
   int batch;
   int total_tokens;
   int num_q_heads;
-  double rope_theta;
   float scale;
-  const void* rope_table;  // the chunk tokens' RoPE table, or null: built in the workspace
+  const void* rope_table;  // RoPE table of rope_positions rows, row p = position p
+  int rope_positions;
   void* workspace;
   size_t workspace_bytes;
   int sm_count;
@@ -115,9 +117,6 @@ struct PrefillLaunch {
 };
 
 size_t prefill_workspace_bytes(int total_tokens, int batch, int max_blocks);
-cudaError_t launch_prefill_rope_table(const int32_t* cu_tokens, const int32_t* start_pos, int batch,
-                                      int total_tokens, int max_blocks, double rope_theta, void* table,
-                                      cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream);
 
 // Largest batch one decode launch serves (sequence lengths and page prefix sums
@@ -128,10 +127,12 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int 
                               int pages_per_split, int sm_count);
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream);
 
-// cos and sin of pos * theta^(-2j/64), j < 32, for every sequence, in fp64,
-// and split into fp32 pairs: table = float4 [batch][32] {cos_hi, cos_lo,
-// sin_hi, sin_lo}, then double2 [batch][32] {cos, sin} (PKV_ROPE_TABLE_BYTES).
-cudaError_t launch_rope_cos_sin(const int32_t* positions, int batch, double rope_theta,
+// cos and sin of pos * theta^(-2j/64), j < 32, for every row, correctly
+// rounded to fp64, and split into fp32 pairs: table = float4 [rows][32]
+// {cos_hi, cos_lo, sin_hi, sin_lo}, then double2 [rows][32] {cos, sin}
+// (PKV_ROPE_TABLE_BYTES). Row r is position positions[r], or r when
+// positions is null.
+cudaError_t launch_rope_cos_sin(const int32_t* positions, int rows, double rope_theta,
                                 void* table, cudaStream_t stream);
 
 cudaError_t launch_split_combine(const float* o_part, const float* lse_part,

@@ -7,12 +7,12 @@
 // and appended like a decode token, and the queries of chunk token t attend
 // causally over the sequence's first start_pos[b] + t + 1 tokens.
 //
-// Five launches (four when the caller hands in the chunk tokens' RoPE
-// table). (1) An expansion kernel gives every chunk token its sequence and
-// position. (2) The RoPE table of those positions, unless given. (3) The
-// append kernel rotates and stores every chunk token exactly as a decode
-// token would be stored, and writes the rotated queries. (4) A one-CTA plan
-// lists the query tiles. (5) Flash attention on the fifth-generation tensor
+// Four launches. (1) An expansion kernel gives every chunk token its sequence
+// and position. (2) The append kernel rotates and stores every chunk token
+// exactly as a decode token would be stored (cos and sin from the row of its
+// position in the caller's RoPE table, built once for all positions), and
+// writes the rotated queries. (3) A one-CTA plan lists the query tiles.
+// (4) Flash attention on the fifth-generation tensor
 // cores: one CTA per (tile of up to 128 (token, query head) rows, kv head)
 // streams the sequence's pages up to the tile's last position, four pages
 // per step, through a TMA ring; tcgen05 MMAs with fp32 accumulators in tensor
@@ -24,7 +24,6 @@
 #include "pkv_device.cuh"
 #include "tc05.cuh"
 #include "pkv_internal.h"
-#include "rope_cr.cuh"
 
 namespace pkv {
 namespace {
@@ -32,10 +31,17 @@ namespace {
 constexpr int kExpandThreads = 256;
 constexpr int kHalfDim = kHeadDim / 2;
 
-// The position of chunk token idx (its sequence found by bisection over
-// cu_tokens), or -1 for a token of a malformed chunk.
-__device__ __forceinline__ long long chunk_position(const int32_t* cu_tokens, const int32_t* start_pos,
-                                                    int batch, int max_blocks, int idx, int* seq) {
+// One thread per chunk token: find its sequence by bisection over cu_tokens
+// and write it and its position; a token of a malformed chunk (a decreasing
+// cu_tokens, a negative start, or a position past max_blocks*16) gets
+// sequence -PKV_ERR_SEQ_LEN, one at a position past the RoPE table's rows
+// -PKV_ERR_POSITION, and position 0.
+__global__ void prefill_expand_kernel(int max_blocks, int rope_positions,
+                                      const int32_t* __restrict__ cu_tokens,
+                                      const int32_t* __restrict__ start_pos, int batch, int total,
+                                      int32_t* __restrict__ tok_seq, int32_t* __restrict__ tok_pos) {
+  const int idx = blockIdx.x * kExpandThreads + threadIdx.x;
+  if (idx >= total) return;
   int lo = 0, hi = batch - 1;  // largest b with cu_tokens[b] <= idx
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -43,59 +49,22 @@ __device__ __forceinline__ long long chunk_position(const int32_t* cu_tokens, co
   }
   const int c0 = cu_tokens[lo], c1 = cu_tokens[lo + 1];
   const long long pos = static_cast<long long>(start_pos[lo]) + (idx - c0);
-  *seq = lo;
-  const bool ok = c0 <= idx && idx < c1 && start_pos[lo] >= 0 &&
-                  pos + 1 <= static_cast<long long>(max_blocks) * kPage;
-  return ok ? pos : -1;
-}
-
-// One thread per chunk token: find its sequence by bisection over cu_tokens
-// and write it (-1 when the sequence's chunk is malformed: a decreasing
-// cu_tokens, a negative start, or a position past max_blocks*16) and its
-// position (0 when malformed).
-__global__ void prefill_expand_kernel(int max_blocks, const int32_t* __restrict__ cu_tokens,
-                                      const int32_t* __restrict__ start_pos, int batch, int total,
-                                      int32_t* __restrict__ tok_seq, int32_t* __restrict__ tok_pos) {
-  const int idx = blockIdx.x * kExpandThreads + threadIdx.x;
-  if (idx >= total) return;
-  int b;
-  const long long pos = chunk_position(cu_tokens, start_pos, batch, max_blocks, idx, &b);
-  tok_seq[idx] = pos >= 0 ? b : -1;
-  tok_pos[idx] = pos >= 0 ? static_cast<int32_t>(pos) : 0;
-}
-
-struct PrefillInvFreq {
-  double v[kHalfDim];  // theta^(-2j/64), from the C library's pow on the host
-};
-
-// Two threads per (chunk token, frequency), one for the cos and one for the
-// sin of its position times inv_freq_j, correctly rounded to fp64 (position 0
-// for a token of a malformed chunk), stored as fp32 pairs {hi, lo} and in
-// fp64: the layout of paged_rope_cos_sin's table.
-constexpr int kRopeThreads = 64;
-__global__ void __launch_bounds__(kRopeThreads)
-    prefill_rope_kernel(const int32_t* __restrict__ cu_tokens,
-                        const int32_t* __restrict__ start_pos, int batch, int total,
-                        int max_blocks, const PrefillInvFreq inv, const RopeSeriesCoef coef,
-                        float2* __restrict__ pairs, double* __restrict__ full) {
-  const int idx = blockIdx.x * blockDim.x + threadIdx.x;  // 2 (token 32 + j) + (0: cos, 1: sin)
-  if (idx >= total * 2 * kHalfDim) return;
-  const int tj = idx >> 1, tkn = tj / kHalfDim, j = tj - tkn * kHalfDim;
-  int seq;
-  const long long pos = chunk_position(cu_tokens, start_pos, batch, max_blocks, tkn, &seq);
-  const double angle = __dmul_rn(static_cast<double>(pos < 0 ? 0 : pos), inv.v[j]);
-  bool certain;
-  const double val = rope_cos_or_sin_cr(angle, (idx & 1) != 0, coef, &certain);
-  const float hi = __double2float_rn(val);
-  pairs[idx] = make_float2(hi, __double2float_rn(__dsub_rn(val, static_cast<double>(hi))));
-  full[idx] = val;
+  int why = 0;
+  if (!(c0 <= idx && idx < c1 && start_pos[lo] >= 0 &&
+        pos + 1 <= static_cast<long long>(max_blocks) * kPage))
+    why = PKV_ERR_SEQ_LEN;
+  else if (pos >= rope_positions)
+    why = PKV_ERR_POSITION;
+  tok_seq[idx] = why ? -why : lo;
+  tok_pos[idx] = why ? 0 : static_cast<int32_t>(pos);
 }
 
 // One CTA per chunk token: its rotated query (fp32, from the fp32 cos/sin of
-// the rope table), its key rotated and rounded to bf16 exactly as fp64
-// arithmetic rounds it (the certified fp32 double-word path, fp64 from the
-// table where it cannot certify: the bytes the decode append stores), and
-// its value, both stored at its position in its sequence's pages.
+// the RoPE table row of its position), its key rotated and rounded to bf16
+// exactly as fp64 arithmetic rounds it (the certified fp32 double-word path,
+// fp64 from the table where it cannot certify: the bytes the decode append
+// stores), and its value, both stored at its position in its sequence's
+// pages. A token of a malformed chunk (position 0) still gets a rotated query.
 constexpr int kAppendThreads = 128;
 __global__ void __launch_bounds__(kAppendThreads)
     prefill_append_kernel(uint16_t* __restrict__ pool, long long num_pages, int hkv, int hq,
@@ -107,7 +76,8 @@ __global__ void __launch_bounds__(kAppendThreads)
                           int* __restrict__ err) {
   __shared__ float4 cs[kHalfDim];
   const int tkn = blockIdx.x, tid = threadIdx.x;
-  if (tid < kHalfDim) cs[tid] = rope_ff[static_cast<size_t>(tkn) * kHalfDim + tid];
+  const int row = tok_pos[tkn];  // the table row: the token's position
+  if (tid < kHalfDim) cs[tid] = rope_ff[static_cast<size_t>(row) * kHalfDim + tid];
   __syncthreads();
   const uint16_t* qb = q + static_cast<size_t>(tkn) * hq * kHeadDim;
   float* qo = q_rot + static_cast<size_t>(tkn) * hq * kHeadDim;
@@ -119,8 +89,8 @@ __global__ void __launch_bounds__(kAppendThreads)
     qo[head * kHeadDim + j + kHalfDim] = x1 * cs[j].x + x0 * cs[j].z;
   }
   const int b = tok_seq[tkn];
-  if (b < 0) {
-    if (tid == 0) atomicOr(err, PKV_ERR_SEQ_LEN);
+  if (b < 0) {  // a malformed chunk, or a position past the RoPE table
+    if (tid == 0) atomicOr(err, -b);
     return;
   }
   const int pos = tok_pos[tkn];
@@ -141,7 +111,7 @@ __global__ void __launch_bounds__(kAppendThreads)
     uint16_t y0, y1;
     if (!(rotated_bf16_fast(x0, x1, c.x, c.y, c.z, c.w, y0) &&
           rotated_bf16_fast(x1, -x0, c.x, c.y, c.z, c.w, y1))) {
-      const double2 cd = rope_dd[static_cast<size_t>(tkn) * kHalfDim + j];
+      const double2 cd = rope_dd[static_cast<size_t>(row) * kHalfDim + j];
       rotate_key_pair(k0, k1, cd.x, cd.y, y0, y1);
     }
     uint16_t* krow = page_base + (hh * 2 + 0) * (kHalfBytes / 2) + slot * kHeadDim;
@@ -195,6 +165,7 @@ struct PrefillAttnParams {
   float* out;           // [T][hq][64]
   const int32_t* block_tables;
   int max_blocks;
+  long long pos_cap;    // positions at or past this (the block table's or the RoPE table's end) are skipped
   const int4* tiles;
   const int* num_tiles;
   int hkv;
@@ -261,7 +232,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   if (static_cast<int>(blockIdx.x) >= *p.num_tiles) return;
   const int4 tile = p.tiles[blockIdx.x];
   const int b = tile.x, row0 = tile.y, n_tok = tile.z, pos0 = tile.w, h = blockIdx.y;
-  const long long room = static_cast<long long>(p.max_blocks) * kPage - pos0;
+  const long long room = p.pos_cap - pos0;
   const int n_ok = pos0 < 0 ? 0 : static_cast<int>(min(static_cast<long long>(n_tok), max(room, 0ll)));
   for (int e = n_ok * G * kHeadDim + tid; e < n_tok * G * kHeadDim; e += C::kThreads) {
     const int t = e / (G * kHeadDim), rest = e - t * (G * kHeadDim);
@@ -585,10 +556,10 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
 
 size_t align256(size_t n) { return (n + 255) / 256 * 256; }
 
-// Workspace: each chunk token's sequence and position, the rope table of the
-// chunk tokens (fp32 pairs, then fp64), then the tile list and its count.
+// Workspace: each chunk token's sequence and position, then the tile list
+// and its count.
 struct PrefillLayout {
-  size_t seq, pos, rope, tiles, count, total;
+  size_t seq, pos, tiles, count, total;
 };
 
 // An upper bound on the tiles of any split of total_tokens over the batch
@@ -602,8 +573,7 @@ PrefillLayout layout(int total_tokens, int batch, int max_blocks) {
   PrefillLayout l;
   l.seq = 0;
   l.pos = l.seq + align256(sizeof(int32_t) * static_cast<size_t>(total_tokens));
-  l.rope = l.pos + align256(sizeof(int32_t) * static_cast<size_t>(total_tokens));
-  l.tiles = l.rope + align256(static_cast<size_t>(total_tokens) * kHalfDim * (sizeof(float4) + sizeof(double2)));
+  l.tiles = l.pos + align256(sizeof(int32_t) * static_cast<size_t>(total_tokens));
   l.count = l.tiles + align256(sizeof(int4) * max_tiles(total_tokens, batch));
   l.total = l.count + 256;
   return l;
@@ -626,6 +596,9 @@ cudaError_t launch_attn(const PrefillLaunch& a, const PrefillLayout& l, cudaStre
   p.out = a.out;
   p.block_tables = a.block_tables;
   p.max_blocks = a.max_blocks;
+  p.pos_cap = static_cast<long long>(a.max_blocks) * kPage < a.rope_positions
+                  ? static_cast<long long>(a.max_blocks) * kPage
+                  : static_cast<long long>(a.rope_positions);
   p.tiles = tiles;
   p.num_tiles = count;
   p.hkv = a.num_kv_heads;
@@ -647,21 +620,6 @@ cudaError_t launch_attn(const PrefillLaunch& a, const PrefillLayout& l, cudaStre
 
 }  // namespace
 
-cudaError_t launch_prefill_rope_table(const int32_t* cu_tokens, const int32_t* start_pos, int batch,
-                                      int total_tokens, int max_blocks, double rope_theta, void* table,
-                                      cudaStream_t stream) {
-  if (total_tokens == 0) return cudaSuccess;
-  PrefillInvFreq inv;
-  for (int j = 0; j < kHalfDim; ++j)
-    inv.v[j] = std::pow(rope_theta, -(2.0 * j) / static_cast<double>(kHeadDim));
-  const int n = total_tokens * 2 * kHalfDim;
-  float2* pairs = static_cast<float2*>(table);
-  double* full = reinterpret_cast<double*>(pairs + n);
-  prefill_rope_kernel<<<(n + kRopeThreads - 1) / kRopeThreads, kRopeThreads, 0, stream>>>(
-      cu_tokens, start_pos, batch, total_tokens, max_blocks, inv, rope_series_coef(), pairs, full);
-  return cudaGetLastError();
-}
-
 size_t prefill_workspace_bytes(int total_tokens, int batch, int max_blocks) {
   return layout(total_tokens, batch, max_blocks).total;
 }
@@ -672,23 +630,15 @@ cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream) {
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   int32_t* tok_seq = reinterpret_cast<int32_t*>(ws + l.seq);
   int32_t* tok_pos = reinterpret_cast<int32_t*>(ws + l.pos);
-  void* rope = ws + l.rope;
   prefill_expand_kernel<<<(a.total_tokens + kExpandThreads - 1) / kExpandThreads, kExpandThreads, 0,
-                          stream>>>(a.max_blocks, a.cu_tokens, a.start_pos, a.batch, a.total_tokens,
-                                    tok_seq, tok_pos);
+                          stream>>>(a.max_blocks, a.rope_positions, a.cu_tokens, a.start_pos,
+                                    a.batch, a.total_tokens, tok_seq, tok_pos);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // cos/sin of every chunk token's position (fp32 pairs, then fp64): the
-  // caller's table (built once for all layers), else one in the workspace
-  if (a.rope_table) {
-    rope = const_cast<void*>(a.rope_table);
-  } else {
-    e = launch_rope_cos_sin(tok_pos, a.total_tokens, a.rope_theta, rope, stream);
-    if (e != cudaSuccess) return e;
-  }
-  const float4* rope_ff = static_cast<const float4*>(rope);
+  // the caller's RoPE table: fp32 pair rows, then fp64 rows, one per position
+  const float4* rope_ff = static_cast<const float4*>(a.rope_table);
   const double2* rope_dd =
-      reinterpret_cast<const double2*>(rope_ff + static_cast<size_t>(a.total_tokens) * kHalfDim);
+      reinterpret_cast<const double2*>(rope_ff + static_cast<size_t>(a.rope_positions) * kHalfDim);
   prefill_append_kernel<<<a.total_tokens, kAppendThreads, 0, stream>>>(
       const_cast<uint16_t*>(reinterpret_cast<const uint16_t*>(a.pool)), a.num_pages, a.num_kv_heads,
       a.num_q_heads, a.q, a.k, a.v, a.q_rot, a.block_tables, a.max_blocks, tok_seq, tok_pos, rope_ff,

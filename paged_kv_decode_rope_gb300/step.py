@@ -28,7 +28,8 @@ class DecodeStep:
     def __init__(self, pool_storage: torch.Tensor, *, num_kv_heads: int, num_q_heads: int,
                  num_layers: int, block_tables: torch.Tensor, seq_lens: torch.Tensor,
                  positions: torch.Tensor, rope_theta: float, scale: float,
-                 pages_per_split: int = 0, fused_q_rot: bool = True):
+                 pages_per_split: int = 0, fused_q_rot: bool = True,
+                 rope_positions: int | None = None):
         dev = pool_storage.device
         self.num_layers = num_layers
         self.batch = int(seq_lens.shape[0])
@@ -50,16 +51,19 @@ class DecodeStep:
         self.out = torch.empty_like(self.q_rot)
         self.workspace = B.alloc_decode_workspace(self.batch, num_q_heads, num_kv_heads,
                                                   self.max_blocks, pages_per_split, device=dev)
-        self.rope_cos_sin = B.alloc_rope_table(self.batch, device=dev)
+        # cos/sin of every position a token of these block tables can have,
+        # built once (the fused step reads the row of each new token's position)
+        self.rope_positions = rope_positions or self.max_blocks * B.PAGE_SIZE
+        self.rope = B.build_rope_table(self.rope_theta, self.rope_positions, device=dev)
 
     def launches_per_step(self, fused: bool = True) -> int:
         """Kernels one step launches: per layer one decode per batch chunk of
-        2048, plus per layer the append kernel when not fused, or once per step
-        the cos/sin table when fused."""
+        2048, plus the append kernel when not fused (the cos/sin table was
+        built once, at construction)."""
         if not self.batch:
             return 0
         chunks = -(-self.batch // 2048)
-        return self.num_layers * (chunks + (0 if fused else 1)) + (1 if fused else 0)
+        return self.num_layers * (chunks + (0 if fused else 1))
 
     def append(self, layer: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
         B.paged_kv_append_rope(self.pool, q[layer], k[layer], v[layer], self.q_rot[layer],
@@ -70,14 +74,11 @@ class DecodeStep:
         B.paged_gqa_decode(self.pool, self.q_rot[layer], self.out[layer], self.block_tables[layer],
                            self.seq_lens, self.scale, self.workspace, self.pages_per_split, stream)
 
-    def rope_table(self, stream=None) -> None:
-        """The step's cos/sin table (same positions in every layer)."""
-        B.paged_rope_cos_sin(self.positions, self.rope_theta, self.rope_cos_sin, stream)
-
     def fused_layer(self, layer: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
                     stream=None) -> None:
-        B.paged_decode_step(self.pool, q[layer], k[layer], v[layer], self.rope_cos_sin, self.out[layer],
-                            self.block_tables[layer], self.seq_lens, self.scale, self.workspace,
+        B.paged_decode_step(self.pool, q[layer], k[layer], v[layer], self.rope, self.positions,
+                            self.out[layer], self.block_tables[layer], self.seq_lens, self.scale,
+                            self.workspace,
                             q_rot=self.q_rot[layer] if self.fused_q_rot else None,
                             pages_per_split=self.pages_per_split,
                             stream=stream)
@@ -85,8 +86,6 @@ class DecodeStep:
     def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None,
             fused: bool = True) -> torch.Tensor:
         """q [NL,B,Hq,64], k/v [NL,B,Hkv,64] bf16 on the device -> out [NL,B,Hq,64] fp32."""
-        if fused:
-            self.rope_table(stream)
         for layer in range(self.num_layers):
             if fused:
                 self.fused_layer(layer, q, k, v, stream)
@@ -137,8 +136,6 @@ class DecodeStep:
             for lo, ev in ready:
                 if lo == layer:
                     cur.wait_event(ev)
-            if layer == 0:
-                self.rope_table()
             self.fused_layer(layer, dev_in["q"], dev_in["k"], dev_in["v"])
             ev_done[layer].record(cur)
         with torch.cuda.stream(cs_out):

@@ -79,7 +79,9 @@ class DecodeTrace:
         page_elems = 2 * num_kv_heads * B.PAGE_SIZE * B.HEAD_DIM
         self.pool = torch.zeros(num_pages * page_elems, dtype=torch.bfloat16, device=self.device)
         self.kvpool = B.kv_pool_create(self.pool, num_kv_heads)
-        self.rope = B.alloc_rope_table(max_batch, device=self.device)
+        # cos/sin of every position up to the context length, built once
+        self.rope = B.build_rope_table(self.rope_theta, self.max_blocks * B.PAGE_SIZE,
+                                       device=self.device)
         self.ws = B.alloc_decode_workspace(max_batch, num_q_heads, num_kv_heads, self.max_blocks,
                                            device=self.device)
         self.ids = {}        # request index -> scheduler id
@@ -136,14 +138,11 @@ class DecodeTrace:
                             device=dev)
         out = torch.empty_like(q_rot)
         ws = B.alloc_prefill_workspace(total, nb, self.max_blocks, device=dev)
-        table = B.alloc_prefill_rope_table(total, device=dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        B.paged_prefill_rope_table(d_cu, d_start, total, self.max_blocks, self.rope_theta, table)
         for layer in range(self.num_layers):
             B.paged_prefill(self.kvpool, q[layer], k[layer], v[layer], q_rot[layer], out[layer],
-                            d_bt[layer], d_cu, d_start, self.rope_theta, self.scale, ws,
-                            rope_table=table)
+                            d_bt[layer], d_cu, d_start, self.rope, self.scale, ws)
         e1.record()
         torch.cuda.synchronize()
         self.prefill_ms += e0.elapsed_time(e1)
@@ -227,10 +226,9 @@ class DecodeTrace:
         out = torch.empty(self.num_layers, nb, self.hq, B.HEAD_DIM, dtype=torch.float32, device=dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        B.paged_rope_cos_sin(d_pos, self.rope_theta, self.rope)
         for layer in range(self.num_layers):
-            B.paged_decode_step(self.kvpool, dq[layer], dk[layer], dv[layer], self.rope, out[layer],
-                                d_bt[layer], d_sl, self.scale, self.ws)
+            B.paged_decode_step(self.kvpool, dq[layer], dk[layer], dv[layer], self.rope, d_pos,
+                                out[layer], d_bt[layer], d_sl, self.scale, self.ws)
         e1.record()
         torch.cuda.synchronize()
         self.device_ms += e0.elapsed_time(e1)

@@ -24,7 +24,7 @@ class DeviceWorkload:
     """A workload's tensors on the GPU, plus the step object running it."""
 
     def __init__(self, wl: workloads.Workload, pages_per_split: int = 0, device="cuda",
-                 fused_q_rot: bool = True):
+                 fused_q_rot: bool = True, rope_positions: int | None = None):
         from paged_kv_decode_rope_gb300 import DecodeStep
         self.wl = wl
         self.pool = wl.pool.to(device, copy=True).contiguous()  # wl.pool stays the "before" state
@@ -36,7 +36,8 @@ class DeviceWorkload:
                                num_layers=wl.num_layers, block_tables=self.block_tables,
                                seq_lens=self.seq_lens, positions=self.positions,
                                rope_theta=wl.rope_theta, scale=wl.scale,
-                               pages_per_split=pages_per_split, fused_q_rot=fused_q_rot)
+                               pages_per_split=pages_per_split, fused_q_rot=fused_q_rot,
+                               rope_positions=rope_positions)
 
     def run(self, fused: bool = True):
         out = self.step.run(self.q, self.k, self.v, fused=fused)

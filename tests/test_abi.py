@@ -138,12 +138,12 @@ def test_binding_rejects_mismatched_shapes_before_the_library():
             append(**{name: t})
 
     def step(**kw):
-        a = dict(q=q, k=k, v=v, out=out, block_tables=bt, seq_lens=sl)
+        a = dict(q=q, k=k, v=v, out=out, block_tables=bt, seq_lens=sl, positions=pos)
         a.update(kw)
-        B.paged_decode_step(pool, a["q"], a["k"], a["v"], table, a["out"], a["block_tables"],
-                            a["seq_lens"], 0.125, ws)
+        B.paged_decode_step(pool, a["q"], a["k"], a["v"], table, a["positions"], a["out"],
+                            a["block_tables"], a["seq_lens"], 0.125, ws)
 
-    for name in ("k", "v", "q", "block_tables", "seq_lens"):
+    for name in ("k", "v", "q", "block_tables", "seq_lens", "positions"):
         with pytest.raises(ValueError, match=f"{name} must have shape"):
             step(**{name: bad[name]})
     with pytest.raises(ValueError, match="out must have shape"):
@@ -159,20 +159,14 @@ def test_binding_rejects_mismatched_shapes_before_the_library():
     pqr, pout = torch.zeros(10, 32, 64, dtype=f32), torch.zeros(10, 32, 64, dtype=f32)
     pbt, cu, st = torch.zeros(2, 16, dtype=i32), torch.tensor([0, 4, 10], dtype=i32), torch.zeros(2, dtype=i32)
     with pytest.raises(ValueError, match="cu_tokens must have shape"):
-        B.paged_prefill(pool, pq, pk, pk, pqr, pout, pbt, cu[:2], st, 1e4, 0.125, ws)
+        B.paged_prefill(pool, pq, pk, pk, pqr, pout, pbt, cu[:2], st, table, 0.125, ws)
     with pytest.raises(ValueError, match="k must have shape"):
-        B.paged_prefill(pool, pq, pk[:9], pk, pqr, pout, pbt, cu, st, 1e4, 0.125, ws)
-    with pytest.raises(ValueError, match="rope table too small"):
-        B.paged_prefill(pool, pq, pk, pk, pqr, pout, pbt, cu, st, 1e4, 0.125, ws,
-                        rope_table=torch.zeros(1024, dtype=torch.uint8))
+        B.paged_prefill(pool, pq, pk[:9], pk, pqr, pout, pbt, cu, st, table, 0.125, ws)
     with pytest.raises(ValueError, match="start_pos must have shape"):
-        B.paged_prefill_rope_table(cu, torch.zeros(2, 1, dtype=i32), 10, 16, 1e4,
-                                   torch.zeros(10 * 1024, dtype=torch.uint8))
-    with pytest.raises(ValueError, match="cu_tokens must have shape"):
-        B.paged_prefill_rope_table(cu, torch.zeros(3, dtype=i32), 10, 16, 1e4,
-                                   torch.zeros(10 * 1024, dtype=torch.uint8))
+        B.paged_prefill(pool, pq, pk, pk, pqr, pout, pbt, cu, torch.zeros(2, 1, dtype=i32), table,
+                        0.125, ws)
     with pytest.raises(ValueError, match="rope table too small"):
-        B.paged_prefill_rope_table(cu, st, 10, 16, 1e4, torch.zeros(9 * 1024, dtype=torch.uint8))
+        B.paged_rope_table_build(1e4, 10, torch.zeros(9 * 1024, dtype=torch.uint8))
     # split results and their merge
     rows = 4 * 32
     with pytest.raises(ValueError, match="o_part must have shape"):
@@ -200,7 +194,8 @@ def test_binding_constants_match_the_header():
     assert B.HEAD_DIM == macro("PKV_HEAD_DIM")
     assert B.PAGE_SIZE == macro("PKV_PAGE_SIZE")
     assert B.MAX_GROUP == macro("PKV_MAX_GROUP")
-    assert (B.ERR_SEQ_LEN, B.ERR_PAGE_ID, B.ERR_TIMEOUT, B.ERR_SPLITS) == tuple(
-        macro(f"PKV_ERR_{n}") for n in ("SEQ_LEN", "PAGE_ID", "TIMEOUT", "SPLITS"))
-    m = re.search(r"#define PKV_ROPE_TABLE_BYTES\(batch\) \(\(size_t\)\(batch\) \* (\d+)u\)", text)
-    assert m and int(m.group(1)) == B.ROPE_TABLE_BYTES_PER_SEQ
+    assert (B.ERR_SEQ_LEN, B.ERR_PAGE_ID, B.ERR_TIMEOUT, B.ERR_SPLITS, B.ERR_POSITION) == tuple(
+        macro(f"PKV_ERR_{n}") for n in ("SEQ_LEN", "PAGE_ID", "TIMEOUT", "SPLITS", "POSITION"))
+    m = re.search(r"#define PKV_ROPE_TABLE_BYTES\(rows\) \(\(size_t\)\(rows\) \* (\d+)u\)", text)
+    assert m and int(m.group(1)) == B.ROPE_TABLE_BYTES_PER_ROW
+    assert B.DEFAULT_MERGE_WAIT_LOOKS == 1 << 20

@@ -150,3 +150,23 @@ def test_merge_wait_timeout_is_reported_and_recoverable():
     assert_close(out.cpu().numpy(), want, "after the workspace was zeroed again")
     assert not bool(st.workspace.any()), "a completed call leaves the workspace zero"
     st.close()
+
+
+def test_position_past_the_rope_table_is_flagged_and_zeroed():
+    """The fused step reads each new token's cos/sin from the row of its
+    position in the RoPE table. A position the table has no row for skips
+    the sequence: nothing appended, its output rows zeroed, ERR_POSITION set;
+    the other sequences are correct."""
+    wl = _wl(4)  # cached lengths 40, 70, 5, 100: positions 40, 70, 5, 100
+    dw = DeviceWorkload(wl, rope_positions=80)  # no row for position 100
+    before = dw.pool.clone()
+    out = dw.run()[0].cpu().numpy()
+    assert dw.step.error_bits(reset=True) == pkv.ERR_POSITION
+    assert np.all(out[3] == 0.0)
+    good = np.array([0, 1, 2])
+    want_pool = u16(wl.pool).reshape(-1).copy()
+    _, want = oracle_layer(want_pool, wl, 0, u16(wl.q)[0], u16(wl.k)[0], u16(wl.v)[0], seqs=good)
+    assert_close(out[good], want, "sequences with a table row")
+    assert np.array_equal(u16(dw.pool).reshape(-1), want_pool), "only sequences 0-2 appended"
+    assert not torch.equal(before, dw.pool)
+    dw.step.close()

@@ -15,7 +15,7 @@ from tests.parity import assert_close, u16
 pytestmark = pytest.mark.gpu
 
 
-def _run(starts, lens, hq=32, hkv=8, theta=500000.0, seed=0, max_blocks=None, table=False):
+def _run(starts, lens, hq=32, hkv=8, theta=500000.0, seed=0, max_blocks=None, rows=None):
     rng = np.random.default_rng(seed)
     gen = torch.Generator().manual_seed(seed)
     ends = [s + n for s, n in zip(starts, lens)]
@@ -51,12 +51,10 @@ def _run(starts, lens, hq=32, hkv=8, theta=500000.0, seed=0, max_blocks=None, ta
     out = torch.empty(total, hq, 64, device=dev)
     ws = pkv.alloc_prefill_workspace(total, len(starts), mb, device=dev)
     d_cu, d_st = torch.from_numpy(cu).to(dev), torch.from_numpy(st).to(dev)
-    rope = None
-    if table:  # the table built once, as for all the layers of a pass
-        rope = pkv.alloc_prefill_rope_table(total, device=dev)
-        pkv.paged_prefill_rope_table(d_cu, d_st, total, mb, theta, rope)
+    # the position table, built once (default: every position the block tables hold)
+    rope = pkv.build_rope_table(theta, rows or mb * 16, device=dev)
     pkv.paged_prefill(kp, q.to(dev), k.to(dev), v.to(dev), q_rot, out, torch.from_numpy(bt).to(dev),
-                      d_cu, d_st, theta, scale, ws, rope_table=rope)
+                      d_cu, d_st, rope, scale, ws)
     torch.cuda.synchronize()
     assert pkv.pkv_get_error(kp) == 0
     got_pool = u16(dpool)
@@ -91,9 +89,9 @@ def test_tiles_after_a_prefix_ending_mid_page():
     _run([100, 7], [70, 33], seed=6)
 
 
-def test_prebuilt_rope_table():
-    _run([0, 17, 300, 64], [16, 1, 45, 33], seed=10, table=True)
-    _run([5, 0], [40, 70], hq=14, hkv=2, theta=1e6, seed=11, table=True)
+def test_rope_table_exactly_as_long_as_the_positions():
+    _run([0, 17, 300, 64], [16, 1, 45, 33], seed=10, rows=345)
+    _run([5, 0], [40, 70], hq=14, hkv=2, theta=1e6, seed=11, rows=70)
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (12, 4), (10, 2), (12, 2), (64, 8)])
@@ -113,12 +111,49 @@ def test_malformed_chunk_is_flagged_and_zeroed():
     q_rot = torch.empty(4, hq, 64, device=dev)
     out = torch.full((4, hq, 64), 7.0, device=dev)
     ws = pkv.alloc_prefill_workspace(4, 1, 2, device=dev)
+    rope = pkv.build_rope_table(500000.0, 64, device=dev)
     # start 30 + 4 tokens needs positions up to 33 > 2 pages * 16: the last two are malformed
     pkv.paged_prefill(kp, q, k, v, q_rot, out, bt, torch.tensor([0, 4], dtype=torch.int32, device=dev),
-                      torch.tensor([30], dtype=torch.int32, device=dev), 500000.0, 0.125, ws)
+                      torch.tensor([30], dtype=torch.int32, device=dev), rope, 0.125, ws)
     torch.cuda.synchronize()
-    assert pkv.pkv_get_error(kp, reset=True) & pkv.ERR_SEQ_LEN
+    assert pkv.pkv_get_error(kp, reset=True) == pkv.ERR_SEQ_LEN
     assert (out[2:] == 0).all() and torch.isfinite(out[:2]).all() and (out[:2] != 7.0).any()
+    kp.close()
+
+
+def test_position_past_the_rope_table_is_flagged_and_zeroed():
+    """Tokens at positions the RoPE table has no row for are not stored, their
+    rows are zeroed and ERR_POSITION is set; the earlier tokens are right."""
+    dev = torch.device("cuda")
+    hkv, hq, theta = 8, 32, 500000.0
+    gen = torch.Generator().manual_seed(8)
+    pool = torch.randn(4 * 2 * hkv * 16 * 64, generator=gen).to(torch.bfloat16)
+    t = 20
+    q = torch.randn(t, hq, 64, generator=gen).to(torch.bfloat16)
+    k = torch.randn(t, hkv, 64, generator=gen).to(torch.bfloat16)
+    v = torch.randn(t, hkv, 64, generator=gen).to(torch.bfloat16)
+    bt = np.array([[2, 0]], np.int32)
+    cu, st = np.array([0, t], np.int32), np.array([0], np.int32)
+    rows = 15  # positions 0..14 have a row; tokens 15..19 do not
+    host = u16(pool).copy()
+    _, want = oracle.prefill(host, num_kv_heads=hkv, q=u16(q)[:rows], k=u16(k)[:rows],
+                             v=u16(v)[:rows], block_tables=bt, max_blocks=2,
+                             cu_tokens=np.array([0, rows], np.int32), start_pos=st, num_q_heads=hq,
+                             theta=theta, scale=0.125)
+    dpool = pool.to(dev)
+    kp = pkv.kv_pool_create(dpool, hkv)
+    q_rot = torch.empty(t, hq, 64, device=dev)
+    out = torch.full((t, hq, 64), 7.0, device=dev)
+    ws = pkv.alloc_prefill_workspace(t, 1, 2, device=dev)
+    pkv.paged_prefill(kp, q.to(dev), k.to(dev), v.to(dev), q_rot, out, torch.from_numpy(bt).to(dev),
+                      torch.from_numpy(cu).to(dev), torch.from_numpy(st).to(dev),
+                      pkv.build_rope_table(theta, rows, device=dev), 0.125, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_get_error(kp, reset=True) == pkv.ERR_POSITION
+    got = out.cpu().numpy()
+    assert np.all(got[rows:] == 0.0)
+    assert_close(got[:rows], want, "tokens with a table row")
+    assert np.array_equal(u16(dpool), host), "only the tokens with a table row are stored"
     kp.close()
 
 
@@ -139,7 +174,8 @@ def test_bad_page_id_is_flagged_and_masked():
     out = torch.empty(t, hq, 64, device=dev)
     ws = pkv.alloc_prefill_workspace(t, 1, 5, device=dev)
     pkv.paged_prefill(kp, q, k, v, q_rot, out, bt, torch.tensor([0, t], dtype=torch.int32, device=dev),
-                      torch.tensor([0], dtype=torch.int32, device=dev), 500000.0, 0.125, ws)
+                      torch.tensor([0], dtype=torch.int32, device=dev),
+                      pkv.build_rope_table(500000.0, 80, device=dev), 0.125, ws)
     torch.cuda.synchronize()
     assert pkv.pkv_get_error(kp, reset=True) & pkv.ERR_PAGE_ID
     assert torch.isfinite(out).all()
@@ -203,10 +239,9 @@ def test_measured_prefill_sizes_every_row(nb, t):
     out = torch.empty(total, hq, 64, device=dev)
     ws = pkv.alloc_prefill_workspace(total, nb, mb, device=dev)
     d_cu, d_st = torch.from_numpy(cu).to(dev), torch.from_numpy(starts).to(dev)
-    rope = pkv.alloc_prefill_rope_table(total, device=dev)
-    pkv.paged_prefill_rope_table(d_cu, d_st, total, mb, theta, rope)
+    rope = pkv.build_rope_table(theta, t, device=dev)
     pkv.paged_prefill(kp, q.to(dev), k.to(dev), v.to(dev), q_rot, out, torch.from_numpy(bt).to(dev),
-                      d_cu, d_st, theta, scale, ws, rope_table=rope)
+                      d_cu, d_st, rope, scale, ws)
     torch.cuda.synchronize()
     assert pkv.pkv_get_error(kp) == 0
 

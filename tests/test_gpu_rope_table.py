@@ -6,7 +6,7 @@ bf16 rounding of an fp64 rotation by them, so they must agree bit for bit
 with the oracle's, which are pinned against a 200-bit evaluation). Checked
 for every position below 2^17 and every frequency at the three bases in use
 (12.6 million angles), at positions up to the largest int32, and for the
-prefill's table of chunk positions. The fp32 pairs must be the fp32 rounding
+position table the decode step and the prefill read (row p = position p). The fp32 pairs must be the fp32 rounding
 of each value and the fp32 rounding of the remainder.
 """
 import math
@@ -71,15 +71,14 @@ def test_table_at_large_positions():
         _check_against_oracle(p, theta, pairs, full)
 
 
-def test_prefill_table_matches_the_chunk_positions():
-    starts = np.array([0, 17, 1000, 5], np.int32)
-    lens = np.array([300, 45, 2048, 1], np.int32)
-    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
-    total, mb = int(cu[-1]), 256
-    table = pkv.alloc_prefill_rope_table(total)
-    pkv.paged_prefill_rope_table(torch.from_numpy(cu).cuda(), torch.from_numpy(starts).cuda(), total,
-                                 mb, 500000.0, table)
+def test_position_table_build_equals_the_gather():
+    """paged_rope_table_build (row p = position p) gives the same bytes as
+    paged_rope_cos_sin over positions 0..n-1, and the oracle's values."""
+    n = 3000
+    built = pkv.build_rope_table(1e6, n)
+    gathered = pkv.alloc_rope_table(n)
+    pkv.paged_rope_cos_sin(torch.arange(n, dtype=torch.int32, device="cuda"), 1e6, gathered)
     torch.cuda.synchronize()
-    pairs, full = _split_table(table, total)
-    pos = np.concatenate([s + np.arange(n) for s, n in zip(starts, lens)])
-    _check_against_oracle(pos, 500000.0, pairs, full)
+    assert torch.equal(built, gathered)
+    pairs, full = _split_table(built, n)
+    _check_against_oracle(np.arange(n), 1e6, pairs, full)
