@@ -173,7 +173,8 @@ size_t paged_gqa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_h
  *                the partial results of segments split between CTAs, and a
  *                zero word means "not written in this call"; every call puts
  *                the words it wrote back to zero, so a workspace is zeroed
- *                once, when it is allocated. (After a call that set
+ *                once, when it is allocated. With pages_per_split = 0 it
+ *                also holds the step's plan (paged_decode_plan), if any. (After a call that set
  *                PKV_ERR_TIMEOUT, zero it again: a CTA that gave up waiting
  *                for a neighbour's partial leaves its slots as they are; see
  *                kv_pool_set_merge_wait_limit.)
@@ -185,6 +186,27 @@ int paged_gqa_decode(const pkv_pool_t *pool, const float *q_rot, float *out,
                      const int32_t *block_tables, int max_blocks, const int32_t *seq_lens,
                      int batch, int num_q_heads, float scale, int pages_per_split,
                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The work plan of a decode step, written into the decode workspace. The
+ * decode cuts the (sequence, kv head, page) work items of a launch into
+ * ranges, one per warp, from the sequence lengths alone; the lengths are the
+ * same in every layer of a step, so this call works the partition out once
+ * (the page prefix sums and every range's first item) and each later
+ * paged_decode_step (positions given) or paged_gqa_decode (positions NULL)
+ * on the same workspace, with the same batch, lengths and shapes, reads it
+ * instead of recomputing it in every CTA. A decode checks the plan against
+ * its own lengths and launch shape and works the partition out itself when
+ * they differ (a stale or missing plan costs time, never correctness).
+ * Arguments as for paged_decode_step; pages_per_split is 0 (the automatic
+ * partition). Batches above 2048 sequences are not planned (returns 0).
+ * Launches one small kernel on `stream`, without programmatic dependent
+ * launch, so a decode launched after it starts only once the plan is in
+ * memory. (Not on the pages: a scheduling aid of this library.)
+ */
+int paged_decode_plan(const pkv_pool_t *pool, const int32_t *seq_lens, const int32_t *positions,
+                      int rope_positions, int batch, int num_q_heads, int max_blocks,
+                      void *workspace, size_t workspace_bytes, void *stream);
 
 /* Bytes of a RoPE table of `rows` rows. */
 #define PKV_ROPE_TABLE_BYTES(rows) ((size_t)(rows) * 1024u)
@@ -323,11 +345,12 @@ int paged_prefill(pkv_pool_t *pool, const void *q, const void *k, const void *v,
  *   Arguments, layouts and results are those of paged_gqa_decode.
  *   Returns -E2BIG when these sizes need more scratch than the array holds
  *   (paged_gqa_decode_workspace_bytes() > PKV_NO_ALLOC_SCRATCH_BYTES). With
- *   pages_per_split = 0 the need does not depend on the batch: it is two
- *   partial slots of (64 + 2) * group floats per warp of the persistent
- *   grid, 2 * SMs * CTAs per SM * warps per CTA * slot bytes; with groups
- *   of 8 on a 152-SM GPU (one CTA of 10 warps per SM) that is 6.1 MiB, so a
- *   GPU with 30% more SMs would get -E2BIG for groups of 8.
+ *   pages_per_split = 0 the need is two partial slots of (64 + 2) * group
+ *   floats per warp of the persistent grid, 2 * SMs * CTAs per SM * warps
+ *   per CTA * slot bytes, plus a plan area of about 8 bytes per sequence
+ *   (22 KB at 2048); with groups of 8 on a 152-SM GPU (one CTA of 10 warps
+ *   per SM) that is 6.2 MiB, so a GPU with 30% more SMs would get -E2BIG
+ *   for groups of 8.
  *   The first call on each device looks up the array's device address (with
  *   that device current) and keeps it for the process; make that first call
  *   before any stream capture. The address does not survive a reset of the
@@ -336,6 +359,8 @@ int paged_prefill(pkv_pool_t *pool, const void *q, const void *k, const void *v,
  *   Each call first clears, on `stream`, the bytes of the array it will use
  *   (a cudaMemsetAsync, which allocates nothing), so the zero state the
  *   decode needs holds even after a call that ended with PKV_ERR_TIMEOUT.
+ *   (This also clears any plan, so this entry point always works out its
+ *   partition itself.)
  *   All calls share the one array: calls that overlap on the GPU (other
  *   streams, other threads) race and give wrong results; order them on one
  *   stream.

@@ -32,6 +32,7 @@ from ._binding import (  # noqa: F401
     kv_pool_page_bytes,
     kv_pool_set_merge_wait_limit,
     lib,
+    paged_decode_plan,
     paged_decode_step,
     paged_gqa_decode,
     paged_gqa_decode_no_alloc,

@@ -39,6 +39,7 @@ _SIGNATURES = {
     "paged_gqa_decode_no_alloc": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f, _i, _vp]),
     "paged_rope_cos_sin": (_i, [_vp, _i, _d, _vp, _vp]),
     "paged_rope_table_build": (_i, [_d, _i, _vp, _vp]),
+    "paged_decode_plan": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp]),
     "paged_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _f,
                                _i, _vp, _sz, _vp]),
     "paged_kv_split_combine": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _vp]),
@@ -305,6 +306,26 @@ def build_rope_table(rope_theta: float, num_positions: int, device=None, stream=
     table = alloc_rope_table(num_positions, device=device)
     paged_rope_table_build(rope_theta, num_positions, table, stream)
     return table
+
+
+def paged_decode_plan(pool: KVPool, seq_lens: torch.Tensor, block_tables: torch.Tensor,
+                      num_q_heads: int, workspace: torch.Tensor, positions: torch.Tensor | None = None,
+                      rope_table: torch.Tensor | None = None, stream=None) -> None:
+    """The step's work plan into ``workspace``: for paged_decode_step give the
+    positions and the RoPE table it will read; for paged_gqa_decode give neither."""
+    (batch,) = _shape(seq_lens, (None,), "seq_lens")
+    _shape(block_tables, (batch, None), "block_tables")
+    if (positions is None) != (rope_table is None):
+        raise ValueError("give positions and rope_table together, or neither")
+    if positions is not None:
+        _shape(positions, (batch,), "positions")
+    rc = lib().paged_decode_plan(
+        pool.handle, _dev(seq_lens, torch.int32, "seq_lens", 1),
+        None if positions is None else _dev(positions, torch.int32, "positions", 1),
+        0 if rope_table is None else rope_table_rows(rope_table), batch, num_q_heads,
+        block_tables.shape[1], _dev(workspace, torch.uint8, "workspace", 1), workspace.numel(),
+        _stream(stream))
+    _check("paged_decode_plan", rc)
 
 
 def paged_decode_step(pool: KVPool, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,

@@ -127,6 +127,8 @@ struct DecodeParams {
   int max_splits;
   int* err;
   uint32_t merge_looks;  // looks of a merger at other CTAs' partials before PKV_ERR_TIMEOUT
+  const int* plan;       // the workspace's plan area (automatic partition only), or null
+  int plan_key;          // this launch shape's plan key
   int ring_offset;  // byte offset of the copy rings in dynamic shared memory (rounded up to 1 KiB)
   // step mode
   const uint16_t* q_raw;    // bf16 [batch][hq][64]
@@ -205,6 +207,83 @@ __device__ void scan_pages(const int* s_len, int* s_pre, int batch, int* s_warp)
   if (tid == kT - 1) s_pre[batch] = wofs + incl;
   __syncthreads();
 }
+
+// The automatic partition of a launch's work items over its warps. Work
+// units are laid out segment by segment (segment s = sequence * hkv + kv
+// head, its pages items P_s .. P_s + np - 1): su units of fixed cost, then pu
+// units per page, so page item i of segment s starts at unit
+// pu * i + su * (s + 1). Range r covers units [r cw, (r + 1) cw) and owns the
+// pages that start there. pages_per_split > 0 gives plain ranges of that many
+// pages (pu = 1, su = 0), as does a work list too long for 32-bit unit
+// arithmetic. Short ranges cut latency when there is little work; once every
+// warp would get a few pages anyway, ranges of at least twice that keep the
+// number of pieces (and merges) down.
+struct Partition {
+  int n_items, pu, su, total_units, cw, n_ranges;
+};
+
+__device__ __forceinline__ Partition make_partition(int total_pages, int batch, int hkv, int nwarps,
+                                                    int pages_per_split) {
+  Partition pt;
+  pt.n_items = total_pages * hkv;
+  const bool weighted = pages_per_split == 0 && pt.n_items < (1 << 28);
+  pt.pu = weighted ? kPageUnits : 1;
+  pt.su = weighted ? kSegUnits : 0;
+  pt.total_units = pt.pu * pt.n_items + pt.su * batch * hkv;
+  const int even = (pt.total_units + nwarps - 1) / nwarps;
+  const int min_pages = even >= pt.pu * kMinRangePages ? 2 * kMinRangePages : kMinRangePages;
+  pt.cw = pages_per_split > 0 ? pages_per_split : max(pt.pu * min_pages, even);
+  pt.n_ranges = (pt.total_units + pt.cw - 1) / pt.cw;
+  return pt;
+}
+
+// First page item starting at or after unit u (n_items if none). Sequence b
+// starts at unit hkv (pu s_pre[b] + su b) and each of its segments spans
+// pu np + su units: find b by bisection, then the segment and page directly.
+__device__ __forceinline__ int partition_item_at(const Partition& pt, int u, const int* s_pre,
+                                                 int batch, int hkv) {
+  if (u >= pt.total_units) return pt.n_items;
+  int lo = 0, hi = batch - 1;  // largest b whose first unit is <= u
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (hkv * (pt.pu * s_pre[mid] + pt.su * mid) <= u) lo = mid; else hi = mid - 1;
+  }
+  const int np = s_pre[lo + 1] - s_pre[lo];
+  const int off = u - hkv * (pt.pu * s_pre[lo] + pt.su * lo);
+  const int seg_units = pt.pu * np + pt.su;
+  const int h = off / seg_units;
+  const int within = off - h * seg_units;
+  const int pg = within <= pt.su ? 0 : (within - pt.su + pt.pu - 1) / pt.pu;
+  return hkv * s_pre[lo] + h * np + pg;  // pg == np: the next segment's first page
+}
+
+// A sequence's length as the decode uses it: 0 (the sequence is skipped)
+// when it is outside [1, cap] or, with positions, when its RoPE position
+// has no row in the table; *bad gets the error bits.
+__device__ __forceinline__ int checked_length(int n, int cap, const int32_t* positions, int b,
+                                              int rope_positions, int* bad) {
+  int e = (n < 1 || n > cap) ? PKV_ERR_SEQ_LEN : 0;
+  if (positions) {
+    const int pos = positions[b];
+    if (pos < 0 || pos >= rope_positions) e |= PKV_ERR_POSITION;
+  }
+  *bad = e;
+  return e ? 0 : n;
+}
+
+// A step's work plan, kept in the decode workspace after the partial slots:
+// the partition depends only on the sequence lengths (and the launch shape),
+// which are the same in every layer of a step, so it is worked out once per
+// step (plan_kernel) instead of by every CTA of every layer. Ints:
+//   [0 .. kPlanHdr)           key (the launch shape it was made for, never 0),
+//                             batch, n_items, pu, su, total_units, cw, n_ranges
+//   [kPlanHdr, + batch)       the lengths as checked_length gives them
+//   [.., + batch + 1)         page prefix sums
+//   [.., + n_ranges + 1)      first item of each range (the last one: n_items)
+// A decode that finds the key of its own launch shape and the same lengths
+// takes the prefix sums and its ranges from the plan; otherwise it works
+// them out itself, so a stale plan costs time, never correctness.
+constexpr int kPlanHdr = 16;
 
 // A piece of a split (sequence, kv head) segment, as one lane holds it: the
 // head g8 = lane / 4 and its dims 8d + 2 tig, +1 (d = 0..7), with the running
@@ -527,6 +606,7 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   int* s_len = reinterpret_cast<int*>(smem + kHdrBytes);
   int* s_pre = s_len + p.batch;
   __shared__ int s_bad;  // PKV_ERR_SEQ_LEN / PKV_ERR_POSITION of sequences skipped here
+  __shared__ int s_plan[kPlanHdr];
   const uint32_t bar0 = smem_addr(smem) + warp * C::kStages * 8;
   const uint32_t ring_base = (smem_addr(smem) + p.ring_offset + 1023u) & ~1023u;
   const uint32_t ring0 = ring_base + warp * C::kStages * kHeadPageBytes;
@@ -547,62 +627,38 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   __syncthreads();
   grid_launch_dependents();
   if (!kStep) grid_dependency_wait();
+  // The lengths, and with a plan in the workspace its header, its lengths,
+  // its prefix sums and the bounds of this warp's first range, all loaded in
+  // one round trip; the plan is taken only if it was made for this launch
+  // shape and these lengths.
   const int cap = p.max_blocks * kPage;
-  for (int b = tid; b < p.batch; b += kT) {
-    int n = p.seq_lens[b];
-    int bad = (n < 1 || n > cap) ? PKV_ERR_SEQ_LEN : 0;
-    if (kStep) {
-      const int pos = p.positions[b];
-      if (pos < 0 || pos >= p.rope_positions) bad |= PKV_ERR_POSITION;
-    }
-    if (bad) {
-      n = 0;
-      atomicOr(&s_bad, bad);
-    }
-    s_len[b] = n;
+  const int* plan = p.plan;
+  const int r_first = blockIdx.x * kW + warp;
+  int agree = plan != nullptr, plan_bnd = 0;
+  if (plan) {
+    if (tid < kPlanHdr) s_plan[tid] = plan[tid];
+    if (lane < 2) plan_bnd = plan[kPlanHdr + 2 * p.batch + 1 + r_first + lane];
+    if (tid == 0) s_pre[p.batch] = plan[kPlanHdr + 2 * p.batch];
   }
-  __syncthreads();
-  scan_pages<kT>(s_len, s_pre, p.batch, s_warp);
-
-  const int n_items = s_pre[p.batch] * p.hkv;
-  const int nwarps = gridDim.x * kW;
-  // Ranges: work units are laid out segment by segment (segment s = sequence
-  // * hkv + kv head, its pages items P_s .. P_s + np - 1): su units of fixed
-  // cost, then pu units per page, so page item i of segment s starts at unit
-  // pu * i + su * (s + 1). Range r covers units [r cw, (r + 1) cw) and owns
-  // the pages that start there. pages_per_split > 0 gives plain ranges of
-  // that many pages (pu = 1, su = 0), as does a work list too long for 32-bit
-  // unit arithmetic.
-  const int n_seg = p.batch * p.hkv;
-  const bool weighted = p.pages_per_split == 0 && n_items < (1 << 28);
-  const int pu = weighted ? kPageUnits : 1;
-  const int su = weighted ? kSegUnits : 0;
-  const int total_units = pu * n_items + su * n_seg;
-  // Short ranges cut latency when there is little work; once every warp
-  // would get a few pages anyway, ranges of at least twice that keep the
-  // number of pieces (and merges) down.
-  const int even = (total_units + nwarps - 1) / nwarps;
-  const int min_pages = even >= pu * kMinRangePages ? 2 * kMinRangePages : kMinRangePages;
-  const int cw = p.pages_per_split > 0 ? p.pages_per_split : max(pu * min_pages, even);
-  const int n_ranges = (total_units + cw - 1) / cw;
-  // First page item starting at or after unit u (n_items if none). Sequence b
-  // starts at unit hkv (pu s_pre[b] + su b) and each of its segments spans
-  // pu np + su units: find b by bisection, then the segment and page directly.
-  auto item_at = [&](int u) -> int {
-    if (u >= total_units) return n_items;
-    int lo = 0, hi = p.batch - 1;  // largest b whose first unit is <= u
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.hkv * (pu * s_pre[mid] + su * mid) <= u) lo = mid; else hi = mid - 1;
+  for (int b = tid; b < p.batch; b += kT) {
+    int bad;
+    const int n = checked_length(p.seq_lens[b], cap, kStep ? p.positions : nullptr, b,
+                                 p.rope_positions, &bad);
+    if (bad) atomicOr(&s_bad, bad);
+    s_len[b] = n;
+    if (plan) {
+      if (plan[kPlanHdr + b] != n) agree = 0;
+      s_pre[b] = plan[kPlanHdr + p.batch + b];
     }
-    const int np = s_pre[lo + 1] - s_pre[lo];
-    const int off = u - p.hkv * (pu * s_pre[lo] + su * lo);
-    const int seg_units = pu * np + su;
-    const int h = off / seg_units;
-    const int within = off - h * seg_units;
-    const int pg = within <= su ? 0 : (within - su + pu - 1) / pu;
-    return p.hkv * s_pre[lo] + h * np + pg;  // pg == np: the next segment's first page
-  };
+  }
+  agree = __syncthreads_and(agree);
+  const bool planned = agree && s_plan[0] == p.plan_key && s_plan[1] == p.batch;
+  if (!planned) scan_pages<kT>(s_len, s_pre, p.batch, s_warp);
+  const Partition pt =
+      planned ? Partition{s_plan[2], s_plan[3], s_plan[4], s_plan[5], s_plan[6], s_plan[7]}
+              : make_partition(s_pre[p.batch], p.batch, p.hkv, gridDim.x * kW, p.pages_per_split);
+  const int n_items = pt.n_items, pu = pt.pu, su = pt.su, cw = pt.cw, n_ranges = pt.n_ranges;
+  auto item_at = [&](int u) { return partition_item_at(pt, u, s_pre, p.batch, p.hkv); };
   // Range of the unit at which segment sg's page item i starts.
   auto range_of = [&](int i, int sg) { return (pu * i + su * (sg + 1)) / cw; };
   const float qs = p.qscale;
@@ -707,9 +763,10 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
   float o[8][4];      // O accumulator, dims 8d..8d+7: rows g8 (from P) and g8+8 (from P's remainder)
   float m_run = -INFINITY, l_run = 0.f;
 
-  // lane 0 finds where range r starts, lane 1 where it ends
+  // lane 0 finds where range r starts, lane 1 where it ends (this warp's
+  // first range: read from the plan when there is one)
   auto range_bounds = [&](int r, int& i0, int& i1) {
-    const int i_lane = item_at((r + (lane & 1)) * cw);
+    const int i_lane = (planned && r == r_first) ? plan_bnd : item_at((r + (lane & 1)) * cw);
     i0 = __shfl_sync(kFull, i_lane, 0);
     i1 = __shfl_sync(kFull, i_lane, 1);
   };
@@ -1115,6 +1172,37 @@ __global__ void __launch_bounds__(Cfg<G>::kThreads, 1)
 }
 
 
+// One CTA: a step's plan (see kPlanHdr) for a decode launch of nwarps warps:
+// every length checked as the decode checks it, the page prefix sums, the
+// partition and the first item of every range.
+constexpr int kPlanThreads = 1024;
+__global__ void __launch_bounds__(kPlanThreads)
+    plan_kernel(const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ positions,
+                int rope_positions, int batch, int hkv, int cap, int nwarps, int key,
+                int* __restrict__ plan) {
+  __shared__ int s_len[kDecodeBatchChunk], s_pre[kDecodeBatchChunk + 1], s_warp[kPlanThreads / 32];
+  for (int b = threadIdx.x; b < batch; b += kPlanThreads) {
+    int bad;
+    s_len[b] = checked_length(seq_lens[b], cap, positions, b, rope_positions, &bad);
+  }
+  __syncthreads();
+  scan_pages<kPlanThreads>(s_len, s_pre, batch, s_warp);
+  const Partition pt = make_partition(s_pre[batch], batch, hkv, nwarps, 0);
+  int* len = plan + kPlanHdr;
+  int* pre = len + batch;
+  int* bnd = pre + batch + 1;
+  for (int b = threadIdx.x; b <= batch; b += kPlanThreads) {
+    if (b < batch) len[b] = s_len[b];
+    pre[b] = s_pre[b];
+  }
+  for (int r = threadIdx.x; r <= pt.n_ranges; r += kPlanThreads)
+    bnd[r] = partition_item_at(pt, r * pt.cw, s_pre, batch, hkv);
+  if (threadIdx.x == 0) {
+    const int hdr[8] = {key, batch, pt.n_items, pt.pu, pt.su, pt.total_units, pt.cw, pt.n_ranges};
+    for (int i = 0; i < 8; ++i) plan[i] = hdr[i];
+  }
+}
+
 template <int G>
 struct Launcher {
   using Fn = void (*)(CUtensorMap, DecodeParams);
@@ -1189,6 +1277,39 @@ int warps_per_cta(int group) { return group <= 4 ? Cfg<4>::kWarps : Cfg<8>::kWar
 
 int slot_floats_for(int group) { return ((group * kHeadDim + 2 * group) + 3) / 4 * 4; }
 
+size_t align256(size_t n) { return (n + 255) / 256 * 256; }
+
+// The decode's grid: one CTA per SM (blocks_per_sm of them), less a few SMs
+// (see launch_decode). 0 when the kernel cannot be configured.
+int decode_grid(int group, int device, int mode) {
+  const int bps = blocks_per_sm_for(group, device, mode);
+  const int sms = device_sm_count(device);
+  if (bps < 1 || sms < 1) return 0;
+  return sms * bps > kSpareSms ? sms * bps - kSpareSms : sms * bps;
+}
+
+// Workspace layout for the automatic partition: the partial slots (two per
+// warp of the grid), then the plan area.
+size_t slots_bytes(int group, long long warps) {
+  return static_cast<size_t>(2 * warps) * slot_floats_for(group) * sizeof(float);
+}
+size_t plan_bytes(int batch, long long warps) {
+  return align256(sizeof(int) * (kPlanHdr + 2 * static_cast<size_t>(batch) + 1 +
+                                 static_cast<size_t>(warps) + 1));
+}
+
+// The launch shape a plan is made for (never 0): kv heads, group, grid,
+// warps per CTA, the length cap, and the RoPE table rows the lengths were
+// checked against (0: positions not checked).
+int plan_key(int hkv, int group, int grid, int cap, int rope_positions) {
+  uint32_t h = 0x9e3779b9u;
+  const uint32_t v[6] = {static_cast<uint32_t>(hkv), static_cast<uint32_t>(group),
+                         static_cast<uint32_t>(grid), static_cast<uint32_t>(warps_per_cta(group)),
+                         static_cast<uint32_t>(cap), static_cast<uint32_t>(rope_positions)};
+  for (uint32_t x : v) h ^= x + 0x9e3779b9u + (h << 6) + (h >> 2);
+  return static_cast<int>(h | 1u);
+}
+
 }  // namespace
 
 size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int max_blocks,
@@ -1209,9 +1330,37 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int 
     const long long items = chunk * num_kv_heads * max_blocks;
     const long long need = (items + pages_per_split - 1) / pages_per_split;
     if (need > ranges) ranges = need;
+    // two partial slots per group of ranges (a group has one range per warp of a CTA)
+    return slots_bytes(group, ranges);
   }
-  // two partial slots per group of ranges (a group has one range per warp of a CTA)
-  return static_cast<size_t>(2 * ranges) * slot_floats_for(group) * sizeof(float);
+  // the automatic partition: the slots, then (one launch) the step's plan
+  size_t bytes = slots_bytes(group, warps);
+  if (batch <= kDecodeBatchChunk) bytes = align256(bytes) + plan_bytes(batch, warps);
+  return bytes;
+}
+
+cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* positions, int rope_positions,
+                        int batch, int num_q_heads, int num_kv_heads, int max_blocks,
+                        void* workspace, cudaStream_t stream) {
+  if (batch == 0 || batch > kDecodeBatchChunk) return cudaSuccess;  // only one-launch batches
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  const int group = num_q_heads / num_kv_heads;
+  const int mode = positions ? kModeStep : kModeDecode;
+  const int grid = decode_grid(group, device, mode);
+  if (grid < 1) return cudaErrorInvalidConfiguration;
+  const int cap = max_blocks * kPage;
+  const int rp = positions ? rope_positions : 0;
+  const int sms = device_sm_count(device);
+  const long long warps = static_cast<long long>(sms) * blocks_per_sm_for(group, device, mode) *
+                          warps_per_cta(group);
+  int* plan = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
+                                     align256(slots_bytes(group, warps)));
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, positions, rp, batch, num_kv_heads, cap,
+                                              grid * warps_per_cta(group),
+                                              plan_key(num_kv_heads, group, grid, cap, rp), plan);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
@@ -1231,7 +1380,16 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
   // previous kernel's CTAs leave their SMs, so the last ones would start
   // late (their set-up runs while the memory system is busiest) and finish
   // last; the page stream does not need every SM.
-  const int grid = sms * bps > kSpareSms ? sms * bps - kSpareSms : sms * bps;
+  const int grid = decode_grid(group, device, mode);
+  // the step's plan, for the automatic partition of a one-launch batch
+  const long long warps = static_cast<long long>(sms) * bps * warps_per_cta(group);
+  const bool use_plan = !partials && a.pages_per_split == 0 && a.batch <= kDecodeBatchChunk &&
+                        a.workspace != nullptr;
+  const int* plan = use_plan ? reinterpret_cast<const int*>(static_cast<const uint8_t*>(a.workspace) +
+                                                            align256(slots_bytes(group, warps)))
+                             : nullptr;
+  const int key = plan_key(a.num_kv_heads, group, grid, a.max_blocks * kPage,
+                           step ? a.rope_positions : 0);
   const double log2e = 1.4426950408889634;
   for (int b0 = 0; b0 < a.batch; b0 += kDecodeBatchChunk) {
     const int nb = a.batch - b0 < kDecodeBatchChunk ? a.batch - b0 : kDecodeBatchChunk;
@@ -1255,6 +1413,8 @@ cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream) {
     p.max_splits = a.max_splits;
     p.err = a.err;
     p.merge_looks = a.merge_looks;
+    p.plan = plan;
+    p.plan_key = key;
     p.ring_offset = static_cast<int>(ring_offset_bytes());
     const size_t qrow0 = static_cast<size_t>(b0) * a.num_q_heads * kHeadDim;
     const size_t krow0 = static_cast<size_t>(b0) * a.num_kv_heads * kHeadDim;

@@ -233,6 +233,22 @@ int paged_gqa_decode(const pkv_pool_t* pool, const float* q_rot, float* out,
   return e == cudaSuccess ? 0 : cuda_fail(e);
 }
 
+int paged_decode_plan(const pkv_pool_t* pool, const int32_t* seq_lens, const int32_t* positions,
+                      int rope_positions, int batch, int num_q_heads, int max_blocks,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (!decode_shape_ok(pool, batch, num_q_heads, max_blocks)) return -EINVAL;
+  if (positions && (rope_positions < 1 || rope_positions >= (1 << 24))) return -EINVAL;
+  if (batch == 0 || batch > pkv::kDecodeBatchChunk) return 0;  // nothing to plan
+  if (!seq_lens || !workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return -EINVAL;
+  const size_t need = paged_gqa_decode_workspace_bytes(batch, num_q_heads, pool->num_kv_heads,
+                                                       max_blocks, 0);
+  if (need == 0 || workspace_bytes < need) return -EINVAL;
+  cudaError_t e = pkv::launch_plan(seq_lens, positions, rope_positions, batch, num_q_heads,
+                                   pool->num_kv_heads, max_blocks, workspace,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? 0 : cuda_fail(e);
+}
+
 int paged_rope_cos_sin(const int32_t* positions, int rows, double rope_theta, void* table,
                        void* stream) {
   if (rows < 0 || rows >= (1 << 24) || !(rope_theta > 0.0) || !std::isfinite(rope_theta))

@@ -126,6 +126,11 @@ constexpr int kDecodeBatchChunk = 2048;
 size_t decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int max_blocks,
                               int pages_per_split, int sm_count);
 cudaError_t launch_decode(const DecodeLaunch& a, cudaStream_t stream);
+// The step's work plan in the decode workspace (positions null: for the
+// decode from q_rot, whose lengths are not checked against positions).
+cudaError_t launch_plan(const int32_t* seq_lens, const int32_t* positions, int rope_positions,
+                        int batch, int num_q_heads, int num_kv_heads, int max_blocks,
+                        void* workspace, cudaStream_t stream);
 
 // cos and sin of pos * theta^(-2j/64), j < 32, for every row, correctly
 // rounded to fp64, and split into fp32 pairs: table = float4 [rows][32]

@@ -1,10 +1,12 @@
 """One batched decode step over all layers, through the C ABI.
 
-Per layer l, on one stream: RoPE of the new token's q and k at its position
-and the append of its K/V into the layer's pages, then every query head's
-attention over its sequence's pages. By default one ``paged_decode_step``
-call does both; with ``fused=False`` the two separate entry points
-``paged_kv_append_rope`` and ``paged_gqa_decode`` run instead. This is
+Once per step, the decode's work plan (``paged_decode_plan``: the partition
+of the work over the warps depends only on the sequence lengths, the same in
+every layer). Then per layer l, on one stream: RoPE of the new token's q and
+k at its position and the append of its K/V into the layer's pages, then
+every query head's attention over its sequence's pages. By default one
+``paged_decode_step`` call does both; with ``fused=False`` the two separate
+entry points ``paged_kv_append_rope`` and ``paged_gqa_decode`` run instead. This is
 the decode half of the per-layer loop the "Hours of YouTube and 85 handtyped
 pages of notes on LLM Inference – Start here" engine runs for each packed
 decode batch (its batched decode item); the projections around it are not
@@ -57,13 +59,26 @@ class DecodeStep:
         self.rope = B.build_rope_table(self.rope_theta, self.rope_positions, device=dev)
 
     def launches_per_step(self, fused: bool = True) -> int:
-        """Kernels one step launches: per layer one decode per batch chunk of
-        2048, plus the append kernel when not fused (the cos/sin table was
-        built once, at construction)."""
+        """Kernels one step launches: the plan (one-launch batches of at most
+        2048 sequences, automatic partition), then per layer one decode per
+        batch chunk of 2048, plus the append kernel when not fused (the
+        cos/sin table was built once, at construction)."""
         if not self.batch:
             return 0
         chunks = -(-self.batch // 2048)
-        return self.num_layers * (chunks + (0 if fused else 1))
+        plan = 1 if self.plans() else 0
+        return plan + self.num_layers * (chunks + (0 if fused else 1))
+
+    def plans(self) -> bool:
+        return self.batch <= 2048 and self.pages_per_split == 0
+
+    def plan(self, fused: bool = True, stream=None) -> None:
+        """The step's work plan (the lengths and positions of this step)."""
+        if not self.plans():
+            return
+        B.paged_decode_plan(self.pool, self.seq_lens, self.block_tables[0], self.num_q_heads,
+                            self.workspace, positions=self.positions if fused else None,
+                            rope_table=self.rope if fused else None, stream=stream)
 
     def append(self, layer: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
         B.paged_kv_append_rope(self.pool, q[layer], k[layer], v[layer], self.q_rot[layer],
@@ -86,6 +101,7 @@ class DecodeStep:
     def run(self, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, stream=None,
             fused: bool = True) -> torch.Tensor:
         """q [NL,B,Hq,64], k/v [NL,B,Hkv,64] bf16 on the device -> out [NL,B,Hq,64] fp32."""
+        self.plan(fused, stream)
         for layer in range(self.num_layers):
             if fused:
                 self.fused_layer(layer, q, k, v, stream)
@@ -106,7 +122,8 @@ class DecodeStep:
         q/k/v in three groups: layer 0 (with the lengths and positions), the
         next three layers (they land while layer 0 runs), then the rest (while
         layers 0-3 run). The step waits for each group just before its first
-        layer. Each such wait costs the chain of decode launches its
+        layer; the step's plan runs once the first group, with the lengths
+        and positions, has landed. Each such wait costs the chain of decode launches its
         programmatic overlap at that layer, several microseconds, so the
         groups are few; more, smaller ones (1, 1, 2, 4, ... layers) were 5-13
         us per step slower on batch 64 and the Qwen shape. copy_streams[1]
@@ -136,6 +153,8 @@ class DecodeStep:
             for lo, ev in ready:
                 if lo == layer:
                     cur.wait_event(ev)
+            if layer == 0:
+                self.plan()
             self.fused_layer(layer, dev_in["q"], dev_in["k"], dev_in["v"])
             ev_done[layer].record(cur)
         with torch.cuda.stream(cs_out):
