@@ -213,8 +213,12 @@ struct TcCfg {
   static constexpr uint32_t kBytes = kStage0 + kStages * 2 * kStep;
 };
 constexpr float kSlack = 8.f;
-// tensor memory: S buffers in columns 0-63 and 64-127, O in 128-191, P_hi in
-// 192-223 and P_lo in 224-255 (two bf16 keys per column)
+// tensor memory: S buffers in columns 0-63 and 64-127, O in 128-191. Step
+// j's P is written over its own S: P_hi in the buffer's first 32 columns and
+// P_lo in the next 32 (two bf16 keys per column), so P is double-buffered
+// with S, and a softmax step does not wait for the previous step's P V
+// (only to rescale O). Columns 192-255 are unused (allocations are powers of
+// two).
 constexpr uint32_t kTmemCols = 256;
 
 template <int G>
@@ -224,7 +228,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   extern __shared__ __align__(1024) uint8_t dsmem[];
   __shared__ __align__(8) uint64_t k_full[C::kStages], k_empty[C::kStages];
   __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
-  __shared__ __align__(8) uint64_t s_full[2], q_ready, p_full, pv_done, drain;
+  __shared__ __align__(8) uint64_t s_full[2], q_ready, p_full[2], pv_done[2], drain;
   __shared__ uint32_t s_tmem;
   __shared__ float s_xchg[2][2][128];  // [step parity][column half][row]: row maxima
   __shared__ float s_lsum[2][128];     // [column half][row]: the halves' sums
@@ -262,16 +266,20 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     mbar_init(smem_addr(&s_full[0]), 1);
     mbar_init(smem_addr(&s_full[1]), 1);
     mbar_init(smem_addr(&q_ready), C::kSoftmaxThreads);
-    mbar_init(smem_addr(&p_full), C::kSoftmaxThreads);
-    mbar_init(smem_addr(&pv_done), 1);
+    // P_j ready and P_j V_j done, one barrier per buffer (j & 1): a wait
+    // for step j never sees a barrier two phases on
+    mbar_init(smem_addr(&p_full[0]), C::kSoftmaxThreads);
+    mbar_init(smem_addr(&p_full[1]), C::kSoftmaxThreads);
+    mbar_init(smem_addr(&pv_done[0]), 1);
+    mbar_init(smem_addr(&pv_done[1]), 1);
     mbar_init(smem_addr(&drain), 1);
   }
   fence_mbar_init();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem, tO = tmem + 128, tPhi = tmem + 192, tPlo = tmem + 224;
-  auto tS = [&](int j) { return tmem + 64 * (j & 1); };
+  const uint32_t tmem = s_tmem, tO = tmem + 128;
+  auto tS = [&](int j) { return tmem + 64 * (j & 1); };  // S_j, then P_j (hi: +0, lo: +32)
   bool failed = false;
 
   if (warp == 8) {
@@ -368,11 +376,19 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       if (!mbar_wait_bounded(smem_addr(&q_ready), 0) || !issue_s(0)) failed = true;
       for (int j = 0; j < n_steps && !failed; ++j) {
         const int st = j % C::kStages;
-        if (j + 1 < n_steps && !issue_s(j + 1)) {
-          failed = true;
-          break;
+        // S_{j+1} goes into the buffer of S_{j-1} / P_{j-1}: once P_{j-1} V_{j-1} is done
+        if (j + 1 < n_steps) {
+          if (j > 0 && !mbar_wait_bounded(smem_addr(&pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          if (!issue_s(j + 1)) {
+            failed = true;
+            break;
+          }
         }
-        if (!mbar_wait_bounded(smem_addr(&p_full), j & 1) ||
+        if (!mbar_wait_bounded(smem_addr(&p_full[j & 1]), (j >> 1) & 1) ||
             !mbar_wait_bounded(smem_addr(&v_full[st]), (j / C::kStages) & 1)) {
           failed = true;
           break;
@@ -382,11 +398,11 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         // P from tensor memory (a 16-key K step is 8 columns); V is MN-major:
         // a 16-key K step is 16 rows = 2048 bytes (+128)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tPhi + 8 * k, dV + 128 * k, idPV, j > 0 || k > 0);
+        for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tS(j) + 8 * k, dV + 128 * k, idPV, j > 0 || k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tPlo + 8 * k, dV + 128 * k, idPV, true);
+        for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tS(j) + 32 + 8 * k, dV + 128 * k, idPV, true);
         umma_commit(smem_addr(&v_empty[st]));
-        umma_commit(smem_addr(&pv_done));
+        umma_commit(smem_addr(&pv_done[j & 1]));
       }
       if (failed) {  // let the MMAs already issued finish before the memory goes away
         umma_commit(smem_addr(&drain));
@@ -468,15 +484,18 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
         for (int i = 0; i < w; ++i) mt[i] = fmaxf(mt[i], mt[i + w]);
-      // the row's maximum: this half's and the partner thread's
+      // the row's maximum: this half's and the partner thread's (the barrier
+      // also means both halves have read S_j, whose columns P_j overwrites)
       s_xchg[j & 1][hf][r] = mt[0];
+      tc_fence_before();
       pair_sync();
+      tc_fence_after();
       const float mx = fmaxf(mt[0], s_xchg[j & 1][hf ^ 1][r]);
-      // O and P belong to P_{j-1} V_{j-1} until it completes
-      if (j > 0 && !mbar_wait_bounded(smem_addr(&pv_done), (j - 1) & 1)) failed = true;
       if (mx > m_ref + kSlack) {
-        // move the reference up; O (this thread's half of the columns) and l follow
+        // move the reference up; O (this thread's half of the columns) and l
+        // follow, once P_{j-1} V_{j-1}, the last product into O, is done
         if (j > 0 && m_ref != -INFINITY) {
+          if (!mbar_wait_bounded(smem_addr(&pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1)) failed = true;
           tc_fence_after();
           const float alpha = fast_exp2(m_ref - mx);
           l_sum *= alpha;
@@ -491,7 +510,8 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         m_ref = mx;
       }
       // P = exp2(S - m_ref) as bf16 high part and remainder, into tensor
-      // memory: this thread's 32 keys are columns 16 hf .. 16 hf + 15
+      // memory over S_j: this thread's 32 keys are columns 16 hf .. 16 hf + 15
+      // of each half
       const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // all scores -inf: P = 0
       float lp[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t hi[16], lo[16];
@@ -504,8 +524,8 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         const float2 f = bf16x2_to_float2(hi[e]);
         lo[e] = pack_bf16x2(p0 - f.x, p1 - f.y);
       }
-      tmem_st16u(tPhi + lane_addr + 16 * hf, hi);
-      tmem_st16u(tPlo + lane_addr + 16 * hf, lo);
+      tmem_st16u(tS(j) + lane_addr + 16 * hf, hi);
+      tmem_st16u(tS(j) + lane_addr + 32 + 16 * hf, lo);
       tmem_wait_st();
       l_sum += (lp[0] + lp[1]) + (lp[2] + lp[3]);
       // V rows that hold no key of the tile (past its last position, or of a
@@ -522,13 +542,16 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(smem_addr(&p_full));
+      mbar_arrive(smem_addr(&p_full[j & 1]));
     }
     // epilogue: O / l for the live rows, l being the sum of both halves' sums
     s_lsum[hf][r] = l_sum;
     pair_sync();
     const float l_row = l_sum + s_lsum[hf ^ 1][r];
-    if (!failed && mbar_wait_bounded(smem_addr(&pv_done), (n_steps - 1) & 1)) {
+    // the last product into O is P V of step n_steps - 1 (products of the
+    // same barrier complete in order; the one before it, step n_steps - 3,
+    // was done before S of step n_steps - 1 was issued)
+    if (!failed && mbar_wait_bounded(smem_addr(&pv_done[(n_steps - 1) & 1]), ((n_steps - 1) >> 1) & 1)) {
       tc_fence_after();
       float o[32];
       tmem_ld32(tO + lane_addr + 32 * hf, o);
