@@ -204,7 +204,7 @@ struct TcCfg {
   static constexpr int kRows = kTokens * G;  // <= 128; rows past it are padding
   static constexpr int kStages = 4;
   static constexpr int kSoftmaxThreads = 256;
-  static constexpr int kThreads = kSoftmaxThreads + 64;
+  static constexpr int kThreads = kSoftmaxThreads + 96;
   static constexpr uint32_t kTile = 128 * 128;  // a 128-row x 128-byte operand tile
   static constexpr uint32_t kStep = 64 * 128;   // 64 K rows (or V rows) of one step
   // dynamic shared memory: Q_hi, Q_lo, then per stage K and V
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   extern __shared__ __align__(1024) uint8_t dsmem[];
   __shared__ __align__(8) uint64_t k_full[C::kStages], k_empty[C::kStages];
   __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
-  __shared__ __align__(8) uint64_t s_full[2], q_ready, p_full[2], pv_done[2], drain;
+  __shared__ __align__(8) uint64_t s_full[2], q_ready, p_full[2], pv_done[2], drain[2];
   __shared__ uint32_t s_tmem;
   __shared__ float s_xchg[2][2][128];  // [step parity][column half][row]: row maxima
   __shared__ float s_lsum[2][128];     // [column half][row]: the halves' sums
@@ -272,7 +272,8 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     mbar_init(smem_addr(&p_full[1]), C::kSoftmaxThreads);
     mbar_init(smem_addr(&pv_done[0]), 1);
     mbar_init(smem_addr(&pv_done[1]), 1);
-    mbar_init(smem_addr(&drain), 1);
+    mbar_init(smem_addr(&drain[0]), 1);
+    mbar_init(smem_addr(&drain[1]), 1);
   }
   fence_mbar_init();
   tc_fence_before();
@@ -351,16 +352,26 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       for (int j = max(0, v_issued - C::kStages); j < v_issued; ++j)
         mbar_wait_bounded(smem_addr(&v_full[j % C::kStages]), (j / C::kStages) & 1);
     }
-  } else if (warp == 9) {
-    // ---- MMA issuer ----
-    if (lane == 0) {
+  } else if (warp == 9 || warp == 10) {
+    // ---- MMA issuers, each a whole warp, converged (one lane issues each
+    // product; every wait's result is made warp-uniform): warp 9 the score
+    // products, warp 10 the P V products. A commit covers only its own
+    // warp's products. ----
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(kFull, mbar_wait_bounded(bar, parity)) != 0;
+    };
+    if (warp == 9) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 64, false);
-      constexpr uint32_t idPV = idesc_bf16_f32(128, 64, true);
       const uint64_t dQhi = smem_desc_sw128(base + C::kQhi), dQlo = smem_desc_sw128(base + C::kQlo);
-      // S_j into buffer j % 2 (its previous scores, S_{j-2}, were read before P_{j-2} was ready)
-      auto issue_s = [&](int j) -> bool {
+      if (!wait_all(smem_addr(&q_ready), 0)) failed = true;
+      for (int j = 0; j < n_steps && !failed; ++j) {
         const int st = j % C::kStages;
-        if (!mbar_wait_bounded(smem_addr(&k_full[st]), (j / C::kStages) & 1)) return false;
+        // S_j goes into the buffer of S_{j-2} / P_{j-2}: once P_{j-2} V_{j-2} is done
+        if (j >= 2 && !wait_all(smem_addr(&pv_done[j & 1]), ((j - 2) >> 1) & 1)) failed = true;
+        if (failed || !wait_all(smem_addr(&k_full[st]), (j / C::kStages) & 1)) {
+          failed = true;
+          break;
+        }
         tc_fence_after();
         const uint64_t dK = smem_desc_sw128(kst(st));
         // K-major tiles: a 16-element K step is 32 bytes along the swizzled
@@ -371,25 +382,13 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         for (int k = 0; k < 4; ++k) umma_bf16(tS(j), dQlo + 2 * k, dK + 2 * k, idS, true);
         umma_commit(smem_addr(&k_empty[st]));
         umma_commit(smem_addr(&s_full[j & 1]));
-        return true;
-      };
-      if (!mbar_wait_bounded(smem_addr(&q_ready), 0) || !issue_s(0)) failed = true;
+      }
+    } else {
+      constexpr uint32_t idPV = idesc_bf16_f32(128, 64, true);
       for (int j = 0; j < n_steps && !failed; ++j) {
         const int st = j % C::kStages;
-        // S_{j+1} goes into the buffer of S_{j-1} / P_{j-1}: once P_{j-1} V_{j-1} is done
-        if (j + 1 < n_steps) {
-          if (j > 0 && !mbar_wait_bounded(smem_addr(&pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1)) {
-            failed = true;
-            break;
-          }
-          tc_fence_after();
-          if (!issue_s(j + 1)) {
-            failed = true;
-            break;
-          }
-        }
-        if (!mbar_wait_bounded(smem_addr(&p_full[j & 1]), (j >> 1) & 1) ||
-            !mbar_wait_bounded(smem_addr(&v_full[st]), (j / C::kStages) & 1)) {
+        if (!wait_all(smem_addr(&p_full[j & 1]), (j >> 1) & 1) ||
+            !wait_all(smem_addr(&v_full[st]), (j / C::kStages) & 1)) {
           failed = true;
           break;
         }
@@ -404,10 +403,10 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         umma_commit(smem_addr(&v_empty[st]));
         umma_commit(smem_addr(&pv_done[j & 1]));
       }
-      if (failed) {  // let the MMAs already issued finish before the memory goes away
-        umma_commit(smem_addr(&drain));
-        mbar_wait_bounded(smem_addr(&drain), 0);
-      }
+    }
+    if (failed) {  // let this warp's products already issued finish before the memory goes away
+      umma_commit(smem_addr(&drain[warp - 9]));
+      mbar_wait_bounded(smem_addr(&drain[warp - 9]), 0);
     }
   } else {
     // ---- softmax and epilogue: row r = tid % 128 (tensor-memory lane r), column half hf ----

@@ -66,35 +66,45 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_ma
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-// D (tensor memory) [+]= A (shared) x B (shared), issued by one thread.
+// D (tensor memory) [+]= A (shared) x B (shared). Called by a whole warp,
+// converged, with warp-uniform arguments; one lane (elect.sync) issues it.
+// Issuing from a converged warp keeps the operands in uniform registers: a
+// single thread issuing (the rest of its warp inactive) was measured to issue
+// M = 128, N = 64 products up to three times more slowly whenever other warps
+// kept the same SM sub-partition busy.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, bool accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
       : "memory");
 }
 
-// D (tensor memory) [+]= A (tensor memory) x B (shared), issued by one thread.
+// D (tensor memory) [+]= A (tensor memory) x B (shared), issued like umma_bf16.
 // A is M = 128 lanes x K bf16, two elements per 32-bit column (element 2c in
 // the low half of column c), so a K = 16 step spans 8 columns.
 __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                                  uint32_t idesc, bool accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, e;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
       : "memory");
 }
 
-// Arrive (once) on the mbarrier when every MMA this thread issued before has
-// completed.
+// Arrive (once) on the mbarrier when every MMA issued before has completed.
+// Called by the issuing warp, converged; one lane issues it.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
 }
 
 // 32 consecutive columns of this warp's 32 lanes: lane l gets row l's values.
