@@ -49,6 +49,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// The same, called by a whole warp, converged, with warp-uniform arguments:
+// one elected lane arrives.
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(bar), "r"(bytes)
+      : "memory");
+}
+
 // Raise the phase's expected transaction bytes without arriving.
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -94,6 +104,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// The same, called by a whole warp, converged, with warp-uniform arguments:
+// one elected lane issues the copy (a lone thread issuing was measured to fall
+// far behind when other warps kept its SM sub-partition busy).
+__device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const void* map, int x, int y,
+                                                  uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n\t}" ::"r"(dst),
       "l"(map), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }

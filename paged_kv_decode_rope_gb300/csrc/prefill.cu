@@ -192,19 +192,22 @@ struct PrefillAttnParams {
 // Warps 0-7 run the softmax and the epilogue, two threads per row (warps w
 // and w + 4 share tensor-memory lanes 32 (w % 4) ..; one takes columns 0-31,
 // the other 32-63, and they exchange row maxima and sums through shared
-// memory), warp 8 issues the TMA copies
-// (each page's 16 K rows into the stage's K tile and its 16 V rows into the
-// V tile, with separate barriers so K of a later step can load as soon as
-// its stage's scores are done), and one thread of warp 9 issues the MMAs:
-// S_{j+1} goes out before P_j is ready, so the tensor core computes the next
-// scores while the softmax works on these. Every wait is bounded.
+// memory), warp 8 issues the TMA copies of the K rows (each page's 16 K rows
+// into the stage's K tile) and warp 11 those of the V rows (into the V tile),
+// with separate barriers so K of a later step loads as soon as its stage's
+// scores are done, warp 9 issues the score products and warp 10 the P V
+// products. S_j goes out as soon as its buffer and K tile are free, so the
+// tensor core computes the next scores while the softmax works on these.
+// Every issuing warp runs converged and one elected lane issues (a lone
+// thread issuing fell far behind while the softmax warps kept its SM
+// sub-partition busy). Every wait is bounded.
 template <int G>
 struct TcCfg {
   static constexpr int kTokens = 128 / G;
   static constexpr int kRows = kTokens * G;  // <= 128; rows past it are padding
   static constexpr int kStages = 4;
   static constexpr int kSoftmaxThreads = 256;
-  static constexpr int kThreads = kSoftmaxThreads + 96;
+  static constexpr int kThreads = kSoftmaxThreads + 128;
   static constexpr uint32_t kTile = 128 * 128;  // a 128-row x 128-byte operand tile
   static constexpr uint32_t kStep = 64 * 128;   // 64 K rows (or V rows) of one step
   // dynamic shared memory: Q_hi, Q_lo, then per stage K and V
@@ -283,12 +286,18 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   auto tS = [&](int j) { return tmem + 64 * (j & 1); };  // S_j, then P_j (hi: +0, lo: +32)
   bool failed = false;
 
-  if (warp == 8) {
-    // ---- TMA producer: step j's four pages into stage j % kStages. The
-    // warp reads the page ids 32 at a time (lane i: page 32 m + i), the next
-    // 32 while it issues the current ones, so no step waits for a block-table
-    // load; lane 0 issues the copies. ----
-    int k_issued = 0, v_issued = 0;
+  if (warp == 8 || warp == 11) {
+    // ---- TMA producers, warp 8 for K and warp 11 for V: step j's four
+    // pages into stage j % kStages. A warp reads the page ids 32 at a time
+    // (lane i: page 32 m + i), the next 32 while it issues the current ones,
+    // so no step waits for a block-table load; the whole warp runs the loop
+    // and one elected lane issues each copy. K and V have a warp each so
+    // that the K copies, needed first, never queue behind a wait for a V
+    // stage. ----
+    const int kind = warp == 8 ? 0 : 1;  // 0: K rows, 1: V rows
+    uint64_t* full = kind ? v_full : k_full;
+    uint64_t* empty = kind ? v_empty : k_empty;
+    int issued = 0;
     int pid = lane < n_pages ? bt[lane] : -1;
     int pid_next = 32 + lane < n_pages ? bt[32 + lane] : -1;
     for (int j = 0; j < n_steps && !failed; ++j) {
@@ -314,44 +323,27 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         pages[q] = page;
         bytes += kHalfBytes;
       }
-      if (bad && lane == 0) atomicOr(p.err, PKV_ERR_PAGE_ID);
-      // K tile: free once the stage's scores are done
-      if (use > 0 && !mbar_wait_bounded(smem_addr(&k_empty[st]), (use - 1) & 1)) failed = true;
+      if (bad && kind == 0 && lane == 0) atomicOr(p.err, PKV_ERR_PAGE_ID);
+      // the stage is free once its scores (K) or its P V product (V) are done
+      if (use > 0 && !mbar_wait_bounded(smem_addr(&empty[st]), (use - 1) & 1)) failed = true;
       if (__any_sync(kFull, failed)) {
         failed = true;
         break;
       }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(smem_addr(&k_full[st]), bytes);
-        for (int q = 0; q < 4; ++q)
-          if (pages[q] >= 0)
-            tma_load_2d(kst(st) + q * kHalfBytes, &kv16_map, 0, (pages[q] * p.hkv + h) * (2 * kPage),
-                        smem_addr(&k_full[st]));
-      }
-      k_issued = j + 1;
-      // V tile: free once the stage's P V product is done
-      if (use > 0 && !mbar_wait_bounded(smem_addr(&v_empty[st]), (use - 1) & 1)) failed = true;
-      if (__any_sync(kFull, failed)) {
-        failed = true;
-        break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(smem_addr(&v_full[st]), bytes);
-        for (int q = 0; q < 4; ++q)
-          if (pages[q] >= 0)
-            tma_load_2d(vst(st) + q * kHalfBytes, &kv16_map, 0,
-                        (pages[q] * p.hkv + h) * (2 * kPage) + kPage, smem_addr(&v_full[st]));
-      }
-      v_issued = j + 1;
+      const uint32_t dst = (kind ? vst(st) : kst(st)), bar = smem_addr(&full[st]);
+      mbar_arrive_expect_tx_elect(bar, bytes);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (pages[q] >= 0)
+          tma_load_2d_elect(dst + q * kHalfBytes, &kv16_map, 0, (pages[q] * p.hkv + h) * (2 * kPage) + kind * kPage,
+                            bar);
+      issued = j + 1;
     }
     // let the copies still in flight (the last kStages steps at most) land
     // before shared memory goes away
-    if (failed && lane == 0) {
-      for (int j = max(0, k_issued - C::kStages); j < k_issued; ++j)
-        mbar_wait_bounded(smem_addr(&k_full[j % C::kStages]), (j / C::kStages) & 1);
-      for (int j = max(0, v_issued - C::kStages); j < v_issued; ++j)
-        mbar_wait_bounded(smem_addr(&v_full[j % C::kStages]), (j / C::kStages) & 1);
-    }
+    if (failed && lane == 0)
+      for (int j = max(0, issued - C::kStages); j < issued; ++j)
+        mbar_wait_bounded(smem_addr(&full[j % C::kStages]), (j / C::kStages) & 1);
   } else if (warp == 9 || warp == 10) {
     // ---- MMA issuers, each a whole warp, converged (one lane issues each
     // product; every wait's result is made warp-uniform): warp 9 the score
