@@ -298,32 +298,32 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     uint64_t* full = kind ? v_full : k_full;
     uint64_t* empty = kind ? v_empty : k_empty;
     int issued = 0;
-    int pid = lane < n_pages ? bt[lane] : -1;
+    // lane i: the copy's row coordinate for page 32 m + i of window m (-1:
+    // past the last page, or a bad id), and the window's valid pages as a
+    // bit mask; worked out once per window of eight steps
+    uint32_t valid = 0;
+    auto window = [&](int pid, int m) {
+      const int pg = 32 * m + lane;
+      const bool in = pg < n_pages;
+      const bool ok = in && pid >= 0 && static_cast<long long>(pid) < p.num_pages;
+      if (kind == 0 && __any_sync(kFull, in && !ok) && lane == 0) atomicOr(p.err, PKV_ERR_PAGE_ID);
+      valid = __ballot_sync(kFull, ok);
+      return ok ? (pid * p.hkv + h) * (2 * kPage) + kind * kPage : -1;
+    };
+    int row = window(lane < n_pages ? bt[lane] : -1, 0);
     int pid_next = 32 + lane < n_pages ? bt[32 + lane] : -1;
     for (int j = 0; j < n_steps && !failed; ++j) {
       const int st = j % C::kStages, use = j / C::kStages;
       if (j > 0 && (j & 7) == 0) {  // the next 32 pages
-        pid = pid_next;
+        row = window(pid_next, j >> 3);
         const int nxt = 4 * j + 32 + lane;
         pid_next = nxt < n_pages ? bt[nxt] : -1;
       }
-      int pages[4];
-      uint32_t bytes = 0;
-      int bad = 0;
+      const int l0 = (4 * j) & 31;
+      const uint32_t vbits = (valid >> l0) & 0xFu;
+      int rows[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int pg = 4 * j + q;
-        const int page = __shfl_sync(kFull, pid, (4 * j + q) & 31);
-        pages[q] = -1;
-        if (pg >= n_pages) continue;
-        if (page < 0 || static_cast<long long>(page) >= p.num_pages) {
-          bad = 1;
-          continue;
-        }
-        pages[q] = page;
-        bytes += kHalfBytes;
-      }
-      if (bad && kind == 0 && lane == 0) atomicOr(p.err, PKV_ERR_PAGE_ID);
+      for (int q = 0; q < 4; ++q) rows[q] = __shfl_sync(kFull, row, l0 + q);
       // the stage is free once its scores (K) or its P V product (V) are done
       if (use > 0 && !mbar_wait_bounded(smem_addr(&empty[st]), (use - 1) & 1)) failed = true;
       if (__any_sync(kFull, failed)) {
@@ -331,12 +331,10 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         break;
       }
       const uint32_t dst = (kind ? vst(st) : kst(st)), bar = smem_addr(&full[st]);
-      mbar_arrive_expect_tx_elect(bar, bytes);
+      mbar_arrive_expect_tx_elect(bar, static_cast<uint32_t>(__popc(vbits)) * kHalfBytes);
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (pages[q] >= 0)
-          tma_load_2d_elect(dst + q * kHalfBytes, &kv16_map, 0, (pages[q] * p.hkv + h) * (2 * kPage) + kind * kPage,
-                            bar);
+        if ((vbits >> q) & 1u) tma_load_2d_elect(dst + q * kHalfBytes, &kv16_map, 0, rows[q], bar);
       issued = j + 1;
     }
     // let the copies still in flight (the last kStages steps at most) land
