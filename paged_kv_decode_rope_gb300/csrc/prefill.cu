@@ -181,7 +181,7 @@ struct PrefillAttnParams {
 // A tile is TcCfg<G>::kTokens chunk tokens x G query heads = up to 128 rows
 // (row R = token R / G, head R % G): the M = 128 of one tcgen05 MMA. Keys go
 // in steps of 64 (four pages). Per step j:
-//   S_j = Q_hi K_j^T + Q_lo K_j^T    (tensor memory, 128 x 64 fp32, two buffers)
+//   S_j = Q_hi K_j^T + Q_lo K_j^T    (tensor memory, 128 x 64 fp32, three buffers)
 //   softmax warps: row R = tensor-memory lane R, one thread per row
 //   O += P_hi V_j + P_lo V_j         (tensor memory, 128 x 64 fp32; P in tensor memory)
 // Q and P enter as bf16 plus their bf16 rounding remainders (each about 16
@@ -216,12 +216,13 @@ struct TcCfg {
   static constexpr uint32_t kBytes = kStage0 + kStages * 2 * kStep;
 };
 constexpr float kSlack = 8.f;
-// tensor memory: S buffers in columns 0-63 and 64-127, O in 128-191. Step
-// j's P is written over its own S: P_hi in the buffer's first 32 columns and
-// P_lo in the next 32 (two bf16 keys per column), so P is double-buffered
-// with S, and a softmax step does not wait for the previous step's P V
-// (only to rescale O). Columns 192-255 are unused (allocations are powers of
-// two).
+// tensor memory: three S buffers in columns 0-63, 64-127 and 128-191 (step j
+// uses buffer j % 3), O in 192-255. Step j's P is written over its own S:
+// P_hi in the buffer's first 32 columns and P_lo in the next 32 (two bf16
+// keys per column). A softmax step does not wait for the previous step's
+// P V (only to rescale O), and S_j goes into the buffer of P_{j-3}, whose
+// product is normally long done.
+constexpr int kSBufs = 3;
 constexpr uint32_t kTmemCols = 256;
 
 template <int G>
@@ -231,7 +232,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   extern __shared__ __align__(1024) uint8_t dsmem[];
   __shared__ __align__(8) uint64_t k_full[C::kStages], k_empty[C::kStages];
   __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
-  __shared__ __align__(8) uint64_t s_full[2], q_ready, p_full[2], pv_done[2], drain[2];
+  __shared__ __align__(8) uint64_t s_full[kSBufs], q_ready, p_full[kSBufs], pv_done[kSBufs], drain[2];
   __shared__ uint32_t s_tmem;
   __shared__ float s_xchg[2][2][128];  // [step parity][column half][row]: row maxima
   __shared__ float s_lsum[2][128];     // [column half][row]: the halves' sums
@@ -266,15 +267,14 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       mbar_init(smem_addr(&v_full[st]), 1);
       mbar_init(smem_addr(&v_empty[st]), 1);
     }
-    mbar_init(smem_addr(&s_full[0]), 1);
-    mbar_init(smem_addr(&s_full[1]), 1);
     mbar_init(smem_addr(&q_ready), C::kSoftmaxThreads);
-    // P_j ready and P_j V_j done, one barrier per buffer (j & 1): a wait
-    // for step j never sees a barrier two phases on
-    mbar_init(smem_addr(&p_full[0]), C::kSoftmaxThreads);
-    mbar_init(smem_addr(&p_full[1]), C::kSoftmaxThreads);
-    mbar_init(smem_addr(&pv_done[0]), 1);
-    mbar_init(smem_addr(&pv_done[1]), 1);
+    // S_j done, P_j ready and P_j V_j done, one barrier each per buffer
+    // (j % 3): a wait for step j never sees its barrier two phases on
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(smem_addr(&s_full[i]), 1);
+      mbar_init(smem_addr(&p_full[i]), C::kSoftmaxThreads);
+      mbar_init(smem_addr(&pv_done[i]), 1);
+    }
     mbar_init(smem_addr(&drain[0]), 1);
     mbar_init(smem_addr(&drain[1]), 1);
   }
@@ -282,8 +282,10 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = s_tmem, tO = tmem + 128;
-  auto tS = [&](int j) { return tmem + 64 * (j & 1); };  // S_j, then P_j (hi: +0, lo: +32)
+  const uint32_t tmem = s_tmem, tO = tmem + 64 * kSBufs;
+  auto tS = [&](int j) { return tmem + 64 * (j % kSBufs); };  // S_j, then P_j (hi: +0, lo: +32)
+  auto buf = [](int j) { return j % kSBufs; };                   // step j's S / P / P V barriers
+  auto par = [](int j) { return static_cast<uint32_t>((j / kSBufs) & 1); };  // and their phase parity
   bool failed = false;
 
   if (warp == 8 || warp == 11) {
@@ -356,8 +358,8 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       if (!wait_all(smem_addr(&q_ready), 0)) failed = true;
       for (int j = 0; j < n_steps && !failed; ++j) {
         const int st = j % C::kStages;
-        // S_j goes into the buffer of S_{j-2} / P_{j-2}: once P_{j-2} V_{j-2} is done
-        if (j >= 2 && !wait_all(smem_addr(&pv_done[j & 1]), ((j - 2) >> 1) & 1)) failed = true;
+        // S_j goes into the buffer of P_{j-3}: once P_{j-3} V_{j-3} is done
+        if (j >= kSBufs && !wait_all(smem_addr(&pv_done[buf(j)]), par(j - kSBufs))) failed = true;
         if (failed || !wait_all(smem_addr(&k_full[st]), (j / C::kStages) & 1)) {
           failed = true;
           break;
@@ -371,13 +373,13 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
 #pragma unroll
         for (int k = 0; k < 4; ++k) umma_bf16(tS(j), dQlo + 2 * k, dK + 2 * k, idS, true);
         umma_commit(smem_addr(&k_empty[st]));
-        umma_commit(smem_addr(&s_full[j & 1]));
+        umma_commit(smem_addr(&s_full[buf(j)]));
       }
     } else {
       constexpr uint32_t idPV = idesc_bf16_f32(128, 64, true);
       for (int j = 0; j < n_steps && !failed; ++j) {
         const int st = j % C::kStages;
-        if (!wait_all(smem_addr(&p_full[j & 1]), (j >> 1) & 1) ||
+        if (!wait_all(smem_addr(&p_full[buf(j)]), par(j)) ||
             !wait_all(smem_addr(&v_full[st]), (j / C::kStages) & 1)) {
           failed = true;
           break;
@@ -391,7 +393,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
 #pragma unroll
         for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tS(j) + 32 + 8 * k, dV + 128 * k, idPV, true);
         umma_commit(smem_addr(&v_empty[st]));
-        umma_commit(smem_addr(&pv_done[j & 1]));
+        umma_commit(smem_addr(&pv_done[buf(j)]));
       }
     }
     if (failed) {  // let this warp's products already issued finish before the memory goes away
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         bad_nextwin = 32 * (j / 8 + 1) < n_pages ? bad_bits(j / 8 + 1) : 0u;
       }
       const int bad = static_cast<int>((bad_win >> ((4 * j) & 31)) & 0xFu);
-      if (!mbar_wait_bounded(smem_addr(&s_full[j & 1]), (j >> 1) & 1)) failed = true;
+      if (!mbar_wait_bounded(smem_addr(&s_full[buf(j)]), par(j))) failed = true;
       tc_fence_after();
       float sv[32];
       tmem_ld32(tS(j) + lane_addr + 32 * hf, sv);
@@ -484,7 +486,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         // move the reference up; O (this thread's half of the columns) and l
         // follow, once P_{j-1} V_{j-1}, the last product into O, is done
         if (j > 0 && m_ref != -INFINITY) {
-          if (!mbar_wait_bounded(smem_addr(&pv_done[(j - 1) & 1]), ((j - 1) >> 1) & 1)) failed = true;
+          if (!mbar_wait_bounded(smem_addr(&pv_done[buf(j - 1)]), par(j - 1))) failed = true;
           tc_fence_after();
           const float alpha = fast_exp2(m_ref - mx);
           l_sum *= alpha;
@@ -531,16 +533,16 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(smem_addr(&p_full[j & 1]));
+      mbar_arrive(smem_addr(&p_full[buf(j)]));
     }
     // epilogue: O / l for the live rows, l being the sum of both halves' sums
     s_lsum[hf][r] = l_sum;
     pair_sync();
     const float l_row = l_sum + s_lsum[hf ^ 1][r];
-    // the last product into O is P V of step n_steps - 1 (products of the
-    // same barrier complete in order; the one before it, step n_steps - 3,
-    // was done before S of step n_steps - 1 was issued)
-    if (!failed && mbar_wait_bounded(smem_addr(&pv_done[(n_steps - 1) & 1]), ((n_steps - 1) >> 1) & 1)) {
+    // the last product into O is P V of step n_steps - 1 (the one before it
+    // on the same barrier, step n_steps - 4, was done before S of step
+    // n_steps - 1 was issued)
+    if (!failed && mbar_wait_bounded(smem_addr(&pv_done[buf(n_steps - 1)]), par(n_steps - 1))) {
       tc_fence_after();
       float o[32];
       tmem_ld32(tO + lane_addr + 32 * hf, o);
