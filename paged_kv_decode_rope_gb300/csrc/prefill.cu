@@ -225,6 +225,40 @@ constexpr float kSlack = 8.f;
 constexpr int kSBufs = 3;
 constexpr uint32_t kTmemCols = 256;
 
+// Two fp32 values in one 64-bit register, and the paired fp32 arithmetic of
+// sm_100 and later (each half rounded exactly as the scalar operation).
+__device__ __forceinline__ uint64_t f32x2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 unpack_f32x2(uint64_t v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return make_float2(a, b);
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max of three floats in one instruction (sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 template <int G>
 __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap kv16_map, const PrefillAttnParams p) {
@@ -468,13 +502,15 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         for (int i = 0; i < 32; ++i)
           if (k0 + i > pos || ((bad >> (2 * hf + (i >> 4))) & 1)) sv[i] = -INFINITY;
       }
-      float mt[8];
+      // this half's maximum, with three-input maxima (32 -> 11 -> 4 -> 1)
+      float mt[11];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mt[i] = fmaxf(fmaxf(sv[4 * i], sv[4 * i + 1]), fmaxf(sv[4 * i + 2], sv[4 * i + 3]));
+      for (int i = 0; i < 10; ++i) mt[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
+      mt[10] = fmaxf(sv[30], sv[31]);
 #pragma unroll
-      for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-        for (int i = 0; i < w; ++i) mt[i] = fmaxf(mt[i], mt[i + w]);
+      for (int i = 0; i < 3; ++i) mt[i] = fmax3(mt[3 * i], mt[3 * i + 1], mt[3 * i + 2]);
+      mt[3] = fmaxf(mt[9], mt[10]);
+      mt[0] = fmaxf(fmax3(mt[0], mt[1], mt[2]), mt[3]);
       // the row's maximum: this half's and the partner thread's (the barrier
       // also means both halves have read S_j, whose columns P_j overwrites)
       s_xchg[j & 1][hf][r] = mt[0];
@@ -493,8 +529,13 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
           float o[32];
           tmem_ld32(tO + lane_addr + 32 * hf, o);
           tmem_wait_ld();
+          const uint64_t aa = f32x2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          for (int i = 0; i < 32; i += 2) {
+            const float2 v = unpack_f32x2(mul_f32x2(f32x2(o[i], o[i + 1]), aa));
+            o[i] = v.x;
+            o[i + 1] = v.y;
+          }
           tmem_st32(tO + lane_addr + 32 * hf, o);
           tmem_wait_st();
         }
@@ -503,22 +544,30 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       // P = exp2(S - m_ref) as bf16 high part and remainder, into tensor
       // memory over S_j: this thread's 32 keys are columns 16 hf .. 16 hf + 15
       // of each half
+      // (pairs of keys in paired fp32 arithmetic; the row sum in four
+      // partial sums, keys 4i + c into sum c)
       const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // all scores -inf: P = 0
-      float lp[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t mm = f32x2(m_use, m_use);
+      uint64_t lp[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
       uint32_t hi[16], lo[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const float p0 = fast_exp2(sv[2 * e] - m_use);
-        const float p1 = fast_exp2(sv[2 * e + 1] - m_use);
-        lp[e & 3] += p0 + p1;
+        const float2 d = unpack_f32x2(sub_f32x2(f32x2(sv[2 * e], sv[2 * e + 1]), mm));
+        const float p0 = fast_exp2(d.x), p1 = fast_exp2(d.y);
+        const uint64_t pp = f32x2(p0, p1);
+        lp[e & 1] = add_f32x2(lp[e & 1], pp);
         hi[e] = pack_bf16x2(p0, p1);
         const float2 f = bf16x2_to_float2(hi[e]);
-        lo[e] = pack_bf16x2(p0 - f.x, p1 - f.y);
+        const float2 rem = unpack_f32x2(sub_f32x2(pp, f32x2(f.x, f.y)));
+        lo[e] = pack_bf16x2(rem.x, rem.y);
       }
       tmem_st16u(tS(j) + lane_addr + 16 * hf, hi);
       tmem_st16u(tS(j) + lane_addr + 32 + 16 * hf, lo);
       tmem_wait_st();
-      l_sum += (lp[0] + lp[1]) + (lp[2] + lp[3]);
+      {
+        const float2 a = unpack_f32x2(lp[0]), b = unpack_f32x2(lp[1]);
+        l_sum += (a.x + a.y) + (b.x + b.y);
+      }
       // V rows that hold no key of the tile (past its last position, or of a
       // page with a bad id) are zeroed once the stage's V copies have landed,
       // so that their bits cannot reach O
