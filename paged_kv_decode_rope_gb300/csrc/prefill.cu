@@ -579,8 +579,8 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
           if (64 * j + key > last_pos || ((bad >> (key >> 4)) & 1))
             *reinterpret_cast<uint4*>(vrow + key * 128 + (idx & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
+        fence_proxy_async_smem();  // the zeroed rows, before the tensor core reads V
       }
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_addr(&p_full[buf(j)]));
     }
