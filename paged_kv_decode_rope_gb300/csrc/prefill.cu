@@ -252,6 +252,19 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
+// Bounded wait for the copy and product warps, which are normally ahead of
+// the softmax: after a first test, they sleep between tests instead of
+// polling, so that their spinning does not take issue slots from the softmax
+// warps on the same sub-partition.
+__device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    __nanosleep(32);
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  return false;
+}
+
 // max of three floats in one instruction (sm_100 and later)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -361,7 +374,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
 #pragma unroll
       for (int q = 0; q < 4; ++q) rows[q] = __shfl_sync(kFull, row, l0 + q);
       // the stage is free once its scores (K) or its P V product (V) are done
-      if (use > 0 && !mbar_wait_bounded(smem_addr(&empty[st]), (use - 1) & 1)) failed = true;
+      if (use > 0 && !mbar_wait_idle(smem_addr(&empty[st]), (use - 1) & 1)) failed = true;
       if (__any_sync(kFull, failed)) {
         failed = true;
         break;
@@ -384,7 +397,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     // products, warp 10 the P V products. A commit covers only its own
     // warp's products. ----
     auto wait_all = [&](uint32_t bar, uint32_t parity) {
-      return __all_sync(kFull, mbar_wait_bounded(bar, parity)) != 0;
+      return __all_sync(kFull, mbar_wait_idle(bar, parity)) != 0;
     };
     if (warp == 9) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 64, false);
