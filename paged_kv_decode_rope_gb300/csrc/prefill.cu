@@ -182,7 +182,7 @@ struct PrefillAttnParams {
 // (row R = token R / G, head R % G): the M = 128 of one tcgen05 MMA. Keys go
 // in steps of 64 (four pages). Per step j:
 //   S_j = Q_hi K_j^T + Q_lo K_j^T    (tensor memory, 128 x 64 fp32, three buffers)
-//   softmax warps: row R = tensor-memory lane R, one thread per row
+//   softmax warps: P_j = exp2(S_j - m) over S_j's columns, row R = tensor-memory lane R
 //   O += P_hi V_j + P_lo V_j         (tensor memory, 128 x 64 fp32; P in tensor memory)
 // Q and P enter as bf16 plus their bf16 rounding remainders (each about 16
 // bits), as in the decode. The softmax keeps a reference maximum per row and
@@ -200,7 +200,8 @@ struct PrefillAttnParams {
 // tensor core computes the next scores while the softmax works on these.
 // Every issuing warp runs converged and one elected lane issues (a lone
 // thread issuing fell far behind while the softmax warps kept its SM
-// sub-partition busy). Every wait is bounded.
+// sub-partition busy); these warps, normally ahead of the softmax, sleep
+// between barrier tests. Every wait is bounded.
 template <int G>
 struct TcCfg {
   static constexpr int kTokens = 128 / G;
