@@ -532,29 +532,32 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       pair_sync();
       tc_fence_after();
       const float mx = fmaxf(mt[0], s_xchg[j & 1][hf ^ 1][r]);
-      if (mx > m_ref + kSlack) {
-        // move the reference up; O (this thread's half of the columns) and l
-        // follow, once P_{j-1} V_{j-1}, the last product into O, is done
-        if (j > 0 && m_ref != -INFINITY) {
-          if (!mbar_wait_bounded(smem_addr(&pv_done[buf(j - 1)]), par(j - 1))) failed = true;
-          tc_fence_after();
-          const float alpha = fast_exp2(m_ref - mx);
-          l_sum *= alpha;
-          float o[32];
-          tmem_ld32(tO + lane_addr + 32 * hf, o);
-          tmem_wait_ld();
-          const uint64_t aa = f32x2(alpha, alpha);
+      // Move the reference up where a score passed it by more than kSlack;
+      // O (this thread's half of the columns) and l follow, O once P_{j-1}
+      // V_{j-1}, the last product into it, is done. The tensor-memory loads
+      // and stores are warp-wide, so a warp rescales O when any of its rows
+      // moves, the other rows by exactly 1.
+      const bool moves = mx > m_ref + kSlack;
+      const bool rescale = moves && j > 0 && m_ref != -INFINITY;
+      if (__any_sync(kFull, rescale)) {
+        if (!mbar_wait_bounded(smem_addr(&pv_done[buf(j - 1)]), par(j - 1))) failed = true;
+        tc_fence_after();
+        const float alpha = rescale ? fast_exp2(m_ref - mx) : 1.f;
+        l_sum *= alpha;
+        float o[32];
+        tmem_ld32(tO + lane_addr + 32 * hf, o);
+        tmem_wait_ld();
+        const uint64_t aa = f32x2(alpha, alpha);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 v = unpack_f32x2(mul_f32x2(f32x2(o[i], o[i + 1]), aa));
-            o[i] = v.x;
-            o[i + 1] = v.y;
-          }
-          tmem_st32(tO + lane_addr + 32 * hf, o);
-          tmem_wait_st();
+        for (int i = 0; i < 32; i += 2) {
+          const float2 v = unpack_f32x2(mul_f32x2(f32x2(o[i], o[i + 1]), aa));
+          o[i] = v.x;
+          o[i + 1] = v.y;
         }
-        m_ref = mx;
+        tmem_st32(tO + lane_addr + 32 * hf, o);
+        tmem_wait_st();
       }
+      if (moves) m_ref = mx;
       // P = exp2(S - m_ref) as bf16 high part and remainder, into tensor
       // memory over S_j: this thread's 32 keys are columns 16 hf .. 16 hf + 15
       // of each half
@@ -603,9 +606,11 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     pair_sync();
     const float l_row = l_sum + s_lsum[hf ^ 1][r];
     // the last product into O is P V of step n_steps - 1 (the one before it
-    // on the same barrier, step n_steps - 4, was done before S of step
-    // n_steps - 1 was issued)
-    if (!failed && mbar_wait_bounded(smem_addr(&pv_done[buf(n_steps - 1)]), par(n_steps - 1))) {
+    // on the same barrier, of step n_steps - 1 - kSBufs, was done before S of
+    // step n_steps - 1 was issued). The decision is warp-uniform: the
+    // tensor-memory load below is warp-wide.
+    const bool done = !failed && mbar_wait_bounded(smem_addr(&pv_done[buf(n_steps - 1)]), par(n_steps - 1));
+    if (__all_sync(kFull, done)) {
       tc_fence_after();
       float o[32];
       tmem_ld32(tO + lane_addr + 32 * hf, o);
