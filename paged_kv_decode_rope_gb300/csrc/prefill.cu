@@ -282,8 +282,6 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   __shared__ __align__(8) uint64_t v_full[C::kStages], v_empty[C::kStages];
   __shared__ __align__(8) uint64_t s_full[kSBufs], q_ready, p_full[kSBufs], pv_done[kSBufs], drain[2];
   __shared__ uint32_t s_tmem;
-  __shared__ float s_xchg[2][2][128];  // [step parity][column half][row]: row maxima
-  __shared__ float s_lsum[2][128];     // [column half][row]: the halves' sums
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (static_cast<int>(blockIdx.x) >= *p.num_tiles) return;
   const int4 tile = p.tiles[blockIdx.x];
@@ -449,29 +447,46 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       mbar_wait_bounded(smem_addr(&drain[warp - 9]), 0);
     }
   } else {
-    // ---- softmax and epilogue: row r = tid % 128 (tensor-memory lane r), column half hf ----
-    const int r = tid & 127, hf = tid >> 7;
-    const int t = r / G, gi = r - t * G;
-    const bool live = r < C::kRows && t < n_ok;
-    const int pos = pos0 + min(t, n_ok - 1);
-    const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    auto pair_sync = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
-    // Q rows: scaled, as bf16 high part and remainder, 128-byte swizzled
-    // (this thread: dims 32 hf .. 32 hf + 31, chunks 4 hf .. 4 hf + 3)
-    {
-      float x[32];
-      const float* qr = p.q_rot + (static_cast<size_t>(row0 + (live ? t : 0)) * p.hq + h * G + gi) * kHeadDim + 32 * hf;
+    // ---- softmax and epilogue. Warp w owns rows L .. L + 15, L = 32 (w % 4)
+    // + 16 (w / 4) (tensor-memory lanes). Its thread t holds rows L + t / 4
+    // (hh = 0) and L + t / 4 + 8 (hh = 1) and, of each, the key pairs
+    // 8 i + 2 q and 8 i + 2 q + 1 (i = 0..7, q = t % 4): the 16x256b layout,
+    // in which S word 4 i + 2 hh + e is key 8 i + 2 q + e of row hh. The four
+    // threads of a row are lanes of one warp, so row maxima and sums combine
+    // by shuffles, and the warp's reads of S_j are done before its P_j stores
+    // over the same columns.
+    const int q = lane & 3;
+    const int lrow = 32 * (warp & 3) + 16 * (warp >> 2);  // the warp's first row
+    const uint32_t lane_addr = static_cast<uint32_t>(lrow) << 16;
+    int tok[2], gix[2], pos[2];
+    bool live[2];
 #pragma unroll
-      for (int d = 0; d < 32; d += 4) {
-        const float4 v = live ? *reinterpret_cast<const float4*>(qr + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int hh = 0; hh < 2; ++hh) {
+      const int rw = lrow + (lane >> 2) + 8 * hh;
+      tok[hh] = rw / G;
+      gix[hh] = rw - tok[hh] * G;
+      live[hh] = rw < C::kRows && tok[hh] < n_ok;
+      pos[hh] = pos0 + min(tok[hh], n_ok - 1);
+    }
+    // Q rows: scaled, as bf16 high part and remainder, 128-byte swizzled
+    // (this thread: dims 16 q .. 16 q + 15 of its two rows, chunks 2 q and 2 q + 1)
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int rw = lrow + (lane >> 2) + 8 * hh;
+      const float* qr =
+          p.q_rot + (static_cast<size_t>(row0 + (live[hh] ? tok[hh] : 0)) * p.hq + h * G + gix[hh]) * kHeadDim + 16 * q;
+      float x[16];
+#pragma unroll
+      for (int d = 0; d < 16; d += 4) {
+        const float4 v = live[hh] ? *reinterpret_cast<const float4*>(qr + d) : make_float4(0.f, 0.f, 0.f, 0.f);
         x[d] = v.x * p.qscale;
         x[d + 1] = v.y * p.qscale;
         x[d + 2] = v.z * p.qscale;
         x[d + 3] = v.w * p.qscale;
       }
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int c = 4 * hf + cc;
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * q + cc;
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -480,14 +495,15 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
           const float2 f = bf16x2_to_float2(hi[e]);
           lo[e] = pack_bf16x2(a0 - f.x, a1 - f.y);
         }
-        const uint32_t off = r * 128 + ((c ^ (r & 7)) << 4);
+        const uint32_t off = rw * 128 + ((c ^ (rw & 7)) << 4);
         *reinterpret_cast<uint4*>(gbase + C::kQhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(gbase + C::kQlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_addr(&q_ready));
     }
-    float m_ref = -INFINITY, l_sum = 0.f;
+    fence_proxy_async_smem();
+    mbar_arrive(smem_addr(&q_ready));
+
+    float m_ref[2] = {-INFINITY, -INFINITY}, l_sum[2] = {0.f, 0.f};
     // which pages have a bad id: bit i of bad_win for page 32 m + i, from the
     // warp's window of page ids (lane i reads page 32 m + i), the next window
     // loaded while this one is used
@@ -499,7 +515,7 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     uint32_t bad_win = bad_bits(0), bad_nextwin = n_pages > 32 ? bad_bits(1) : 0u;
     for (int j = 0; j < n_steps; ++j) {
       const int st = j % C::kStages;
-      const int k0 = 64 * j + 32 * hf;  // key position of this thread's first column
+      const int kb = 64 * j + 2 * q;  // key position of this thread's first key
       if (j > 0 && (j & 7) == 0) {
         bad_win = bad_nextwin;
         bad_nextwin = 32 * (j / 8 + 1) < n_pages ? bad_bits(j / 8 + 1) : 0u;
@@ -508,82 +524,107 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       if (!mbar_wait_bounded(smem_addr(&s_full[buf(j)]), par(j))) failed = true;
       tc_fence_after();
       float sv[32];
-      tmem_ld32(tS(j) + lane_addr + 32 * hf, sv);
+      tmem_ld_16x256b_x8(tS(j) + lane_addr, sv);
       tmem_wait_ld();
-      // keys past the row's position, and pages with a bad id, get no weight
-      if (k0 + 31 > pos || bad) {
+      // keys past the row's position, and pages with a bad id (page i / 2 of
+      // the step holds pair i), get no weight
+      if (64 * j + 63 > pos[0] || bad) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (k0 + i > pos || ((bad >> (2 * hf + (i >> 4))) & 1)) sv[i] = -INFINITY;
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+              if (kb + 8 * i + e > pos[hh] || ((bad >> (i >> 1)) & 1)) sv[4 * i + 2 * hh + e] = -INFINITY;
       }
-      // this half's maximum, with three-input maxima (32 -> 11 -> 4 -> 1)
-      float mt[11];
+      // each row's maximum: this thread's 16 keys (three-input maxima), then
+      // the row's four threads (lanes 4 (t / 4) .. + 3)
+      float mx[2];
 #pragma unroll
-      for (int i = 0; i < 10; ++i) mt[i] = fmax3(sv[3 * i], sv[3 * i + 1], sv[3 * i + 2]);
-      mt[10] = fmaxf(sv[30], sv[31]);
+      for (int hh = 0; hh < 2; ++hh) {
+        float m6[6];
 #pragma unroll
-      for (int i = 0; i < 3; ++i) mt[i] = fmax3(mt[3 * i], mt[3 * i + 1], mt[3 * i + 2]);
-      mt[3] = fmaxf(mt[9], mt[10]);
-      mt[0] = fmaxf(fmax3(mt[0], mt[1], mt[2]), mt[3]);
-      // the row's maximum: this half's and the partner thread's (the barrier
-      // also means both halves have read S_j, whose columns P_j overwrites)
-      s_xchg[j & 1][hf][r] = mt[0];
-      tc_fence_before();
-      pair_sync();
-      tc_fence_after();
-      const float mx = fmaxf(mt[0], s_xchg[j & 1][hf ^ 1][r]);
+        for (int k = 0; k < 5; ++k) {
+          const int a = 3 * k, b2 = 3 * k + 1, c = 3 * k + 2;  // values a, b2, c of 0..15
+          m6[k] = fmax3(sv[4 * (a >> 1) + 2 * hh + (a & 1)], sv[4 * (b2 >> 1) + 2 * hh + (b2 & 1)],
+                        sv[4 * (c >> 1) + 2 * hh + (c & 1)]);
+        }
+        m6[5] = sv[4 * 7 + 2 * hh + 1];
+        float m = fmaxf(fmax3(m6[0], m6[1], m6[2]), fmax3(m6[3], m6[4], m6[5]));
+        m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+        mx[hh] = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+      }
       // Move the reference up where a score passed it by more than kSlack;
-      // O (this thread's half of the columns) and l follow, O once P_{j-1}
-      // V_{j-1}, the last product into it, is done. The tensor-memory loads
-      // and stores are warp-wide, so a warp rescales O when any of its rows
-      // moves, the other rows by exactly 1.
-      const bool moves = mx > m_ref + kSlack;
-      const bool rescale = moves && j > 0 && m_ref != -INFINITY;
-      if (__any_sync(kFull, rescale)) {
+      // O and l follow, O once P_{j-1} V_{j-1}, the last product into it, is
+      // done. The tensor-memory loads and stores are warp-wide, so a warp
+      // rescales O when any of its rows moves, the other rows by exactly 1.
+      bool moves[2], resc[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        moves[hh] = mx[hh] > m_ref[hh] + kSlack;
+        resc[hh] = moves[hh] && j > 0 && m_ref[hh] != -INFINITY;
+      }
+      if (__any_sync(kFull, resc[0] || resc[1])) {
         if (!mbar_wait_bounded(smem_addr(&pv_done[buf(j - 1)]), par(j - 1))) failed = true;
         tc_fence_after();
-        const float alpha = rescale ? fast_exp2(m_ref - mx) : 1.f;
-        l_sum *= alpha;
-        float o[32];
-        tmem_ld32(tO + lane_addr + 32 * hf, o);
-        tmem_wait_ld();
-        const uint64_t aa = f32x2(alpha, alpha);
+        uint64_t aa[2];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const float2 v = unpack_f32x2(mul_f32x2(f32x2(o[i], o[i + 1]), aa));
-          o[i] = v.x;
-          o[i + 1] = v.y;
+        for (int hh = 0; hh < 2; ++hh) {
+          const float alpha = resc[hh] ? fast_exp2(m_ref[hh] - mx[hh]) : 1.f;
+          l_sum[hh] *= alpha;
+          aa[hh] = f32x2(alpha, alpha);
         }
-        tmem_st32(tO + lane_addr + 32 * hf, o);
+        float o[32];
+        tmem_ld_16x256b_x8(tO + lane_addr, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int w = 4 * i + 2 * hh;
+            const float2 v = unpack_f32x2(mul_f32x2(f32x2(o[w], o[w + 1]), aa[hh]));
+            o[w] = v.x;
+            o[w + 1] = v.y;
+          }
+        tmem_st_16x256b_x8(tO + lane_addr, o);
         tmem_wait_st();
       }
-      if (moves) m_ref = mx;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        if (moves[hh]) m_ref[hh] = mx[hh];
       // P = exp2(S - m_ref) as bf16 high part and remainder, into tensor
-      // memory over S_j: this thread's 32 keys are columns 16 hf .. 16 hf + 15
-      // of each half
-      // (pairs of keys in paired fp32 arithmetic; the row sum in four
-      // partial sums, keys 4i + c into sum c)
-      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;  // all scores -inf: P = 0
-      const uint64_t mm = f32x2(m_use, m_use);
-      uint64_t lp[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
+      // memory over S_j (16x128b: word 2 i + hh is column 4 i + q, the pair
+      // 8 i + 2 q, + 1 of row hh; P_hi in columns 0-31, P_lo in 32-63), in
+      // paired fp32 arithmetic
+      uint64_t mm[2], lp[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float m_use = m_ref[hh] == -INFINITY ? 0.f : m_ref[hh];  // all scores -inf: P = 0
+        mm[hh] = f32x2(m_use, m_use);
+        lp[hh] = f32x2(0.f, 0.f);
+      }
       uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float2 d = unpack_f32x2(sub_f32x2(f32x2(sv[2 * e], sv[2 * e + 1]), mm));
-        const float p0 = fast_exp2(d.x), p1 = fast_exp2(d.y);
-        const uint64_t pp = f32x2(p0, p1);
-        lp[e & 1] = add_f32x2(lp[e & 1], pp);
-        hi[e] = pack_bf16x2(p0, p1);
-        const float2 f = bf16x2_to_float2(hi[e]);
-        const float2 rem = unpack_f32x2(sub_f32x2(pp, f32x2(f.x, f.y)));
-        lo[e] = pack_bf16x2(rem.x, rem.y);
-      }
-      tmem_st16u(tS(j) + lane_addr + 16 * hf, hi);
-      tmem_st16u(tS(j) + lane_addr + 32 + 16 * hf, lo);
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int w = 4 * i + 2 * hh;
+          const float2 d = unpack_f32x2(sub_f32x2(f32x2(sv[w], sv[w + 1]), mm[hh]));
+          const float p0 = fast_exp2(d.x), p1 = fast_exp2(d.y);
+          const uint64_t pp = f32x2(p0, p1);
+          lp[hh] = add_f32x2(lp[hh], pp);
+          hi[2 * i + hh] = pack_bf16x2(p0, p1);
+          const float2 f = bf16x2_to_float2(hi[2 * i + hh]);
+          const float2 rem = unpack_f32x2(sub_f32x2(pp, f32x2(f.x, f.y)));
+          lo[2 * i + hh] = pack_bf16x2(rem.x, rem.y);
+        }
+      tmem_st_16x128b_x8(tS(j) + lane_addr, hi);
+      tmem_st_16x128b_x8(tS(j) + lane_addr + 32, lo);
       tmem_wait_st();
-      {
-        const float2 a = unpack_f32x2(lp[0]), b = unpack_f32x2(lp[1]);
-        l_sum += (a.x + a.y) + (b.x + b.y);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float2 a = unpack_f32x2(lp[hh]);
+        l_sum[hh] += a.x + a.y;
       }
       // V rows that hold no key of the tile (past its last position, or of a
       // page with a bad id) are zeroed once the stage's V copies have landed,
@@ -601,11 +642,8 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       tc_fence_before();
       mbar_arrive(smem_addr(&p_full[buf(j)]));
     }
-    // epilogue: O / l for the live rows, l being the sum of both halves' sums
-    s_lsum[hf][r] = l_sum;
-    pair_sync();
-    const float l_row = l_sum + s_lsum[hf ^ 1][r];
-    // the last product into O is P V of step n_steps - 1 (the one before it
+    // epilogue: O / l for the live rows, l summed over the row's four threads.
+    // The last product into O is P V of step n_steps - 1 (the one before it
     // on the same barrier, of step n_steps - 1 - kSBufs, was done before S of
     // step n_steps - 1 was issued). The decision is warp-uniform: the
     // tensor-memory load below is warp-wide.
@@ -613,15 +651,21 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
     if (__all_sync(kFull, done)) {
       tc_fence_after();
       float o[32];
-      tmem_ld32(tO + lane_addr + 32 * hf, o);
+      tmem_ld_16x256b_x8(tO + lane_addr, o);
       tmem_wait_ld();
-      if (live) {
-        const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
-        float* dst = p.out + (static_cast<size_t>(row0 + t) * p.hq + h * G + gi) * kHeadDim + 32 * hf;
 #pragma unroll
-        for (int d = 0; d < 32; d += 4)
-          *reinterpret_cast<float4*>(dst + d) =
-              make_float4(o[d] * inv, o[d + 1] * inv, o[d + 2] * inv, o[d + 3] * inv);
+      for (int hh = 0; hh < 2; ++hh) {
+        float l = l_sum[hh];
+        l += __shfl_xor_sync(kFull, l, 1);
+        l += __shfl_xor_sync(kFull, l, 2);
+        if (live[hh]) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          float* dst = p.out + (static_cast<size_t>(row0 + tok[hh]) * p.hq + h * G + gix[hh]) * kHeadDim + 2 * q;
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            *reinterpret_cast<float2*>(dst + 8 * i) =
+                make_float2(o[4 * i + 2 * hh] * inv, o[4 * i + 2 * hh + 1] * inv);
+        }
       }
     } else {
       failed = true;
