@@ -303,6 +303,7 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks
  *     earlier tokens and itself), as paged_gqa_decode computes it.
  *   q            bf16 [total_tokens][num_q_heads][64];  k, v bf16 [total_tokens][num_kv_heads][64]
  *   q_rot, out   fp32 [total_tokens][num_q_heads][64] out
+ *                (q, v, q_rot, out and rope_table 16-byte aligned: -EINVAL otherwise)
  *   block_tables int32 [batch][max_blocks], the pages of every token up to
  *                start_pos[b] + chunk length assigned;  cu_tokens int32 [batch+1]
  *                (cu_tokens[0] = 0, non-decreasing, cu_tokens[batch] = total_tokens);

@@ -335,7 +335,7 @@ int paged_prefill(pkv_pool_t* pool, const void* q, const void* k, const void* v,
   if (!q || !k || !v || !q_rot || !out || !block_tables || !cu_tokens || !start_pos ||
       !rope_table || !workspace)
     return -EINVAL;
-  if (!aligned16(q_rot) || !aligned16(out) || !aligned16(v) || !aligned16(rope_table) ||
+  if (!aligned16(q) || !aligned16(q_rot) || !aligned16(out) || !aligned16(v) || !aligned16(rope_table) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return -EINVAL;
   int device = 0;

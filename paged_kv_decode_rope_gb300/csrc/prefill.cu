@@ -81,12 +81,25 @@ __global__ void __launch_bounds__(kAppendThreads)
   __syncthreads();
   const uint16_t* qb = q + static_cast<size_t>(tkn) * hq * kHeadDim;
   float* qo = q_rot + static_cast<size_t>(tkn) * hq * kHeadDim;
-  for (int idx = tid; idx < hq * kHalfDim; idx += kAppendThreads) {
-    const int head = idx / kHalfDim, j = idx - head * kHalfDim;
-    const float x0 = __uint_as_float(static_cast<uint32_t>(qb[head * kHeadDim + j]) << 16);
-    const float x1 = __uint_as_float(static_cast<uint32_t>(qb[head * kHeadDim + j + kHalfDim]) << 16);
-    qo[head * kHeadDim + j] = x0 * cs[j].x - x1 * cs[j].z;
-    qo[head * kHeadDim + j + kHalfDim] = x1 * cs[j].x + x0 * cs[j].z;
+  // four pairs (j0 .. j0 + 3, and 32 further) per item: 8-byte loads of the
+  // bf16 halves, 16-byte stores of the fp32 results
+  for (int idx = tid; idx < hq * (kHalfDim / 4); idx += kAppendThreads) {
+    const int head = idx / (kHalfDim / 4), j0 = 4 * (idx - head * (kHalfDim / 4));
+    const uint2 a = *reinterpret_cast<const uint2*>(qb + head * kHeadDim + j0);
+    const uint2 bq = *reinterpret_cast<const uint2*>(qb + head * kHeadDim + j0 + kHalfDim);
+    const float x0[4] = {__uint_as_float(a.x << 16), __uint_as_float(a.x & 0xffff0000u),
+                         __uint_as_float(a.y << 16), __uint_as_float(a.y & 0xffff0000u)};
+    const float x1[4] = {__uint_as_float(bq.x << 16), __uint_as_float(bq.x & 0xffff0000u),
+                         __uint_as_float(bq.y << 16), __uint_as_float(bq.y & 0xffff0000u)};
+    float y0[4], y1[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 c = cs[j0 + e];
+      y0[e] = x0[e] * c.x - x1[e] * c.z;
+      y1[e] = x1[e] * c.x + x0[e] * c.z;
+    }
+    *reinterpret_cast<float4*>(qo + head * kHeadDim + j0) = make_float4(y0[0], y0[1], y0[2], y0[3]);
+    *reinterpret_cast<float4*>(qo + head * kHeadDim + j0 + kHalfDim) = make_float4(y1[0], y1[1], y1[2], y1[3]);
   }
   const int b = tok_seq[tkn];
   if (b < 0) {  // a malformed chunk, or a position past the RoPE table

@@ -253,3 +253,28 @@ def test_measured_prefill_sizes_every_row(nb, t):
     np.testing.assert_allclose(q_rot.cpu().numpy(), want_qrot, rtol=1e-5, atol=2e-5)
     assert_close(out.cpu().numpy(), want, f"prefill {nb} x {t}")
     kp.close()
+
+
+def test_misaligned_query_is_rejected():
+    """The append reads the queries in 8-byte pieces: a q that does not start
+    on a 16-byte boundary is refused with EINVAL before any launch."""
+    dev = torch.device("cuda")
+    hkv, hq, t = 8, 32, 4
+    pool = torch.zeros(8 * 2 * hkv * 16 * 64, dtype=torch.bfloat16, device=dev)
+    kp = pkv.kv_pool_create(pool, hkv)
+    flat = torch.zeros(t * hq * 64 + 1, dtype=torch.bfloat16, device=dev)
+    q = flat[1:].view(t, hq, 64)  # contiguous, 2 bytes past a 16-byte boundary
+    k = torch.zeros(t, hkv, 64, dtype=torch.bfloat16, device=dev)
+    v = torch.zeros(t, hkv, 64, dtype=torch.bfloat16, device=dev)
+    q_rot = torch.empty(t, hq, 64, device=dev)
+    out = torch.full((t, hq, 64), 5.0, device=dev)
+    ws = pkv.alloc_prefill_workspace(t, 1, 1, device=dev)
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.paged_prefill(kp, q, k, v, q_rot, out, torch.zeros(1, 1, dtype=torch.int32, device=dev),
+                          torch.tensor([0, t], dtype=torch.int32, device=dev),
+                          torch.zeros(1, dtype=torch.int32, device=dev),
+                          pkv.build_rope_table(500000.0, 16, device=dev), 0.125, ws)
+    assert ei.value.rc == -22
+    torch.cuda.synchronize()
+    assert torch.all(out == 5.0), "nothing ran"
+    kp.close()
