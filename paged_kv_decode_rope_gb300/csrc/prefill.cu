@@ -202,10 +202,9 @@ struct PrefillAttnParams {
 // moves it (rescaling the row of O in tensor memory) only when a score passes
 // it by more than kSlack in the base-2 domain, so P <= 2^kSlack; numerator
 // and denominator share the reference, so the result is the same softmax.
-// Warps 0-7 run the softmax and the epilogue, two threads per row (warps w
-// and w + 4 share tensor-memory lanes 32 (w % 4) ..; one takes columns 0-31,
-// the other 32-63, and they exchange row maxima and sums through shared
-// memory), warp 8 issues the TMA copies of the K rows (each page's 16 K rows
+// Warps 0-7 run the softmax and the epilogue, 16 rows a warp and four
+// threads a row (the 16x256b tensor-memory layout; the four threads combine
+// row maxima and sums by shuffles), warp 8 issues the TMA copies of the K rows (each page's 16 K rows
 // into the stage's K tile) and warp 11 those of the V rows (into the V tile),
 // with separate barriers so K of a later step loads as soon as its stage's
 // scores are done, warp 9 issues the score products and warp 10 the P V
