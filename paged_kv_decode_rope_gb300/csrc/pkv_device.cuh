@@ -98,19 +98,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
-// 2-D tiled TMA load of a box at (x, y) of `map` into shared memory.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-
-// The same, called by a whole warp, converged, with warp-uniform arguments:
-// one elected lane issues the copy (a lone thread issuing was measured to fall
-// far behind when other warps kept its SM sub-partition busy).
+// 2-D tiled TMA load of a box at (x, y) of `map` into shared memory, called
+// by a whole warp, converged, with warp-uniform arguments: one elected lane
+// issues the copy (a lone thread issuing was measured to fall far behind when
+// other warps kept its SM sub-partition busy).
 __device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const void* map, int x, int y,
                                                   uint32_t bar) {
   asm volatile(
@@ -122,9 +113,10 @@ __device__ __forceinline__ void tma_load_2d_elect(uint32_t dst, const void* map,
       : "memory");
 }
 
-// The same load with an L2 cache policy (from l2_policy_evict_first): the
-// pages stream through once per launch, so they should leave L2 before the
-// small data around them (split pieces, tables, query rows) does.
+// A 2-D tiled TMA load issued by the calling thread, with an L2 cache policy
+// (from l2_policy_evict_first): the pages stream through once per launch, so
+// they should leave L2 before the small data around them (split pieces,
+// tables, query rows) does.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* map, int x, int y,
                                                  uint32_t bar, uint64_t policy) {
   asm volatile(
@@ -194,12 +186,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 // Wait until every cp_async16 this thread issued has landed.
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-__device__ __forceinline__ double lds64d(uint32_t addr) {
-  double v;
-  asm volatile("ld.shared.f64 %0, [%1];" : "=d"(v) : "r"(addr));
-  return v;
 }
 
 __device__ __forceinline__ uint16_t lds16(uint32_t addr) {
