@@ -64,14 +64,25 @@ TRAFFIC = {
     ("qwen05b_b32_l24_u1024_4096", 3): ("a671bb6e5f6338d8", 41515136),
     ("qwen05b_b32_l24_u1024_4096", 4): ("a671bb6e5f6338d8", 43570560),
 }
+# DRAM traffic (read + write bytes) per prefill_tc_kernel launch, one layer of
+# a fresh-prompt pass, from one ncu capture (mean of three launches), with the
+# hash of the prefill source it was taken on; reported only while unchanged.
+PREFILL_TRAFFIC = {
+    # (sequences, prompt tokens) -> (sha256 prefix of prefill.cu, read + write bytes per launch)
+    (4, 2048): ("463e5fe3a539056c", 111111339),
+}
 # The other workloads the 70% target names, timed as sub-records of the default line.
 SUB_WORKLOADS = ["llama1b_b256_l16_skew", "qwen05b_b32_l24_u1024_4096"]
 
 
-def _decode_source_hash() -> str:
-    p = os.path.join(ROOT, "paged_kv_decode_rope_gb300", "csrc", "gqa_decode.cu")
+def _source_hash(name: str) -> str:
+    p = os.path.join(ROOT, "paged_kv_decode_rope_gb300", "csrc", name)
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _decode_source_hash() -> str:
+    return _source_hash("gqa_decode.cu")
 
 
 def _peaks() -> tuple[float, str]:
@@ -93,15 +104,16 @@ def _tensor_peak(sustained: bool = True) -> tuple[float, str]:
         return (1700.0 if sustained else 1900.0), "fallback"
 
 
-def prefill_roofline(pairs: float, ms: float, peak: float, source: str) -> dict:
+def prefill_roofline(pairs: float, ms: float, peak: float, source: str, traffic: int | None = None) -> dict:
     """The prefill pass's roofline: causal attention is a dense contraction,
     bound by the bf16 tensor cores. Algorithmic flops are 2 products x 2 x 64
     per (query head, visible key) pair; the kernel's hi/lo operand split and
-    the masked halves of diagonal steps are work on top of that, not counted."""
+    the masked halves of diagonal steps are work on top of that, not counted.
+    traffic: the attention kernel's DRAM bytes per launch, where measured."""
     achieved = pairs * 4 * 64 / (ms / 1e3) / 1e12
     return {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05), with the pass's append",
             "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_source": f"{source} (MEASURED_PEAKS.json bf16_tflops_sustained, cuBLAS bf16)"
                            if source == "measured" else "fallback (1.7 PFLOP/s sustained)",
             "flops_per_pass": pairs * 4 * 64}
@@ -580,6 +592,11 @@ def run_trace(args, ws, rank, local) -> int:
     return 0
 
 
+def _prefill_traffic(nb: int, t: int) -> int | None:
+    ent = PREFILL_TRAFFIC.get((nb, t))
+    return ent[1] if ent and ent[0] == _source_hash("prefill.cu") else None
+
+
 def run_prefill(args, ws, rank, local) -> int:
     """Chunked causal prefill of fresh prompts (Llama-3.2-1B shape, 16 layers):
     B sequences of T tokens each, one paged_prefill call per layer, captured as a
@@ -643,7 +660,8 @@ def run_prefill(args, ws, rank, local) -> int:
                 "higher_is_better": True, "ms_per_pass": round(ms, 4), "steps": args.steps,
                 "warmup": args.warmup,
                 "attention_tflops": round(pairs * 4 * 64 / (ms / 1e3) / 1e12, 2),
-                "roofline": prefill_roofline(pairs, ms, *_tensor_peak(sustained=True)),
+                "roofline": prefill_roofline(pairs, ms, *_tensor_peak(sustained=True),
+                                             traffic=_prefill_traffic(nb, t)),
                 "config": {"sequences": nb, "prompt_tokens": t, "layers": nl, "q_heads": hq,
                            "kv_heads": hkv, "start": 0},
                 "data": "synthetic (seeded)",

@@ -56,3 +56,15 @@ def test_prefill_roofline_counts_algorithmic_flops_against_the_tensor_peak():
     assert abs(r["frac"] - r["achieved"] / 1710.2) < 1e-4
     peak, src = bench._tensor_peak()
     assert peak > 0 and src in ("measured", "fallback")
+
+
+def test_prefill_traffic_only_while_the_source_is_the_measured_one(monkeypatch):
+    # (4, 2048) has a stored capture; it is reported only for the source it was taken on
+    want = bench.PREFILL_TRAFFIC[(4, 2048)]
+    monkeypatch.setattr(bench, "_source_hash", lambda name: want[0])
+    assert bench._prefill_traffic(4, 2048) == want[1]
+    assert bench._prefill_traffic(1, 8192) is None
+    monkeypatch.setattr(bench, "_source_hash", lambda name: "0" * 16)
+    assert bench._prefill_traffic(4, 2048) is None
+    r = bench.prefill_roofline(1e9, 3.0, 1710.2, "measured", traffic=want[1])
+    assert r["traffic"] == want[1] and r["bound"] == "tensor"
