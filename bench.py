@@ -48,21 +48,21 @@ TRAFFIC = {
     # (workload, seed) -> (sha256 prefix of gqa_decode.cu, read + write bytes per layer call),
     # ncu dram__bytes_read.sum + dram__bytes_write.sum of the first layer launches of a 2-layer
     # copy of the workload (same lengths, pool fitted), mean over the eager warm-up launches
-    ("llama1b_b64_l16_u2048", 0): ("a671bb6e5f6338d8", 158885803),
-    ("llama1b_b64_l16_u2048", 1): ("a671bb6e5f6338d8", 142355413),
-    ("llama1b_b64_l16_u2048", 2): ("a671bb6e5f6338d8", 143540437),
-    ("llama1b_b64_l16_u2048", 3): ("a671bb6e5f6338d8", 130578944),
-    ("llama1b_b64_l16_u2048", 4): ("a671bb6e5f6338d8", 138815146),
-    ("llama1b_b256_l16_skew", 0): ("a671bb6e5f6338d8", 156277803),
-    ("llama1b_b256_l16_skew", 1): ("a671bb6e5f6338d8", 157170219),
-    ("llama1b_b256_l16_skew", 2): ("a671bb6e5f6338d8", 154305706),
-    ("llama1b_b256_l16_skew", 3): ("a671bb6e5f6338d8", 147188821),
-    ("llama1b_b256_l16_skew", 4): ("a671bb6e5f6338d8", 147722752),
-    ("qwen05b_b32_l24_u1024_4096", 0): ("a671bb6e5f6338d8", 47027414),
-    ("qwen05b_b32_l24_u1024_4096", 1): ("a671bb6e5f6338d8", 44067669),
-    ("qwen05b_b32_l24_u1024_4096", 2): ("a671bb6e5f6338d8", 42223573),
-    ("qwen05b_b32_l24_u1024_4096", 3): ("a671bb6e5f6338d8", 41515136),
-    ("qwen05b_b32_l24_u1024_4096", 4): ("a671bb6e5f6338d8", 43570560),
+    ("llama1b_b64_l16_u2048", 0): ("82a357034b7135d5", 158961451),
+    ("llama1b_b64_l16_u2048", 1): ("82a357034b7135d5", 142436266),
+    ("llama1b_b64_l16_u2048", 2): ("82a357034b7135d5", 143683242),
+    ("llama1b_b64_l16_u2048", 3): ("82a357034b7135d5", 130654805),
+    ("llama1b_b64_l16_u2048", 4): ("82a357034b7135d5", 138696533),
+    ("llama1b_b256_l16_skew", 0): ("82a357034b7135d5", 156204928),
+    ("llama1b_b256_l16_skew", 1): ("82a357034b7135d5", 157123200),
+    ("llama1b_b256_l16_skew", 2): ("82a357034b7135d5", 154208000),
+    ("llama1b_b256_l16_skew", 3): ("82a357034b7135d5", 147307605),
+    ("llama1b_b256_l16_skew", 4): ("82a357034b7135d5", 147698901),
+    ("qwen05b_b32_l24_u1024_4096", 0): ("82a357034b7135d5", 47021568),
+    ("qwen05b_b32_l24_u1024_4096", 1): ("82a357034b7135d5", 44072491),
+    ("qwen05b_b32_l24_u1024_4096", 2): ("82a357034b7135d5", 42225579),
+    ("qwen05b_b32_l24_u1024_4096", 3): ("82a357034b7135d5", 41516715),
+    ("qwen05b_b32_l24_u1024_4096", 4): ("82a357034b7135d5", 43569621),
 }
 # DRAM traffic (read + write bytes) per prefill_tc_kernel launch, one layer of
 # a fresh-prompt pass, from one ncu capture (mean of three launches), with the

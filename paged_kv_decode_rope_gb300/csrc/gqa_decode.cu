@@ -58,7 +58,8 @@ namespace {
 
 constexpr int kScanOffset = 512;           // scan scratch (16 ints) after the mbarriers
 constexpr int kHdrBytes = 1024;            // mbarriers (<= 64 warp-stages * 8 B) + scan scratch
-constexpr int kMinRangePages = 4;          // smallest automatic range (fewer, cheaper merges)
+constexpr int kMinRangePages = 4;          // an even cut at or above this: ranges of twice it
+constexpr int kSmallRangePages = 2;        // smallest automatic range, for little work
 // Automatic partition weights: a page costs kPageUnits, and each (sequence,
 // kv head) segment adds kSegUnits for the fixed work of its pieces (query
 // rows, the new token, the merges and result stores), about 1 1/4 pages
@@ -215,9 +216,11 @@ __device__ void scan_pages(const int* s_len, int* s_pre, int batch, int* s_warp)
 // pu * i + su * (s + 1). Range r covers units [r cw, (r + 1) cw) and owns the
 // pages that start there. pages_per_split > 0 gives plain ranges of that many
 // pages (pu = 1, su = 0), as does a work list too long for 32-bit unit
-// arithmetic. Short ranges cut latency when there is little work; once every
-// warp would get a few pages anyway, ranges of at least twice that keep the
-// number of pieces (and merges) down.
+// arithmetic. Short ranges cut latency when there is little work (two pages:
+// more warps and SMs stream the few pages; one page was slower, four pages
+// 12-14% slower on batch 8 and a single short sequence); once every warp
+// would get kMinRangePages pages anyway, ranges of at least twice that keep
+// the number of pieces (and merges) down.
 struct Partition {
   int n_items, pu, su, total_units, cw, n_ranges;
 };
@@ -231,7 +234,7 @@ __device__ __forceinline__ Partition make_partition(int total_pages, int batch, 
   pt.su = weighted ? kSegUnits : 0;
   pt.total_units = pt.pu * pt.n_items + pt.su * batch * hkv;
   const int even = (pt.total_units + nwarps - 1) / nwarps;
-  const int min_pages = even >= pt.pu * kMinRangePages ? 2 * kMinRangePages : kMinRangePages;
+  const int min_pages = even >= pt.pu * kMinRangePages ? 2 * kMinRangePages : kSmallRangePages;
   pt.cw = pages_per_split > 0 ? pages_per_split : max(pt.pu * min_pages, even);
   pt.n_ranges = (pt.total_units + pt.cw - 1) / pt.cw;
   return pt;
