@@ -20,6 +20,7 @@
 // each) run the online softmax on its row of S.
 #include <atomic>
 #include <climits>
+#include <cub/block/block_scan.cuh>
 
 #include "pkv_device.cuh"
 #include "tc05.cuh"
@@ -142,35 +143,66 @@ __global__ void __launch_bounds__(kAppendThreads)
 constexpr int kPlanThreads = 1024;
 
 // Lists the tiles as {b, first chunk row, tokens, position of the first
-// token}: sequence b's chunk gives ceil(len / tokens) tiles. One CTA; slots
-// are reserved with a shared-memory counter, so sequences land in arbitrary
-// order (tiles are independent); within a sequence the last tile, which reads
-// the most pages, goes first. Rows are clipped to [0, total); tiles past
-// `capacity` (only possible when chunks overlap) are dropped and flagged.
-__global__ void prefill_plan_kernel(const int32_t* __restrict__ cu_tokens,
-                                    const int32_t* __restrict__ start_pos, int batch, int total,
-                                    int tokens_per_tile, int capacity, int4* __restrict__ tiles,
-                                    int* __restrict__ num_tiles, int* __restrict__ err) {
-  __shared__ int s_count;
-  if (threadIdx.x == 0) s_count = 0;
+// token}: sequence b's chunk gives ceil(len / tokens) tiles. One CTA. The
+// tiles are ordered by the number of 64-key steps they take, most first (a
+// counting sort over kPlanBuckets buckets, the last one shared by every tile
+// of that many steps or more; the order within a bucket is arbitrary), so
+// that the CTAs handed out last, as SMs free up, are the short ones. Rows are
+// clipped to [0, total); tiles past `capacity` (only possible when chunks
+// overlap) are dropped and flagged.
+constexpr int kPlanBuckets = 2048;
+__global__ void __launch_bounds__(kPlanThreads)
+    prefill_plan_kernel(const int32_t* __restrict__ cu_tokens, const int32_t* __restrict__ start_pos,
+                        int batch, int total, int tokens_per_tile, int capacity,
+                        int4* __restrict__ tiles, int* __restrict__ num_tiles, int* __restrict__ err) {
+  using Scan = cub::BlockScan<int, kPlanThreads>;
+  __shared__ typename Scan::TempStorage scan_tmp;
+  __shared__ int s_hist[kPlanBuckets];  // tiles per bucket, then the bucket's next slot
+  static_assert(kPlanBuckets == 2 * kPlanThreads, "two buckets a thread in the scan");
+  for (int k = threadIdx.x; k < kPlanBuckets; k += kPlanThreads) s_hist[k] = 0;
   __syncthreads();
-  for (int b = threadIdx.x; b < batch; b += kPlanThreads) {
+  // a tile's bucket: its steps (from the keys before its last token), most first
+  auto bucket = [&](long long pos0, int ntok) {
+    if (pos0 < 0 || pos0 > INT_MAX) return kPlanBuckets - 1;  // no work: last
+    const long long steps = (pos0 + ntok - 1) / 64 + 1;
+    return kPlanBuckets - 1 - static_cast<int>(min(steps, static_cast<long long>(kPlanBuckets - 1)));
+  };
+  // a warp per sequence, its lanes over the sequence's tiles
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int b = warp; b < batch; b += kPlanThreads / 32) {
     const int c0 = max(cu_tokens[b], 0), c1 = min(cu_tokens[b + 1], total);
     const int len = c1 - c0;
     if (len <= 0) continue;
     const int nt = (len + tokens_per_tile - 1) / tokens_per_tile;
-    const int base = atomicAdd(&s_count, nt);
-    for (int i = 0; i < nt; ++i) {
-      const int j = nt - 1 - i, t0 = j * tokens_per_tile;
-      const long long pos0 = static_cast<long long>(start_pos[b]) + t0;  // -1: does not fit
-      if (base + i < capacity)
-        tiles[base + i] = make_int4(b, c0 + t0, min(tokens_per_tile, len - t0),
-                                    pos0 > INT_MAX ? -1 : static_cast<int>(pos0));
+    for (int j = lane; j < nt; j += 32) {
+      const int t0 = j * tokens_per_tile;
+      atomicAdd(&s_hist[bucket(static_cast<long long>(start_pos[b]) + t0, min(tokens_per_tile, len - t0))], 1);
     }
-    if (base + nt > capacity) atomicOr(err, PKV_ERR_SEQ_LEN);
   }
   __syncthreads();
-  if (threadIdx.x == 0) *num_tiles = min(s_count, capacity);
+  int cnt[2] = {s_hist[2 * threadIdx.x], s_hist[2 * threadIdx.x + 1]}, first[2], all;
+  Scan(scan_tmp).ExclusiveSum(cnt, first, all);
+  __syncthreads();
+  s_hist[2 * threadIdx.x] = first[0];
+  s_hist[2 * threadIdx.x + 1] = first[1];
+  __syncthreads();
+  for (int b = warp; b < batch; b += kPlanThreads / 32) {
+    const int c0 = max(cu_tokens[b], 0), c1 = min(cu_tokens[b + 1], total);
+    const int len = c1 - c0;
+    if (len <= 0) continue;
+    const int nt = (len + tokens_per_tile - 1) / tokens_per_tile;
+    for (int j = lane; j < nt; j += 32) {
+      const int t0 = j * tokens_per_tile, ntok = min(tokens_per_tile, len - t0);
+      const long long pos0 = static_cast<long long>(start_pos[b]) + t0;  // -1: does not fit
+      const int slot = atomicAdd(&s_hist[bucket(pos0, ntok)], 1);
+      if (slot < capacity)
+        tiles[slot] = make_int4(b, c0 + t0, ntok, pos0 > INT_MAX ? -1 : static_cast<int>(pos0));
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (all > capacity) atomicOr(err, PKV_ERR_SEQ_LEN);
+    *num_tiles = min(all, capacity);
+  }
 }
 
 struct PrefillAttnParams {
