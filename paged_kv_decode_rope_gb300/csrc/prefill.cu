@@ -327,9 +327,14 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   __shared__ __align__(8) uint64_t s_full[kSBufs], q_ready, p_full[kSBufs], pv_done[kSBufs], drain[2];
   __shared__ uint32_t s_tmem;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (static_cast<int>(blockIdx.x) >= *p.num_tiles) return;
-  const int4 tile = p.tiles[blockIdx.x];
-  const int b = tile.x, row0 = tile.y, n_tok = tile.z, pos0 = tile.w, h = blockIdx.y;
+  // CTA x works on tile x / hkv for kv head x % hkv: the hardware hands CTAs
+  // out in order of x, so the order of the tiles (most steps first) holds
+  // across all kv heads
+  const int ti = static_cast<int>(blockIdx.x / static_cast<unsigned>(p.hkv));
+  const int h = static_cast<int>(blockIdx.x - static_cast<unsigned>(ti) * static_cast<unsigned>(p.hkv));
+  if (ti >= *p.num_tiles) return;
+  const int4 tile = p.tiles[ti];
+  const int b = tile.x, row0 = tile.y, n_tok = tile.z, pos0 = tile.w;
   const long long room = p.pos_cap - pos0;
   const int n_ok = pos0 < 0 ? 0 : static_cast<int>(min(static_cast<long long>(n_tok), max(room, 0ll)));
   for (int e = n_ok * G * kHeadDim + tid; e < n_tok * G * kHeadDim; e += C::kThreads) {
@@ -783,7 +788,9 @@ cudaError_t launch_attn(const PrefillLaunch& a, const PrefillLayout& l, cudaStre
     if (e != cudaSuccess) return e;
     attr_set[G].store(true, std::memory_order_relaxed);
   }
-  const dim3 grid(static_cast<unsigned>(grid_x), static_cast<unsigned>(a.num_kv_heads));
+  const size_t n_ctas = grid_x * static_cast<size_t>(a.num_kv_heads);
+  if (n_ctas > 0x7fffffffu) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(n_ctas));
   prefill_tc_kernel<G><<<grid, C::kThreads, smem, stream>>>(*a.kv16_map, p);
   return cudaGetLastError();
 }
