@@ -16,7 +16,7 @@
 // cores: one CTA per (tile of up to 128 (token, query head) rows, kv head)
 // streams the sequence's pages up to the tile's last position, four pages
 // per step, through a TMA ring; tcgen05 MMAs with fp32 accumulators in tensor
-// memory compute S = Q K^T and O += P V, and two threads per row (32 columns
+// memory compute S = Q K^T and O += P V, and four threads per row (16 keys
 // each) run the online softmax on its row of S.
 #include <atomic>
 #include <climits>
