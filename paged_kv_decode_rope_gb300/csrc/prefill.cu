@@ -310,6 +310,21 @@ __device__ __forceinline__ bool mbar_wait_idle(uint32_t bar, uint32_t parity) {
   return false;
 }
 
+// p0 - h.lo and p1 - h.hi for the two bf16 halves of h, each in one
+// mixed-precision fma (bf16 times bf16 -1, plus fp32; sm_100 and later):
+// exact when h is p rounded to bf16, so the remainder of the split
+__device__ __forceinline__ float2 bf16x2_remainder(uint32_t h, float p0, float p1) {
+  float r0, r1;
+  asm("{\n\t.reg .b16 h0, h1, m1;\n\t"
+      "mov.b32 {h0, h1}, %2;\n\t"
+      "mov.b16 m1, 0xBF80;\n\t"
+      "fma.rn.f32.bf16 %0, h0, m1, %3;\n\t"
+      "fma.rn.f32.bf16 %1, h1, m1, %4;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "r"(h), "f"(p0), "f"(p1));
+  return make_float2(r0, r1);
+}
+
 // max of three floats in one instruction (sm_100 and later)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
@@ -660,11 +675,9 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
           const int w = 4 * i + 2 * hh;
           const float2 d = unpack_f32x2(sub_f32x2(f32x2(sv[w], sv[w + 1]), mm[hh]));
           const float p0 = fast_exp2(d.x), p1 = fast_exp2(d.y);
-          const uint64_t pp = f32x2(p0, p1);
-          lp[hh] = add_f32x2(lp[hh], pp);
+          lp[hh] = add_f32x2(lp[hh], f32x2(p0, p1));
           hi[2 * i + hh] = pack_bf16x2(p0, p1);
-          const float2 f = bf16x2_to_float2(hi[2 * i + hh]);
-          const float2 rem = unpack_f32x2(sub_f32x2(pp, f32x2(f.x, f.y)));
+          const float2 rem = bf16x2_remainder(hi[2 * i + hh], p0, p1);
           lo[2 * i + hh] = pack_bf16x2(rem.x, rem.y);
         }
       tmem_st_16x128b_x8(tS(j) + lane_addr, hi);
