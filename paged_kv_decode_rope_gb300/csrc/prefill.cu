@@ -253,6 +253,12 @@ struct TcCfg {
   static constexpr int kStages = 4;
   static constexpr int kSoftmaxThreads = 256;
   static constexpr int kThreads = kSoftmaxThreads + 128;
+  // registers a thread after the split (setmaxnreg): the launch gives 80 to
+  // each of the 384 threads (two CTAs an SM); the copy and product
+  // warpgroup keeps 48, the two softmax warpgroups take 96
+  // (128 x 48 + 256 x 96 = 384 x 80)
+  static constexpr int kIssueRegs = 48;
+  static constexpr int kSoftmaxRegs = 96;
   static constexpr uint32_t kTile = 128 * 128;  // a 128-row x 128-byte operand tile
   static constexpr uint32_t kStep = 64 * 128;   // 64 K rows (or V rows) of one step
   // dynamic shared memory: Q_hi, Q_lo, then per stage K and V
@@ -323,6 +329,18 @@ __device__ __forceinline__ float2 bf16x2_remainder(uint32_t h, float p0, float p
       : "=f"(r0), "=f"(r1)
       : "r"(h), "f"(p0), "f"(p1));
   return make_float2(r0, r1);
+}
+
+// Move registers between the warpgroups of a CTA (every warp of a warpgroup
+// executes the same instruction): dec gives back down to N a thread, inc
+// waits until N a thread are free.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // max of three floats in one instruction (sm_100 and later)
@@ -398,119 +416,125 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   auto par = [](int j) { return static_cast<uint32_t>((j / kSBufs) & 1); };  // and their phase parity
   bool failed = false;
 
-  if (warp == 8 || warp == 11) {
-    // ---- TMA producers, warp 8 for K and warp 11 for V: step j's four
-    // pages into stage j % kStages. A warp reads the page ids 32 at a time
-    // (lane i: page 32 m + i), the next 32 while it issues the current ones,
-    // so no step waits for a block-table load; the whole warp runs the loop
-    // and one elected lane issues each copy. K and V have a warp each so
-    // that the K copies, needed first, never queue behind a wait for a V
-    // stage. ----
-    const int kind = warp == 8 ? 0 : 1;  // 0: K rows, 1: V rows
-    uint64_t* full = kind ? v_full : k_full;
-    uint64_t* empty = kind ? v_empty : k_empty;
-    int issued = 0;
-    // lane i: the copy's row coordinate for page 32 m + i of window m (-1:
-    // past the last page, or a bad id), and the window's valid pages as a
-    // bit mask; worked out once per window of eight steps
-    uint32_t valid = 0;
-    auto window = [&](int pid, int m) {
-      const int pg = 32 * m + lane;
-      const bool in = pg < n_pages;
-      const bool ok = in && pid >= 0 && static_cast<long long>(pid) < p.num_pages;
-      if (kind == 0 && __any_sync(kFull, in && !ok) && lane == 0) atomicOr(p.err, PKV_ERR_PAGE_ID);
-      valid = __ballot_sync(kFull, ok);
-      return ok ? (pid * p.hkv + h) * (2 * kPage) + kind * kPage : -1;
-    };
-    int row = window(lane < n_pages ? bt[lane] : -1, 0);
-    int pid_next = 32 + lane < n_pages ? bt[32 + lane] : -1;
-    for (int j = 0; j < n_steps && !failed; ++j) {
-      const int st = j % C::kStages, use = j / C::kStages;
-      if (j > 0 && (j & 7) == 0) {  // the next 32 pages
-        row = window(pid_next, j >> 3);
-        const int nxt = 4 * j + 32 + lane;
-        pid_next = nxt < n_pages ? bt[nxt] : -1;
-      }
-      const int l0 = (4 * j) & 31;
-      const uint32_t vbits = (valid >> l0) & 0xFu;
-      int rows[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) rows[q] = __shfl_sync(kFull, row, l0 + q);
-      // the stage is free once its scores (K) or its P V product (V) are done
-      if (use > 0 && !mbar_wait_idle(smem_addr(&empty[st]), (use - 1) & 1)) failed = true;
-      if (__any_sync(kFull, failed)) {
-        failed = true;
-        break;
-      }
-      const uint32_t dst = (kind ? vst(st) : kst(st)), bar = smem_addr(&full[st]);
-      mbar_arrive_expect_tx_elect(bar, static_cast<uint32_t>(__popc(vbits)) * kHalfBytes);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if ((vbits >> q) & 1u) tma_load_2d_elect(dst + q * kHalfBytes, &kv16_map, 0, rows[q], bar);
-      issued = j + 1;
-    }
-    // let the copies still in flight (the last kStages steps at most) land
-    // before shared memory goes away
-    if (failed && lane == 0)
-      for (int j = max(0, issued - C::kStages); j < issued; ++j)
-        mbar_wait_bounded(smem_addr(&full[j % C::kStages]), (j / C::kStages) & 1);
-  } else if (warp == 9 || warp == 10) {
-    // ---- MMA issuers, each a whole warp, converged (one lane issues each
-    // product; every wait's result is made warp-uniform): warp 9 the score
-    // products, warp 10 the P V products. A commit covers only its own
-    // warp's products. ----
-    auto wait_all = [&](uint32_t bar, uint32_t parity) {
-      return __all_sync(kFull, mbar_wait_idle(bar, parity)) != 0;
-    };
-    if (warp == 9) {
-      constexpr uint32_t idS = idesc_bf16_f32(128, 64, false);
-      const uint64_t dQhi = smem_desc_sw128(base + C::kQhi), dQlo = smem_desc_sw128(base + C::kQlo);
-      if (!wait_all(smem_addr(&q_ready), 0)) failed = true;
+  if (warp >= 8) {
+    // the copy and product warps (one warpgroup) give registers to the
+    // softmax warpgroups
+    regs_dec<TcCfg<G>::kIssueRegs>();
+    if (warp == 8 || warp == 11) {
+      // ---- TMA producers, warp 8 for K and warp 11 for V: step j's four
+      // pages into stage j % kStages. A warp reads the page ids 32 at a time
+      // (lane i: page 32 m + i), the next 32 while it issues the current ones,
+      // so no step waits for a block-table load; the whole warp runs the loop
+      // and one elected lane issues each copy. K and V have a warp each so
+      // that the K copies, needed first, never queue behind a wait for a V
+      // stage. ----
+      const int kind = warp == 8 ? 0 : 1;  // 0: K rows, 1: V rows
+      uint64_t* full = kind ? v_full : k_full;
+      uint64_t* empty = kind ? v_empty : k_empty;
+      int issued = 0;
+      // lane i: the copy's row coordinate for page 32 m + i of window m (-1:
+      // past the last page, or a bad id), and the window's valid pages as a
+      // bit mask; worked out once per window of eight steps
+      uint32_t valid = 0;
+      auto window = [&](int pid, int m) {
+        const int pg = 32 * m + lane;
+        const bool in = pg < n_pages;
+        const bool ok = in && pid >= 0 && static_cast<long long>(pid) < p.num_pages;
+        if (kind == 0 && __any_sync(kFull, in && !ok) && lane == 0) atomicOr(p.err, PKV_ERR_PAGE_ID);
+        valid = __ballot_sync(kFull, ok);
+        return ok ? (pid * p.hkv + h) * (2 * kPage) + kind * kPage : -1;
+      };
+      int row = window(lane < n_pages ? bt[lane] : -1, 0);
+      int pid_next = 32 + lane < n_pages ? bt[32 + lane] : -1;
       for (int j = 0; j < n_steps && !failed; ++j) {
-        const int st = j % C::kStages;
-        // S_j goes into the buffer of P_{j-3}: once P_{j-3} V_{j-3} is done
-        if (j >= kSBufs && !wait_all(smem_addr(&pv_done[buf(j)]), par(j - kSBufs))) failed = true;
-        if (failed || !wait_all(smem_addr(&k_full[st]), (j / C::kStages) & 1)) {
+        const int st = j % C::kStages, use = j / C::kStages;
+        if (j > 0 && (j & 7) == 0) {  // the next 32 pages
+          row = window(pid_next, j >> 3);
+          const int nxt = 4 * j + 32 + lane;
+          pid_next = nxt < n_pages ? bt[nxt] : -1;
+        }
+        const int l0 = (4 * j) & 31;
+        const uint32_t vbits = (valid >> l0) & 0xFu;
+        int rows[4];
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) rows[q] = __shfl_sync(kFull, row, l0 + q);
+        // the stage is free once its scores (K) or its P V product (V) are done
+        if (use > 0 && !mbar_wait_idle(smem_addr(&empty[st]), (use - 1) & 1)) failed = true;
+        if (__any_sync(kFull, failed)) {
           failed = true;
           break;
         }
-        tc_fence_after();
-        const uint64_t dK = smem_desc_sw128(kst(st));
-        // K-major tiles: a 16-element K step is 32 bytes along the swizzled
-        // row (+2 in the descriptor's 16-byte address units)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16(tS(j), dQhi + 2 * k, dK + 2 * k, idS, k > 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16(tS(j), dQlo + 2 * k, dK + 2 * k, idS, true);
-        umma_commit(smem_addr(&k_empty[st]));
-        umma_commit(smem_addr(&s_full[buf(j)]));
+        const uint32_t dst = (kind ? vst(st) : kst(st)), bar = smem_addr(&full[st]);
+        mbar_arrive_expect_tx_elect(bar, static_cast<uint32_t>(__popc(vbits)) * kHalfBytes);
+  #pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if ((vbits >> q) & 1u) tma_load_2d_elect(dst + q * kHalfBytes, &kv16_map, 0, rows[q], bar);
+        issued = j + 1;
       }
+      // let the copies still in flight (the last kStages steps at most) land
+      // before shared memory goes away
+      if (failed && lane == 0)
+        for (int j = max(0, issued - C::kStages); j < issued; ++j)
+          mbar_wait_bounded(smem_addr(&full[j % C::kStages]), (j / C::kStages) & 1);
     } else {
-      constexpr uint32_t idPV = idesc_bf16_f32(128, 64, true);
-      for (int j = 0; j < n_steps && !failed; ++j) {
-        const int st = j % C::kStages;
-        if (!wait_all(smem_addr(&p_full[buf(j)]), par(j)) ||
-            !wait_all(smem_addr(&v_full[st]), (j / C::kStages) & 1)) {
-          failed = true;
-          break;
+      // ---- MMA issuers, each a whole warp, converged (one lane issues each
+      // product; every wait's result is made warp-uniform): warp 9 the score
+      // products, warp 10 the P V products. A commit covers only its own
+      // warp's products. ----
+      auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(kFull, mbar_wait_idle(bar, parity)) != 0;
+      };
+      if (warp == 9) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, 64, false);
+        const uint64_t dQhi = smem_desc_sw128(base + C::kQhi), dQlo = smem_desc_sw128(base + C::kQlo);
+        if (!wait_all(smem_addr(&q_ready), 0)) failed = true;
+        for (int j = 0; j < n_steps && !failed; ++j) {
+          const int st = j % C::kStages;
+          // S_j goes into the buffer of P_{j-3}: once P_{j-3} V_{j-3} is done
+          if (j >= kSBufs && !wait_all(smem_addr(&pv_done[buf(j)]), par(j - kSBufs))) failed = true;
+          if (failed || !wait_all(smem_addr(&k_full[st]), (j / C::kStages) & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dK = smem_desc_sw128(kst(st));
+          // K-major tiles: a 16-element K step is 32 bytes along the swizzled
+          // row (+2 in the descriptor's 16-byte address units)
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) umma_bf16(tS(j), dQhi + 2 * k, dK + 2 * k, idS, k > 0);
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) umma_bf16(tS(j), dQlo + 2 * k, dK + 2 * k, idS, true);
+          umma_commit(smem_addr(&k_empty[st]));
+          umma_commit(smem_addr(&s_full[buf(j)]));
         }
-        tc_fence_after();
-        const uint64_t dV = smem_desc_sw128(vst(st));
-        // P from tensor memory (a 16-key K step is 8 columns); V is MN-major:
-        // a 16-key K step is 16 rows = 2048 bytes (+128)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tS(j) + 8 * k, dV + 128 * k, idPV, j > 0 || k > 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tS(j) + 32 + 8 * k, dV + 128 * k, idPV, true);
-        umma_commit(smem_addr(&v_empty[st]));
-        umma_commit(smem_addr(&pv_done[buf(j)]));
+      } else {
+        constexpr uint32_t idPV = idesc_bf16_f32(128, 64, true);
+        for (int j = 0; j < n_steps && !failed; ++j) {
+          const int st = j % C::kStages;
+          if (!wait_all(smem_addr(&p_full[buf(j)]), par(j)) ||
+              !wait_all(smem_addr(&v_full[st]), (j / C::kStages) & 1)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dV = smem_desc_sw128(vst(st));
+          // P from tensor memory (a 16-key K step is 8 columns); V is MN-major:
+          // a 16-key K step is 16 rows = 2048 bytes (+128)
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tS(j) + 8 * k, dV + 128 * k, idPV, j > 0 || k > 0);
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) umma_bf16_tmem_a(tO, tS(j) + 32 + 8 * k, dV + 128 * k, idPV, true);
+          umma_commit(smem_addr(&v_empty[st]));
+          umma_commit(smem_addr(&pv_done[buf(j)]));
+        }
       }
-    }
-    if (failed) {  // let this warp's products already issued finish before the memory goes away
-      umma_commit(smem_addr(&drain[warp - 9]));
-      mbar_wait_bounded(smem_addr(&drain[warp - 9]), 0);
+      if (failed) {  // let this warp's products already issued finish before the memory goes away
+        umma_commit(smem_addr(&drain[warp - 9]));
+        mbar_wait_bounded(smem_addr(&drain[warp - 9]), 0);
+      }
     }
   } else {
+    regs_inc<TcCfg<G>::kSoftmaxRegs>();
     // ---- softmax and epilogue. Warp w owns rows L .. L + 15, L = 32 (w % 4)
     // + 16 (w / 4) (tensor-memory lanes). Its thread t holds rows L + t / 4
     // (hh = 0) and L + t / 4 + 8 (hh = 1) and, of each, the key pairs
