@@ -611,35 +611,75 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
       const int bad = static_cast<int>((bad_win >> ((4 * j) & 31)) & 0xFu);
       if (!mbar_wait_bounded(smem_addr(&s_full[buf(j)]), par(j))) failed = true;
       tc_fence_after();
+      // S_j, with the keys that get no weight (past the row's position, or
+      // of a page with a bad id: page i / 2 of the step holds pair i) at -inf
       float sv[32];
-      tmem_ld_16x256b_x8(tS(j) + lane_addr, sv);
-      tmem_wait_ld();
-      // keys past the row's position, and pages with a bad id (page i / 2 of
-      // the step holds pair i), get no weight
-      if (64 * j + 63 > pos[0] || bad) {
+      auto load_s = [&]() {
+        tmem_ld_16x256b_x8(tS(j) + lane_addr, sv);
+        tmem_wait_ld();
+        if (64 * j + 63 > pos[0] || bad) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+              for (int e = 0; e < 2; ++e)
+                if (kb + 8 * i + e > pos[hh] || ((bad >> (i >> 1)) & 1)) sv[4 * i + 2 * hh + e] = -INFINITY;
+        }
+      };
+      // P = exp2(S - m_ref) as bf16 high part and remainder, into tensor
+      // memory over S_j (16x128b: word 2 i + hh is column 4 i + q, the pair
+      // 8 i + 2 q, + 1 of row hh; P_hi in columns 0-31, P_lo in 32-63), in
+      // paired fp32 arithmetic, with the row sums and, alongside, this
+      // thread's maximum of each of its rows (three-input maxima)
+      uint32_t hi[16], lo[16];
+      uint64_t lp[2];
+      float mt[2];
+      auto make_p = [&]() {
+        uint64_t mm[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const float m_use = m_ref[hh] == -INFINITY ? 0.f : m_ref[hh];  // all scores -inf: P = 0
+          mm[hh] = f32x2(m_use, m_use);
+          lp[hh] = f32x2(0.f, 0.f);
+          mt[hh] = -INFINITY;
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i)
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
+          for (int hh = 0; hh < 2; ++hh) {
+            const int w = 4 * i + 2 * hh;
+            mt[hh] = fmax3(mt[hh], sv[w], sv[w + 1]);
+            const float2 d = unpack_f32x2(sub_f32x2(f32x2(sv[w], sv[w + 1]), mm[hh]));
+            const float p0 = fast_exp2(d.x), p1 = fast_exp2(d.y);
+            lp[hh] = add_f32x2(lp[hh], f32x2(p0, p1));
+            hi[2 * i + hh] = pack_bf16x2(p0, p1);
+            const float2 rem = bf16x2_remainder(hi[2 * i + hh], p0, p1);
+            lo[2 * i + hh] = pack_bf16x2(rem.x, rem.y);
+          }
+      };
+      // From the second step on, where the reference rarely moves, P is made
+      // with the reference as it stands, before the row maxima are known, so
+      // that the maxima's shuffles overlap the exponentials; a warp where a
+      // row's reference moves drops it and makes P again from S_j, still in
+      // tensor memory. The first step takes the maxima first.
+      const bool spec = j > 0;
+      load_s();
+      if (spec) {
+        make_p();
+      } else {
 #pragma unroll
-            for (int e = 0; e < 2; ++e)
-              if (kb + 8 * i + e > pos[hh] || ((bad >> (i >> 1)) & 1)) sv[4 * i + 2 * hh + e] = -INFINITY;
+        for (int hh = 0; hh < 2; ++hh) {
+          mt[hh] = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mt[hh] = fmax3(mt[hh], sv[4 * i + 2 * hh], sv[4 * i + 2 * hh + 1]);
+        }
       }
-      // each row's maximum: this thread's 16 keys (three-input maxima), then
-      // the row's four threads (lanes 4 (t / 4) .. + 3)
+      // each row's maximum: the row's four threads (lanes 4 (t / 4) .. + 3)
       float mx[2];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        float m6[6];
-#pragma unroll
-        for (int k = 0; k < 5; ++k) {
-          const int a = 3 * k, b2 = 3 * k + 1, c = 3 * k + 2;  // values a, b2, c of 0..15
-          m6[k] = fmax3(sv[4 * (a >> 1) + 2 * hh + (a & 1)], sv[4 * (b2 >> 1) + 2 * hh + (b2 & 1)],
-                        sv[4 * (c >> 1) + 2 * hh + (c & 1)]);
-        }
-        m6[5] = sv[4 * 7 + 2 * hh + 1];
-        float m = fmaxf(fmax3(m6[0], m6[1], m6[2]), fmax3(m6[3], m6[4], m6[5]));
-        m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+        const float m = fmaxf(mt[hh], __shfl_xor_sync(kFull, mt[hh], 1));
         mx[hh] = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
       }
       // Move the reference up where a score passed it by more than kSlack;
@@ -652,58 +692,40 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
         moves[hh] = mx[hh] > m_ref[hh] + kSlack;
         resc[hh] = moves[hh] && j > 0 && m_ref[hh] != -INFINITY;
       }
-      if (__any_sync(kFull, resc[0] || resc[1])) {
-        if (!mbar_wait_bounded(smem_addr(&pv_done[buf(j - 1)]), par(j - 1))) failed = true;
-        tc_fence_after();
-        uint64_t aa[2];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const float alpha = resc[hh] ? fast_exp2(m_ref[hh] - mx[hh]) : 1.f;
-          l_sum[hh] *= alpha;
-          aa[hh] = f32x2(alpha, alpha);
-        }
-        float o[32];
-        tmem_ld_16x256b_x8(tO + lane_addr, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
+      if (__any_sync(kFull, moves[0] || moves[1])) {  // a speculative P is dropped
+        if (__any_sync(kFull, resc[0] || resc[1])) {
+          if (!mbar_wait_bounded(smem_addr(&pv_done[buf(j - 1)]), par(j - 1))) failed = true;
+          tc_fence_after();
+          uint64_t aa[2];
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            const int w = 4 * i + 2 * hh;
-            const float2 v = unpack_f32x2(mul_f32x2(f32x2(o[w], o[w + 1]), aa[hh]));
-            o[w] = v.x;
-            o[w + 1] = v.y;
+            const float alpha = resc[hh] ? fast_exp2(m_ref[hh] - mx[hh]) : 1.f;
+            l_sum[hh] *= alpha;
+            aa[hh] = f32x2(alpha, alpha);
           }
-        tmem_st_16x256b_x8(tO + lane_addr, o);
-        tmem_wait_st();
-      }
+          float o[32];
+          tmem_ld_16x256b_x8(tO + lane_addr, o);
+          tmem_wait_ld();
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-        if (moves[hh]) m_ref[hh] = mx[hh];
-      // P = exp2(S - m_ref) as bf16 high part and remainder, into tensor
-      // memory over S_j (16x128b: word 2 i + hh is column 4 i + q, the pair
-      // 8 i + 2 q, + 1 of row hh; P_hi in columns 0-31, P_lo in 32-63), in
-      // paired fp32 arithmetic
-      uint64_t mm[2], lp[2];
+          for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const float m_use = m_ref[hh] == -INFINITY ? 0.f : m_ref[hh];  // all scores -inf: P = 0
-        mm[hh] = f32x2(m_use, m_use);
-        lp[hh] = f32x2(0.f, 0.f);
-      }
-      uint32_t hi[16], lo[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int w = 4 * i + 2 * hh;
-          const float2 d = unpack_f32x2(sub_f32x2(f32x2(sv[w], sv[w + 1]), mm[hh]));
-          const float p0 = fast_exp2(d.x), p1 = fast_exp2(d.y);
-          lp[hh] = add_f32x2(lp[hh], f32x2(p0, p1));
-          hi[2 * i + hh] = pack_bf16x2(p0, p1);
-          const float2 rem = bf16x2_remainder(hi[2 * i + hh], p0, p1);
-          lo[2 * i + hh] = pack_bf16x2(rem.x, rem.y);
+            for (int hh = 0; hh < 2; ++hh) {
+              const int w = 4 * i + 2 * hh;
+              const float2 v = unpack_f32x2(mul_f32x2(f32x2(o[w], o[w + 1]), aa[hh]));
+              o[w] = v.x;
+              o[w + 1] = v.y;
+            }
+          tmem_st_16x256b_x8(tO + lane_addr, o);
+          tmem_wait_st();
         }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          if (moves[hh]) m_ref[hh] = mx[hh];
+        if (spec) load_s();
+        make_p();
+      } else if (!spec) {
+        make_p();
+      }
       tmem_st_16x128b_x8(tS(j) + lane_addr, hi);
       tmem_st_16x128b_x8(tS(j) + lane_addr + 32, lo);
       tmem_wait_st();
