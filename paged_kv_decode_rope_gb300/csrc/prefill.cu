@@ -418,7 +418,9 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
 
   if (warp >= 8) {
     // the copy and product warps (one warpgroup) give registers to the
-    // softmax warpgroups
+    // softmax warpgroups, first thing and unconditionally, so the softmax
+    // warps' increase (the shares add up to the launch's total) never waits
+    // for more than this
     regs_dec<TcCfg<G>::kIssueRegs>();
     if (warp == 8 || warp == 11) {
       // ---- TMA producers, warp 8 for K and warp 11 for V: step j's four
