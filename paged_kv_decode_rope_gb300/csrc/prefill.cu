@@ -259,6 +259,8 @@ struct TcCfg {
   // (128 x 48 + 256 x 96 = 384 x 80)
   static constexpr int kIssueRegs = 48;
   static constexpr int kSoftmaxRegs = 96;
+  static_assert(128 * kIssueRegs + kSoftmaxThreads * kSoftmaxRegs <= kThreads * 80,
+                "the register shares exceed what two CTAs an SM give a CTA");
   static constexpr uint32_t kTile = 128 * 128;  // a 128-row x 128-byte operand tile
   static constexpr uint32_t kStep = 64 * 128;   // 64 K rows (or V rows) of one step
   // dynamic shared memory: Q_hi, Q_lo, then per stage K and V
@@ -847,6 +849,14 @@ cudaError_t launch_attn(const PrefillLaunch& a, const PrefillLayout& l, cudaStre
   if (!attr_set[G].load(std::memory_order_relaxed)) {
     e = cudaFuncSetAttribute(prefill_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // The warpgroups' register shares must fit in what the launch gives the
+    // CTA (the compiler's count a thread x its threads), or the softmax
+    // warps' increase would wait for registers that never come: refuse.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, prefill_tc_kernel<G>);
+    if (e != cudaSuccess) return e;
+    if (128 * C::kIssueRegs + C::kSoftmaxThreads * C::kSoftmaxRegs > C::kThreads * fa.numRegs)
+      return cudaErrorInvalidConfiguration;
     attr_set[G].store(true, std::memory_order_relaxed);
   }
   const size_t n_ctas = grid_x * static_cast<size_t>(a.num_kv_heads);
