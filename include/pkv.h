@@ -312,10 +312,10 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks
  *                (paged_rope_table_build), built once for the model's theta
  *   workspace    device memory of at least paged_prefill_workspace_bytes(),
  *                256-byte aligned, contents irrelevant
- * Launches four kernels on `stream`: an expansion of the chunk tokens (each
- * token's sequence and position), the append (every chunk token stored as a
- * decode token would be, with the same certified key rounding, the cos and
- * sin read from the table row of its position), a tile plan, and a
+ * Launches three kernels on `stream`: a preparation (each chunk token's
+ * sequence and position, and the tile plan), the append (every chunk token
+ * stored as a decode token would be, with the same certified key rounding,
+ * the cos and sin read from the table row of its position), and a
  * flash-attention kernel on the tcgen05 tensor cores, one CTA per (sequence,
  * kv head, tile of up to 128 (token, query head) rows) that streams the
  * sequence's pages once per tile. Tokens of a malformed chunk (cu_tokens

@@ -7,12 +7,12 @@
 // and appended like a decode token, and the queries of chunk token t attend
 // causally over the sequence's first start_pos[b] + t + 1 tokens.
 //
-// Four launches. (1) An expansion kernel gives every chunk token its sequence
-// and position. (2) The append kernel rotates and stores every chunk token
-// exactly as a decode token would be stored (cos and sin from the row of its
-// position in the caller's RoPE table, built once for all positions), and
-// writes the rotated queries. (3) A one-CTA plan lists the query tiles.
-// (4) Flash attention on the fifth-generation tensor
+// Three launches. (1) A preparation kernel: one block lists the query tiles,
+// the others give every chunk token its sequence and position. (2) The append
+// kernel rotates and stores every chunk token exactly as a decode token would
+// be stored (cos and sin from the row of its position in the caller's RoPE
+// table, built once for all positions), and writes the rotated queries.
+// (3) Flash attention on the fifth-generation tensor
 // cores: one CTA per (tile of up to 128 (token, query head) rows, kv head)
 // streams the sequence's pages up to the tile's last position, four pages
 // per step, through a TMA ring; tcgen05 MMAs with fp32 accumulators in tensor
@@ -29,7 +29,6 @@
 namespace pkv {
 namespace {
 
-constexpr int kExpandThreads = 256;
 constexpr int kHalfDim = kHeadDim / 2;
 
 // One thread per chunk token: find its sequence by bisection over cu_tokens
@@ -37,11 +36,10 @@ constexpr int kHalfDim = kHeadDim / 2;
 // cu_tokens, a negative start, or a position past max_blocks*16) gets
 // sequence -PKV_ERR_SEQ_LEN, one at a position past the RoPE table's rows
 // -PKV_ERR_POSITION, and position 0.
-__global__ void prefill_expand_kernel(int max_blocks, int rope_positions,
-                                      const int32_t* __restrict__ cu_tokens,
-                                      const int32_t* __restrict__ start_pos, int batch, int total,
-                                      int32_t* __restrict__ tok_seq, int32_t* __restrict__ tok_pos) {
-  const int idx = blockIdx.x * kExpandThreads + threadIdx.x;
+__device__ void expand_token(int idx, int max_blocks, int rope_positions,
+                             const int32_t* __restrict__ cu_tokens,
+                             const int32_t* __restrict__ start_pos, int batch, int total,
+                             int32_t* __restrict__ tok_seq, int32_t* __restrict__ tok_pos) {
   if (idx >= total) return;
   int lo = 0, hi = batch - 1;  // largest b with cu_tokens[b] <= idx
   while (lo < hi) {
@@ -151,10 +149,9 @@ constexpr int kPlanThreads = 1024;
 // clipped to [0, total); tiles past `capacity` (only possible when chunks
 // overlap) are dropped and flagged.
 constexpr int kPlanBuckets = 2048;
-__global__ void __launch_bounds__(kPlanThreads)
-    prefill_plan_kernel(const int32_t* __restrict__ cu_tokens, const int32_t* __restrict__ start_pos,
-                        int batch, int total, int tokens_per_tile, int capacity,
-                        int4* __restrict__ tiles, int* __restrict__ num_tiles, int* __restrict__ err) {
+__device__ void plan_tiles(const int32_t* __restrict__ cu_tokens, const int32_t* __restrict__ start_pos,
+                           int batch, int total, int tokens_per_tile, int capacity,
+                           int4* __restrict__ tiles, int* __restrict__ num_tiles, int* __restrict__ err) {
   using Scan = cub::BlockScan<int, kPlanThreads>;
   __shared__ typename Scan::TempStorage scan_tmp;
   __shared__ int s_hist[kPlanBuckets];  // tiles per bucket, then the bucket's next slot
@@ -203,6 +200,23 @@ __global__ void __launch_bounds__(kPlanThreads)
     if (all > capacity) atomicOr(err, PKV_ERR_SEQ_LEN);
     *num_tiles = min(all, capacity);
   }
+}
+
+// The preparation of a prefill call, one launch: block 0 makes the tile plan
+// (plan_tiles, the longest part), the other blocks expand the chunk tokens
+// (expand_token, one thread a token).
+__global__ void __launch_bounds__(kPlanThreads)
+    prefill_prep_kernel(int max_blocks, int rope_positions, const int32_t* __restrict__ cu_tokens,
+                        const int32_t* __restrict__ start_pos, int batch, int total,
+                        int32_t* __restrict__ tok_seq, int32_t* __restrict__ tok_pos,
+                        int tokens_per_tile, int capacity, int4* __restrict__ tiles,
+                        int* __restrict__ num_tiles, int* __restrict__ err) {
+  if (blockIdx.x == 0) {
+    plan_tiles(cu_tokens, start_pos, batch, total, tokens_per_tile, capacity, tiles, num_tiles, err);
+    return;
+  }
+  expand_token(static_cast<int>(blockIdx.x - 1) * kPlanThreads + static_cast<int>(threadIdx.x),
+               max_blocks, rope_positions, cu_tokens, start_pos, batch, total, tok_seq, tok_pos);
 }
 
 struct PrefillAttnParams {
@@ -817,17 +831,32 @@ PrefillLayout layout(int total_tokens, int batch, int max_blocks) {
   return l;
 }
 
+// The three launches of a prefill call for groups of G query heads: the
+// preparation (token expansion and tile plan), the append, the attention.
 template <int G>
-cudaError_t launch_attn(const PrefillLaunch& a, const PrefillLayout& l, cudaStream_t stream) {
+cudaError_t launch_all(const PrefillLaunch& a, const PrefillLayout& l, cudaStream_t stream) {
   using C = TcCfg<G>;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  int32_t* tok_seq = reinterpret_cast<int32_t*>(ws + l.seq);
+  int32_t* tok_pos = reinterpret_cast<int32_t*>(ws + l.pos);
   int4* tiles = reinterpret_cast<int4*>(ws + l.tiles);
   int* count = reinterpret_cast<int*>(ws + l.count);
   const size_t grid_x = static_cast<size_t>(a.total_tokens + C::kTokens - 1) / C::kTokens + a.batch;
-  prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(a.cu_tokens, a.start_pos, a.batch,
-                                                      a.total_tokens, C::kTokens,
-                                                      static_cast<int>(grid_x), tiles, count, a.err);
+  const int expand_blocks = (a.total_tokens + kPlanThreads - 1) / kPlanThreads;
+  prefill_prep_kernel<<<1 + expand_blocks, kPlanThreads, 0, stream>>>(
+      a.max_blocks, a.rope_positions, a.cu_tokens, a.start_pos, a.batch, a.total_tokens, tok_seq,
+      tok_pos, C::kTokens, static_cast<int>(grid_x), tiles, count, a.err);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the caller's RoPE table: fp32 pair rows, then fp64 rows, one per position
+  const float4* rope_ff = static_cast<const float4*>(a.rope_table);
+  const double2* rope_dd =
+      reinterpret_cast<const double2*>(rope_ff + static_cast<size_t>(a.rope_positions) * kHalfDim);
+  prefill_append_kernel<<<a.total_tokens, kAppendThreads, 0, stream>>>(
+      const_cast<uint16_t*>(reinterpret_cast<const uint16_t*>(a.pool)), a.num_pages, a.num_kv_heads,
+      a.num_q_heads, a.q, a.k, a.v, a.q_rot, a.block_tables, a.max_blocks, tok_seq, tok_pos, rope_ff,
+      rope_dd, a.err);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   PrefillAttnParams p;
   p.q_rot = a.q_rot;
@@ -875,34 +904,16 @@ size_t prefill_workspace_bytes(int total_tokens, int batch, int max_blocks) {
 cudaError_t launch_prefill(const PrefillLaunch& a, cudaStream_t stream) {
   if (a.total_tokens == 0) return cudaSuccess;
   const PrefillLayout l = layout(a.total_tokens, a.batch, a.max_blocks);
-  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
-  int32_t* tok_seq = reinterpret_cast<int32_t*>(ws + l.seq);
-  int32_t* tok_pos = reinterpret_cast<int32_t*>(ws + l.pos);
-  prefill_expand_kernel<<<(a.total_tokens + kExpandThreads - 1) / kExpandThreads, kExpandThreads, 0,
-                          stream>>>(a.max_blocks, a.rope_positions, a.cu_tokens, a.start_pos,
-                                    a.batch, a.total_tokens, tok_seq, tok_pos);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // the caller's RoPE table: fp32 pair rows, then fp64 rows, one per position
-  const float4* rope_ff = static_cast<const float4*>(a.rope_table);
-  const double2* rope_dd =
-      reinterpret_cast<const double2*>(rope_ff + static_cast<size_t>(a.rope_positions) * kHalfDim);
-  prefill_append_kernel<<<a.total_tokens, kAppendThreads, 0, stream>>>(
-      const_cast<uint16_t*>(reinterpret_cast<const uint16_t*>(a.pool)), a.num_pages, a.num_kv_heads,
-      a.num_q_heads, a.q, a.k, a.v, a.q_rot, a.block_tables, a.max_blocks, tok_seq, tok_pos, rope_ff,
-      rope_dd, a.err);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
 
   switch (a.num_q_heads / a.num_kv_heads) {
-    case 1: return launch_attn<1>(a, l, stream);
-    case 2: return launch_attn<2>(a, l, stream);
-    case 3: return launch_attn<3>(a, l, stream);
-    case 4: return launch_attn<4>(a, l, stream);
-    case 5: return launch_attn<5>(a, l, stream);
-    case 6: return launch_attn<6>(a, l, stream);
-    case 7: return launch_attn<7>(a, l, stream);
-    case 8: return launch_attn<8>(a, l, stream);
+    case 1: return launch_all<1>(a, l, stream);
+    case 2: return launch_all<2>(a, l, stream);
+    case 3: return launch_all<3>(a, l, stream);
+    case 4: return launch_all<4>(a, l, stream);
+    case 5: return launch_all<5>(a, l, stream);
+    case 6: return launch_all<6>(a, l, stream);
+    case 7: return launch_all<7>(a, l, stream);
+    case 8: return launch_all<8>(a, l, stream);
     default: return cudaErrorInvalidValue;
   }
 }
