@@ -316,7 +316,8 @@ size_t paged_prefill_workspace_bytes(int total_tokens, int batch, int max_blocks
  * sequence and position, and the tile plan), the append (every chunk token
  * stored as a decode token would be, with the same certified key rounding,
  * the cos and sin read from the table row of its position), and a
- * flash-attention kernel on the tcgen05 tensor cores, one CTA per (sequence,
+ * flash-attention kernel (launched to overlap the append's end, through
+ * programmatic dependent launch; it lets no later kernel start early) on the tcgen05 tensor cores, one CTA per (sequence,
  * kv head, tile of up to 128 (token, query head) rows) that streams the
  * sequence's pages once per tile. Tokens of a malformed chunk (cu_tokens
  * decreasing, a negative start, or a position past max_blocks*16) are not

@@ -75,6 +75,9 @@ __global__ void __launch_bounds__(kAppendThreads)
                           int* __restrict__ err) {
   __shared__ float4 cs[kHalfDim];
   const int tkn = blockIdx.x, tid = threadIdx.x;
+  // the attention kernel after this one may start its set-up (it waits for
+  // this kernel before it reads anything this kernel writes)
+  grid_launch_dependents();
   const int row = tok_pos[tkn];  // the table row: the token's position
   if (tid < kHalfDim) cs[tid] = rope_ff[static_cast<size_t>(row) * kHalfDim + tid];
   __syncthreads();
@@ -426,6 +429,10 @@ __global__ void __launch_bounds__(TcCfg<G>::kThreads, 2)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Everything above (the tile, the zeroed rows, tensor memory and the
+  // barriers) overlaps the end of the append kernel before this one; the
+  // rotated queries and the pool pages it writes are read only from here on.
+  grid_dependency_wait();
   const uint32_t tmem = s_tmem, tO = tmem + 64 * kSBufs;
   auto tS = [&](int j) { return tmem + 64 * (j % kSBufs); };  // S_j, then P_j (hi: +0, lo: +32)
   auto buf = [](int j) { return j % kSBufs; };                   // step j's S / P / P V barriers
@@ -891,8 +898,18 @@ cudaError_t launch_all(const PrefillLaunch& a, const PrefillLayout& l, cudaStrea
   const size_t n_ctas = grid_x * static_cast<size_t>(a.num_kv_heads);
   if (n_ctas > 0x7fffffffu) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(n_ctas));
-  prefill_tc_kernel<G><<<grid, C::kThreads, smem, stream>>>(*a.kv16_map, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the kernel's set-up overlaps the append's end
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<G>, *a.kv16_map, p);
 }
 
 }  // namespace
