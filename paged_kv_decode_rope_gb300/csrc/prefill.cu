@@ -251,12 +251,16 @@ struct PrefillAttnParams {
 // moves it (rescaling the row of O in tensor memory) only when a score passes
 // it by more than kSlack in the base-2 domain, so P <= 2^kSlack; numerator
 // and denominator share the reference, so the result is the same softmax.
-// Warps 0-7 run the softmax and the epilogue, 16 rows a warp and four
-// threads a row (the 16x256b tensor-memory layout; the four threads combine
-// row maxima and sums by shuffles), warp 8 issues the TMA copies of the K rows (each page's 16 K rows
-// into the stage's K tile) and warp 11 those of the V rows (into the V tile),
-// with separate barriers so K of a later step loads as soon as its stage's
-// scores are done, warp 9 issues the score products and warp 10 the P V
+// Warps 0-7 (two warpgroups) run the softmax and the epilogue, 16 rows a
+// warp and four threads a row (the 16x256b tensor-memory layout; the four
+// threads combine row maxima and sums by shuffles); from the second step on
+// they make P with the reference as it stands while the row maxima are
+// worked out, and make it again in the rare warp whose reference moves.
+// Warps 8-11 (one warpgroup, which hands registers to the softmax
+// warpgroups) issue: warp 8 the TMA copies of the K rows (each page's 16 K
+// rows into the stage's K tile) and warp 11 those of the V rows (into the V
+// tile), with separate barriers so K of a later step loads as soon as its
+// stage's scores are done, warp 9 the score products and warp 10 the P V
 // products. S_j goes out as soon as its buffer and K tile are free, so the
 // tensor core computes the next scores while the softmax works on these.
 // Every issuing warp runs converged and one elected lane issues (a lone
