@@ -64,6 +64,12 @@ __device__ void expand_token(int idx, int max_blocks, int rope_positions,
 // fp64 from the table where it cannot certify: the bytes the decode append
 // stores), and its value, both stored at its position in its sequence's
 // pages. A token of a malformed chunk (position 0) still gets a rotated query.
+// A thread loads its first two query items (four pairs each), its first two
+// key pairs, its first 16-byte piece of the value rows and the block-table
+// entry before the barrier that makes the cos/sin row visible, so that the
+// token costs two dependent round trips (its position, then the rest) for
+// the usual shapes (up to 64 query and 8 kv heads); items past those are
+// loaded in the loops.
 constexpr int kAppendThreads = 128;
 __global__ void __launch_bounds__(kAppendThreads)
     prefill_append_kernel(uint16_t* __restrict__ pool, long long num_pages, int hkv, int hq,
@@ -75,69 +81,99 @@ __global__ void __launch_bounds__(kAppendThreads)
                           int* __restrict__ err) {
   __shared__ float4 cs[kHalfDim];
   const int tkn = blockIdx.x, tid = threadIdx.x;
-  // the attention kernel after this one may start its set-up (it waits for
-  // this kernel before it reads anything this kernel writes)
-  grid_launch_dependents();
-  const int row = tok_pos[tkn];  // the table row: the token's position
-  if (tid < kHalfDim) cs[tid] = rope_ff[static_cast<size_t>(row) * kHalfDim + tid];
-  __syncthreads();
+  const int b = tok_seq[tkn];
+  const int pos = tok_pos[tkn];  // also the token's row of the RoPE table (0 when malformed)
+  const int nq = hq * (kHalfDim / 4), nk = hkv * kHalfDim, nv = hkv * (kRowBytes / 16);
   const uint16_t* qb = q + static_cast<size_t>(tkn) * hq * kHeadDim;
-  float* qo = q_rot + static_cast<size_t>(tkn) * hq * kHeadDim;
-  // four pairs (j0 .. j0 + 3, and 32 further) per item: 8-byte loads of the
-  // bf16 halves, 16-byte stores of the fp32 results
-  for (int idx = tid; idx < hq * (kHalfDim / 4); idx += kAppendThreads) {
+  const uint16_t* kb = k + static_cast<size_t>(tkn) * hkv * kHeadDim;
+  const uint4* vb = reinterpret_cast<const uint4*>(v + static_cast<size_t>(tkn) * hkv * kHeadDim);
+  // query item idx: head idx / 8, pairs j0 .. j0 + 3 (8-byte loads of the
+  // bf16 halves j0 .. j0 + 3 and j0 + 32 .. j0 + 35)
+  auto q_load = [&](int idx, uint2& a, uint2& c) {
     const int head = idx / (kHalfDim / 4), j0 = 4 * (idx - head * (kHalfDim / 4));
-    const uint2 a = *reinterpret_cast<const uint2*>(qb + head * kHeadDim + j0);
-    const uint2 bq = *reinterpret_cast<const uint2*>(qb + head * kHeadDim + j0 + kHalfDim);
+    a = *reinterpret_cast<const uint2*>(qb + head * kHeadDim + j0);
+    c = *reinterpret_cast<const uint2*>(qb + head * kHeadDim + j0 + kHalfDim);
+  };
+  auto k_load = [&](int idx, uint16_t& k0, uint16_t& k1) {
+    const int hh = idx / kHalfDim, j = idx - hh * kHalfDim;
+    k0 = kb[hh * kHeadDim + j];
+    k1 = kb[hh * kHeadDim + j + kHalfDim];
+  };
+  uint2 qa0 = make_uint2(0u, 0u), qc0 = qa0, qa1 = qa0, qc1 = qa0;
+  uint16_t k00 = 0, k10 = 0, k01 = 0, k11 = 0;
+  uint4 v0 = make_uint4(0u, 0u, 0u, 0u);
+  long long page = -1;
+  if (tid < nq) q_load(tid, qa0, qc0);
+  if (tid + kAppendThreads < nq) q_load(tid + kAppendThreads, qa1, qc1);
+  if (b >= 0) {
+    page = block_tables[static_cast<size_t>(b) * max_blocks + pos / kPage];
+    if (tid < nk) k_load(tid, k00, k10);
+    if (tid + kAppendThreads < nk) k_load(tid + kAppendThreads, k01, k11);
+    if (tid < nv) v0 = vb[tid];
+  }
+  if (tid < kHalfDim) cs[tid] = rope_ff[static_cast<size_t>(pos) * kHalfDim + tid];
+  __syncthreads();
+  // the rotated query: 16-byte stores of the fp32 results
+  float* qo = q_rot + static_cast<size_t>(tkn) * hq * kHeadDim;
+  auto q_rotate = [&](int idx, uint2 a, uint2 c) {
+    const int head = idx / (kHalfDim / 4), j0 = 4 * (idx - head * (kHalfDim / 4));
     const float x0[4] = {__uint_as_float(a.x << 16), __uint_as_float(a.x & 0xffff0000u),
                          __uint_as_float(a.y << 16), __uint_as_float(a.y & 0xffff0000u)};
-    const float x1[4] = {__uint_as_float(bq.x << 16), __uint_as_float(bq.x & 0xffff0000u),
-                         __uint_as_float(bq.y << 16), __uint_as_float(bq.y & 0xffff0000u)};
+    const float x1[4] = {__uint_as_float(c.x << 16), __uint_as_float(c.x & 0xffff0000u),
+                         __uint_as_float(c.y << 16), __uint_as_float(c.y & 0xffff0000u)};
     float y0[4], y1[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float4 c = cs[j0 + e];
-      y0[e] = x0[e] * c.x - x1[e] * c.z;
-      y1[e] = x1[e] * c.x + x0[e] * c.z;
+      const float4 t = cs[j0 + e];
+      y0[e] = x0[e] * t.x - x1[e] * t.z;
+      y1[e] = x1[e] * t.x + x0[e] * t.z;
     }
     *reinterpret_cast<float4*>(qo + head * kHeadDim + j0) = make_float4(y0[0], y0[1], y0[2], y0[3]);
     *reinterpret_cast<float4*>(qo + head * kHeadDim + j0 + kHalfDim) = make_float4(y1[0], y1[1], y1[2], y1[3]);
+  };
+  if (tid < nq) q_rotate(tid, qa0, qc0);
+  if (tid + kAppendThreads < nq) q_rotate(tid + kAppendThreads, qa1, qc1);
+  for (int idx = tid + 2 * kAppendThreads; idx < nq; idx += kAppendThreads) {
+    uint2 a, c;
+    q_load(idx, a, c);
+    q_rotate(idx, a, c);
   }
-  const int b = tok_seq[tkn];
   if (b < 0) {  // a malformed chunk, or a position past the RoPE table
     if (tid == 0) atomicOr(err, -b);
     return;
   }
-  const int pos = tok_pos[tkn];
-  const long long page = block_tables[static_cast<size_t>(b) * max_blocks + pos / kPage];
   if (page < 0 || page >= num_pages) {
     if (tid == 0) atomicOr(err, PKV_ERR_PAGE_ID);
     return;
   }
   const int slot = pos % kPage;
   uint16_t* page_base = pool + static_cast<size_t>(page) * hkv * (kHeadPageBytes / 2);
-  const uint16_t* kb = k + static_cast<size_t>(tkn) * hkv * kHeadDim;
-  for (int idx = tid; idx < hkv * kHalfDim; idx += kAppendThreads) {
+  auto k_store = [&](int idx, uint16_t k0, uint16_t k1) {
     const int hh = idx / kHalfDim, j = idx - hh * kHalfDim;
-    const uint16_t k0 = kb[hh * kHeadDim + j], k1 = kb[hh * kHeadDim + j + kHalfDim];
     const float x0 = __uint_as_float(static_cast<uint32_t>(k0) << 16);
     const float x1 = __uint_as_float(static_cast<uint32_t>(k1) << 16);
     const float4 c = cs[j];
     uint16_t y0, y1;
     if (!(rotated_bf16_fast(x0, x1, c.x, c.y, c.z, c.w, y0) &&
           rotated_bf16_fast(x1, -x0, c.x, c.y, c.z, c.w, y1))) {
-      const double2 cd = rope_dd[static_cast<size_t>(row) * kHalfDim + j];
+      const double2 cd = rope_dd[static_cast<size_t>(pos) * kHalfDim + j];
       rotate_key_pair(k0, k1, cd.x, cd.y, y0, y1);
     }
     uint16_t* krow = page_base + (hh * 2 + 0) * (kHalfBytes / 2) + slot * kHeadDim;
     krow[j] = y0;
     krow[j + kHalfDim] = y1;
+  };
+  if (tid < nk) k_store(tid, k00, k10);
+  if (tid + kAppendThreads < nk) k_store(tid + kAppendThreads, k01, k11);
+  for (int idx = tid + 2 * kAppendThreads; idx < nk; idx += kAppendThreads) {
+    uint16_t k0, k1;
+    k_load(idx, k0, k1);
+    k_store(idx, k0, k1);
   }
-  const uint4* vb = reinterpret_cast<const uint4*>(v + static_cast<size_t>(tkn) * hkv * kHeadDim);
-  for (int idx = tid; idx < hkv * (kRowBytes / 16); idx += kAppendThreads) {
+  for (int idx = tid; idx < nv; idx += kAppendThreads) {
     const int hh = idx / (kRowBytes / 16), c = idx - hh * (kRowBytes / 16);
     uint4* vrow = reinterpret_cast<uint4*>(page_base + (hh * 2 + 1) * (kHalfBytes / 2) + slot * kHeadDim);
-    vrow[c] = vb[hh * (kRowBytes / 16) + c];
+    vrow[c] = idx == tid ? v0 : vb[idx];
   }
 }
 
