@@ -69,7 +69,7 @@ TRAFFIC = {
 # hash of the prefill source it was taken on; reported only while unchanged.
 PREFILL_TRAFFIC = {
     # (sequences, prompt tokens) -> (sha256 prefix of prefill.cu, read + write bytes per launch)
-    (4, 2048): ("37b7599ed6be5199", 111688704),
+    (4, 2048): ("48b626bfea4feb4a", 111688704),
 }
 # The other workloads the 70% target names, timed as sub-records of the default line.
 SUB_WORKLOADS = ["llama1b_b256_l16_skew", "qwen05b_b32_l24_u1024_4096"]
